@@ -1,0 +1,59 @@
+"""Plants plausible mistakes in copies of the oracle source and checks that the
+pins catch every one (CPU only).  The real oracle is never modified: each
+mutant is compiled from a patched copy into a temporary directory."""
+import os
+import subprocess
+
+import pytest
+
+from oracle import oracle as O
+import oracle_pins as P
+
+SRC = os.path.join(os.path.dirname(O.__file__), "pq2_oracle.c")
+
+# (name, original text, mistaken text)
+MUTANTS = [
+    ("decode_offset", "& 3u) - 1;", "& 3u) - 0;"),
+    ("decode_field_width", "(byte >> (2 * field))", "(byte >> (field))"),
+    ("scale_big_endian", "(blk[0] | (blk[1] << 8))", "(blk[1] | (blk[0] << 8))"),
+    ("code_byte_offset", "blk[2 + j]", "blk[1 + j]"),
+    ("scale_reciprocal", "float s = amax / 127.0f;", "float s = amax * (1.0f / 127.0f);"),
+    ("scale_128", "float s = amax / 127.0f;", "float s = amax / 128.0f;"),
+    ("round_half_away", "nearbyintf(x[i] / d)", "roundf(x[i] / d)"),
+    ("round_trunc", "nearbyintf(x[i] / d)", "truncf(x[i] / d)"),
+    ("divide_by_reciprocal", "nearbyintf(x[i] / d)", "nearbyintf(x[i] * (1.0f / d))"),
+    ("zero_group_scale_stored", "sx[m * G + g] = s;", "sx[m * G + g] = d;"),
+    ("dot_sign", "acc += w * (int32_t)q[m * K + k];", "acc -= w * (int32_t)q[m * K + k];"),
+    ("dot_field_order", "(int)(k % 4));\n          acc", "(int)((k / 32) % 4));\n          acc"),
+    ("weight_scale_dropped", "t = t * ws;", "t = t * xs;"),
+    ("last_group_dropped", "for (int64_t g = 0; g < G; ++g) {\n        int32_t dot",
+     "for (int64_t g = 0; g + 1 < G; ++g) {\n        int32_t dot"),
+    ("planes_transposed", "q[m * K + g * ORC_GROUP + 4 * j + s]", "q[m * K + g * ORC_GROUP + 4 * s + j]"),
+    ("half_exponent_bias", "(int)expo - 25", "(int)expo - 24"),
+    ("half_subnormal", "ldexp((double)frac, -24)", "ldexp((double)frac, -25)"),
+    ("bf16_ties_up", "lower > 0x8000u ||", "lower >= 0x8000u ||"),
+    ("widen_kind_swap", "if (kind == 0)\n        a[m * K + k] = orc_bf16_to_float",
+     "if (kind == 1)\n        a[m * K + k] = orc_bf16_to_float"),
+    ("fp64_term_sign", "acc64 += term;", "acc64 -= term;"),
+    ("qsum_off_by_one", "for (int i = 0; i < ORC_GROUP; ++i) t +=", "for (int i = 1; i < ORC_GROUP; ++i) t +="),
+]
+
+
+@pytest.mark.parametrize("name,orig,bad", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(tmp_path, name, orig, bad):
+    src = open(SRC).read()
+    assert src.count(orig) >= 1, f"mutation anchor not found: {name}"
+    mutated = src.replace(orig, bad, 1)
+    c_path = tmp_path / f"{name}.c"
+    so_path = tmp_path / f"{name}.so"
+    c_path.write_text(mutated)
+    subprocess.run(["gcc", *O._CFLAGS, str(c_path), "-o", str(so_path), "-lm"],
+                   check=True)
+    lib = O.load(str(so_path))
+    failed = []
+    for pin in P.ALL_PINS:
+        try:
+            pin(lib)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"no pin caught mutant {name}"
