@@ -1,0 +1,373 @@
+#!/usr/bin/env python3
+"""Benchmark of the ternary (PQ2) x INT8 small-batch projection on GB300.
+
+Workload (one GPU): attn_qkv, K=5120 inputs, N=10240 outputs, M = 1, 2, 3, 4
+tokens; ternary 2-bit codes iid uniform over {0,1,2} with fp16 group-128
+scales uniform in [0.005, 0.05]; bf16 activations N(0,1) with a seeded 1% of
+the channels scaled by 20; INT8 per-128-group activation quantisation, fp32
+accumulation, bf16 output.
+
+A step is one complete projection call (quantise + GEMV) for each of M = 1..4,
+every call on a different weight matrix; the distinct matrices (more than 4x
+the L2 size in total) rotate, so weights always stream from HBM.  Steps are
+replayed from CUDA graphs and timed with CUDA events on the launching stream.
+
+  value       mean microseconds per complete call over the step (device time)
+  e2e         the same through host buffers: pinned host x -> device, the
+              calls, device -> pinned host y, all inside the timed region
+  roofline    pq2_mmv alone: packed weight bytes K*N*34/128 per launch over
+              its CUDA-event time per launch, against the measured HBM peak
+  cpu_baseline the CPU oracle on the host cores, on a bounded sample
+
+`--impl reference` times the CPU oracle on the same workload instead (the
+reference arm of this comparison).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("µs/call and HBM GB/s (frac of peak) for ternary×INT8 matmul at "
+          "M=1–8; prefill TOPS")
+K_DIM, N_DIM, MS = 5120, 10240, (1, 2, 3, 4)
+WORKLOAD = ("attn_qkv K=5120 N=10240, M=1,2,3,4 per step (quantise + GEMV each); ternary "
+            "codes U{0,1,2}, fp16 group-128 scales U[0.005,0.05]; bf16 x N(0,1) with 1% "
+            "channels x20; fp32 accumulate, bf16 out")
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- reference
+def run_reference(args):
+    """The CPU oracle on the same workload.  Each step is one complete call
+    for M = 1..4 restricted to a fixed sample of REF_ROWS of the N output
+    rows (quantisation of the whole x included), single-threaded; the time
+    is scaled by N / REF_ROWS to a full call."""
+    from oracle import oracle as O
+    from ternary_weight_int8_gb300 import synth
+
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    ref_rows = 1024
+    raw = synth.raw_weights(N_DIM, K_DIM, seed=1234)
+    codes, scales = O.prepare(raw.numpy(), K_DIM)
+    codes, scales = codes[:ref_rows].copy(), scales[:ref_rows].copy()
+    xs = {M: synth.bits_u16(synth.activations(M, K_DIM, seed=77 + M, outlier_frac=0.01))
+          for M in MS}
+    O.load()
+
+    def step():
+        for M in MS:
+            O.linear(xs[M], "bf16", codes, scales)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) * (N_DIM / ref_rows)
+    us = dt / (args.steps * len(MS)) * 1e6
+    sample = (f"{args.steps} steps of M=1..4 calls on {ref_rows} of {N_DIM} output rows, "
+              f"time scaled by {N_DIM / ref_rows:g}")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(us, 3), "unit": "us/call",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "i8", "data": "synthetic",
+        "config": {"workload": WORKLOAD,
+                   "runs": "CPU oracle (plain C, IEEE fp32/fp64, one thread)"},
+        "cpu_baseline": {"value": round(us, 3), "unit": "us/call", "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(us, 3), "unit": "us/call", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------- ours
+def cpu_baseline_sample(budget_s=12.0):
+    """The oracle as it stands on one host core: complete calls for M = 1..4
+    on the full attn_qkv shape, repeated for about budget_s seconds."""
+    import torch
+    from oracle import oracle as O
+    from ternary_weight_int8_gb300 import synth
+    raw = synth.raw_weights(N_DIM, K_DIM, seed=4321)
+    codes, scales = O.prepare(raw.numpy(), K_DIM)
+    xs = {M: synth.bits_u16(synth.activations(M, K_DIM, seed=5 + M, outlier_frac=0.01))
+          for M in MS}
+    O.load()
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        for M in MS:
+            O.linear(xs[M], "bf16", codes, scales)
+            calls += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(dt / calls * 1e6, 3), "unit": "us/call", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{calls} complete attn_qkv calls (M=1..4 cycled) in {dt:.1f} s"}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from ternary_weight_int8_gb300 import pq2, synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lib = pq2.lib()
+
+    # -------------------------------------------------- inputs (resident)
+    wbytes = N_DIM * K_DIM * 34 // 128
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_mats = max(16, math.ceil(4 * l2 / wbytes))
+    n_mats = (n_mats + len(MS) - 1) // len(MS) * len(MS)
+    mats = []
+    for i in range(n_mats):
+        raw = synth.raw_weights(N_DIM, K_DIM, seed=1000 * rank + i, device=dev)
+        mats.append(pq2.pq2_prepare(raw, K_DIM))
+        del raw
+    xs = {M: synth.activations(M, K_DIM, seed=77 + M, device=dev, outlier_frac=0.01)
+          for M in MS}
+    qbuf = {M: pq2.pq2_quantize_act(xs[M], pq2.PQ2_Q_PLANES) for M in MS}
+    ys = {M: torch.empty((M, N_DIM), dtype=torch.bfloat16, device=dev) for M in MS}
+    # host-side buffers for the end-to-end leg
+    hx = {M: xs[M].cpu().pin_memory() for M in MS}
+    hy = {M: torch.empty((M, N_DIM), dtype=torch.bfloat16).pin_memory() for M in MS}
+    dx = {M: torch.empty_like(xs[M]) for M in MS}
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+
+    wss = {M: torch.empty(pq2.linear_workspace_bytes(M, K_DIM), dtype=torch.uint8, device=dev)
+           for M in MS}
+
+    def complete(M, mat, x, s):
+        """One complete call through the public entry point: quantise + GEMV."""
+        c, sc = mats[mat]
+        st = lib.pq2_linear(x.data_ptr(), pq2.PQ2_BF16, K_DIM, M, N_DIM, K_DIM, c.data_ptr(),
+                            sc.data_ptr(), ys[M].data_ptr(), pq2.PQ2_BF16, wss[M].data_ptr(),
+                            wss[M].numel(), status.data_ptr(), s)
+        if st:
+            raise RuntimeError(f"pq2_linear failed ({st})")
+
+    def mmv_only(M, mat, s):
+        """The GEMV alone on pre-quantised activations: back-to-back
+        independent projections (nothing in flight writes their inputs), so
+        each call may stream its inputs while the previous call finishes."""
+        q, sx, qs = qbuf[M]
+        c, sc = mats[mat]
+        st = lib.pq2_mmv_ex(q.data_ptr(), sx.data_ptr(), qs.data_ptr(), c.data_ptr(),
+                            sc.data_ptr(), ys[M].data_ptr(), pq2.PQ2_BF16, M, N_DIM, K_DIM,
+                            lib.pq2_mmv_decoder(M), pq2.PQ2_MMV_INDEPENDENT,
+                            status.data_ptr(), s)
+        if st:
+            raise RuntimeError(f"pq2_mmv failed ({st})")
+
+    n_graphs = n_mats // len(MS)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            fn()  # warm the launch path (sets kernel attributes) outside capture
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+        return g
+
+    # step graphs: graph j runs the 4 calls on matrices 4j..4j+3
+    step_graphs = [capture(lambda j=j: [complete(M, 4 * j + i, xs[M], sp)
+                                        for i, M in enumerate(MS)]) for j in range(n_graphs)]
+
+    def e2e_step(j):
+        for i, M in enumerate(MS):
+            dx[M].copy_(hx[M], non_blocking=True)
+            complete(M, 4 * j + i, dx[M], sp)
+            hy[M].copy_(ys[M], non_blocking=True)
+
+    e2e_graphs = [capture(lambda j=j: e2e_step(j)) for j in range(n_graphs)]
+
+    def timed(graphs, steps, warmup):
+        with torch.cuda.stream(stream):
+            for i in range(warmup):
+                graphs[i % len(graphs)].replay()
+            if world > 1:
+                dist.barrier()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(steps):
+                graphs[i % len(graphs)].replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    # soak (untimed) while the clock sampler runs, then the timed region
+    with ClockSampler(local) as clocks:
+        t_end = time.time() + 1.5
+        while time.time() < t_end:
+            timed(step_graphs, 200, 0)
+        total_ms = timed(step_graphs, args.steps, args.warmup)
+        e2e_ms = timed(e2e_graphs, args.steps, args.warmup)
+    ms_step = total_ms / args.steps
+    us_call = ms_step * 1e3 / len(MS)
+    e2e_us = e2e_ms / args.steps * 1e3 / len(MS)
+
+    # ------------------------------------------- per-M and kernel-only legs
+    per_m = {}
+    peak, peak_kind = measured_peaks()
+    for M in MS:
+        g_c = [capture(lambda j=j: [complete(M, (4 * j + i) % n_mats, xs[M], sp)
+                                    for i in range(4)]) for j in range(n_graphs)]
+        g_k = [capture(lambda j=j: [mmv_only(M, (4 * j + i) % n_mats, sp)
+                                    for i in range(4)]) for j in range(n_graphs)]
+        reps = max(50, args.steps)
+        c_ms = timed(g_c, reps, 5) / (reps * 4)
+        k_ms = timed(g_k, reps, 5) / (reps * 4)
+        per_m[str(M)] = {
+            "complete_us": round(c_ms * 1e3, 3),
+            "mmv_us": round(k_ms * 1e3, 3),
+            "mmv_gbs": round(wbytes / (k_ms * 1e-3) / 1e9, 1),
+            "mmv_frac": round(wbytes / (k_ms * 1e-3) / 1e9 / peak, 3),
+        }
+    # dominant kernel: pq2_mmv over the step's M mix, kernel-only
+    mean_k_us = statistics.mean(per_m[str(M)]["mmv_us"] for M in MS)
+    achieved = wbytes / (mean_k_us * 1e-6) / 1e9
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+
+    result = {
+        "metric": METRIC, "value": round(us_call, 3), "unit": "us/call", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "i8",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: {n_mats} distinct weight matrices "
+                         f"({n_mats * wbytes / 1e6:.0f} MB) rotated",
+                   "timing": "CUDA graph replays, CUDA events on the launching stream"},
+        "e2e": {"value": round(e2e_us, 3), "unit": "us/call",
+                "h2d_bytes_per_step": sum(M * K_DIM * 2 for M in MS),
+                "d2h_bytes_per_step": sum(M * N_DIM * 2 for M in MS)},
+        "gpu_launches": 2 * len(MS) * args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 3), "traffic": None,
+                     "kernel": "pq2_mmv", "peak_source": peak_kind,
+                     "bytes_per_launch": wbytes},
+        "per_m": per_m,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_baseline_sample()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,233 @@
+/*
+ * pq2.h — C ABI of libpq2, the GB300 (sm_103a) library for the small-batch
+ * and prefill matrix multiply of a ternary-quantised LLM ("PQ2" weights).
+ *
+ * The method (pages "Kernel experiments: recorded evidence", abbreviated KE,
+ * and "Baseline and the integer breakthrough", abbreviated BIB):
+ *   * weights: each row of K weights is K/128 blocks of 34 bytes — an fp16
+ *     scale s_w followed by 32 code bytes; weight k of a block is the 2-bit
+ *     field k%4 of code byte k/4, and code c means weight c-1 (KE Test 1,
+ *     Diagram 1; BIB "Unpack four weights with fewer instructions").
+ *   * activations: each group of 128 consecutive activations of a row is
+ *     quantised to INT8 with s_x = max|x|/127 (fp32), q = clamp(round half to
+ *     even(x / s_x), -127, 127) (KE Test 6; BIB "Calculate with small
+ *     integers", step 1).
+ *   * output: y[m][n] = sum over groups g of dot_g * s_x[m][g] * s_w[n][g],
+ *     dot_g the exact int32 dot of the group's weights and q (BIB steps 3-4),
+ *     accumulated in fp32.
+ *
+ * Conventions shared by every entry point:
+ *   * Pointers marked (device) are CUDA device pointers owned by the caller;
+ *     the library never allocates, frees or keeps them.  Buffers passed to
+ *     one call must not overlap unless stated.
+ *   * `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *     enqueued on it; no call synchronises the host with the device.
+ *   * Shapes: K > 0 and K % 128 == 0, N >= 1, M in the entry point's range.
+ *   * Argument errors are returned before anything is enqueued.  A launch
+ *     failure returns PQ2_ERR_LAUNCH.  Device-side waits are bounded: a wait
+ *     that gives up writes PQ2_ERR_TIMEOUT to *dev_status (when given) and
+ *     the kernel returns early; results are then invalid.
+ *   * The library only runs on compute capability 10.3 (GB300); any other
+ *     device returns PQ2_ERR_ARCH.  Inputs must be finite (NaN/Inf in x
+ *     give unspecified q).
+ */
+#ifndef PQ2_H
+#define PQ2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point (and written to dev_status). */
+enum {
+  PQ2_OK = 0,
+  PQ2_ERR_NULL = 1,      /* a required pointer is NULL                       */
+  PQ2_ERR_SHAPE = 2,     /* M, N, K, a stride or a size is out of range      */
+  PQ2_ERR_ALIGN = 3,     /* a pointer or stride breaks its alignment rule    */
+  PQ2_ERR_DTYPE = 4,     /* unknown dtype or layout enum                     */
+  PQ2_ERR_ARCH = 5,      /* current device is not compute capability 10.3   */
+  PQ2_ERR_LAUNCH = 6,    /* the CUDA launch reported an error                */
+  PQ2_ERR_TIMEOUT = 7,   /* a bounded device wait gave up (dev_status only)  */
+  PQ2_ERR_CUDA = 8       /* a CUDA runtime query failed (no device, ...)     */
+};
+
+/* Element types of activations (x) and outputs (y). */
+enum { PQ2_BF16 = 0, PQ2_F16 = 1, PQ2_F32 = 2 };
+
+/* Layouts of the quantised activations written by pq2_quantize_act.
+ *  PQ2_Q_ROWS   int8 q[M][K], row-major, natural order.
+ *  PQ2_Q_PLANES int8, plane order inside every 128-group: element i of a
+ *               group is stored at (i%4)*32 + i/4 (KE Test 21, plane-order
+ *               quantisation), so that plane s of a 4-byte code word meets
+ *               one contiguous 4-byte slice of q.  Operand of pq2_mmv.
+ *  PQ2_Q_F16    fp16 q[M][K], row-major, the same integer values widened
+ *               exactly (|q| <= 127).  Operand of pq2_mm: sm_103a has no
+ *               8-bit integer tcgen05 MMA, so the prefill contraction runs on
+ *               the fp16 tensor path, whose fp32 sums of integer products
+ *               below 2^24 are exact (a 128-group dot is at most 32512). */
+enum { PQ2_Q_ROWS = 0, PQ2_Q_PLANES = 1, PQ2_Q_F16 = 2 };
+
+/* Version of the prepared plane layout; bump whenever what a kernel reads
+ * changes, so callers can key caches on it (BIB: a layout switch must change
+ * the compile identity). */
+int pq2_layout_version(void);
+
+/* Static, never-NULL description of a status code. */
+const char *pq2_status_string(int status);
+
+/* Bytes of a prepared matrix: codes N*K/4 plus scales N*(K/128)*2 — still
+ * exactly 34 bytes per 128 weights (KE Test 4).  0 if the shape is invalid. */
+size_t pq2_prepared_bytes(int64_t N, int64_t K);
+
+/* pq2_prepare — split raw blocks into a code plane and a scale plane
+ * (KE Test 1 prepare_pq2 with separate buffers; Test 4 shared prepared
+ * layout).  A pure byte move: values are unchanged.
+ *   raw            (device) u8, N rows of K/128 blocks of 34 bytes, rows
+ *                  raw_row_stride bytes apart (>= K/128*34).
+ *   codes          (device) u8[N][K/4]; 16-byte aligned.
+ *   scales         (device) fp16 bit patterns [N][K/128]; 2-byte aligned.
+ * raw must not overlap codes or scales. */
+int pq2_prepare(const uint8_t *raw, int64_t raw_row_stride, int64_t N,
+                int64_t K, uint8_t *codes, uint16_t *scales, void *stream);
+
+/* pq2_quantize_act — per-128-group INT8 quantisation of activations
+ * (KE Test 6 _quantize; BIB "Calculate with small integers", step 1):
+ *   s = max|x| / 127 (fp32 IEEE division); d = s > 0 ? s : 1;
+ *   q = clamp(round-half-even(x / d), -127, 127) (IEEE division).
+ *   x        (device) x_dtype [M][ldx], ldx >= K elements.
+ *   M        1 .. 1<<20.
+ *   q        (device) written in q_layout: int8 [M][K] for ROWS/PLANES,
+ *            fp16 [M][K] for F16; 16-byte aligned.
+ *   sx       (device) fp32 [M][K/128] activation scales; 4-byte aligned.
+ *   qsum     (device, may be NULL) int32 [M][K/128], sum of q per group
+ *            (KE Test 21, the correction for the codes' -1 offset). */
+int pq2_quantize_act(const void *x, int x_dtype, int64_t ldx, int64_t M,
+                     int64_t K, void *q, int q_layout, float *sx,
+                     int32_t *qsum, void *stream);
+
+/* Decoders of the 2-bit codes used by the small-batch kernel; both give the
+ * same exact int32 group dots.
+ *  PQ2_DECODE_ADDXOR  the pages' add/XOR expansion (KE Test 1 _expand_byte;
+ *                     BIB "Unpack four weights with fewer instructions"):
+ *                     four codes spread one per byte, + 0x7F7F7F7F,
+ *                     ^ 0x80808080, giving signed bytes c-1 for a signed
+ *                     dp4a.
+ *  PQ2_DECODE_PLANES  masked planes (KE Test 21): byte & (3 << 2s) = c*4^s
+ *                     for an unsigned x signed dp4a, each plane shifted back
+ *                     and the -1 offset removed once per group with sum(q). */
+enum { PQ2_DECODE_ADDXOR = 0, PQ2_DECODE_PLANES = 1 };
+
+/* pq2_mmv — small-batch (M = 1..8) ternary x INT8 GEMV with weight reuse
+ * (BIB "Calculate with small integers"; KE Tests 6, 12, 14): every packed
+ * weight byte is read from HBM once and used for all M columns; codes are
+ * decoded in registers and multiplied with dp4a 4-way int8 dot products,
+ * 32 per 128-group, into an exact int32 group dot, which is then scaled as
+ * (float(dot) * s_x) * s_w and added in fp32.  The decoder is chosen from M
+ * only (see pq2_mmv_decoder); pq2_mmv_ex takes it explicitly.
+ *   q_planes (device) int8 [M][K] in PQ2_Q_PLANES order; 16-byte aligned.
+ *   sx       (device) fp32 [M][K/128]; 4-byte aligned.
+ *   qsum     (device) int32 [M][K/128] group sums of q (from
+ *            pq2_quantize_act); 4-byte aligned.
+ *   codes    (device) u8 [N][K/4] from pq2_prepare; 16-byte aligned.
+ *   scales   (device) fp16 [N][K/128] from pq2_prepare; 2-byte aligned.
+ *   y        (device) y_dtype [M][N] (PQ2_F32 or PQ2_BF16, bf16 = round to
+ *            nearest even of the fp32 result); aligned to its element.
+ *   dev_status (device, may be NULL) int32; PQ2_ERR_TIMEOUT is stored there
+ *            if a device wait gives up; never cleared by the library.
+ * Batch invariance: the fp32 operation sequence of output column m depends
+ * only on (N, K) and the device's SM count, never on M, and the group dots
+ * are exact, so column m is bit-identical for every M that contains it. */
+int pq2_mmv(const int8_t *q_planes, const float *sx, const int32_t *qsum,
+            const uint8_t *codes, const uint16_t *scales, void *y,
+            int y_dtype, int64_t M, int64_t N, int64_t K, int32_t *dev_status,
+            void *stream);
+
+/* Flags of pq2_mmv_ex.  Every libpq2 kernel is launched with programmatic
+ * dependent launch, and a call releases the next one only once the kernel
+ * before it has completed, so while a call starts at most the two kernels
+ * enqueued immediately before it on the stream can still be running.
+ *  PQ2_MMV_OVERLAP_WEIGHTS  the call may stream codes and scales from HBM
+ *      before those two kernels complete.  Legal when neither of them writes
+ *      codes or scales (e.g. the weights were prepared by an earlier call).
+ *  PQ2_MMV_INDEPENDENT      the call may also read q_planes, sx and qsum
+ *      early: legal when neither of those two kernels writes any input of
+ *      this call (e.g. back-to-back projections of the same quantised
+ *      activations).  y is always written only after the kernel before the
+ *      call has completed. */
+enum { PQ2_MMV_OVERLAP_WEIGHTS = 1, PQ2_MMV_INDEPENDENT = 2 };
+
+/* pq2_mmv with an explicit decoder (PQ2_DECODE_ADDXOR or PQ2_DECODE_PLANES)
+ * and flags; results are bit-identical to pq2_mmv for every decoder. */
+int pq2_mmv_ex(const int8_t *q_planes, const float *sx, const int32_t *qsum,
+               const uint8_t *codes, const uint16_t *scales, void *y,
+               int y_dtype, int64_t M, int64_t N, int64_t K, int decode,
+               int flags, int32_t *dev_status, void *stream);
+
+/* pq2_linear — the complete projection y = x W^T for M = 1..8 (quantise,
+ * then the small-batch GEMV), as the pages time it ("complete call",
+ * KE Tests 3, 6): pq2_quantize_act into the caller's workspace, then
+ * pq2_mmv launched so that it streams the weights while the quantisation
+ * runs (programmatic dependent launch; safe because the kernel it overlaps
+ * is this call's own quantisation, which only writes the workspace).
+ * Results are bit-identical to pq2_quantize_act + pq2_mmv.
+ *   x         (device) x_dtype [M][ldx], ldx >= K.
+ *   workspace (device) pq2_linear_workspace_bytes(M, K) bytes, 256-byte
+ *             aligned, holding q, s_x and sum(q); contents are scratch.
+ *   codes, scales, y, y_dtype, dev_status as for pq2_mmv. */
+int pq2_linear(const void *x, int x_dtype, int64_t ldx, int64_t M, int64_t N,
+               int64_t K, const uint8_t *codes, const uint16_t *scales,
+               void *y, int y_dtype, void *workspace, size_t workspace_bytes,
+               int32_t *dev_status, void *stream);
+
+/* Workspace bytes pq2_linear needs for M columns of K inputs (0 if the
+ * shape is invalid). */
+size_t pq2_linear_workspace_bytes(int64_t M, int64_t K);
+
+/* The decoder pq2_mmv uses for M columns (host only). */
+int pq2_mmv_decoder(int64_t M);
+
+/* pq2_mm — prefill (M >= 16) ternary x INT8 matmul as a dense tensor-core
+ * contraction (KE Test 7 "INT8 tensor-core MMQ prefill"; BIB "Use matrix
+ * hardware for prefill"): per 128-group the exact dot of q and the decoded
+ * codes is formed on tcgen05 tensor cores (fp16 operands holding the integer
+ * values, fp32 accumulation confined to one group, hence exact), then scaled
+ * by s_x * s_w into an fp32 accumulator.
+ *   q_f16    (device) fp16 [M][K] from pq2_quantize_act(PQ2_Q_F16);
+ *            16-byte aligned.
+ *   sx       (device) fp32 [M][K/128].
+ *   codes, scales as for pq2_mmv.
+ *   y        (device) y_dtype [M][N] (PQ2_F32 or PQ2_BF16).
+ *   M        16 .. 1<<20.
+ *   dev_status as for pq2_mmv. */
+int pq2_mm(const uint16_t *q_f16, const float *sx, const uint8_t *codes,
+           const uint16_t *scales, void *y, int y_dtype, int64_t M, int64_t N,
+           int64_t K, int32_t *dev_status, void *stream);
+
+/* Paths of pq2_debug_group_dots. */
+enum { PQ2_PATH_MMV_ADDXOR = 0, PQ2_PATH_MM = 1, PQ2_PATH_MMV_PLANES = 2 };
+
+/* pq2_debug_group_dots — the exact per-group int32 dots
+ * dots[m][n][g] = sum_{k in g} (c_{n,k} - 1) q_{m,k} computed by the SAME
+ * device decode and dot code as pq2_mmv with either decoder (paths 0 and 2,
+ * q int8 in PQ2_Q_PLANES order, qsum required for path 2, M 1..8) or as
+ * pq2_mm (path 1, q fp16 PQ2_Q_F16, M >= 16), for parity checks.
+ *   dots (device) int32 [M][N][K/128]. */
+int pq2_debug_group_dots(const void *q, const int32_t *qsum,
+                         const uint8_t *codes, int64_t M, int64_t N, int64_t K,
+                         int path, int32_t *dots, int32_t *dev_status,
+                         void *stream);
+
+/* pq2_mmv_geometry — the launch geometry pq2_mmv uses for (N, K) on a device
+ * with sm_count SMs (host only, no CUDA call): CTAs, threads per CTA,
+ * interleaved K splits per row and row count of the largest CTA.  It does
+ * not depend on M. Returns PQ2_ERR_SHAPE for invalid shapes. */
+int pq2_mmv_geometry(int64_t N, int64_t K, int sm_count, int *ctas,
+                     int *threads, int *splits, int *rows_max);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PQ2_H */

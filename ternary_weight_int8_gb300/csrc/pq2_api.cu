@@ -1,0 +1,242 @@
+// pq2_api.cu — the C ABI of libpq2: argument validation, device checks and
+// dispatch to the kernels.  Every argument error is reported before any CUDA
+// call, so invalid calls never touch the device.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "pq2.h"
+#include "pq2_internal.h"
+
+namespace {
+
+constexpr int kLayoutVersion = 1;  // code plane [N][K/4] then fp16 scales [N][K/128]
+constexpr int64_t kMaxK = (int64_t)1 << 24;
+constexpr int64_t kMaxN = (int64_t)1 << 30;
+constexpr int64_t kMaxM = (int64_t)1 << 20;
+constexpr int kMaxDevices = 64;
+
+// Per-device cache: 0 = unknown, 1 = sm_103 (GB300), 2 = other architecture.
+std::atomic<int> g_arch[kMaxDevices];
+std::atomic<int> g_sms[kMaxDevices];
+
+bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+bool valid_k(int64_t K) { return K >= 128 && K % 128 == 0 && K <= kMaxK; }
+bool valid_n(int64_t N) { return N >= 1 && N <= kMaxN; }
+
+// Compute capability 10.3 check and SM count of the current device.
+int device_check(int* sm_count) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return PQ2_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return PQ2_ERR_CUDA;
+  int arch = g_arch[dev].load(std::memory_order_acquire);
+  if (arch == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return PQ2_ERR_CUDA;
+    }
+    g_sms[dev].store(sms, std::memory_order_relaxed);
+    arch = (major == 10 && minor == 3) ? 1 : 2;
+    g_arch[dev].store(arch, std::memory_order_release);
+  }
+  if (arch != 1) return PQ2_ERR_ARCH;
+  *sm_count = g_sms[dev].load(std::memory_order_relaxed);
+  return PQ2_OK;
+}
+
+int elem_bytes(int dtype) { return dtype == PQ2_F32 ? 4 : 2; }
+
+int check_mmv_args(const int8_t* q, const float* sx, const int32_t* qsum,
+                   const uint8_t* codes, const uint16_t* scales, const void* y,
+                   int y_dtype, int64_t M, int64_t N, int64_t K, int decode) {
+  if (!q || !sx || !qsum || !codes || !scales || !y) return PQ2_ERR_NULL;
+  if (M < 1 || M > 8 || !valid_n(N) || !valid_k(K)) return PQ2_ERR_SHAPE;
+  if (y_dtype != PQ2_F32 && y_dtype != PQ2_BF16) return PQ2_ERR_DTYPE;
+  if (decode != PQ2_DECODE_ADDXOR && decode != PQ2_DECODE_PLANES) return PQ2_ERR_DTYPE;
+  if (!aligned(q, 16) || !aligned(codes, 16) || !aligned(sx, 4) || !aligned(qsum, 4) ||
+      !aligned(scales, 2) || !aligned(y, elem_bytes(y_dtype)))
+    return PQ2_ERR_ALIGN;
+  return PQ2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pq2_layout_version(void) { return kLayoutVersion; }
+
+const char* pq2_status_string(int status) {
+  switch (status) {
+    case PQ2_OK: return "ok";
+    case PQ2_ERR_NULL: return "a required pointer is NULL";
+    case PQ2_ERR_SHAPE: return "shape, stride or size out of range";
+    case PQ2_ERR_ALIGN: return "pointer or stride misaligned";
+    case PQ2_ERR_DTYPE: return "unknown dtype, layout or decoder";
+    case PQ2_ERR_ARCH: return "device is not compute capability 10.3 (GB300)";
+    case PQ2_ERR_LAUNCH: return "CUDA launch failed";
+    case PQ2_ERR_TIMEOUT: return "a bounded device wait gave up";
+    case PQ2_ERR_CUDA: return "CUDA runtime query failed";
+    default: return "unknown status";
+  }
+}
+
+size_t pq2_prepared_bytes(int64_t N, int64_t K) {
+  if (!valid_n(N) || !valid_k(K)) return 0;
+  return (size_t)N * (size_t)(K / 4) + (size_t)N * (size_t)(K / 128) * 2;
+}
+
+int pq2_prepare(const uint8_t* raw, int64_t raw_row_stride, int64_t N, int64_t K,
+                uint8_t* codes, uint16_t* scales, void* stream) {
+  if (!raw || !codes || !scales) return PQ2_ERR_NULL;
+  if (!valid_n(N) || !valid_k(K) || raw_row_stride < K / 128 * 34) return PQ2_ERR_SHAPE;
+  if (!aligned(codes, 16) || !aligned(scales, 2)) return PQ2_ERR_ALIGN;
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  return pq2::launch_prepare(raw, raw_row_stride, N, K, codes, scales,
+                             static_cast<cudaStream_t>(stream));
+}
+
+int pq2_quantize_act(const void* x, int x_dtype, int64_t ldx, int64_t M, int64_t K,
+                     void* q, int q_layout, float* sx, int32_t* qsum, void* stream) {
+  if (!x || !q || !sx) return PQ2_ERR_NULL;
+  if (x_dtype != PQ2_BF16 && x_dtype != PQ2_F16 && x_dtype != PQ2_F32) return PQ2_ERR_DTYPE;
+  if (q_layout != PQ2_Q_ROWS && q_layout != PQ2_Q_PLANES && q_layout != PQ2_Q_F16)
+    return PQ2_ERR_DTYPE;
+  if (M < 1 || M > kMaxM || !valid_k(K) || ldx < K || ldx > ((int64_t)1 << 40))
+    return PQ2_ERR_SHAPE;
+  if (!aligned(x, elem_bytes(x_dtype)) || !aligned(q, 16) || !aligned(sx, 4) ||
+      (qsum && !aligned(qsum, 4)))
+    return PQ2_ERR_ALIGN;
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  return pq2::launch_quantize(x, x_dtype, ldx, M, K, q, q_layout, sx, qsum,
+                              static_cast<cudaStream_t>(stream));
+}
+
+// The masked-plane decoder needs one LOP3 per code byte where the add/XOR
+// expansion needs about three, and on GB300 both share the half-rate integer
+// pipe with dp4a; it is the faster decoder for every M.
+int pq2_mmv_decoder(int64_t M) {
+  (void)M;
+  return PQ2_DECODE_PLANES;
+}
+
+int pq2_mmv_ex(const int8_t* q, const float* sx, const int32_t* qsum, const uint8_t* codes,
+               const uint16_t* scales, void* y, int y_dtype, int64_t M, int64_t N,
+               int64_t K, int decode, int flags, int32_t* dev_status, void* stream) {
+  if (int st = check_mmv_args(q, sx, qsum, codes, scales, y, y_dtype, M, N, K, decode))
+    return st;
+  if (flags & ~(PQ2_MMV_OVERLAP_WEIGHTS | PQ2_MMV_INDEPENDENT)) return PQ2_ERR_DTYPE;
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  const int overlap = (flags & PQ2_MMV_INDEPENDENT) ? 2 : (flags & PQ2_MMV_OVERLAP_WEIGHTS) ? 1 : 0;
+  return pq2::launch_mmv(q, sx, qsum, codes, scales, y, y_dtype, nullptr, M, N, K, decode,
+                         overlap, sms, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+int pq2_mmv(const int8_t* q, const float* sx, const int32_t* qsum, const uint8_t* codes,
+            const uint16_t* scales, void* y, int y_dtype, int64_t M, int64_t N, int64_t K,
+            int32_t* dev_status, void* stream) {
+  return pq2_mmv_ex(q, sx, qsum, codes, scales, y, y_dtype, M, N, K,
+                    pq2_mmv_decoder(M < 1 ? 1 : M), 0, dev_status, stream);
+}
+
+size_t pq2_linear_workspace_bytes(int64_t M, int64_t K) {
+  if (M < 1 || M > kMaxM || !valid_k(K)) return 0;
+  const size_t G = (size_t)(K / 128);
+  const size_t q_bytes = (size_t)M * (size_t)K * (M <= 8 ? 1 : 2);
+  const size_t sx_off = (q_bytes + 255) / 256 * 256;
+  const size_t qs_off = (sx_off + (size_t)M * G * 4 + 255) / 256 * 256;
+  return qs_off + (size_t)M * G * 4;
+}
+
+int pq2_linear(const void* x, int x_dtype, int64_t ldx, int64_t M, int64_t N, int64_t K,
+               const uint8_t* codes, const uint16_t* scales, void* y, int y_dtype,
+               void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (!x || !codes || !scales || !y || !workspace) return PQ2_ERR_NULL;
+  if (x_dtype != PQ2_BF16 && x_dtype != PQ2_F16 && x_dtype != PQ2_F32) return PQ2_ERR_DTYPE;
+  if (y_dtype != PQ2_F32 && y_dtype != PQ2_BF16) return PQ2_ERR_DTYPE;
+  if (M < 1 || M > 8 || !valid_n(N) || !valid_k(K) || ldx < K || ldx > ((int64_t)1 << 40))
+    return PQ2_ERR_SHAPE;
+  if (workspace_bytes < pq2_linear_workspace_bytes(M, K)) return PQ2_ERR_SHAPE;
+  if (!aligned(x, elem_bytes(x_dtype)) || !aligned(workspace, 256) || !aligned(codes, 16) ||
+      !aligned(scales, 2) || !aligned(y, elem_bytes(y_dtype)))
+    return PQ2_ERR_ALIGN;
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  const size_t G = (size_t)(K / 128);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t sx_off = ((size_t)M * (size_t)K + 255) / 256 * 256;
+  const size_t qs_off = (sx_off + (size_t)M * G * 4 + 255) / 256 * 256;
+  int8_t* q = reinterpret_cast<int8_t*>(ws);
+  float* sx = reinterpret_cast<float*>(ws + sx_off);
+  int32_t* qs = reinterpret_cast<int32_t*>(ws + qs_off);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (int st = pq2::launch_quantize(x, x_dtype, ldx, M, K, q, PQ2_Q_PLANES, sx, qs, s)) return st;
+  return pq2::launch_mmv(q, sx, qs, codes, scales, y, y_dtype, nullptr, M, N, K,
+                         pq2_mmv_decoder(M), 1, sms, dev_status, s);
+}
+
+int pq2_mm(const uint16_t* q_f16, const float* sx, const uint8_t* codes,
+           const uint16_t* scales, void* y, int y_dtype, int64_t M, int64_t N, int64_t K,
+           int32_t* dev_status, void* stream) {
+  if (!q_f16 || !sx || !codes || !scales || !y) return PQ2_ERR_NULL;
+  if (M < 16 || M > kMaxM || !valid_n(N) || !valid_k(K)) return PQ2_ERR_SHAPE;
+  if (y_dtype != PQ2_F32 && y_dtype != PQ2_BF16) return PQ2_ERR_DTYPE;
+  if (!aligned(q_f16, 16) || !aligned(codes, 16) || !aligned(sx, 4) || !aligned(scales, 2) ||
+      !aligned(y, elem_bytes(y_dtype)))
+    return PQ2_ERR_ALIGN;
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  return pq2::launch_mm(q_f16, sx, codes, scales, y, y_dtype, nullptr, M, N, K, sms,
+                        dev_status, static_cast<cudaStream_t>(stream));
+}
+
+int pq2_debug_group_dots(const void* q, const int32_t* qsum, const uint8_t* codes,
+                         int64_t M, int64_t N, int64_t K, int path, int32_t* dots,
+                         int32_t* dev_status, void* stream) {
+  if (!q || !codes || !dots) return PQ2_ERR_NULL;
+  if (path != PQ2_PATH_MMV_ADDXOR && path != PQ2_PATH_MM && path != PQ2_PATH_MMV_PLANES)
+    return PQ2_ERR_DTYPE;
+  if (path == PQ2_PATH_MMV_PLANES && !qsum) return PQ2_ERR_NULL;
+  if (!valid_n(N) || !valid_k(K)) return PQ2_ERR_SHAPE;
+  if (path == PQ2_PATH_MM ? (M < 16 || M > kMaxM) : (M < 1 || M > 8)) return PQ2_ERR_SHAPE;
+  if (!aligned(q, 16) || !aligned(codes, 16) || !aligned(dots, 4) ||
+      (qsum && !aligned(qsum, 4)))
+    return PQ2_ERR_ALIGN;
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (path == PQ2_PATH_MM)
+    return pq2::launch_mm(static_cast<const uint16_t*>(q), nullptr, codes, nullptr, nullptr,
+                          PQ2_F32, dots, M, N, K, sms, dev_status, s);
+  // The dot-only variant reads neither scales nor y; sx is unused as well.
+  return pq2::launch_mmv(static_cast<const int8_t*>(q), nullptr, qsum, codes, nullptr, nullptr,
+                         PQ2_F32, dots, M, N, K,
+                         path == PQ2_PATH_MMV_PLANES ? pq2::kDecodeMaskPlanes
+                                                     : pq2::kDecodeAddXor,
+                         0, sms, dev_status, s);
+}
+
+int pq2_mmv_geometry(int64_t N, int64_t K, int sm_count, int* ctas, int* threads,
+                     int* splits, int* rows_max) {
+  pq2::MmvGeometry g;
+  if (!pq2::mmv_geometry(N, K, sm_count, &g)) return PQ2_ERR_SHAPE;
+  if (ctas) *ctas = g.ctas;
+  if (threads) *threads = g.threads;
+  if (splits) *splits = g.splits;
+  if (rows_max) *rows_max = g.rows_max;
+  return PQ2_OK;
+}
+
+}  // extern "C"

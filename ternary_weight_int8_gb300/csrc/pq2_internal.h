@@ -1,0 +1,51 @@
+// pq2_internal.h — host-side declarations shared by the libpq2 translation
+// units (launchers called by the C ABI in pq2_api.cu).  Not installed.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "pq2.h"
+
+namespace pq2 {
+
+// Geometry of pq2_mmv, a pure function of (N, K, SM count): never of M.
+struct MmvGeometry {
+  int ctas;      // CTAs (one per SM, fewer when N is small)
+  int threads;   // consumer threads per CTA (multiple of 32)
+  int splits;    // S: interleaved K splits per row inside a CTA
+  int rows_max;  // rows of the largest CTA
+  int steps;     // ceil(G / S): pipeline steps (one group per thread each)
+};
+
+bool mmv_geometry(int64_t N, int64_t K, int sm_count, MmvGeometry* g);
+
+// Decoders of the code bytes used by the small-batch kernel.
+enum MmvDecode {
+  kDecodeAddXor = 0,     // spread + 0x7F7F7F7F, ^ 0x80808080, signed dp4a
+  kDecodeMaskPlanes = 1  // masked planes, unsigned dp4a, minus sum(q)
+};
+
+int launch_prepare(const uint8_t* raw, int64_t raw_stride, int64_t N,
+                   int64_t K, uint8_t* codes, uint16_t* scales,
+                   cudaStream_t stream);
+
+int launch_quantize(const void* x, int x_dtype, int64_t ldx, int64_t M,
+                    int64_t K, void* q, int q_layout, float* sx, int32_t* qsum,
+                    cudaStream_t stream);
+
+// overlap 1: the CTAs may stream the weight planes before the preceding
+// kernels on the stream have completed (programmatic dependent launch);
+// overlap 2: every input may be read early (see PQ2_MMV_INDEPENDENT).
+int launch_mmv(const int8_t* q, const float* sx, const int32_t* qsum,
+               const uint8_t* codes, const uint16_t* scales, void* y,
+               int y_dtype, int32_t* dots, int64_t M, int64_t N, int64_t K,
+               int decode, int overlap, int sm_count, int32_t* status,
+               cudaStream_t stream);
+
+int launch_mm(const uint16_t* q_f16, const float* sx, const uint8_t* codes,
+              const uint16_t* scales, void* y, int y_dtype, int32_t* dots,
+              int64_t M, int64_t N, int64_t K, int sm_count, int32_t* status,
+              cudaStream_t stream);
+
+}  // namespace pq2

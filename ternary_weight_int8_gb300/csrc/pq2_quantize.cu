@@ -1,0 +1,208 @@
+// pq2_quantize.cu — weight-plane preparation and per-group INT8 activation
+// quantisation (sm_103a).
+//
+// Preparation: page "Kernel experiments: recorded evidence" (KE), Test 1
+// (prepare_pq2, separate buffers) and Test 4 (shared prepared layout).
+// Quantisation: KE Test 6 (_quantize) and page "Baseline and the integer
+// breakthrough" (BIB), "Calculate with small integers", step 1; plane order
+// and group sums: KE Test 21 (plane-order quantisation).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "pq2_device.cuh"
+#include "pq2_internal.h"
+
+namespace pq2 {
+namespace {
+
+// One thread per 34-byte block: bytes 0-1 are the little-endian fp16 scale,
+// bytes 2..33 the 32 code bytes (weight k in bits 2(k%4) of byte k/4).
+// Raw rows have an arbitrary byte stride, so the block is read bytewise; the
+// code plane row is 16-byte aligned and written with two 16-byte stores.
+__global__ void prepare_kernel(const uint8_t* __restrict__ raw,
+                               int64_t raw_stride, int64_t N, int G,
+                               uint8_t* __restrict__ codes,
+                               uint16_t* __restrict__ scales) {
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= N * G) return;
+  const int64_t n = idx / G;
+  const int g = (int)(idx % G);
+  const uint8_t* b = raw + n * raw_stride + (int64_t)g * 34;
+  scales[idx] = (uint16_t)(b[0] | (b[1] << 8));
+  uint32_t w[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    w[j] = (uint32_t)b[2 + 4 * j] | ((uint32_t)b[3 + 4 * j] << 8) |
+           ((uint32_t)b[4 + 4 * j] << 16) | ((uint32_t)b[5 + 4 * j] << 24);
+  uint4* dst = reinterpret_cast<uint4*>(codes + n * (int64_t)G * 32 +
+                                        (int64_t)g * 32);
+  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+template <int XT>
+__device__ __forceinline__ float to_f32(const void* x, int64_t i);
+template <>
+__device__ __forceinline__ float to_f32<PQ2_BF16>(const void* x, int64_t i) {
+  return __bfloat162float(static_cast<const __nv_bfloat16*>(x)[i]);
+}
+template <>
+__device__ __forceinline__ float to_f32<PQ2_F16>(const void* x, int64_t i) {
+  return __half2float(static_cast<const __half*>(x)[i]);
+}
+template <>
+__device__ __forceinline__ float to_f32<PQ2_F32>(const void* x, int64_t i) {
+  return static_cast<const float*>(x)[i];
+}
+
+// Four consecutive activations starting at element i (i % 4 == 0).  With
+// `vec` the four are fetched with one 8-byte (16-bit types) or 16-byte (fp32)
+// load; the host sets it only when base and row stride allow it.
+template <int XT>
+__device__ __forceinline__ void load4(const void* x, int64_t i, bool vec,
+                                      float a[4]) {
+  if (vec) {
+    if (XT == PQ2_F32) {
+      const float4 v = *reinterpret_cast<const float4*>(
+          static_cast<const float*>(x) + i);
+      a[0] = v.x; a[1] = v.y; a[2] = v.z; a[3] = v.w;
+    } else {
+      const uint2 v = *reinterpret_cast<const uint2*>(
+          static_cast<const uint16_t*>(x) + i);
+      const uint16_t h[4] = {(uint16_t)(v.x & 0xffff), (uint16_t)(v.x >> 16),
+                             (uint16_t)(v.y & 0xffff), (uint16_t)(v.y >> 16)};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (XT == PQ2_BF16)
+          a[j] = __uint_as_float((uint32_t)h[j] << 16);
+        else
+          a[j] = __half2float(__ushort_as_half(h[j]));
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) a[j] = to_f32<XT>(x, i + j);
+  }
+}
+
+// One warp per (row m, group g); lane L owns elements 4L..4L+3 of the group.
+//   s = max|a| / 127, d = s > 0 ? s : 1, q = clamp(rne(a / d), -127, 127)
+// with IEEE round-to-nearest divisions, exactly as the definition states.
+template <int XT>
+__global__ void __launch_bounds__(256) quantize_kernel(
+    const void* __restrict__ x, int64_t ldx, int64_t M, int G, bool vec,
+    void* __restrict__ q, int layout, float* __restrict__ sx,
+    int32_t* __restrict__ qsum) {
+  // Launched with programmatic dependent launch: let the next kernel start
+  // its independent prologue now (it waits for this grid before it reads q,
+  // s_x or sum(q)), and wait for the previous grid before touching memory.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= M * G) return;
+  const int64_t m = warp / G;
+  const int g = (int)(warp % G);
+  const int64_t K = (int64_t)G * kGroup;
+
+  float a[4];
+  load4<XT>(x, m * ldx + (int64_t)g * kGroup + 4 * lane, vec, a);
+  float amax = fmaxf(fmaxf(fabsf(a[0]), fabsf(a[1])),
+                     fmaxf(fabsf(a[2]), fabsf(a[3])));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const float s = __fdiv_rn(amax, 127.0f);
+  const float d = s > 0.0f ? s : 1.0f;
+  int qi[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float r = rintf(__fdiv_rn(a[j], d));
+    r = fminf(fmaxf(r, -127.0f), 127.0f);
+    qi[j] = (int)r;
+  }
+  const uint32_t packed = (uint32_t)(qi[0] & 0xff) | ((uint32_t)(qi[1] & 0xff) << 8) |
+                          ((uint32_t)(qi[2] & 0xff) << 16) | ((uint32_t)(qi[3] & 0xff) << 24);
+  const int64_t base = m * K + (int64_t)g * kGroup;
+  if (layout == PQ2_Q_ROWS) {
+    reinterpret_cast<uint32_t*>(static_cast<int8_t*>(q) + base)[lane] = packed;
+  } else if (layout == PQ2_Q_PLANES) {
+    // Plane word (s, w) = q[16w + 4b + s] for b = 0..3: byte s of the packed
+    // words of lanes 4w..4w+3.  Lane L = 8s + w assembles it, so the warp
+    // writes the group's 128 bytes as one coalesced line.
+    const int s_out = lane >> 3, w_out = lane & 7;
+    uint32_t out = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t v = __shfl_sync(0xffffffffu, packed, 4 * w_out + b);
+      out |= ((v >> (8 * s_out)) & 0xffu) << (8 * b);
+    }
+    reinterpret_cast<uint32_t*>(static_cast<int8_t*>(q) + base)[lane] = out;
+  } else {
+    __half2 h01 = __halves2half2(__int2half_rn(qi[0]), __int2half_rn(qi[1]));
+    __half2 h23 = __halves2half2(__int2half_rn(qi[2]), __int2half_rn(qi[3]));
+    uint2 v;
+    v.x = *reinterpret_cast<uint32_t*>(&h01);
+    v.y = *reinterpret_cast<uint32_t*>(&h23);
+    reinterpret_cast<uint2*>(static_cast<__half*>(q) + base)[lane] = v;
+  }
+  if (qsum) {
+    int t = qi[0] + qi[1] + qi[2] + qi[3];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+      t += __shfl_xor_sync(0xffffffffu, t, off);
+    if (lane == 0) qsum[m * G + g] = t;
+  }
+  if (lane == 0) sx[m * G + g] = s;
+}
+
+}  // namespace
+
+int launch_prepare(const uint8_t* raw, int64_t raw_stride, int64_t N,
+                   int64_t K, uint8_t* codes, uint16_t* scales,
+                   cudaStream_t stream) {
+  const int G = (int)(K / kGroup);
+  const int64_t blocks_needed = (N * G + 255) / 256;
+  prepare_kernel<<<(unsigned)blocks_needed, 256, 0, stream>>>(
+      raw, raw_stride, N, G, codes, scales);
+  return cudaGetLastError() == cudaSuccess ? PQ2_OK : PQ2_ERR_LAUNCH;
+}
+
+int launch_quantize(const void* x, int x_dtype, int64_t ldx, int64_t M,
+                    int64_t K, void* q, int q_layout, float* sx, int32_t* qsum,
+                    cudaStream_t stream) {
+  const int G = (int)(K / kGroup);
+  const int elem = x_dtype == PQ2_F32 ? 4 : 2;
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(x);
+  const bool vec = (addr % (4 * elem) == 0) && (ldx % 4 == 0);
+  const int64_t warps = M * G;
+  const unsigned blocks = (unsigned)((warps + 7) / 8);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+  switch (x_dtype) {
+    case PQ2_BF16:
+      e = cudaLaunchKernelEx(&cfg, quantize_kernel<PQ2_BF16>, x, ldx, M, G, vec, q, q_layout, sx, qsum);
+      break;
+    case PQ2_F16:
+      e = cudaLaunchKernelEx(&cfg, quantize_kernel<PQ2_F16>, x, ldx, M, G, vec, q, q_layout, sx, qsum);
+      break;
+    default:
+      e = cudaLaunchKernelEx(&cfg, quantize_kernel<PQ2_F32>, x, ldx, M, G, vec, q, q_layout, sx, qsum);
+      break;
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return PQ2_ERR_LAUNCH;
+  }
+  return PQ2_OK;
+}
+
+}  // namespace pq2

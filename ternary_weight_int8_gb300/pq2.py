@@ -1,0 +1,223 @@
+"""Thin Python binding of libpq2 (ctypes).  Argument marshalling only: every
+step of the path runs in the library's CUDA kernels.  torch supplies device
+memory and streams.  There is no fallback: if libpq2.so is missing or a call
+fails, an exception is raised.
+
+Two levels:
+  * ``lib()`` — the raw C functions with their exact C signatures (pointers
+    as integers), used by tests that exercise the C ABI directly;
+  * ``pq2_prepare``, ``pq2_quantize_act``, ``pq2_mmv``, ``pq2_mm``,
+    ``pq2_debug_group_dots`` — the same names taking torch tensors, allocating
+    outputs with torch when not given, and passing the current torch stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpq2.so")
+
+PQ2_OK, PQ2_ERR_NULL, PQ2_ERR_SHAPE, PQ2_ERR_ALIGN, PQ2_ERR_DTYPE = 0, 1, 2, 3, 4
+PQ2_ERR_ARCH, PQ2_ERR_LAUNCH, PQ2_ERR_TIMEOUT, PQ2_ERR_CUDA = 5, 6, 7, 8
+PQ2_BF16, PQ2_F16, PQ2_F32 = 0, 1, 2
+PQ2_Q_ROWS, PQ2_Q_PLANES, PQ2_Q_F16 = 0, 1, 2
+PQ2_DECODE_ADDXOR, PQ2_DECODE_PLANES = 0, 1
+PQ2_PATH_MMV_ADDXOR, PQ2_PATH_MM, PQ2_PATH_MMV_PLANES = 0, 1, 2
+PQ2_MMV_OVERLAP_WEIGHTS, PQ2_MMV_INDEPENDENT = 1, 2
+GROUP = 128
+
+# C signatures, mirroring include/pq2.h.
+_P, _I, _I64, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+SIGNATURES = {
+    "pq2_layout_version": (_I, []),
+    "pq2_status_string": (ctypes.c_char_p, [_I]),
+    "pq2_prepared_bytes": (_SZ, [_I64, _I64]),
+    "pq2_prepare": (_I, [_P, _I64, _I64, _I64, _P, _P, _P]),
+    "pq2_quantize_act": (_I, [_P, _I, _I64, _I64, _I64, _P, _I, _P, _P, _P]),
+    "pq2_mmv": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P]),
+    "pq2_mmv_ex": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _I, _P, _P]),
+    "pq2_linear": (_I, [_P, _I, _I64, _I64, _I64, _I64, _P, _P, _P, _I, _P, _SZ, _P, _P]),
+    "pq2_linear_workspace_bytes": (_SZ, [_I64, _I64]),
+    "pq2_mmv_decoder": (_I, [_I64]),
+    "pq2_mm": (_I, [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P]),
+    "pq2_debug_group_dots": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P, _P, _P]),
+    "pq2_mmv_geometry": (_I, [_I64, _I64, _I, _P, _P, _P, _P]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class Pq2Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        msg = lib().pq2_status_string(status).decode()
+        super().__init__(f"{fn} failed with status {status}: {msg}")
+
+
+def lib():
+    """Load libpq2.so (it must have been built, see build.py)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(
+                    f"libpq2.so not found at {LIB_PATH}; build it with "
+                    "`python -m ternary_weight_int8_gb300.build`")
+            h = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(h, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = h
+    return _lib
+
+
+def _check(fn: str, status: int):
+    if status != PQ2_OK:
+        raise Pq2Error(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+_DT = {torch.bfloat16: PQ2_BF16, torch.float16: PQ2_F16, torch.float32: PQ2_F32}
+
+
+def prepared_bytes(N: int, K: int) -> int:
+    return lib().pq2_prepared_bytes(N, K)
+
+
+def pq2_prepare(raw: torch.Tensor, K: int, codes=None, scales=None, stream=None):
+    """Raw blocks u8[N][>=K/128*34] (CUDA) -> (codes u8[N][K/4], scales fp16[N][K/128])."""
+    N = raw.shape[0]
+    if raw.dtype != torch.uint8 or raw.dim() != 2 or raw.stride(1) != 1:
+        raise ValueError("raw must be a 2-D uint8 tensor with unit column stride")
+    if codes is None:
+        codes = torch.empty((N, K // 4), dtype=torch.uint8, device=raw.device)
+    if scales is None:
+        scales = torch.empty((N, K // GROUP), dtype=torch.float16, device=raw.device)
+    _check("pq2_prepare", lib().pq2_prepare(_ptr(raw), raw.stride(0), N, K, _ptr(codes),
+                                            _ptr(scales), _stream(stream)))
+    return codes, scales
+
+
+def pq2_quantize_act(x: torch.Tensor, layout: int = PQ2_Q_PLANES, q=None, sx=None,
+                     qsum=None, want_qsum: bool = True, stream=None):
+    """x[M][K] (bf16/f16/f32, CUDA, unit column stride) -> (q, sx, qsum)."""
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit column stride")
+    M, K = x.shape
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.float16 if layout == PQ2_Q_F16 else torch.int8,
+                        device=x.device)
+    if sx is None:
+        sx = torch.empty((M, K // GROUP), dtype=torch.float32, device=x.device)
+    if qsum is None and want_qsum:
+        qsum = torch.empty((M, K // GROUP), dtype=torch.int32, device=x.device)
+    _check("pq2_quantize_act",
+           lib().pq2_quantize_act(_ptr(x), _DT[x.dtype], x.stride(0), M, K, _ptr(q), layout,
+                                  _ptr(sx), _ptr(qsum), _stream(stream)))
+    return q, sx, qsum
+
+
+def pq2_mmv(q_planes, sx, qsum, codes, scales, y=None, out_dtype=torch.float32,
+            decode=None, flags=0, status=None, stream=None):
+    """Small-batch GEMV, M = 1..8: y[M][N] = sum_g dot * s_x * s_w."""
+    M, K = q_planes.shape
+    N = codes.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=q_planes.device)
+    yd = _DT[y.dtype]
+    args = (_ptr(q_planes), _ptr(sx), _ptr(qsum), _ptr(codes), _ptr(scales), _ptr(y), yd, M,
+            N, K)
+    if decode is None and not flags:
+        st = lib().pq2_mmv(*args, _ptr(status), _stream(stream))
+    else:
+        dec = mmv_decoder(M) if decode is None else decode
+        st = lib().pq2_mmv_ex(*args, dec, flags, _ptr(status), _stream(stream))
+    _check("pq2_mmv", st)
+    return y
+
+
+def linear_workspace_bytes(M: int, K: int) -> int:
+    return lib().pq2_linear_workspace_bytes(M, K)
+
+
+def pq2_linear(x, codes, scales, y=None, out_dtype=torch.float32, workspace=None,
+               status=None, stream=None):
+    """Complete projection for M = 1..8: quantise x and run the GEMV, with the
+    GEMV streaming its weights while the quantisation runs."""
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit column stride")
+    M, K = x.shape
+    N = codes.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    wb = linear_workspace_bytes(M, K)
+    if workspace is None:
+        workspace = torch.empty(wb, dtype=torch.uint8, device=x.device)
+    _check("pq2_linear", lib().pq2_linear(
+        _ptr(x), _DT[x.dtype], x.stride(0), M, N, K, _ptr(codes), _ptr(scales), _ptr(y),
+        _DT[y.dtype], _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(status), _stream(stream)))
+    return y
+
+
+def pq2_mm(q_f16, sx, codes, scales, y=None, out_dtype=torch.float32, status=None,
+           stream=None):
+    """Prefill matmul, M >= 16, on tcgen05 tensor cores."""
+    M, K = q_f16.shape
+    N = codes.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=q_f16.device)
+    _check("pq2_mm", lib().pq2_mm(_ptr(q_f16), _ptr(sx), _ptr(codes), _ptr(scales), _ptr(y),
+                                  _DT[y.dtype], M, N, K, _ptr(status), _stream(stream)))
+    return y
+
+
+def pq2_debug_group_dots(q, codes, path: int, qsum=None, dots=None, status=None,
+                         stream=None):
+    """Exact int32 group dots [M][N][K/128] from the kernels' own decode/dot code."""
+    M, K = q.shape
+    N = codes.shape[0]
+    if dots is None:
+        dots = torch.empty((M, N, K // GROUP), dtype=torch.int32, device=q.device)
+    _check("pq2_debug_group_dots",
+           lib().pq2_debug_group_dots(_ptr(q), _ptr(qsum), _ptr(codes), M, N, K, path,
+                                      _ptr(dots), _ptr(status), _stream(stream)))
+    return dots
+
+
+def mmv_geometry(N: int, K: int, sm_count: int):
+    """(ctas, threads, splits, rows_max) of pq2_mmv for (N, K) — host only."""
+    out = [ctypes.c_int() for _ in range(4)]
+    _check("pq2_mmv_geometry", lib().pq2_mmv_geometry(
+        N, K, sm_count, *[ctypes.addressof(o) for o in out]))
+    return tuple(o.value for o in out)
+
+
+def mmv_decoder(M: int) -> int:
+    return lib().pq2_mmv_decoder(M)
+
+
+def linear(x, codes, scales, out_dtype=torch.float32, stream=None):
+    """The complete projection: pq2_linear (M <= 8) or quantise + pq2_mm."""
+    M = x.shape[0]
+    if M <= 8:
+        return pq2_linear(x, codes, scales, out_dtype=out_dtype, stream=stream)
+    q, sx, _ = pq2_quantize_act(x, PQ2_Q_F16, want_qsum=False, stream=stream)
+    return pq2_mm(q, sx, codes, scales, out_dtype=out_dtype, stream=stream)

@@ -1,0 +1,65 @@
+"""Helpers for the GPU parity tests: seeded inputs on the device, oracle
+references on the host, guard-banded output buffers."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import oracle as O
+from ternary_weight_int8_gb300 import synth
+
+G = 128
+
+
+def weights(N, K, seed, code_values=3, device="cuda", raw_pad=0):
+    """Raw blocks on the device (row stride padded by raw_pad bytes) and the
+    oracle's planes of the same bytes."""
+    raw = synth.raw_weights(N, K, seed, device="cpu", code_values=code_values)
+    if raw_pad:
+        padded = torch.zeros((N, raw.shape[1] + raw_pad), dtype=torch.uint8)
+        padded[:, :raw.shape[1]] = raw
+        raw_dev = padded.to(device)[:, :raw.shape[1]]
+    else:
+        raw_dev = raw.to(device)
+    codes_o, scales_o = O.prepare(raw.numpy(), K)
+    return raw_dev, codes_o, scales_o
+
+
+def guarded(shape, dtype, device="cuda", guard=64, fill=None):
+    """A tensor view with `guard` elements of poison on both sides; returns
+    (view, backing, poison value)."""
+    n = int(np.prod(shape))
+    backing = torch.empty(n + 2 * guard, dtype=dtype, device=device)
+    if dtype.is_floating_point:
+        poison = float("nan") if fill is None else fill
+    else:
+        poison = -0x5A5A5A5A if dtype == torch.int32 else (0x5A if dtype == torch.uint8 else -91)
+    backing.fill_(poison)
+    view = backing[guard:guard + n].view(shape)
+    return view, backing, guard
+
+
+def guards_intact(backing, guard):
+    b = backing.detach().cpu()
+    head, tail = b[:guard], b[-guard:]
+    if b.dtype.is_floating_point:
+        return bool(torch.isnan(head).all() and torch.isnan(tail).all())
+    return bool((head == head[0]).all() and (tail == head[0]).all())
+
+
+def x_bits(x):
+    return synth.bits_u16(x) if x.dtype in (torch.bfloat16, torch.float16) else \
+        x.detach().cpu().float().numpy()
+
+
+def kind(x):
+    return {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}[x.dtype]
+
+
+def oracle_reference(x, codes_o, scales_o):
+    """(q, sx, qsum, dots, y32, y64, bound) from the oracle for activations x."""
+    a = O.widen(x_bits(x), kind(x))
+    q, sx = O.quantize(a)
+    dots = O.group_dots(q, codes_o)
+    y32, y64, bound = O.scale_accumulate(dots, sx, scales_o)
+    return q, sx, O.qsum(q), dots, y32, y64, bound

@@ -1,0 +1,162 @@
+"""The C ABI on the host (no GPU needed): the library loads, exports every
+function include/pq2.h declares, and rejects invalid arguments before any
+CUDA call.  Also the launch geometry of pq2_mmv, which must not depend on M."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from ternary_weight_int8_gb300 import build, pq2
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pq2.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(pq2.LIB_PATH):
+        build.build()
+    return pq2.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pq2_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ["pq2_prepare", "pq2_quantize_act", "pq2_mmv", "pq2_mm"]:
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert names
+    for name in names:
+        assert hasattr(L, name), name
+        assert name in pq2.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings_and_sizes(L):
+    for s in range(0, 9):
+        assert L.pq2_status_string(s)
+    assert L.pq2_status_string(12345) == b"unknown status"
+    assert L.pq2_layout_version() >= 1
+    assert L.pq2_prepared_bytes(17408, 5120) == 17408 * 5120 * 34 // 128
+    assert L.pq2_prepared_bytes(10, 100) == 0
+    assert L.pq2_prepared_bytes(0, 128) == 0
+
+
+A = 1 << 20   # a 16-byte aligned fake address: never dereferenced
+
+
+def test_prepare_validation(L):
+    assert L.pq2_prepare(None, 34, 1, 128, A, A, None) == pq2.PQ2_ERR_NULL
+    assert L.pq2_prepare(A, 33, 1, 128, A, A, None) == pq2.PQ2_ERR_SHAPE
+    assert L.pq2_prepare(A, 34, 0, 128, A, A, None) == pq2.PQ2_ERR_SHAPE
+    assert L.pq2_prepare(A, 34, 1, 129, A, A, None) == pq2.PQ2_ERR_SHAPE
+    assert L.pq2_prepare(A, 34, 1, 128, A + 8, A, None) == pq2.PQ2_ERR_ALIGN
+    assert L.pq2_prepare(A, 34, 1, 128, A, A + 1, None) == pq2.PQ2_ERR_ALIGN
+
+
+def test_quantize_validation(L):
+    f = L.pq2_quantize_act
+    assert f(None, 0, 128, 1, 128, A, 1, A, A, None) == pq2.PQ2_ERR_NULL
+    assert f(A, 3, 128, 1, 128, A, 1, A, A, None) == pq2.PQ2_ERR_DTYPE
+    assert f(A, 0, 128, 1, 128, A, 3, A, A, None) == pq2.PQ2_ERR_DTYPE
+    assert f(A, 0, 127, 1, 128, A, 1, A, A, None) == pq2.PQ2_ERR_SHAPE
+    assert f(A, 0, 128, 0, 128, A, 1, A, A, None) == pq2.PQ2_ERR_SHAPE
+    assert f(A, 0, 256, 1, 192, A, 1, A, A, None) == pq2.PQ2_ERR_SHAPE
+    assert f(A + 1, 0, 128, 1, 128, A, 1, A, A, None) == pq2.PQ2_ERR_ALIGN
+    assert f(A, 2, 128, 1, 128, A, 1, A + 2, A, None) == pq2.PQ2_ERR_ALIGN
+    assert f(A, 0, 128, 1, 128, A + 4, 1, A, A, None) == pq2.PQ2_ERR_ALIGN
+
+
+def test_mmv_validation(L):
+    f = L.pq2_mmv
+    ok = [A, A, A, A, A, A, pq2.PQ2_F32, 1, 10, 128, None, None]
+    for i in range(6):
+        bad = list(ok); bad[i] = None
+        assert f(*bad) == pq2.PQ2_ERR_NULL
+    for idx, val, err in [(7, 0, pq2.PQ2_ERR_SHAPE), (7, 9, pq2.PQ2_ERR_SHAPE),
+                          (8, 0, pq2.PQ2_ERR_SHAPE), (9, 64, pq2.PQ2_ERR_SHAPE),
+                          (6, pq2.PQ2_F16, pq2.PQ2_ERR_DTYPE), (0, A + 4, pq2.PQ2_ERR_ALIGN),
+                          (3, A + 8, pq2.PQ2_ERR_ALIGN), (1, A + 2, pq2.PQ2_ERR_ALIGN),
+                          (4, A + 1, pq2.PQ2_ERR_ALIGN), (5, A + 2, pq2.PQ2_ERR_ALIGN)]:
+        bad = list(ok); bad[idx] = val
+        assert f(*bad) == err, (idx, val)
+    ex = ok[:10] + [5, 0] + ok[10:]
+    assert L.pq2_mmv_ex(*ex) == pq2.PQ2_ERR_DTYPE
+    ex = ok[:10] + [pq2.PQ2_DECODE_PLANES, 8] + ok[10:]
+    assert L.pq2_mmv_ex(*ex) == pq2.PQ2_ERR_DTYPE
+
+
+def test_linear_validation(L):
+    f = L.pq2_linear
+    ws = L.pq2_linear_workspace_bytes(4, 5120)
+    assert ws >= 4 * 5120 + 2 * 4 * 40 * 4 and ws % 4 == 0
+    assert L.pq2_linear_workspace_bytes(0, 5120) == 0
+    assert L.pq2_linear_workspace_bytes(4, 100) == 0
+    ok = [A, pq2.PQ2_BF16, 5120, 4, 64, 5120, A, A, A, pq2.PQ2_F32, A, ws, None, None]
+    for i in (0, 6, 7, 8, 10):
+        bad = list(ok); bad[i] = None
+        assert f(*bad) == pq2.PQ2_ERR_NULL, i
+    for idx, val, err in [(3, 9, pq2.PQ2_ERR_SHAPE), (3, 0, pq2.PQ2_ERR_SHAPE),
+                          (2, 5000, pq2.PQ2_ERR_SHAPE), (11, ws - 1, pq2.PQ2_ERR_SHAPE),
+                          (1, 9, pq2.PQ2_ERR_DTYPE), (9, pq2.PQ2_F16, pq2.PQ2_ERR_DTYPE),
+                          (10, A + 16, pq2.PQ2_ERR_ALIGN), (6, A + 8, pq2.PQ2_ERR_ALIGN),
+                          (0, A + 1, pq2.PQ2_ERR_ALIGN)]:
+        bad = list(ok); bad[idx] = val
+        assert f(*bad) == err, (idx, val)
+
+
+def test_mm_and_debug_validation(L):
+    assert L.pq2_mm(A, A, A, A, A, 2, 15, 10, 128, None, None) == pq2.PQ2_ERR_SHAPE
+    assert L.pq2_mm(A, A, A, A, None, 2, 16, 10, 128, None, None) == pq2.PQ2_ERR_NULL
+    assert L.pq2_mm(A + 2, A, A, A, A, 2, 16, 10, 128, None, None) == pq2.PQ2_ERR_ALIGN
+    d = L.pq2_debug_group_dots
+    assert d(A, None, A, 1, 10, 128, 7, A, None, None) == pq2.PQ2_ERR_DTYPE
+    assert d(A, None, A, 1, 10, 128, 2, A, None, None) == pq2.PQ2_ERR_NULL
+    assert d(A, A, A, 9, 10, 128, 0, A, None, None) == pq2.PQ2_ERR_SHAPE
+    assert d(A, A, A, 8, 10, 128, 1, A, None, None) == pq2.PQ2_ERR_SHAPE
+
+
+def test_valid_call_without_gpu_reports_cuda_error(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert L.pq2_mmv(A, A, A, A, A, A, pq2.PQ2_F32, 1, 10, 128, None, None) in (
+        pq2.PQ2_ERR_CUDA, pq2.PQ2_ERR_ARCH)
+
+
+@pytest.mark.parametrize("N,K", [(14336, 4096), (10240, 5120), (17408, 5120), (5120, 17408),
+                                 (6144, 5120), (5, 384), (1, 128), (100000, 1024),
+                                 (153, 17408)])
+@pytest.mark.parametrize("sms", [152, 148, 8])
+def test_mmv_geometry(L, N, K, sms):
+    ctas, threads, splits, rows_max = pq2.mmv_geometry(N, K, sms)
+    G = K // 128
+    assert 1 <= ctas and rows_max == -(-N // ctas)
+    assert ctas <= max(sms, -(-N // 256)) and rows_max <= 256
+    assert threads % 32 == 0 and 32 <= threads <= 352
+    assert rows_max * splits <= threads < rows_max * splits + 32
+    # a row's splits share one warp: S is a power of two dividing 32
+    assert 1 <= splits <= min(G, 16) and 32 % splits == 0
+    # every row is covered: the CTA row ranges tile [0, N)
+    bounds = [N * c // ctas for c in range(ctas + 1)]
+    assert bounds[0] == 0 and bounds[-1] == N
+    assert max(b - a for a, b in zip(bounds, bounds[1:])) == rows_max
+
+
+def test_mmv_geometry_fills_the_gb300_shapes(L):
+    """On 152 SMs the configured projection shapes keep >= 89% of the
+    consumer lanes and steps busy."""
+    for N, K in [(14336, 4096), (10240, 5120), (17408, 5120), (5120, 17408), (6144, 5120)]:
+        ctas, threads, splits, R = pq2.mmv_geometry(N, K, 152)
+        G = K // 128
+        steps = -(-G // splits)
+        eff = (R * splits / threads) * (G / (splits * steps))
+        assert ctas == 152 and eff >= 0.89, (N, K, eff)
