@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kMaxBlock, 2)
         if (!independent) issue(i, false, true);
         continue;
       }
-      if (i >= p.ring && !mbar_wait(&empty[slot], ((i / p.ring) - 1) & 1)) ok = false;
+      if (i >= p.ring) ok = ok && mbar_wait(&empty[slot], ((i / p.ring) - 1) & 1);
       issue(i, true, true);
     }
     if (!ok && lane == 0) report(p.status, PQ2_ERR_TIMEOUT);
@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(kMaxBlock, 2)
     named_bar_sync(1, p.cons_threads);
   }
   bool ok = true;
-  if (!DOTS && p.sw_bulk && !mbar_wait(swbar, 0)) ok = false;
+  if (!DOTS && p.sw_bulk) ok = ok && mbar_wait(swbar, 0);
 
   const int z = tid % S;
   const int r = tid / S;
@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(kMaxBlock, 2)
 
   for (int i = 0; i < p.stages_total; ++i) {
     const int slot = i % p.ring;
-    if (!mbar_wait(&full[slot], (i / p.ring) & 1)) ok = false;
+    ok = ok && mbar_wait(&full[slot], (i / p.ring) & 1);
     const uint8_t* st = ring + (size_t)slot * p.stage_bytes;
     const int g0 = i * Gs;
     if (active && ok) {
