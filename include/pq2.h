@@ -63,11 +63,14 @@ enum { PQ2_BF16 = 0, PQ2_F16 = 1, PQ2_F32 = 2 };
  *               group is stored at (i%4)*32 + i/4 (KE Test 21, plane-order
  *               quantisation), so that plane s of a 4-byte code word meets
  *               one contiguous 4-byte slice of q.  Operand of pq2_mmv.
- *  PQ2_Q_F16    fp16 q[M][K], row-major, the same integer values widened
- *               exactly (|q| <= 127).  Operand of pq2_mm: sm_103a has no
- *               8-bit integer tcgen05 MMA, so the prefill contraction runs on
- *               the fp16 tensor path, whose fp32 sums of integer products
- *               below 2^24 are exact (a 128-group dot is at most 32512). */
+ *  PQ2_Q_F16    fp16, the same integer values widened exactly (|q| <= 127),
+ *               in the K order pq2_mm's weight decode produces: inside every
+ *               16 consecutive elements (the 16 weights of one 4-byte code
+ *               word), element 4b + s (code byte b, field s) is stored at
+ *               position 4s + 2(b & 1) + (b >> 1).  Operand of pq2_mm: sm_103a
+ *               has no 8-bit integer tcgen05 MMA, so the prefill contraction
+ *               runs on the fp16 tensor path, whose fp32 sums of integer
+ *               products below 2^24 are exact. */
 enum { PQ2_Q_ROWS = 0, PQ2_Q_PLANES = 1, PQ2_Q_F16 = 2 };
 
 /* Version of the prepared plane layout; bump whenever what a kernel reads
@@ -166,14 +169,14 @@ int pq2_mmv_ex(const int8_t *q_planes, const float *sx, const int32_t *qsum,
                int y_dtype, int64_t M, int64_t N, int64_t K, int decode,
                int flags, int32_t *dev_status, void *stream);
 
-/* pq2_linear — the complete projection y = x W^T for M = 1..8 (quantise,
- * then the small-batch GEMV), as the pages time it ("complete call",
- * KE Tests 3, 6): pq2_quantize_act into the caller's workspace, then
- * pq2_mmv launched so that it streams the weights while the quantisation
- * runs (programmatic dependent launch; safe because the kernel it overlaps
- * is this call's own quantisation, which only writes the workspace).
- * Results are bit-identical to pq2_quantize_act + pq2_mmv.
- *   x         (device) x_dtype [M][ldx], ldx >= K.
+/* pq2_linear — the complete projection y = x W^T (quantise, then the GEMV),
+ * as the pages time it ("complete call", KE Tests 3, 6): pq2_quantize_act
+ * into the caller's workspace, then pq2_mmv (M = 1..8) launched so that it
+ * streams the weights while the quantisation runs (programmatic dependent
+ * launch; safe because the kernel it overlaps is this call's own
+ * quantisation, which only writes the workspace), or pq2_mm (M >= 16).
+ * Results are bit-identical to pq2_quantize_act + pq2_mmv / pq2_mm.
+ *   x         (device) x_dtype [M][ldx], ldx >= K; M 1..8 or 16 .. 1<<20.
  *   workspace (device) pq2_linear_workspace_bytes(M, K) bytes, 256-byte
  *             aligned, holding q, s_x and sum(q); contents are scratch.
  *   codes, scales, y, y_dtype, dev_status as for pq2_mmv. */
@@ -192,19 +195,20 @@ int pq2_mmv_decoder(int64_t M);
 /* pq2_mm — prefill (M >= 16) ternary x INT8 matmul as a dense tensor-core
  * contraction (KE Test 7 "INT8 tensor-core MMQ prefill"; BIB "Use matrix
  * hardware for prefill"): per 128-group the exact dot of q and the decoded
- * codes is formed on tcgen05 tensor cores (fp16 operands holding the integer
+ * codes is formed on tcgen05 tensor cores (fp16 operands holding integer
  * values, fp32 accumulation confined to one group, hence exact), then scaled
  * by s_x * s_w into an fp32 accumulator.
  *   q_f16    (device) fp16 [M][K] from pq2_quantize_act(PQ2_Q_F16);
  *            16-byte aligned.
  *   sx       (device) fp32 [M][K/128].
+ *   qsum     (device) int32 [M][K/128] group sums of q.
  *   codes, scales as for pq2_mmv.
  *   y        (device) y_dtype [M][N] (PQ2_F32 or PQ2_BF16).
  *   M        16 .. 1<<20.
  *   dev_status as for pq2_mmv. */
-int pq2_mm(const uint16_t *q_f16, const float *sx, const uint8_t *codes,
-           const uint16_t *scales, void *y, int y_dtype, int64_t M, int64_t N,
-           int64_t K, int32_t *dev_status, void *stream);
+int pq2_mm(const uint16_t *q_f16, const float *sx, const int32_t *qsum,
+           const uint8_t *codes, const uint16_t *scales, void *y, int y_dtype,
+           int64_t M, int64_t N, int64_t K, int32_t *dev_status, void *stream);
 
 /* Paths of pq2_debug_group_dots. */
 enum { PQ2_PATH_MMV_ADDXOR = 0, PQ2_PATH_MM = 1, PQ2_PATH_MMV_PLANES = 2 };
@@ -213,7 +217,7 @@ enum { PQ2_PATH_MMV_ADDXOR = 0, PQ2_PATH_MM = 1, PQ2_PATH_MMV_PLANES = 2 };
  * dots[m][n][g] = sum_{k in g} (c_{n,k} - 1) q_{m,k} computed by the SAME
  * device decode and dot code as pq2_mmv with either decoder (paths 0 and 2,
  * q int8 in PQ2_Q_PLANES order, qsum required for path 2, M 1..8) or as
- * pq2_mm (path 1, q fp16 PQ2_Q_F16, M >= 16), for parity checks.
+ * pq2_mm (path 1, q fp16 PQ2_Q_F16 and qsum, M >= 16), for parity checks.
  *   dots (device) int32 [M][N][K/128]. */
 int pq2_debug_group_dots(const void *q, const int32_t *qsum,
                          const uint8_t *codes, int64_t M, int64_t N, int64_t K,

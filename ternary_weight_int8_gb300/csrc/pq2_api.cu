@@ -166,7 +166,8 @@ int pq2_linear(const void* x, int x_dtype, int64_t ldx, int64_t M, int64_t N, in
   if (!x || !codes || !scales || !y || !workspace) return PQ2_ERR_NULL;
   if (x_dtype != PQ2_BF16 && x_dtype != PQ2_F16 && x_dtype != PQ2_F32) return PQ2_ERR_DTYPE;
   if (y_dtype != PQ2_F32 && y_dtype != PQ2_BF16) return PQ2_ERR_DTYPE;
-  if (M < 1 || M > 8 || !valid_n(N) || !valid_k(K) || ldx < K || ldx > ((int64_t)1 << 40))
+  if (M < 1 || M > kMaxM || (M > 8 && M < 16) || !valid_n(N) || !valid_k(K) || ldx < K ||
+      ldx > ((int64_t)1 << 40))
     return PQ2_ERR_SHAPE;
   if (workspace_bytes < pq2_linear_workspace_bytes(M, K)) return PQ2_ERR_SHAPE;
   if (!aligned(x, elem_bytes(x_dtype)) || !aligned(workspace, 256) || !aligned(codes, 16) ||
@@ -175,30 +176,36 @@ int pq2_linear(const void* x, int x_dtype, int64_t ldx, int64_t M, int64_t N, in
   int sms = 0;
   if (int st = device_check(&sms)) return st;
   const size_t G = (size_t)(K / 128);
+  const bool small = M <= 8;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const size_t sx_off = ((size_t)M * (size_t)K + 255) / 256 * 256;
+  const size_t q_bytes = (size_t)M * (size_t)K * (small ? 1 : 2);
+  const size_t sx_off = (q_bytes + 255) / 256 * 256;
   const size_t qs_off = (sx_off + (size_t)M * G * 4 + 255) / 256 * 256;
-  int8_t* q = reinterpret_cast<int8_t*>(ws);
   float* sx = reinterpret_cast<float*>(ws + sx_off);
   int32_t* qs = reinterpret_cast<int32_t*>(ws + qs_off);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (int st = pq2::launch_quantize(x, x_dtype, ldx, M, K, q, PQ2_Q_PLANES, sx, qs, s)) return st;
-  return pq2::launch_mmv(q, sx, qs, codes, scales, y, y_dtype, nullptr, M, N, K,
-                         pq2_mmv_decoder(M), 1, sms, dev_status, s);
+  if (int st = pq2::launch_quantize(x, x_dtype, ldx, M, K, ws,
+                                    small ? PQ2_Q_PLANES : PQ2_Q_F16, sx, qs, s))
+    return st;
+  if (!small)
+    return pq2::launch_mm(reinterpret_cast<const uint16_t*>(ws), sx, qs, codes, scales, y,
+                          y_dtype, nullptr, M, N, K, sms, dev_status, s);
+  return pq2::launch_mmv(reinterpret_cast<const int8_t*>(ws), sx, qs, codes, scales, y,
+                         y_dtype, nullptr, M, N, K, pq2_mmv_decoder(M), 1, sms, dev_status, s);
 }
 
-int pq2_mm(const uint16_t* q_f16, const float* sx, const uint8_t* codes,
+int pq2_mm(const uint16_t* q_f16, const float* sx, const int32_t* qsum, const uint8_t* codes,
            const uint16_t* scales, void* y, int y_dtype, int64_t M, int64_t N, int64_t K,
            int32_t* dev_status, void* stream) {
-  if (!q_f16 || !sx || !codes || !scales || !y) return PQ2_ERR_NULL;
+  if (!q_f16 || !sx || !qsum || !codes || !scales || !y) return PQ2_ERR_NULL;
   if (M < 16 || M > kMaxM || !valid_n(N) || !valid_k(K)) return PQ2_ERR_SHAPE;
   if (y_dtype != PQ2_F32 && y_dtype != PQ2_BF16) return PQ2_ERR_DTYPE;
-  if (!aligned(q_f16, 16) || !aligned(codes, 16) || !aligned(sx, 4) || !aligned(scales, 2) ||
-      !aligned(y, elem_bytes(y_dtype)))
+  if (!aligned(q_f16, 16) || !aligned(codes, 16) || !aligned(sx, 4) || !aligned(qsum, 4) ||
+      !aligned(scales, 2) || !aligned(y, elem_bytes(y_dtype)))
     return PQ2_ERR_ALIGN;
   int sms = 0;
   if (int st = device_check(&sms)) return st;
-  return pq2::launch_mm(q_f16, sx, codes, scales, y, y_dtype, nullptr, M, N, K, sms,
+  return pq2::launch_mm(q_f16, sx, qsum, codes, scales, y, y_dtype, nullptr, M, N, K, sms,
                         dev_status, static_cast<cudaStream_t>(stream));
 }
 
@@ -208,7 +215,7 @@ int pq2_debug_group_dots(const void* q, const int32_t* qsum, const uint8_t* code
   if (!q || !codes || !dots) return PQ2_ERR_NULL;
   if (path != PQ2_PATH_MMV_ADDXOR && path != PQ2_PATH_MM && path != PQ2_PATH_MMV_PLANES)
     return PQ2_ERR_DTYPE;
-  if (path == PQ2_PATH_MMV_PLANES && !qsum) return PQ2_ERR_NULL;
+  if ((path == PQ2_PATH_MMV_PLANES || path == PQ2_PATH_MM) && !qsum) return PQ2_ERR_NULL;
   if (!valid_n(N) || !valid_k(K)) return PQ2_ERR_SHAPE;
   if (path == PQ2_PATH_MM ? (M < 16 || M > kMaxM) : (M < 1 || M > 8)) return PQ2_ERR_SHAPE;
   if (!aligned(q, 16) || !aligned(codes, 16) || !aligned(dots, 4) ||
@@ -218,8 +225,8 @@ int pq2_debug_group_dots(const void* q, const int32_t* qsum, const uint8_t* code
   if (int st = device_check(&sms)) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (path == PQ2_PATH_MM)
-    return pq2::launch_mm(static_cast<const uint16_t*>(q), nullptr, codes, nullptr, nullptr,
-                          PQ2_F32, dots, M, N, K, sms, dev_status, s);
+    return pq2::launch_mm(static_cast<const uint16_t*>(q), nullptr, qsum, codes, nullptr,
+                          nullptr, PQ2_F32, dots, M, N, K, sms, dev_status, s);
   // The dot-only variant reads neither scales nor y; sx is unused as well.
   return pq2::launch_mmv(static_cast<const int8_t*>(q), nullptr, qsum, codes, nullptr, nullptr,
                          PQ2_F32, dots, M, N, K,

@@ -8,24 +8,29 @@
 // breakthrough", "Use matrix hardware for prefill".
 //
 // GB300 design.  sm_103a has no 8-bit integer tcgen05 MMA, so the contraction
-// runs as kind::f16: A = q widened to fp16 (exact, |q| <= 127), B = the codes
-// decoded to fp16 c-1 in {-1, 0, 1, 2} (exact).  Each 128-group is one
-// accumulation of eight K=16 MMAs into a fresh fp32 TMEM tile: every partial
-// sum is an integer of magnitude <= 32512 < 2^24, so the group dot is exact,
-// exactly the int32 per-group partial of the method.  The epilogue then scales
-// it by s_x * s_w and adds it into an fp32 accumulator.
+// runs as kind::f16.  The weights are the MMA's A operand and live in tensor
+// memory: decoder threads (one weight row each) turn a 4-byte code word into
+// eight fp16x2 words of c - 1 with a shift, a LOP3 and one exact HSUB2 each
+// (the fp16 value of 0x6400 | c is 1024 + c) and store them with tcgen05.st,
+// so decoded weights never touch shared memory.  q (B operand, fp16, exact)
+// streams into shared memory by TMA in the matching K order
+// (pq2_quantize_act's PQ2_Q_F16 layout).  Each 128-group is one accumulation
+// of eight K=16 MMAs into a fresh fp32 TMEM tile: every partial sum is an
+// integer of magnitude <= 32512 < 2^24, so D is the exact int32 per-group
+// partial of the method.  The epilogue scales it by s_x * s_w into fp32.
 //
-// One CTA computes a tile of 128 tokens x 128 output rows:
+// One CTA computes a tile of 128 output rows x 128 tokens:
 //   warp 0      TMA producer: q tiles (two 64-column boxes per group, 128-byte
-//               swizzle, the canonical K-major layout of the MMA) and code
-//               tiles (32 bytes x 128 rows per group)
+//               swizzle, the canonical K-major layout) and code tiles
 //   warp 1      TMEM allocation; lane 0 issues the MMAs and commits
-//   warps 2-3   decoders: code bytes -> fp16 B tile in the same swizzled layout
-//   warps 4-11  epilogue: one token row and half the columns per thread, reads
-//               the group's fp32 D from TMEM (double-buffered), scales and
-//               accumulates, stores y
-// Every wait is bounded; a wait that gives up records PQ2_ERR_TIMEOUT and the
-// protocol continues without the work so that no thread is left waiting.
+//   warps 2-5   decoders: one weight row per thread, codes -> TMEM A tile
+//   warps 6-21  epilogue: one weight row and 32 tokens per thread, reads D
+//               (three buffers in flight), scales it and adds it into fp32
+//               running sums in registers, finally stores y (coalesced)
+// A warp may only reach the TMEM lanes 32*(warp % 4) .. +31, so each role
+// spans four consecutive warps (one per lane quarter).
+// Every wait is bounded and fails fast: a wait that gives up records
+// PQ2_ERR_TIMEOUT and the protocol continues without the work.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -39,19 +44,22 @@
 namespace pq2 {
 namespace {
 
-constexpr int BM = 128;          // tokens per tile (MMA M)
-constexpr int BN = 128;          // output rows per tile (MMA N)
-constexpr int kStagesA = 3;      // q tile stages
+constexpr int BW = 128;          // weight rows per tile (MMA M, A in TMEM)
+constexpr int BT = 128;          // tokens per tile (MMA N, B in shared memory)
+constexpr int kStagesQ = 6;      // q tile stages
 constexpr int kStagesC = 4;      // code tile stages
-constexpr int kStagesB = 2;      // decoded weight tile stages
-constexpr int kGC = 8;           // groups per weight-scale chunk
-constexpr int kThreads = 384;
-constexpr int kEpiThreads = 256;  // warps 4-11: two per TMEM lane quarter
-constexpr int kEpiCols = BN / 2;  // columns per epilogue thread
-constexpr int kABytes = BM * kGroup * 2;   // 32 KB: q tile of one group (fp16)
-constexpr int kBBytes = BN * kGroup * 2;   // 32 KB: decoded weights of one group
-constexpr int kCBytes = BN * kGroupCodeBytes;  // 4 KB: code bytes of one group
-constexpr int kTmemCols = 2 * BN;          // two fp32 D buffers
+constexpr int kGC = 4;           // groups per scale chunk
+constexpr int kEpiWarps = 16;     // warps 6-21: four per TMEM lane quarter
+constexpr int kThreads = (6 + kEpiWarps) * 32;
+constexpr int kEpiCols = BT / 4;  // tokens per epilogue thread
+constexpr int kDBuf = 2;          // D buffers in flight
+constexpr int kABuf = 4;          // decoded weight (A) buffers in flight
+constexpr int kQBytes = BT * kGroup * 2;       // 32 KB: q tile of one group (fp16)
+constexpr int kCBytes = BW * kGroupCodeBytes;  // 4 KB: code bytes of one group
+constexpr int kDCol = 0;                       // D buffers: columns [0, kDBuf*BT)
+constexpr int kACol = kDBuf * BT;              // A buffers: 64 columns each
+constexpr int kTmemCols = 512;
+static_assert(kACol + kABuf * 64 <= kTmemCols, "tensor memory budget");
 
 struct MmParams {
   const float* sx;         // [M][G]
@@ -64,14 +72,17 @@ struct MmParams {
 };
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kStagesA * kABytes;
-constexpr int kOffC = kOffB + kStagesB * kBBytes;
-constexpr int kOffSW = kOffC + kStagesC * kCBytes;        // 2 chunks of [kGC][BN] fp16
-constexpr int kOffBar = kOffSW + 2 * kGC * BN * 2;
-constexpr int kNumBars = 2 * kStagesA + 2 * kStagesC + 2 * kStagesB + 4;
+constexpr int kOffQ = 0;
+constexpr int kOffC = kOffQ + kStagesQ * kQBytes;
+// Scale ring: 2 chunks of {s_x [kGC][BT] fp32, s_w [BW][kGC] fp16}.
+constexpr int kSxBytes = kGC * BT * 4;
+constexpr int kSwBytes = BW * kGC * 2;
+constexpr int kSBytes = kSxBytes + kSwBytes;
+constexpr int kOffS = kOffC + kStagesC * kCBytes;
+constexpr int kOffBar = kOffS + 2 * kSBytes;
+constexpr int kNumBars = 2 * kStagesQ + 2 * kStagesC + 2 * kABuf + 2 * kDBuf + 4;
 constexpr int kOffTmemAddr = kOffBar + kNumBars * 8;
-constexpr int kSmemBytes = kOffTmemAddr + 16 + 1024;     // + alignment slack
+constexpr int kSmemBytes = kOffTmemAddr + 16 + 1024;  // + alignment slack
 
 // ------------------------------------------------------------ tcgen05 PTX
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
@@ -93,13 +104,13 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// D[tmem] (+)= A[smem] * B[smem]^T, fp16 inputs, fp32 accumulation.
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                        uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem]^T, fp16 inputs, fp32 accumulation.
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // Arrive once on `bar` when every MMA issued so far by this thread is done.
@@ -118,12 +129,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
         "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
       : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-// Generic-proxy shared-memory writes -> visible to the tensor core.
-__device__ __forceinline__ void fence_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 __device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x, int y,
                                        uint64_t* bar) {
@@ -147,7 +166,8 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
   return d;
 }
 
-// Instruction descriptor: kind::f16, D fp32, A and B fp16, both K-major.
+// Instruction descriptor: kind::f16, D fp32, A and B fp16, both K-major
+// (A may come from tensor memory).
 __host__ __device__ constexpr uint32_t instr_desc_f16(int m, int n) {
   return (1u << 4)                      // D format: f32
          | (0u << 7) | (0u << 10)       // A, B format: f16
@@ -156,13 +176,20 @@ __host__ __device__ constexpr uint32_t instr_desc_f16(int m, int n) {
          | ((uint32_t)(m >> 4) << 24);  // M / 16
 }
 
-// Two codes (bits 0-1 and 2-3 of x) -> fp16x2 (c0 - 1, c1 - 1): the halves
-// 0x6400 | c are 1024 + c exactly, and subtracting 1025 is exact.
-__device__ __forceinline__ uint32_t decode_pair(uint32_t x) {
-  const uint32_t u = (x & 3u) | ((x & 0xCu) << 14) | 0x64006400u;
-  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&u),
-                            __halves2half2(__ushort_as_half(0x6401), __ushort_as_half(0x6401)));
-  return *reinterpret_cast<const uint32_t*>(&r);
+// Eight fp16x2 words of one code word w, in the operand K order: word
+// j = 2s + pb holds the weights c - 1 of (byte pb, field s) and (byte pb + 2,
+// field s), i.e. weights 4pb + s and 4(pb + 2) + s.  The halves 0x6400 | c
+// are exactly 1024 + c; subtracting 1025 (one HSUB2) is exact.
+__device__ __forceinline__ void decode_word(uint32_t w, uint32_t* out) {
+  const __half2 k1025 = __halves2half2(__ushort_as_half(0x6401), __ushort_as_half(0x6401));
+#pragma unroll
+  for (int s = 0; s < 4; ++s)
+#pragma unroll
+    for (int pb = 0; pb < 2; ++pb) {
+      const uint32_t u = ((w >> (2 * s + 8 * pb)) & 0x00030003u) | 0x64006400u;
+      const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&u), k1025);
+      out[2 * s + pb] = *reinterpret_cast<const uint32_t*>(&r);
+    }
 }
 
 template <bool DOTS>
@@ -173,25 +200,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_s = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* a_full = bars;
-  uint64_t* a_empty = a_full + kStagesA;
-  uint64_t* c_full = a_empty + kStagesA;
+  uint64_t* q_full = bars;
+  uint64_t* q_empty = q_full + kStagesQ;
+  uint64_t* c_full = q_empty + kStagesQ;
   uint64_t* c_empty = c_full + kStagesC;
-  uint64_t* b_full = c_empty + kStagesC;
-  uint64_t* b_empty = b_full + kStagesB;
-  uint64_t* d_full = b_empty + kStagesB;
-  uint64_t* d_empty = d_full + 2;
+  uint64_t* a_full = c_empty + kStagesC;
+  uint64_t* a_empty = a_full + kABuf;
+  uint64_t* d_full = a_empty + kABuf;
+  uint64_t* d_empty = d_full + kDBuf;
+  uint64_t* s_full = d_empty + kDBuf;
+  uint64_t* s_empty = s_full + 2;
   uint32_t* tmem_addr_s = reinterpret_cast<uint32_t*>(smem + kOffTmemAddr);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
+  // Token tiles vary fastest: CTAs running together read different q tiles
+  // (no L2 hot spot) and share a few weight tiles.
+  const int m0 = blockIdx.x * BT, n0 = blockIdx.y * BW;
   const int G = p.G;
 
   if (tid == 0) {
-    for (int i = 0; i < kStagesA; ++i) { mbar_init(&a_full[i], 1); mbar_init(&a_empty[i], 1); }
-    for (int i = 0; i < kStagesC; ++i) { mbar_init(&c_full[i], 1); mbar_init(&c_empty[i], 2); }
-    for (int i = 0; i < kStagesB; ++i) { mbar_init(&b_full[i], 2); mbar_init(&b_empty[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&d_full[i], 1); mbar_init(&d_empty[i], kEpiThreads / 32); }
+    for (int i = 0; i < kStagesQ; ++i) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
+    for (int i = 0; i < kStagesC; ++i) { mbar_init(&c_full[i], 1); mbar_init(&c_empty[i], 4); }
+    for (int i = 0; i < kABuf; ++i) {
+      mbar_init(&a_full[i], 4);
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 32);
+      mbar_init(&s_empty[i], kEpiWarps);
+    }
+    for (int i = 0; i < kDBuf; ++i) {
+      mbar_init(&d_full[i], 1);
+      mbar_init(&d_empty[i], kEpiWarps);
+    }
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -209,175 +250,190 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool ok = true;
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // All 32 lanes stage the scales of each chunk of kGC groups (s_x of the
+    // tile's tokens, s_w of its rows) into the scale ring; lane 0 issues the
+    // TMA copies of q and codes group by group.
+    const int nchunks = (G + kGC - 1) / kGC;
+    constexpr int kPer = kGC * BT / 32;
+    float xv[kPer];
+    uint16_t wv[kPer];
+    // Scales of chunk ch: loaded into registers one chunk ahead, stored into
+    // the ring slot when the chunk starts, so their latency overlaps the TMA
+    // issue of the previous chunk.
+    auto load_scales = [&](int ch) {
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int idx = lane + 32 * j;  // idx = gg * BT + t
+        const int gg = idx / BT, t = idx % BT, g = ch * kGC + gg, m = m0 + t;
+        xv[j] = (!DOTS && g < G && m < p.M) ? __ldg(p.sx + (size_t)m * G + g) : 0.0f;
+        const int r = idx / kGC, gw = ch * kGC + idx % kGC, n = n0 + r;  // idx = r*kGC + gg
+        wv[j] = (!DOTS && gw < G && n < p.N) ? __ldg(p.scales + (size_t)n * G + gw)
+                                             : (uint16_t)0;
+      }
+    };
+    auto store_scales = [&](int ch) {
+      const int slot = ch & 1;
+      if (ch >= 2) ok = ok && mbar_wait(&s_empty[slot], ((ch >> 1) - 1) & 1);
+      float* sxs = reinterpret_cast<float*>(smem + kOffS + slot * kSBytes);  // [kGC][BT]
+      uint16_t* sws = reinterpret_cast<uint16_t*>(smem + kOffS + slot * kSBytes + kSxBytes);
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        sxs[lane + 32 * j] = xv[j];
+        sws[lane + 32 * j] = wv[j];
+      }
+      mbar_arrive(&s_full[slot]);
+    };
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(&map_q) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(&map_c) : "memory");
-      for (int g = 0; g < G; ++g) {
-        const int sa = g % kStagesA, sc = g % kStagesC;
-        if (g >= kStagesA) ok = ok && mbar_wait(&a_empty[sa], ((g / kStagesA) - 1) & 1);
-        uint8_t* a = smem + kOffA + sa * kABytes;
-        mbar_arrive_expect_tx(&a_full[sa], kABytes);
-        tma_2d(a, &map_q, g * kGroup, m0, &a_full[sa]);
-        tma_2d(a + kABytes / 2, &map_q, g * kGroup + 64, m0, &a_full[sa]);
+    }
+    load_scales(0);
+    for (int g = 0; g < G; ++g) {
+      if (g % kGC == 0) {
+        store_scales(g / kGC);
+        if (g / kGC + 1 < nchunks) load_scales(g / kGC + 1);
+      }
+      if (lane == 0) {
+        const int sq = g % kStagesQ, sc = g % kStagesC;
         if (g >= kStagesC) ok = ok && mbar_wait(&c_empty[sc], ((g / kStagesC) - 1) & 1);
         mbar_arrive_expect_tx(&c_full[sc], kCBytes);
         tma_2d(smem + kOffC + sc * kCBytes, &map_c, g * kGroupCodeBytes, n0, &c_full[sc]);
+        if (g >= kStagesQ) ok = ok && mbar_wait(&q_empty[sq], ((g / kStagesQ) - 1) & 1);
+        uint8_t* qs = smem + kOffQ + sq * kQBytes;
+        mbar_arrive_expect_tx(&q_full[sq], kQBytes);
+        tma_2d(qs, &map_q, g * kGroup, m0, &q_full[sq]);
+        tma_2d(qs + kQBytes / 2, &map_q, g * kGroup + 64, m0, &q_full[sq]);
       }
+      __syncwarp();
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      constexpr uint32_t idesc = instr_desc_f16(BM, BN);
+      constexpr uint32_t idesc = instr_desc_f16(BW, BT);
       for (int g = 0; g < G; ++g) {
-        const int sa = g % kStagesA, sb = g % kStagesB, d = g & 1;
-        ok = ok && mbar_wait(&a_full[sa], (g / kStagesA) & 1);
-        ok = ok && mbar_wait(&b_full[sb], (g / kStagesB) & 1);
-        if (g >= 2) ok = ok && mbar_wait(&d_empty[d], ((g >> 1) - 1) & 1);
+        const int sq = g % kStagesQ, b = g % kABuf, db = g % kDBuf;
+        ok = ok && mbar_wait(&a_full[b], (g / kABuf) & 1);
+        ok = ok && mbar_wait(&q_full[sq], (g / kStagesQ) & 1);
+        if (g >= kDBuf) ok = ok && mbar_wait(&d_empty[db], ((g / kDBuf) - 1) & 1);
         tc_fence_after();
-        const uint32_t a_base = smem_u32(smem + kOffA + sa * kABytes);
-        const uint32_t b_base = smem_u32(smem + kOffB + sb * kBBytes);
-        const uint32_t d_tmem = tmem_base + d * BN;
+        const uint32_t q_base = smem_u32(smem + kOffQ + sq * kQBytes);
+        const uint32_t d_tmem = tmem_base + kDCol + db * BT;
+        const uint32_t a_tmem = tmem_base + kACol + b * 64;  // b = g % kABuf
         if (ok) {
 #pragma unroll
           for (int k = 0; k < kGroup / 16; ++k) {
-            // K step k: 64-column atom k/4, 32-byte offset (k%4) inside the
-            // 128-byte swizzled row.
-            const uint32_t off = (k >> 2) * (BM * 128) + (k & 3) * 32;
-            const uint32_t boff = (k >> 2) * (BN * 128) + (k & 3) * 32;
-            mma_f16(d_tmem, smem_desc_sw128(a_base + off), smem_desc_sw128(b_base + boff),
-                    idesc, k > 0 ? 1u : 0u);
+            // K step k: A columns 8k..8k+7; B 64-column atom k/4, 32-byte
+            // offset (k%4) inside the 128-byte swizzled row.
+            const uint32_t boff = (k >> 2) * (BT * 128) + (k & 3) * 32;
+            mma_f16_ta(d_tmem, a_tmem + 8 * k, smem_desc_sw128(q_base + boff), idesc,
+                       k > 0 ? 1u : 0u);
           }
         }
-        mma_commit(&a_empty[sa]);
-        mma_commit(&b_empty[sb]);
-        mma_commit(&d_full[d]);
+        mma_commit(&q_empty[sq]);
+        mma_commit(&a_empty[b]);
+        mma_commit(&d_full[db]);
       }
     }
-  } else if (warp < 4) {
+  } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------------ decoders
-    const int dt = tid - 64;  // 0..63, two rows each
+    const int quarter = warp & 3;
+    const int row = 32 * quarter + lane;
+    const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
     for (int g = 0; g < G; ++g) {
-      const int sc = g % kStagesC, sb = g % kStagesB;
+      const int sc = g % kStagesC, b = g % kABuf;
       ok = ok && mbar_wait(&c_full[sc], (g / kStagesC) & 1);
-      if (g >= kStagesB) ok = ok && mbar_wait(&b_empty[sb], ((g / kStagesB) - 1) & 1);
-      const uint8_t* cs = smem + kOffC + sc * kCBytes;
-      uint8_t* bs = smem + kOffB + sb * kBBytes;
+      if (g >= kABuf) ok = ok && mbar_wait(&a_empty[b], ((g / kABuf) - 1) & 1);
+      tc_fence_after();
+      const uint8_t* cs = smem + kOffC + sc * kCBytes + row * kGroupCodeBytes;
+      const uint4 c0 = *reinterpret_cast<const uint4*>(cs);
+      const uint4 c1 = *reinterpret_cast<const uint4*>(cs + 16);
+      const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      const uint32_t taddr = tmem_base + lane_base + kACol + b * 64;
 #pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int n = dt + 64 * rr;
-        const uint4 c0 = *reinterpret_cast<const uint4*>(cs + n * kGroupCodeBytes);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(cs + n * kGroupCodeBytes + 16);
-        const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        // 16 chunks of 16 bytes = 8 weights = 2 code bytes each.
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const uint32_t two = (cw[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-          uint4 v;
-          v.x = decode_pair(two & 0xF);
-          v.y = decode_pair((two >> 4) & 0xF);
-          v.z = decode_pair((two >> 8) & 0xF);
-          v.w = decode_pair((two >> 12) & 0xF);
-          const int atom = j >> 3, jj = j & 7;
-          uint8_t* dst = bs + atom * (BN * 128) + (n >> 3) * 1024 + (n & 7) * 128 +
-                         ((jj ^ (n & 7)) << 4);
-          *reinterpret_cast<uint4*>(dst) = v;
-        }
+      for (int h = 0; h < 4; ++h) {
+        uint32_t v[16];
+        decode_word(cw[2 * h], v);
+        decode_word(cw[2 * h + 1], v + 8);
+        tmem_st16(taddr + 16 * h, v);
       }
-      fence_async_smem();
+      tmem_st_wait();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&c_empty[sc]);
-        mbar_arrive(&b_full[sb]);
+        mbar_arrive(&a_full[b]);
       }
     }
-  } else {
+  } else if (warp >= 6) {
     // ------------------------------------------------------------ epilogue
-    const int et = tid - 128;      // 0..255
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
-    const int half = (warp - 4) >> 2;
-    const int col0 = half * kEpiCols;
+    const int col0 = ((warp - 6) >> 2) * kEpiCols;
     const int row = 32 * quarter + lane;
-    const int m = m0 + row;
-    __half* sw_s = reinterpret_cast<__half*>(smem + kOffSW);  // [2][kGC][BN]
+    const int n = n0 + row;
+    const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
     float acc[kEpiCols];
 #pragma unroll
-    for (int n = 0; n < kEpiCols; ++n) acc[n] = 0.0f;
+    for (int j = 0; j < kEpiCols; ++j) acc[j] = 0.0f;
     const int nchunks = (G + kGC - 1) / kGC;
-    // Weight-scale chunk loader: kGC x BN fp16, 4 values per thread.
-    constexpr int kSwPer = kGC * BN / kEpiThreads;
-    uint16_t swv[kSwPer];
-    float sxv[kGC], sxn[kGC];
-    auto load_chunk = [&](int ch) {
-#pragma unroll
-      for (int j = 0; j < kSwPer; ++j) {
-        const int idx = et + kEpiThreads * j;  // idx = gg * BN + n
-        const int gg = idx / BN, n = idx % BN, g = ch * kGC + gg;
-        swv[j] = (!DOTS && g < G && n0 + n < p.N) ? __ldg(p.scales + (size_t)(n0 + n) * G + g)
-                                                  : (uint16_t)0;
-      }
-#pragma unroll
-      for (int gg = 0; gg < kGC; ++gg) {
-        const int g = ch * kGC + gg;
-        sxn[gg] = (!DOTS && g < G && m < p.M) ? __ldg(p.sx + (size_t)m * G + g) : 0.0f;
-      }
-    };
-    load_chunk(0);
     for (int ch = 0; ch < nchunks; ++ch) {
-      uint16_t* dst = reinterpret_cast<uint16_t*>(sw_s) + (ch & 1) * kGC * BN;
-#pragma unroll
-      for (int j = 0; j < kSwPer; ++j) dst[et + kEpiThreads * j] = swv[j];
-#pragma unroll
-      for (int gg = 0; gg < kGC; ++gg) sxv[gg] = sxn[gg];
-      named_bar_sync(1, kEpiThreads);
-      if (ch + 1 < nchunks) load_chunk(ch + 1);
-      const __half* swc = sw_s + (ch & 1) * kGC * BN + col0;
+      const int slot = ch & 1;
+      ok = ok && mbar_wait(&s_full[slot], (ch >> 1) & 1);
+      const float* sxs = reinterpret_cast<const float*>(smem + kOffS + slot * kSBytes);
+      const __half* sws = reinterpret_cast<const __half*>(smem + kOffS + slot * kSBytes + kSxBytes);
 #pragma unroll 1
       for (int gg = 0; gg < kGC; ++gg) {
         const int g = ch * kGC + gg;
         if (g >= G) break;
-        const int d = g & 1;
-        ok = ok && mbar_wait(&d_full[d], (g >> 1) & 1);
+        const int db = g % kDBuf;
+        ok = ok && mbar_wait(&d_full[db], (g / kDBuf) & 1);
         tc_fence_after();
-        const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16) + d * BN + col0;
+        const float* sxg = sxs + gg * BT + col0;
+        const float sw = __half2float(sws[row * kGC + gg]);
+        const uint32_t taddr = tmem_base + lane_base + kDCol + db * BT + col0;
 #pragma unroll
-        for (int cb = 0; cb < kEpiCols / 16; ++cb) {
+        for (int hh = 0; hh < kEpiCols / 16; ++hh) {
           uint32_t v[16];
-          tmem_ld16(taddr + cb * 16, v);
+          tmem_ld16(taddr + 16 * hh, v);
           tmem_ld_wait();
-          if (DOTS) {
-            if (m < p.M) {
+          if (hh == kEpiCols / 16 - 1) {
+            // D has been read: release the buffer to the MMA before the math.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&d_empty[db]);
+          }
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const int n = n0 + col0 + cb * 16 + j;
-                if (n < p.N)
-                  p.dots[((size_t)m * p.N + n) * G + g] = (int32_t)__uint_as_float(v[j]);
+          for (int j4 = 0; j4 < 4; ++j4) {
+            // four tokens' s_x per 16-byte broadcast load
+            const float4 xv = *reinterpret_cast<const float4*>(sxg + 16 * hh + 4 * j4);
+            const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const int t = 16 * hh + 4 * j4 + jj;
+              const float dot = __uint_as_float(v[4 * j4 + jj]);  // exact integer group dot
+              if (DOTS) {
+                const int m = m0 + col0 + t;
+                if (m < p.M && n < p.N) p.dots[((size_t)m * p.N + n) * G + g] = (int32_t)dot;
+              } else {
+                acc[t] = __fmaf_rn(__fmul_rn(dot, xa[jj]), sw, acc[t]);
               }
-            }
-          } else {
-            const float sx = sxv[gg];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float t = __fmul_rn(__uint_as_float(v[j]), sx);
-              acc[cb * 16 + j] = __fmaf_rn(t, __half2float(swc[gg * BN + cb * 16 + j]),
-                                           acc[cb * 16 + j]);
             }
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&d_empty[d]);
       }
-      named_bar_sync(1, kEpiThreads);  // the scale buffer of this chunk may be reused
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[slot]);
     }
-    if (!DOTS && m < p.M) {
-      if (p.y_bf16) {
-        __nv_bfloat16* yr = static_cast<__nv_bfloat16*>(p.y) + (size_t)m * p.N + n0 + col0;
-        for (int n = 0; n < kEpiCols; ++n)
-          if (n0 + col0 + n < p.N) yr[n] = __float2bfloat16_rn(acc[n]);
-      } else {
-        float* yr = static_cast<float*>(p.y) + (size_t)m * p.N + n0 + col0;
-        for (int n = 0; n < kEpiCols; ++n)
-          if (n0 + col0 + n < p.N) yr[n] = acc[n];
+    if (!DOTS && n < p.N) {
+#pragma unroll
+      for (int t = 0; t < kEpiCols; ++t) {
+        const int m = m0 + col0 + t;
+        if (m < p.M) {
+          const size_t o = (size_t)m * p.N + n;
+          if (p.y_bf16)
+            static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(acc[t]);
+          else
+            static_cast<float*>(p.y)[o] = acc[t];
+        }
       }
     }
   }
@@ -424,7 +480,7 @@ int launch_mm_t(const CUtensorMap& mq, const CUtensorMap& mc, const MmParams& p,
     configured = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((p.N + BN - 1) / BN, (p.M + BM - 1) / BM);
+  cfg.gridDim = dim3((p.M + BT - 1) / BT, (p.N + BW - 1) / BW);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
@@ -442,12 +498,12 @@ int launch_mm_t(const CUtensorMap& mq, const CUtensorMap& mc, const MmParams& p,
 
 }  // namespace
 
-int launch_mm(const uint16_t* q_f16, const float* sx, const uint8_t* codes,
+int launch_mm(const uint16_t* q_f16, const float* sx, const int32_t* qsum, const uint8_t* codes,
               const uint16_t* scales, void* y, int y_dtype, int32_t* dots, int64_t M,
               int64_t N, int64_t K, int sm_count, int32_t* status, cudaStream_t stream) {
   (void)sm_count;
   if (M > (int64_t)1 << 20 || N > (int64_t)1 << 30) return PQ2_ERR_SHAPE;
-  if ((N + BN - 1) / BN > 0x7fffffff || (M + BM - 1) / BM > 65535) return PQ2_ERR_SHAPE;
+  if ((M + BT - 1) / BT > 0x7fffffff || (N + BW - 1) / BW > 65535) return PQ2_ERR_SHAPE;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return PQ2_ERR_LAUNCH;
   CUtensorMap mq, mc;
@@ -455,7 +511,7 @@ int launch_mm(const uint16_t* q_f16, const float* sx, const uint8_t* codes,
     // q: fp16 [M][K], box 64 x 128 (128-byte rows), 128-byte swizzle.
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)BM};
+    const cuuint32_t box[2] = {64, (cuuint32_t)BT};
     const cuuint32_t es[2] = {1, 1};
     if (enc(&mq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(q_f16), dims, strides,
             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -466,7 +522,7 @@ int launch_mm(const uint16_t* q_f16, const float* sx, const uint8_t* codes,
     // codes: u8 [N][K/4], box 32 x 128 (one group of 128 rows), no swizzle.
     const cuuint64_t dims[2] = {(cuuint64_t)(K / 4), (cuuint64_t)N};
     const cuuint64_t strides[1] = {(cuuint64_t)(K / 4)};
-    const cuuint32_t box[2] = {(cuuint32_t)kGroupCodeBytes, (cuuint32_t)BN};
+    const cuuint32_t box[2] = {(cuuint32_t)kGroupCodeBytes, (cuuint32_t)BW};
     const cuuint32_t es[2] = {1, 1};
     if (enc(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), dims, strides,
             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -474,6 +530,7 @@ int launch_mm(const uint16_t* q_f16, const float* sx, const uint8_t* codes,
       return PQ2_ERR_LAUNCH;
   }
   MmParams p{};
+  (void)qsum;
   p.sx = sx; p.scales = scales; p.y = y; p.dots = dots; p.status = status;
   p.M = (int)M; p.N = (int)N; p.K = (int)K; p.G = (int)(K / kGroup);
   p.y_bf16 = y_dtype == PQ2_BF16;

@@ -139,8 +139,20 @@ __global__ void __launch_bounds__(256) quantize_kernel(
     }
     reinterpret_cast<uint32_t*>(static_cast<int8_t*>(q) + base)[lane] = out;
   } else {
-    __half2 h01 = __halves2half2(__int2half_rn(qi[0]), __int2half_rn(qi[1]));
-    __half2 h23 = __halves2half2(__int2half_rn(qi[2]), __int2half_rn(qi[3]));
+    // Operand order of the prefill MMA: inside each 16-element chunk (lanes
+    // 4c..4c+3, element 4b + s held by lane 4c + b), element 4b + s goes to
+    // position 4s + 2(b & 1) + (b >> 1).  Lane L = 4c + s' writes positions
+    // 4s'..4s'+3, i.e. element s' of lanes 4c + 0, 2, 1, 3.
+    const int c = lane >> 2, s_out = lane & 3;
+    int o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int b = (j >> 1) | ((j & 1) << 1);  // 0, 2, 1, 3
+      const uint32_t v = __shfl_sync(0xffffffffu, packed, 4 * c + b);
+      o[j] = (int)(int8_t)((v >> (8 * s_out)) & 0xffu);
+    }
+    __half2 h01 = __halves2half2(__int2half_rn(o[0]), __int2half_rn(o[1]));
+    __half2 h23 = __halves2half2(__int2half_rn(o[2]), __int2half_rn(o[3]));
     uint2 v;
     v.x = *reinterpret_cast<uint32_t*>(&h01);
     v.y = *reinterpret_cast<uint32_t*>(&h23);

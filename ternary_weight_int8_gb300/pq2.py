@@ -43,7 +43,7 @@ SIGNATURES = {
     "pq2_linear": (_I, [_P, _I, _I64, _I64, _I64, _I64, _P, _P, _P, _I, _P, _SZ, _P, _P]),
     "pq2_linear_workspace_bytes": (_SZ, [_I64, _I64]),
     "pq2_mmv_decoder": (_I, [_I64]),
-    "pq2_mm": (_I, [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P]),
+    "pq2_mm": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P]),
     "pq2_debug_group_dots": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P, _P, _P]),
     "pq2_mmv_geometry": (_I, [_I64, _I64, _I, _P, _P, _P, _P]),
 }
@@ -177,15 +177,16 @@ def pq2_linear(x, codes, scales, y=None, out_dtype=torch.float32, workspace=None
     return y
 
 
-def pq2_mm(q_f16, sx, codes, scales, y=None, out_dtype=torch.float32, status=None,
+def pq2_mm(q_f16, sx, qsum, codes, scales, y=None, out_dtype=torch.float32, status=None,
            stream=None):
     """Prefill matmul, M >= 16, on tcgen05 tensor cores."""
     M, K = q_f16.shape
     N = codes.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=out_dtype, device=q_f16.device)
-    _check("pq2_mm", lib().pq2_mm(_ptr(q_f16), _ptr(sx), _ptr(codes), _ptr(scales), _ptr(y),
-                                  _DT[y.dtype], M, N, K, _ptr(status), _stream(stream)))
+    _check("pq2_mm", lib().pq2_mm(_ptr(q_f16), _ptr(sx), _ptr(qsum), _ptr(codes), _ptr(scales),
+                                  _ptr(y), _DT[y.dtype], M, N, K, _ptr(status),
+                                  _stream(stream)))
     return y
 
 
@@ -215,9 +216,11 @@ def mmv_decoder(M: int) -> int:
 
 
 def linear(x, codes, scales, out_dtype=torch.float32, stream=None):
-    """The complete projection: pq2_linear (M <= 8) or quantise + pq2_mm."""
+    """The complete projection: pq2_linear (M <= 8 or M >= 16), or quantise
+    + pq2_mm for 8 < M < 16 with the batch padded to 16 rows."""
     M = x.shape[0]
-    if M <= 8:
+    if M <= 8 or M >= 16:
         return pq2_linear(x, codes, scales, out_dtype=out_dtype, stream=stream)
-    q, sx, _ = pq2_quantize_act(x, PQ2_Q_F16, want_qsum=False, stream=stream)
-    return pq2_mm(q, sx, codes, scales, out_dtype=out_dtype, stream=stream)
+    xp = torch.zeros((16, x.shape[1]), dtype=x.dtype, device=x.device)
+    xp[:M] = x
+    return pq2_linear(xp, codes, scales, out_dtype=out_dtype, stream=stream)[:M]

@@ -63,3 +63,15 @@ def oracle_reference(x, codes_o, scales_o):
     dots = O.group_dots(q, codes_o)
     y32, y64, bound = O.scale_accumulate(dots, sx, scales_o)
     return q, sx, O.qsum(q), dots, y32, y64, bound
+
+
+def mm_operand_order(q: np.ndarray) -> np.ndarray:
+    """The PQ2_Q_F16 layout (include/pq2.h): inside every 16 consecutive
+    elements, element 4b + s goes to position 4s + 2(b & 1) + (b >> 1)."""
+    M, K = q.shape
+    out = np.empty_like(q)
+    for i in range(16):
+        b, s = i // 4, i % 4
+        p = 4 * s + 2 * (b & 1) + (b >> 1)
+        out[:, p::16] = q[:, i::16]
+    return out

@@ -104,7 +104,7 @@ def test_linear_validation(L):
     for i in (0, 6, 7, 8, 10):
         bad = list(ok); bad[i] = None
         assert f(*bad) == pq2.PQ2_ERR_NULL, i
-    for idx, val, err in [(3, 9, pq2.PQ2_ERR_SHAPE), (3, 0, pq2.PQ2_ERR_SHAPE),
+    for idx, val, err in [(3, 12, pq2.PQ2_ERR_SHAPE), (3, 0, pq2.PQ2_ERR_SHAPE),
                           (2, 5000, pq2.PQ2_ERR_SHAPE), (11, ws - 1, pq2.PQ2_ERR_SHAPE),
                           (1, 9, pq2.PQ2_ERR_DTYPE), (9, pq2.PQ2_F16, pq2.PQ2_ERR_DTYPE),
                           (10, A + 16, pq2.PQ2_ERR_ALIGN), (6, A + 8, pq2.PQ2_ERR_ALIGN),
@@ -114,9 +114,11 @@ def test_linear_validation(L):
 
 
 def test_mm_and_debug_validation(L):
-    assert L.pq2_mm(A, A, A, A, A, 2, 15, 10, 128, None, None) == pq2.PQ2_ERR_SHAPE
-    assert L.pq2_mm(A, A, A, A, None, 2, 16, 10, 128, None, None) == pq2.PQ2_ERR_NULL
-    assert L.pq2_mm(A + 2, A, A, A, A, 2, 16, 10, 128, None, None) == pq2.PQ2_ERR_ALIGN
+    assert L.pq2_mm(A, A, A, A, A, A, 2, 15, 10, 128, None, None) == pq2.PQ2_ERR_SHAPE
+    assert L.pq2_mm(A, A, A, A, A, None, 2, 16, 10, 128, None, None) == pq2.PQ2_ERR_NULL
+    assert L.pq2_mm(A, A, None, A, A, A, 2, 16, 10, 128, None, None) == pq2.PQ2_ERR_NULL
+    assert L.pq2_mm(A + 2, A, A, A, A, A, 2, 16, 10, 128, None, None) == pq2.PQ2_ERR_ALIGN
+    assert L.pq2_debug_group_dots(A, None, A, 16, 10, 128, 1, A, None, None) == pq2.PQ2_ERR_NULL
     d = L.pq2_debug_group_dots
     assert d(A, None, A, 1, 10, 128, 7, A, None, None) == pq2.PQ2_ERR_DTYPE
     assert d(A, None, A, 1, 10, 128, 2, A, None, None) == pq2.PQ2_ERR_NULL

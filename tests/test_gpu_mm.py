@@ -40,10 +40,10 @@ def test_mm_group_dots_bitexact(M, N, K):
     codes, scales, codes_o, scales_o = _prep(N, K, seed=M + N + K, code_values=4)
     x = synth.activations(M, K, seed=M * 3 + K, outlier_frac=0.01)
     q_o, _, _, dots_o, *_ = U.oracle_reference(x, codes_o, scales_o)
-    q, sx, _ = pq2.pq2_quantize_act(x.cuda(), pq2.PQ2_Q_F16, want_qsum=False)
+    q, sx, qs = pq2.pq2_quantize_act(x.cuda(), pq2.PQ2_Q_F16)
     dots, back, guard = U.guarded((M, N, K // G), torch.int32)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    pq2.pq2_debug_group_dots(q, codes, pq2.PQ2_PATH_MM, dots=dots, status=status)
+    pq2.pq2_debug_group_dots(q, codes, pq2.PQ2_PATH_MM, qsum=qs, dots=dots, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     assert np.array_equal(dots.cpu().numpy(), dots_o)
@@ -64,8 +64,8 @@ def test_mm_extreme_dots_exact():
     x[1::3] = -127.0
     x[2::5, ::3] = 63.0
     x = x.to(torch.bfloat16)
-    q, sx, _ = pq2.pq2_quantize_act(x.cuda(), pq2.PQ2_Q_F16, want_qsum=False)
-    dots = pq2.pq2_debug_group_dots(q, codes, pq2.PQ2_PATH_MM)
+    q, sx, qs = pq2.pq2_quantize_act(x.cuda(), pq2.PQ2_Q_F16)
+    dots = pq2.pq2_debug_group_dots(q, codes, pq2.PQ2_PATH_MM, qsum=qs)
     torch.cuda.synchronize()
     codes_o, scales_o = O.prepare(raw.numpy(), K)
     q_o, _ = O.quantize(O.widen(synth.bits_u16(x), "bf16"))
@@ -79,11 +79,11 @@ def test_mm_y_within_bound(M, N, K):
     codes, scales, codes_o, scales_o = _prep(N, K, seed=7 * M + N)
     x = synth.activations(M, K, seed=M + 5, outlier_frac=0.01)
     *_, y64, bound = U.oracle_reference(x, codes_o, scales_o)
-    q, sx, _ = pq2.pq2_quantize_act(x.cuda(), pq2.PQ2_Q_F16, want_qsum=False)
+    q, sx, qs = pq2.pq2_quantize_act(x.cuda(), pq2.PQ2_Q_F16)
     y, back, guard = U.guarded((M, N), torch.float32)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    pq2.pq2_mm(q, sx, codes, scales, y=y, status=status)
-    yb = pq2.pq2_mm(q, sx, codes, scales, out_dtype=torch.bfloat16)
+    pq2.pq2_mm(q, sx, qs, codes, scales, y=y, status=status)
+    yb = pq2.pq2_mm(q, sx, qs, codes, scales, out_dtype=torch.bfloat16)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     assert U.guards_intact(back, guard)
@@ -101,8 +101,8 @@ def test_mm_prefill_ffn_up_sampled(M):
     N, K = 17408, 5120
     codes, scales, codes_o, scales_o = _prep(N, K, seed=2024)
     x = synth.activations(M, K, seed=M)
-    q, sx, _ = pq2.pq2_quantize_act(x.cuda(), pq2.PQ2_Q_F16, want_qsum=False)
-    y = pq2.pq2_mm(q, sx, codes, scales)
+    q, sx, qs = pq2.pq2_quantize_act(x.cuda(), pq2.PQ2_Q_F16)
+    y = pq2.pq2_mm(q, sx, qs, codes, scales)
     torch.cuda.synchronize()
     rows = np.arange(M) if M <= 16 else np.sort(
         np.random.default_rng(M).choice(M, 8, replace=False))
@@ -111,8 +111,9 @@ def test_mm_prefill_ffn_up_sampled(M):
     assert ok, worst
 
 
-def test_linear_dispatches_to_mm_for_prefill():
-    N, K, M = 384, 1024, 48
+@pytest.mark.parametrize("M", [12, 48, 300])
+def test_linear_dispatches_to_mm_for_prefill(M):
+    N, K = 384, 1024
     codes, scales, codes_o, scales_o = _prep(N, K, seed=9)
     x = synth.activations(M, K, seed=10)
     y = pq2.linear(x.cuda(), codes, scales)

@@ -74,7 +74,8 @@ def test_quantize_bitexact(dtype, M, K, ld_pad):
         elif layout == pq2.PQ2_Q_PLANES:
             assert np.array_equal(q.cpu().numpy(), O.q_planes(q_o))
         else:
-            assert np.array_equal(q.cpu().float().numpy(), q_o.astype(np.float32))
+            assert np.array_equal(q.cpu().float().numpy(),
+                                  U.mm_operand_order(q_o).astype(np.float32))
         assert np.array_equal(sx.cpu().numpy().view(np.uint32), sx_o.view(np.uint32))
         assert np.array_equal(qs.cpu().numpy(), qs_o)
 
