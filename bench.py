@@ -249,6 +249,11 @@ def run_ours(args):
             raise RuntimeError(f"pq2_mmv failed ({st})")
 
     n_graphs = n_mats // len(MS)
+    # A graph holds `chunk` consecutive steps (a divisor of the step count,
+    # at most one full rotation over the matrices), as a decode step captured
+    # in one graph would; programmatic dependent launch overlaps neighbouring
+    # kernels inside a graph but not across graph launches.
+    chunk = max(d for d in range(1, n_graphs + 1) if args.steps % d == 0)
 
     def capture(fn):
         g = torch.cuda.CUDAGraph()
@@ -259,19 +264,26 @@ def run_ours(args):
                 fn()
         return g
 
-    # step graphs: graph j runs the 4 calls on matrices 4j..4j+3
-    step_graphs = [capture(lambda j=j: [complete(M, 4 * j + i, xs[M], sp)
-                                        for i, M in enumerate(MS)]) for j in range(n_graphs)]
+    def step_calls(j):
+        """Step j: the 4 complete calls (M = 1..4) on matrices 4j'..4j'+3."""
+        j %= n_graphs
+        for i, M in enumerate(MS):
+            complete(M, 4 * j + i, xs[M], sp)
 
     def e2e_step(j):
+        j %= n_graphs
         for i, M in enumerate(MS):
             dx[M].copy_(hx[M], non_blocking=True)
             complete(M, 4 * j + i, dx[M], sp)
             hy[M].copy_(ys[M], non_blocking=True)
 
-    e2e_graphs = [capture(lambda j=j: e2e_step(j)) for j in range(n_graphs)]
+    n_chunks = n_graphs // math.gcd(n_graphs, chunk)
+    step_graphs = [capture(lambda j=j: [step_calls(j * chunk + t) for t in range(chunk)])
+                   for j in range(n_chunks)]
+    e2e_graphs = [capture(lambda j=j: [e2e_step(j * chunk + t) for t in range(chunk)])
+                  for j in range(n_chunks)]
 
-    def timed(graphs, steps, warmup):
+    def timed(graphs, replays, warmup):
         with torch.cuda.stream(stream):
             for i in range(warmup):
                 graphs[i % len(graphs)].replay()
@@ -280,7 +292,7 @@ def run_ours(args):
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            for i in range(steps):
+            for i in range(replays):
                 graphs[i % len(graphs)].replay()
             e1.record(stream)
             torch.cuda.synchronize()
@@ -291,13 +303,14 @@ def run_ours(args):
             ms = float(t.item())
         return ms
 
+    warm_replays = -(-args.warmup // chunk)
     # soak (untimed) while the clock sampler runs, then the timed region
     with ClockSampler(local) as clocks:
         t_end = time.time() + 1.5
         while time.time() < t_end:
-            timed(step_graphs, 200, 0)
-        total_ms = timed(step_graphs, args.steps, args.warmup)
-        e2e_ms = timed(e2e_graphs, args.steps, args.warmup)
+            timed(step_graphs, 20, 0)
+        total_ms = timed(step_graphs, args.steps // chunk, warm_replays)
+        e2e_ms = timed(e2e_graphs, args.steps // chunk, warm_replays)
     ms_step = total_ms / args.steps
     us_call = ms_step * 1e3 / len(MS)
     e2e_us = e2e_ms / args.steps * 1e3 / len(MS)
@@ -306,13 +319,12 @@ def run_ours(args):
     per_m = {}
     peak, peak_kind = measured_peaks()
     for M in MS:
-        g_c = [capture(lambda j=j: [complete(M, (4 * j + i) % n_mats, xs[M], sp)
-                                    for i in range(4)]) for j in range(n_graphs)]
-        g_k = [capture(lambda j=j: [mmv_only(M, (4 * j + i) % n_mats, sp)
-                                    for i in range(4)]) for j in range(n_graphs)]
-        reps = max(50, args.steps)
-        c_ms = timed(g_c, reps, 5) / (reps * 4)
-        k_ms = timed(g_k, reps, 5) / (reps * 4)
+        # one graph = one call on each of the n_mats matrices in turn
+        g_c = [capture(lambda: [complete(M, i, xs[M], sp) for i in range(n_mats)])]
+        g_k = [capture(lambda: [mmv_only(M, i, sp) for i in range(n_mats)])]
+        reps = max(20, args.steps // 10)
+        c_ms = timed(g_c, reps, 3) / (reps * n_mats)
+        k_ms = timed(g_k, reps, 3) / (reps * n_mats)
         per_m[str(M)] = {
             "complete_us": round(c_ms * 1e3, 3),
             "mmv_us": round(k_ms * 1e3, 3),
@@ -333,7 +345,8 @@ def run_ours(args):
         "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2: {n_mats} distinct weight matrices "
                          f"({n_mats * wbytes / 1e6:.0f} MB) rotated",
-                   "timing": "CUDA graph replays, CUDA events on the launching stream"},
+                   "timing": f"CUDA graphs of {chunk} steps ({chunk * len(MS)} calls) "
+                             "replayed, CUDA events on the launching stream"},
         "e2e": {"value": round(e2e_us, 3), "unit": "us/call",
                 "h2d_bytes_per_step": sum(M * K_DIM * 2 for M in MS),
                 "d2h_bytes_per_step": sum(M * N_DIM * 2 for M in MS)},

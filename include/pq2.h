@@ -149,17 +149,24 @@ int pq2_mmv(const int8_t *q_planes, const float *sx, const int32_t *qsum,
             void *stream);
 
 /* Flags of pq2_mmv_ex.  Every libpq2 kernel is launched with programmatic
- * dependent launch, and a call releases the next one only once the kernel
- * before it has completed, so while a call starts at most the two kernels
- * enqueued immediately before it on the stream can still be running.
+ * dependent launch: it may start before the kernel enqueued before it on the
+ * stream completes, and waits for it before reading anything that kernel may
+ * write.  pq2_quantize_act, pq2_mmv and pq2_mmv_ex release the next kernel
+ * as soon as they start; pq2_mm releases it only once the kernel before it
+ * has completed.  So the kernels that may still run when a call starts are
+ * those enqueued at or after the latest "ordering point" before it: a
+ * pq2_mm call, a host synchronisation, an event wait, a copy, or a kernel
+ * launched without programmatic dependent launch (pq2_prepare is one).
+ * Without flags a call needs nothing of this.
  *  PQ2_MMV_OVERLAP_WEIGHTS  the call may stream codes and scales from HBM
- *      before those two kernels complete.  Legal when neither of them writes
- *      codes or scales (e.g. the weights were prepared by an earlier call).
- *  PQ2_MMV_INDEPENDENT      the call may also read q_planes, sx and qsum
- *      early: legal when neither of those two kernels writes any input of
- *      this call (e.g. back-to-back projections of the same quantised
- *      activations).  y is always written only after the kernel before the
- *      call has completed. */
+ *      before earlier kernels complete.  Legal when no kernel that may still
+ *      run writes codes or scales (e.g. the weights were prepared before the
+ *      latest ordering point).
+ *  PQ2_MMV_INDEPENDENT      the call reads every input early and computes
+ *      before earlier kernels complete.  Legal when no kernel that may still run writes any input of this call
+ *      (e.g. back-to-back projections of the same quantised activations).
+ *      y is always written only after the kernel before the call has
+ *      completed. */
 enum { PQ2_MMV_OVERLAP_WEIGHTS = 1, PQ2_MMV_INDEPENDENT = 2 };
 
 /* pq2_mmv with an explicit decoder (PQ2_DECODE_ADDXOR or PQ2_DECODE_PLANES)
@@ -171,10 +178,11 @@ int pq2_mmv_ex(const int8_t *q_planes, const float *sx, const int32_t *qsum,
 
 /* pq2_linear — the complete projection y = x W^T (quantise, then the GEMV),
  * as the pages time it ("complete call", KE Tests 3, 6): pq2_quantize_act
- * into the caller's workspace, then pq2_mmv (M = 1..8) launched so that it
- * streams the weights while the quantisation runs (programmatic dependent
- * launch; safe because the kernel it overlaps is this call's own
- * quantisation, which only writes the workspace), or pq2_mm (M >= 16).
+ * into the caller's workspace, then pq2_mmv (M = 1..8) with
+ * PQ2_MMV_OVERLAP_WEIGHTS, so that it streams the weights while the
+ * quantisation and the kernel before it finish, or pq2_mm (M >= 16).  Hence
+ * codes and scales must not be written by a kernel that may still run when
+ * the call starts (see the flags of pq2_mmv_ex).
  * Results are bit-identical to pq2_quantize_act + pq2_mmv / pq2_mm.
  *   x         (device) x_dtype [M][ldx], ldx >= K; M 1..8 or 16 .. 1<<20.
  *   workspace (device) pq2_linear_workspace_bytes(M, K) bytes, 256-byte

@@ -14,6 +14,9 @@ namespace pq2 {
 constexpr int kGroup = 128;          // weights / activations per group
 constexpr int kGroupCodeBytes = 32;  // code bytes per group (4 codes/byte)
 constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s at 2 GHz
+// Longest single suspension of a waiting thread (it resumes earlier when the
+// phase completes).
+constexpr uint32_t kWaitSuspendNs = 20000;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -57,11 +60,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// As mbar_try_wait, but a thread that finds the phase incomplete is
+// suspended until it completes or `hint_ns` nanoseconds pass.  Waiting
+// warps then leave the issue slots to the warps that work; without the hint
+// the suspension is short and a waiting warp keeps competing for them.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long start = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, kWaitSuspendNs)) {
     if (clock64() - start > kWaitLimitCycles) return false;
   }
   return true;

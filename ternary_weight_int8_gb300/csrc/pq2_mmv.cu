@@ -41,6 +41,7 @@ namespace pq2 {
 namespace {
 
 constexpr int kMaxConsumerThreads = 352;
+constexpr int kRowsPerThread = 2;         // rows sharing each q load
 constexpr int kMaxBlock = kMaxConsumerThreads + 32;
 constexpr int kMaxSplits = 64;
 constexpr int kMaxBoxRows = 256;          // TMA box height limit
@@ -69,7 +70,6 @@ struct MmvParams {
   int overlap;            // 1: stream weights before the grid dependency
                           // resolves; 2: stream every input before it
   int sw_bulk;            // weight-scale slab arrives by one bulk copy (G % 8 == 0)
-  int sx_bulk;            // s_x and sum(q) arrive by bulk copies with stage 0
 };
 
 // Batched global -> shared copy of `count` 16-bit values by `threads`
@@ -84,24 +84,6 @@ __device__ __forceinline__ void preload_u16(uint16_t* dst, const uint16_t* src, 
     for (int j = 0; j < B; ++j) {
       const int i = base + j * threads;
       v[j] = i < count ? __ldg(src + i) : (uint16_t)0;
-    }
-#pragma unroll
-    for (int j = 0; j < B; ++j) {
-      const int i = base + j * threads;
-      if (i < count) dst[i] = v[j];
-    }
-  }
-}
-
-__device__ __forceinline__ void preload_u32(uint32_t* dst, const uint32_t* src, int count,
-                                            int tid, int threads) {
-  constexpr int B = 8;
-  for (int base = tid; base < count; base += B * threads) {
-    uint32_t v[B];
-#pragma unroll
-    for (int j = 0; j < B; ++j) {
-      const int i = base + j * threads;
-      v[j] = i < count ? __ldg(src + i) : 0u;
     }
 #pragma unroll
     for (int j = 0; j < B; ++j) {
@@ -127,86 +109,143 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the arrival is counted in advance, so the phase waits for it).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
                "r"(bytes)
                : "memory");
 }
 
-// Exact int32 dot of one 128-group for every column.
-//   c0, c1 : the group's two 16-byte halves of code bytes (swizzled smem)
+// Shared-memory loads by 32-bit shared address.  The operands live at
+// run-time offsets from the aligned dynamic shared base; explicit ld.shared
+// keeps every read on the shared-memory path.
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
+// Exact int32 dots of one 128-group for RP weight rows and columns
+// m0 .. m0+MB-1.  Each 16-byte chunk of q is loaded once and used for all RP
+// rows, which keeps shared-memory traffic (q is common to every row) low.
+//   c0[r], c1[r] : shared addresses of row r's two 16-byte halves of the
+//                  group's code bytes (swizzled)
 // Plane s of code word w (bytes 4w..4w+3 of the group) holds the codes of
 // weights 16w + 4b + s (b = 0..3); in plane order those activations are the
 // 4 bytes at s*32 + 4w, so one 32-bit q word meets one 32-bit plane word.
-//   qz     : the group's box row of q for column 0 (128 bytes, 128-byte
-//            swizzled with key qsw); column m at qz + m * q_mstride
-template <int M, int DEC>
-__device__ __forceinline__ void group_dot(const uint8_t* c0, const uint8_t* c1,
-                                          const int8_t* qz, int q_mstride, int qsw,
-                                          const int32_t* qs, int qs_mstride, int dot[M]) {
-  // Independent accumulator chains per column: one per plane for M <= 2
-  // (instruction-level parallelism), two for larger M (registers).  Masked
-  // planes: even planes accumulate code * q, odd planes 4 * code * q.
-  constexpr int NA = M <= 2 ? 4 : 2;
-  int acc[NA][M];
+//   qz     : shared address of the group's box row of q for column m0 (128
+//            bytes, 128-byte swizzled with key qsw); column m0+m at
+//            qz + m * q_mstride
+//   qs     : shared address of sum(q) of the group for column m0; column
+//            m0+m at qs + m * qs_mstride
+template <int MB, int RP, int DEC>
+__device__ __forceinline__ void group_dot(const uint32_t (&c0)[RP], const uint32_t (&c1)[RP],
+                                          uint32_t qz, int q_mstride, int qsw, uint32_t qs,
+                                          int qs_mstride, int (&dot)[RP][MB]) {
+  // Independent accumulator chains: one per plane when few (instruction-level
+  // parallelism), else one per plane parity (registers).  Masked planes:
+  // even planes accumulate code * q, odd planes 4 * code * q.
+  constexpr int NA = MB * RP <= 4 ? 4 : 2;
+  int acc[RP][NA][MB];
 #pragma unroll
-  for (int a = 0; a < NA; ++a)
+  for (int r = 0; r < RP; ++r)
 #pragma unroll
-    for (int m = 0; m < M; ++m) acc[a][m] = 0;
+    for (int a = 0; a < NA; ++a)
+#pragma unroll
+      for (int m = 0; m < MB; ++m) acc[r][a][m] = 0;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const uint4 c = *reinterpret_cast<const uint4*>(h ? c1 : c0);
-    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-    uint32_t cs[4];  // the words shifted down by 4 bits: planes 2, 3 in place of 0, 1
+    uint32_t cw[RP][4];
 #pragma unroll
-    for (int w = 0; w < 4; ++w) cs[w] = cw[w] >> 4;
+    for (int r = 0; r < RP; ++r) {
+      const uint4 c = lds128(h ? c1[r] : c0[r]);
+      cw[r][0] = c.x; cw[r][1] = c.y; cw[r][2] = c.z; cw[r][3] = c.w;
+    }
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
-      int4 qv[M];
+      if (s == 2) {
+        // Planes 2 and 3 sit where planes 0 and 1 were once the words are
+        // shifted down by 4 bits.
 #pragma unroll
-      for (int m = 0; m < M; ++m)
-        qv[m] = *reinterpret_cast<const int4*>(qz + m * q_mstride + ((s * 32 + 16 * h) ^ qsw));
+        for (int r = 0; r < RP; ++r)
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        uint32_t wv;
-        if (DEC == kDecodeAddXor) {
-          // Spread: the four codes of plane s, one per byte (values 0..3).
-          // +0x7F7F7F7F cannot carry between bytes; ^0x80808080 maps
-          // 127/128/129/130 to the signed bytes -1/0/+1/+2.
-          const uint32_t spread = (cw[w] >> (2 * s)) & 0x03030303u;
-          wv = (spread + 0x7F7F7F7Fu) ^ 0x80808080u;
-        } else {
-          // Masked plane: bytes code (s even) or 4 * code (s odd), unsigned.
-          wv = ((s < 2) ? cw[w] : cs[w]) & ((s & 1) ? 0x0C0C0C0Cu : 0x03030303u);
-        }
-#pragma unroll
-        for (int m = 0; m < M; ++m) {
-          const int qw = w == 0 ? qv[m].x : w == 1 ? qv[m].y : w == 2 ? qv[m].z : qv[m].w;
-          int& a = acc[NA == 4 ? s : (s & 1)][m];
-          a = (DEC == kDecodeAddXor) ? __dp4a((int)wv, qw, a) : dp4a_us(wv, qw, a);
-        }
+          for (int w = 0; w < 4; ++w) cw[r][w] >>= 4;
       }
+      uint4 qv[MB];
+#pragma unroll
+      for (int m = 0; m < MB; ++m)
+        qv[m] = lds128(qz + m * q_mstride + ((s * 32 + 16 * h) ^ qsw));
+#pragma unroll
+      for (int r = 0; r < RP; ++r)
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint32_t wv;
+          if (DEC == kDecodeAddXor) {
+            // Spread: the four codes of plane s, one per byte (values 0..3).
+            // +0x7F7F7F7F cannot carry between bytes; ^0x80808080 maps
+            // 127/128/129/130 to the signed bytes -1/0/+1/+2.
+            const uint32_t spread = (cw[r][w] >> (2 * (s & 1))) & 0x03030303u;
+            wv = (spread + 0x7F7F7F7Fu) ^ 0x80808080u;
+          } else {
+            // Masked plane: bytes code (s even) or 4 * code (s odd), unsigned.
+            wv = cw[r][w] & ((s & 1) ? 0x0C0C0C0Cu : 0x03030303u);
+          }
+#pragma unroll
+          for (int m = 0; m < MB; ++m) {
+            const int qw =
+                (int)(w == 0 ? qv[m].x : w == 1 ? qv[m].y : w == 2 ? qv[m].z : qv[m].w);
+            int& a = acc[r][NA == 4 ? s : (s & 1)][m];
+            a = (DEC == kDecodeAddXor) ? __dp4a((int)wv, qw, a) : dp4a_us(wv, qw, a);
+          }
+        }
     }
   }
 #pragma unroll
-  for (int m = 0; m < M; ++m) {
-    const int even = NA == 4 ? acc[0][m] + acc[2][m] : acc[0][m];
-    const int odd = NA == 4 ? acc[1][m] + acc[3][m] : acc[1][m];
-    if (DEC == kDecodeAddXor) {
-      dot[m] = even + odd;
-    } else {
-      // `odd` is exactly 4 * sum(code * q) over planes 1 and 3: shift it
-      // back, then remove the codes' -1 offset with the group sum of q.
-      dot[m] = even + (odd >> 2) - qs[m * qs_mstride];
+  for (int m = 0; m < MB; ++m) {
+    // `odd` is exactly 4 * sum(code * q) over planes 1 and 3 (masked planes):
+    // shift it back, then remove the codes' -1 offset with the group sum of q.
+    const int qsm = DEC == kDecodeAddXor ? 0 : (int)lds32(qs + m * qs_mstride);
+#pragma unroll
+    for (int r = 0; r < RP; ++r) {
+      const int even = NA == 4 ? acc[r][0][m] + acc[r][2][m] : acc[r][0][m];
+      const int odd = NA == 4 ? acc[r][1][m] + acc[r][3][m] : acc[r][1][m];
+      dot[r][m] = DEC == kDecodeAddXor ? even + odd : even + (odd >> 2) - qsm;
     }
   }
 }
 
+// Up to four columns two CTAs fit on an SM (a call overlaps the next one);
+// more columns need the registers of one CTA per SM.
 template <int M, int DEC, bool DOTS>
-__global__ void __launch_bounds__(kMaxBlock, 2)
+__global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
     mmv_kernel(const __grid_constant__ CUtensorMap map_hi,
                const __grid_constant__ CUtensorMap map_lo,
-               const __grid_constant__ CUtensorMap map_q, const MmvParams p) {
+               const MmvParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // The 128-byte swizzle needs 1024-byte aligned boxes.
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -226,7 +265,9 @@ __global__ void __launch_bounds__(kMaxBlock, 2)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cons_warps = p.cons_threads >> 5;
   const int S = p.splits, G = p.G, Gs = p.stage_groups;
-  const bool independent = p.overlap >= 2;
+  // An independent call reads no output of earlier kernels: it waits for
+  // them only before storing y.
+  const bool independent = !DOTS && p.overlap >= 2;
 
   if (tid == 0) {
     for (int s = 0; s < p.ring; ++s) {
@@ -237,62 +278,73 @@ __global__ void __launch_bounds__(kMaxBlock, 2)
     fence_barrier_init();
   }
   __syncthreads();
-  // Dependent grids are released only after this grid's own wait (every
-  // thread waits, then triggers), so at most this grid and the one before it
-  // run when the next call starts.
+  // Release the next kernel on the stream now.  Its CTAs then take the SM
+  // slots that this grid's predecessor frees, one by one, which keeps the
+  // grids spread one CTA per SM; released later, a grid finds SMs with
+  // uneven free slots and some SMs receive two of its CTAs.
+  grid_dep_launch();
 
   if (warp == cons_warps) {
     // ---------------------------------------------------------- producer
-    if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(&map_q) : "memory");
-    }
+    if (lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
     bool ok = true;
     const bool need_qs = DEC == kDecodeMaskPlanes;
-    const uint32_t side_b = (uint32_t)(M * G * 4);
     if (!DOTS && p.sw_bulk && lane == 0) {
       if (!p.overlap) grid_dep_wait();
       const uint32_t bytes = (uint32_t)(R * G * 2);
       mbar_arrive_expect_tx(swbar, bytes);
       bulk_g2s(sw_s, p.scales + (size_t)n0 * G, bytes, swbar);
     }
-    // Issue stage i: weights (unless already issued), q boxes, and with
-    // stage 0 s_x and sum(q).  The arrival announces every byte of the stage
-    // that has not been announced before, ahead of the copies it covers.
-    auto issue = [&](int i, bool weights, bool inputs) {
-      const int slot = i % p.ring;
-      const int g0 = i * Gs, nb = min(Gs, G - g0), boxes = (nb + 3) / 4;
-      uint8_t* st = ring + (size_t)slot * p.stage_bytes;
+    // Weights of stage i: TMA boxes announced on the stage barrier without
+    // arriving, so the stage completes only once its inputs are issued too.
+    auto issue_weights = [&](int i) {
       if (lane != 0) return;
-      const uint32_t wbytes = weights ? (uint32_t)(boxes * R * kBoxBytes) : 0u;
-      if (!inputs) {
-        mbar_expect_tx(&full[slot], wbytes);
-      } else {
-        const bool side = (i == 0) && p.sx_bulk;
-        const uint32_t extra = side ? (DOTS ? 0u : side_b) + (need_qs ? side_b : 0u) : 0u;
-        mbar_arrive_expect_tx(&full[slot], wbytes + (uint32_t)(M * Gs * kGroup) + extra);
-        for (int m = 0; m < M; ++m)
-          tma_load_2d(st + p.q_off + m * p.qbox_stride, &map_q, 0, m * G + g0, &full[slot]);
-        if (side) {
-          if (!DOTS) bulk_g2s(sx_s, p.sx, side_b, &full[slot]);
-          if (need_qs) bulk_g2s(qs_s, p.qsum, side_b, &full[slot]);
-        }
-      }
-      for (int b = 0; weights && b < boxes; ++b)
+      const int slot = i % p.ring;
+      const int g0 = i * Gs, boxes = (min(Gs, G - g0) + 3) / 4;
+      uint8_t* st = ring + (size_t)slot * p.stage_bytes;
+      mbar_expect_tx(&full[slot], (uint32_t)(boxes * R * kBoxBytes));
+      for (int b = 0; b < boxes; ++b)
         tma_load_2d(st + b * p.box_stride, map, (g0 + 4 * b) * kGroupCodeBytes, n0, &full[slot]);
     };
-    const int pre = p.overlap ? min(p.ring, p.stages_total) : 0;
-    for (int i = 0; i < pre; ++i) issue(i, true, independent);
-    grid_dep_wait();
-    grid_dep_launch();
-    for (int i = 0; i < p.stages_total; ++i) {
+    // Inputs of stage i (and with stage 0 s_x and sum(q)), copied by the
+    // whole warp with cp.async rather than TMA: the SM's TMA unit serves its
+    // requests in order, and these few small copies must not queue behind
+    // the weights that the next call's CTA on this SM prefetches.  q rows
+    // land in the same 128-byte swizzled layout the consumers read.
+    auto issue_inputs = [&](int i) {
       const int slot = i % p.ring;
+      const int g0 = i * Gs, nb = min(Gs, G - g0);
+      uint8_t* st = ring + (size_t)slot * p.stage_bytes + p.q_off;
+      const int chunks = M * nb * 8;
+      for (int idx = lane; idx < chunks; idx += 32) {
+        const int m = idx / (nb * 8), rem = idx - m * nb * 8, l = rem >> 3, c = rem & 7;
+        cp_async16(st + m * p.qbox_stride + l * kGroup + ((c ^ (l & 7)) << 4),
+                   p.q + ((size_t)m * G + g0 + l) * kGroup + c * 16);
+      }
+      if (i == 0) {
+        for (int idx = lane; idx < M * G; idx += 32) {
+          if (!DOTS) cp_async4(sx_s + idx, p.sx + idx);
+          if (need_qs) cp_async4(qs_s + idx, p.qsum + idx);
+        }
+      }
+      cp_async_mbar_arrive(&full[slot]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[slot]);
+    };
+    const int pre = p.overlap ? min(p.ring, p.stages_total) : 0;
+    for (int i = 0; i < pre; ++i) issue_weights(i);
+    if (independent)
+      for (int i = 0; i < pre; ++i) issue_inputs(i);
+    else
+      grid_dep_wait();
+    for (int i = 0; i < p.stages_total; ++i) {
       if (i < pre) {
-        if (!independent) issue(i, false, true);
+        if (!independent) issue_inputs(i);
         continue;
       }
-      if (i >= p.ring) ok = ok && mbar_wait(&empty[slot], ((i / p.ring) - 1) & 1);
-      issue(i, true, true);
+      if (i >= p.ring) ok = ok && mbar_wait(&empty[i % p.ring], ((i / p.ring) - 1) & 1);
+      issue_weights(i);
+      issue_inputs(i);
     }
     if (!ok && lane == 0) report(p.status, PQ2_ERR_TIMEOUT);
     return;
@@ -300,59 +352,101 @@ __global__ void __launch_bounds__(kMaxBlock, 2)
 
   // ------------------------------------------------------------ consumers
   // Reads before the grid dependency resolves: none by default, the weight
-  // scales with the overlap flag, every input when the call is independent.
+  // scales with the overlap flag; q, s_x and sum(q) arrive through the stage
+  // barriers.
   if (!p.overlap) grid_dep_wait();
-  if (!DOTS && !p.sw_bulk)
+  if (!DOTS && !p.sw_bulk) {
     preload_u16(reinterpret_cast<uint16_t*>(sw_s), p.scales + (size_t)n0 * G, R * G, tid,
                 p.cons_threads);
-  grid_dep_wait();
-  grid_dep_launch();
-  if (!p.sx_bulk) {
-    if (!DOTS)
-      preload_u32(reinterpret_cast<uint32_t*>(sx_s), reinterpret_cast<const uint32_t*>(p.sx),
-                  M * G, tid, p.cons_threads);
-    if (DEC == kDecodeMaskPlanes)
-      preload_u32(reinterpret_cast<uint32_t*>(qs_s), reinterpret_cast<const uint32_t*>(p.qsum),
-                  M * G, tid, p.cons_threads);
     named_bar_sync(1, p.cons_threads);
   }
   bool ok = true;
   if (!DOTS && p.sw_bulk) ok = ok && mbar_wait(swbar, 0);
 
+  // Thread t owns split z = t % S and the RP rows RP*(t / S) ..; an odd
+  // row count leaves the last thread's second row a duplicate of row R-1,
+  // computed but never stored.
+  constexpr int RP = kRowsPerThread;
   const int z = tid % S;
-  const int r = tid / S;
-  const bool active = r < R;
-  const int sw_x = (r & 7) << 4;  // 128-byte swizzle of the code boxes: chunk ^= row % 8
-  float yacc[M];
+  const int rb = tid / S;
+  int rows[RP];
+  bool valid[RP];
 #pragma unroll
-  for (int m = 0; m < M; ++m) yacc[m] = 0.0f;
+  for (int r = 0; r < RP; ++r) {
+    valid[r] = rb * RP + r < R;
+    rows[r] = min(rb * RP + r, R - 1);
+  }
+  const bool active = valid[0];
+  const uint32_t ring_s = smem_u32(ring), sw_base = smem_u32(sw_s);
+  const uint32_t sx_base = smem_u32(sx_s), qs_base = smem_u32(qs_s);
+  float yacc[RP][M];
+#pragma unroll
+  for (int r = 0; r < RP; ++r)
+#pragma unroll
+    for (int m = 0; m < M; ++m) yacc[r][m] = 0.0f;
+
+  // Scale and accumulate the dots of columns m0 .. m0+MB-1 in the method's
+  // order: t = (float(dot) * s_x) * s_w, y += t.
+  auto consume = [&](auto& dot, int m0, int g) {
+    constexpr int MB = sizeof(dot[0]) / sizeof(int);
+    if constexpr (DOTS) {
+#pragma unroll
+      for (int r = 0; r < RP; ++r)
+        if (valid[r])
+#pragma unroll
+          for (int m = 0; m < MB; ++m)
+            p.dots[((size_t)(m0 + m) * p.N + n0 + rows[r]) * G + g] = dot[r][m];
+    } else {
+      float ws[RP];
+#pragma unroll
+      for (int r = 0; r < RP; ++r)
+        ws[r] = __half2float(__ushort_as_half((uint16_t)lds16(sw_base + (rows[r] * G + g) * 2)));
+#pragma unroll
+      for (int m = 0; m < MB; ++m) {
+        const float xs = __uint_as_float(lds32(sx_base + ((m0 + m) * G + g) * 4));
+#pragma unroll
+        for (int r = 0; r < RP; ++r) {
+          float t = __fmul_rn(__int2float_rn(dot[r][m]), xs);
+          t = __fmul_rn(t, ws[r]);
+          yacc[r][m0 + m] = __fadd_rn(yacc[r][m0 + m], t);
+        }
+      }
+    }
+  };
 
   for (int i = 0; i < p.stages_total; ++i) {
     const int slot = i % p.ring;
     ok = ok && mbar_wait(&full[slot], (i / p.ring) & 1);
-    const uint8_t* st = ring + (size_t)slot * p.stage_bytes;
+    const uint32_t st_s = ring_s + slot * p.stage_bytes;
     const int g0 = i * Gs;
     if (active && ok) {
       for (int l = z; l < Gs; l += S) {
         const int g = g0 + l;
         if (g >= G) break;
-        const uint8_t* row = st + (l >> 2) * p.box_stride + r * kBoxBytes;
         const int lo = (l & 3) * 32;  // logical byte offset of the group in the box row
-        int dot[M];
-        group_dot<M, DEC>(row + (lo ^ sw_x), row + ((lo + 16) ^ sw_x),
-                          reinterpret_cast<const int8_t*>(st + p.q_off) + l * kGroup,
-                          p.qbox_stride, (l & 7) << 4, qs_s + g, G, dot);
-        if (DOTS) {
+        uint32_t c0[RP], c1[RP];
 #pragma unroll
-          for (int m = 0; m < M; ++m) p.dots[((size_t)m * p.N + n0 + r) * G + g] = dot[m];
-        } else {
-          const float ws = __half2float(sw_s[r * G + g]);
-#pragma unroll
-          for (int m = 0; m < M; ++m) {
-            float t = __fmul_rn(__int2float_rn(dot[m]), sx_s[m * G + g]);
-            t = __fmul_rn(t, ws);
-            yacc[m] = __fadd_rn(yacc[m], t);
-          }
+        for (int r = 0; r < RP; ++r) {
+          // 128-byte swizzle of the code boxes: 16-byte chunk ^= row % 8
+          const uint32_t rowa = st_s + (l >> 2) * p.box_stride + rows[r] * kBoxBytes;
+          const int sw = (rows[r] & 7) << 4;
+          c0[r] = rowa + (lo ^ sw);
+          c1[r] = rowa + ((lo + 16) ^ sw);
+        }
+        const uint32_t qz = st_s + p.q_off + l * kGroup;
+        const int qsw = (l & 7) << 4;
+        // Columns in blocks of at most four keep the accumulators in registers.
+        constexpr int MA = M <= 4 ? M : 4;
+        {
+          int dot[RP][MA];
+          group_dot<MA, RP, DEC>(c0, c1, qz, p.qbox_stride, qsw, qs_base + g * 4, G * 4, dot);
+          consume(dot, 0, g);
+        }
+        if constexpr (M > 4) {
+          int dot[RP][M - 4];
+          group_dot<M - 4, RP, DEC>(c0, c1, qz + 4 * p.qbox_stride, p.qbox_stride, qsw,
+                                    qs_base + (4 * G + g) * 4, G * 4, dot);
+          consume(dot, 4, g);
         }
       }
     }
@@ -364,17 +458,24 @@ __global__ void __launch_bounds__(kMaxBlock, 2)
     // Combine the S split partials of each row (adjacent lanes) with a fixed
     // butterfly; lane z = 0 stores.  The order is a function of S alone.
 #pragma unroll
-    for (int m = 0; m < M; ++m)
-      for (int off = S >> 1; off > 0; off >>= 1)
-        yacc[m] = __fadd_rn(yacc[m], __shfl_xor_sync(0xffffffffu, yacc[m], off));
-    if (active && z == 0) {
+    for (int r = 0; r < RP; ++r)
 #pragma unroll
-      for (int m = 0; m < M; ++m) {
-        const size_t o = (size_t)m * p.N + n0 + r;
-        if (p.y_bf16)
-          static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(yacc[m]);
-        else
-          static_cast<float*>(p.y)[o] = yacc[m];
+      for (int m = 0; m < M; ++m)
+        for (int off = S >> 1; off > 0; off >>= 1)
+          yacc[r][m] = __fadd_rn(yacc[r][m], __shfl_xor_sync(0xffffffffu, yacc[r][m], off));
+    grid_dep_wait();  // earlier kernels may still read or write y
+    if (z == 0) {
+#pragma unroll
+      for (int r = 0; r < RP; ++r) {
+        if (!valid[r]) continue;
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          const size_t o = (size_t)m * p.N + n0 + rows[r];
+          if (p.y_bf16)
+            static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(yacc[r][m]);
+          else
+            static_cast<float*>(p.y)[o] = yacc[r][m];
+        }
       }
     }
   }
@@ -422,7 +523,7 @@ int align_up(int v, int a) { return (v + a - 1) / a * a; }
 int gcd(int a, int b) { return b ? gcd(b, a % b) : a; }
 
 template <int M, int DEC, bool DOTS>
-int launch_one(const CUtensorMap& hi, const CUtensorMap& lo, const CUtensorMap& qm,
+int launch_one(const CUtensorMap& hi, const CUtensorMap& lo,
                const MmvParams& p, int smem, cudaStream_t stream) {
   auto kern = mmv_kernel<M, DEC, DOTS>;
   static int configured = 0;  // largest dynamic smem size set so far
@@ -442,7 +543,7 @@ int launch_one(const CUtensorMap& hi, const CUtensorMap& lo, const CUtensorMap& 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, hi, lo, qm, p) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kern, hi, lo, p) != cudaSuccess) {
     cudaGetLastError();
     return PQ2_ERR_LAUNCH;
   }
@@ -450,17 +551,17 @@ int launch_one(const CUtensorMap& hi, const CUtensorMap& lo, const CUtensorMap& 
 }
 
 template <int DEC, bool DOTS>
-int launch_m(int M, const CUtensorMap& hi, const CUtensorMap& lo, const CUtensorMap& qm,
+int launch_m(int M, const CUtensorMap& hi, const CUtensorMap& lo,
              const MmvParams& p, int smem, cudaStream_t s) {
   switch (M) {
-    case 1: return launch_one<1, DEC, DOTS>(hi, lo, qm, p, smem, s);
-    case 2: return launch_one<2, DEC, DOTS>(hi, lo, qm, p, smem, s);
-    case 3: return launch_one<3, DEC, DOTS>(hi, lo, qm, p, smem, s);
-    case 4: return launch_one<4, DEC, DOTS>(hi, lo, qm, p, smem, s);
-    case 5: return launch_one<5, DEC, DOTS>(hi, lo, qm, p, smem, s);
-    case 6: return launch_one<6, DEC, DOTS>(hi, lo, qm, p, smem, s);
-    case 7: return launch_one<7, DEC, DOTS>(hi, lo, qm, p, smem, s);
-    case 8: return launch_one<8, DEC, DOTS>(hi, lo, qm, p, smem, s);
+    case 1: return launch_one<1, DEC, DOTS>(hi, lo, p, smem, s);
+    case 2: return launch_one<2, DEC, DOTS>(hi, lo, p, smem, s);
+    case 3: return launch_one<3, DEC, DOTS>(hi, lo, p, smem, s);
+    case 4: return launch_one<4, DEC, DOTS>(hi, lo, p, smem, s);
+    case 5: return launch_one<5, DEC, DOTS>(hi, lo, p, smem, s);
+    case 6: return launch_one<6, DEC, DOTS>(hi, lo, p, smem, s);
+    case 7: return launch_one<7, DEC, DOTS>(hi, lo, p, smem, s);
+    case 8: return launch_one<8, DEC, DOTS>(hi, lo, p, smem, s);
     default: return PQ2_ERR_SHAPE;
   }
 }
@@ -470,8 +571,9 @@ int launch_m(int M, const CUtensorMap& hi, const CUtensorMap& lo, const CUtensor
 // Geometry: P = min(N, #SM) CTAs (more when a CTA would exceed 256 rows),
 // R = ceil(N / P) rows for the largest CTA, and the split count S (a divisor
 // of 32, so a row's splits share a warp) that best fills the consumer lanes
-// (R*S of 32*ceil(R*S/32)) and the groups (G of S*ceil(G/S)) with at least
-// ~6 warps.  A function of (N, K, SM count) only.
+// (ceil(R/2)*S threads, two rows each, of 32*ceil(ceil(R/2)*S/32)) and the
+// groups (G of S*ceil(G/S)) with at least ~6 warps.  A function of (N, K,
+// SM count) only.
 bool mmv_geometry(int64_t N, int64_t K, int sm_count, MmvGeometry* out) {
   if (N < 1 || K < kGroup || K % kGroup || sm_count < 1) return false;
   if (N > (int64_t)1 << 30 || K > (int64_t)1 << 24) return false;
@@ -482,8 +584,9 @@ bool mmv_geometry(int64_t N, int64_t K, int sm_count, MmvGeometry* out) {
   const int R = (int)((N + ctas - 1) / ctas);
   int best_s = 1;
   double best = -1.0;
+  const int pairs = (R + kRowsPerThread - 1) / kRowsPerThread;
   for (int S = 1; S <= std::min(std::min(G, kMaxSplits), 16); S *= 2) {
-    const int lanes = R * S;
+    const int lanes = pairs * S;
     if (lanes > kMaxConsumerThreads) break;
     const int T = align_up(lanes, 32);
     const int steps = (G + S - 1) / S;
@@ -497,7 +600,7 @@ bool mmv_geometry(int64_t N, int64_t K, int sm_count, MmvGeometry* out) {
   out->ctas = (int)ctas;
   out->splits = best_s;
   out->rows_max = R;
-  out->threads = align_up(R * best_s, 32);
+  out->threads = align_up(pairs * best_s, 32);
   out->steps = (G + best_s - 1) / best_s;
   return true;
 }
@@ -517,11 +620,6 @@ int launch_mmv(const int8_t* q, const float* sx, const int32_t* qsum, const uint
   p.overlap = overlap;
   p.y_bf16 = y_dtype == PQ2_BF16;
   p.sw_bulk = (K / kGroup) % 8 == 0 && reinterpret_cast<uintptr_t>(scales) % 16 == 0;
-  {
-    const bool a16 = (reinterpret_cast<uintptr_t>(sx) % 16 == 0) &&
-                     (reinterpret_cast<uintptr_t>(qsum) % 16 == 0);
-    p.sx_bulk = a16 && ((M * (K / kGroup) * 4) % 16 == 0);
-  }
   const int mi = (int)M, R = geo.rows_max, S = geo.splits, G = p.G;
   const int unit = 4 * S / gcd(4, S);
   p.box_stride = align_up(R * kBoxBytes, 1024);
@@ -548,19 +646,18 @@ int launch_mmv(const int8_t* q, const float* sx, const int32_t* qsum, const uint
   p.ring = std::min(std::min(p.stages_total, room / p.stage_bytes), kMaxStages);
   const int smem = 1024 + p.ring_off + p.ring * p.stage_bytes;  // + alignment slack
 
-  CUtensorMap hi, lo, qm;
+  CUtensorMap hi, lo;
   const int rows_lo = (int)(N / geo.ctas);
   if (!encode_map(&hi, codes, N, K / 4, R) ||
-      !encode_map(&lo, codes, N, K / 4, rows_lo > 0 ? rows_lo : R) ||
-      !encode_map(&qm, q, M * (K / kGroup), kGroup, gs))
+      !encode_map(&lo, codes, N, K / 4, rows_lo > 0 ? rows_lo : R))
     return PQ2_ERR_LAUNCH;
   if (dots)
     return decode == kDecodeMaskPlanes
-               ? launch_m<kDecodeMaskPlanes, true>(mi, hi, lo, qm, p, smem, stream)
-               : launch_m<kDecodeAddXor, true>(mi, hi, lo, qm, p, smem, stream);
+               ? launch_m<kDecodeMaskPlanes, true>(mi, hi, lo, p, smem, stream)
+               : launch_m<kDecodeAddXor, true>(mi, hi, lo, p, smem, stream);
   return decode == kDecodeMaskPlanes
-             ? launch_m<kDecodeMaskPlanes, false>(mi, hi, lo, qm, p, smem, stream)
-             : launch_m<kDecodeAddXor, false>(mi, hi, lo, qm, p, smem, stream);
+             ? launch_m<kDecodeMaskPlanes, false>(mi, hi, lo, p, smem, stream)
+             : launch_m<kDecodeAddXor, false>(mi, hi, lo, p, smem, stream);
 }
 
 }  // namespace pq2
