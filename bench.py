@@ -18,6 +18,9 @@ replayed from CUDA graphs and timed with CUDA events on the launching stream.
   roofline    pq2_mmv alone: packed weight bytes K*N*34/128 per launch over
               its CUDA-event time per launch, against the measured HBM peak
   cpu_baseline the CPU oracle on the host cores, on a bounded sample
+  prefill     pq2_mm (and pq2_linear) on ffn_up K=5120 N=17408 at
+              M = 16 .. 4096: microseconds, TOPS and the fraction of the
+              measured dense 16-bit tensor peak
 
 `--impl reference` times the CPU oracle on the same workload instead (the
 reference arm of this comparison).
@@ -40,6 +43,7 @@ sys.path.insert(0, ROOT)
 METRIC = ("µs/call and HBM GB/s (frac of peak) for ternary×INT8 matmul at "
           "M=1–8; prefill TOPS")
 K_DIM, N_DIM, MS = 5120, 10240, (1, 2, 3, 4)
+PREFILL_K, PREFILL_N, PREFILL_MS = 5120, 17408, (16, 128, 512, 2048, 4096)
 WORKLOAD = ("attn_qkv K=5120 N=10240, M=1,2,3,4 per step (quantise + GEMV each); ternary "
             "codes U{0,1,2}, fp16 group-128 scales U[0.005,0.05]; bf16 x N(0,1) with 1% "
             "channels x20; fp32 accumulate, bf16 out")
@@ -53,6 +57,17 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def measured_tensor_peak():
+    """Dense 16-bit tensor peak in TFLOP/s (fp16 and bf16 run at one rate)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
 
 
 class ClockSampler:
@@ -183,6 +198,64 @@ def cpu_baseline_sample(budget_s=12.0):
     return {"value": round(dt / calls * 1e6, 3), "unit": "us/call", "cores": 1,
             "kind": "oracle",
             "sample": f"{calls} complete attn_qkv calls (M=1..4 cycled) in {dt:.1f} s"}
+
+
+def prefill_leg(args, dev, stream, timed, capture):
+    """Prefill: ffn_up (K=5120, N=17408) at M = 16 .. 4096 through pq2_mm
+    (kernel only, on pre-quantised fp16 activations) and pq2_linear
+    (quantise + GEMM); 8 rotated weight matrices (190 MB, above the L2
+    size).  TOPS = 2*M*N*K / time; the fraction is of the measured dense
+    16-bit tensor peak, the rate of the tensor-core kind the kernel uses."""
+    import torch
+    from ternary_weight_int8_gb300 import pq2, synth
+    lib = pq2.lib()
+    K, N, nm = PREFILL_K, PREFILL_N, 8
+    mats = []
+    for i in range(nm):
+        raw = synth.raw_weights(N, K, seed=5000 + i, device=dev)
+        mats.append(pq2.pq2_prepare(raw, K))
+        del raw
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sp = stream.cuda_stream
+    peak, kind = measured_tensor_peak()
+    out = {"workload": f"ffn_up K={K} N={N}, bf16 x N(0,1), bf16 out, {nm} rotated matrices",
+           "peak_tflops": peak, "peak_source": kind, "by_m": {}}
+    for M in PREFILL_MS:
+        x = synth.activations(M, K, seed=900 + M, device=dev)
+        q, sx, qs = pq2.pq2_quantize_act(x, pq2.PQ2_Q_F16)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(pq2.linear_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
+
+        def mm_calls():
+            for c, sc in mats:
+                st = lib.pq2_mm(q.data_ptr(), sx.data_ptr(), qs.data_ptr(), c.data_ptr(),
+                                sc.data_ptr(), y.data_ptr(), pq2.PQ2_BF16, M, N, K,
+                                status.data_ptr(), sp)
+                if st:
+                    raise RuntimeError(f"pq2_mm failed ({st})")
+
+        def linear_calls():
+            for c, sc in mats:
+                st = lib.pq2_linear(x.data_ptr(), pq2.PQ2_BF16, K, M, N, K, c.data_ptr(),
+                                    sc.data_ptr(), y.data_ptr(), pq2.PQ2_BF16, ws.data_ptr(),
+                                    ws.numel(), status.data_ptr(), sp)
+                if st:
+                    raise RuntimeError(f"pq2_linear failed ({st})")
+
+        reps = max(3, min(50, 20000 // M))
+        k_ms = timed([capture(mm_calls)], reps, 3) / (reps * nm)
+        c_ms = timed([capture(linear_calls)], reps, 3) / (reps * nm)
+        tops = 2.0 * M * N * K / (k_ms * 1e-3) / 1e12
+        out["by_m"][str(M)] = {"mm_us": round(k_ms * 1e3, 2), "mm_tflops": round(tops, 1),
+                               "frac": round(tops / peak, 3),
+                               "complete_us": round(c_ms * 1e3, 2),
+                               "complete_tflops": round(2.0 * M * N * K / (c_ms * 1e-3) / 1e12, 1)}
+        del x, q, sx, qs, y, ws
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    del mats
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args):
@@ -331,6 +404,7 @@ def run_ours(args):
             "mmv_gbs": round(wbytes / (k_ms * 1e-3) / 1e9, 1),
             "mmv_frac": round(wbytes / (k_ms * 1e-3) / 1e9 / peak, 3),
         }
+    prefill = prefill_leg(args, dev, stream, timed, capture) if not args.no_prefill else None
     # dominant kernel: pq2_mmv over the step's M mix, kernel-only
     mean_k_us = statistics.mean(per_m[str(M)]["mmv_us"] for M in MS)
     achieved = wbytes / (mean_k_us * 1e-6) / 1e9
@@ -356,6 +430,7 @@ def run_ours(args):
                      "kernel": "pq2_mmv", "peak_source": peak_kind,
                      "bytes_per_launch": wbytes},
         "per_m": per_m,
+        "prefill": prefill,
         "clocks": clocks.summary(),
     }
     if rank == 0 and not args.no_cpu:
@@ -374,6 +449,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill (pq2_mm) leg")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
