@@ -442,6 +442,37 @@ def run_ours(args):
     return 0
 
 
+def run_profile_case(args):
+    """A short fixed sequence for an ncu capture: the attn_qkv GEMV
+    (pq2_mmv, INDEPENDENT calls over 8 rotated matrices) or the ffn_up prefill
+    GEMM (pq2_mm), at --profile-m columns; 3 warm-up calls then 3 calls."""
+    import torch
+    from ternary_weight_int8_gb300 import pq2, synth
+    dev = torch.device("cuda", 0)
+    M = args.profile_m
+    if args.profile_case == "mmv":
+        K, N, nm = K_DIM, N_DIM, 8
+        layout = pq2.PQ2_Q_PLANES
+    else:
+        K, N, nm = PREFILL_K, PREFILL_N, 2
+        layout = pq2.PQ2_Q_F16
+    mats = [pq2.pq2_prepare(synth.raw_weights(N, K, seed=7000 + i, device=dev), K)
+            for i in range(nm)]
+    x = synth.activations(M, K, seed=11, device=dev, outlier_frac=0.01)
+    q, sx, qs = pq2.pq2_quantize_act(x, layout)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    for i in range(6):
+        c, sc = mats[i % nm]
+        if args.profile_case == "mmv":
+            pq2.pq2_mmv(q, sx, qs, c, sc, y=y, flags=pq2.PQ2_MMV_INDEPENDENT)
+        else:
+            pq2.pq2_mm(q, sx, qs, c, sc, y=y)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": args.profile_case, "M": M, "N": N, "K": K,
+                      "launches": 6, "ok": True}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -450,9 +481,14 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill (pq2_mm) leg")
+    ap.add_argument("--profile-case", choices=["mmv", "mm"], default=None,
+                    help="run a short fixed call sequence for an ncu capture and exit")
+    ap.add_argument("--profile-m", type=int, default=1, help="columns for --profile-case")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.profile_case:
+        return run_profile_case(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
