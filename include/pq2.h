@@ -197,6 +197,30 @@ int pq2_linear(const void *x, int x_dtype, int64_t ldx, int64_t M, int64_t N,
  * shape is invalid). */
 size_t pq2_linear_workspace_bytes(int64_t M, int64_t K);
 
+/* Size of the static device scratch of pq2_linear_static (1 MiB). */
+#define PQ2_STATIC_SCRATCH_BYTES ((size_t)1 << 20)
+
+/* pq2_linear_static — pq2_linear for callers that cannot allocate device
+ * memory.  The pages have no counterpart: this is a deployment convenience,
+ * not a step of the method.  The call allocates nothing (no cudaMalloc,
+ * cudaFree or allocating library routine): its workspace (q, s_x and sum(q),
+ * laid out as for pq2_linear) is a file-scope static device array of
+ * PQ2_STATIC_SCRATCH_BYTES per device, whose address is looked up once per
+ * device (on the first call with that device current).
+ *   Arguments, results and errors as for pq2_linear, without the workspace.
+ *   Returns PQ2_ERR_SHAPE, before any CUDA call, when
+ *   pq2_linear_workspace_bytes(M, K) exceeds PQ2_STATIC_SCRATCH_BYTES (for
+ *   example M = 8 with K above 123,264, or M = 16 with K above 31,744);
+ *   PQ2_ERR_CUDA if the scratch address cannot be obtained.
+ * Every call on a device shares the one scratch array.  Nothing in it needs
+ * to start at zero: each call writes all of it that it reads.  Calls that may
+ * run at the same time on the GPU (for example on two streams) race on it;
+ * calls in order on one stream do not. */
+int pq2_linear_static(const void *x, int x_dtype, int64_t ldx, int64_t M,
+                      int64_t N, int64_t K, const uint8_t *codes,
+                      const uint16_t *scales, void *y, int y_dtype,
+                      int32_t *dev_status, void *stream);
+
 /* The decoder pq2_mmv uses for M columns (host only). */
 int pq2_mmv_decoder(int64_t M);
 

@@ -28,6 +28,7 @@ PQ2_Q_ROWS, PQ2_Q_PLANES, PQ2_Q_F16 = 0, 1, 2
 PQ2_DECODE_ADDXOR, PQ2_DECODE_PLANES = 0, 1
 PQ2_PATH_MMV_ADDXOR, PQ2_PATH_MM, PQ2_PATH_MMV_PLANES = 0, 1, 2
 PQ2_MMV_OVERLAP_WEIGHTS, PQ2_MMV_INDEPENDENT = 1, 2
+PQ2_STATIC_SCRATCH_BYTES = 1 << 20
 GROUP = 128
 
 # C signatures, mirroring include/pq2.h.
@@ -42,6 +43,7 @@ SIGNATURES = {
     "pq2_mmv_ex": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _I, _P, _P]),
     "pq2_linear": (_I, [_P, _I, _I64, _I64, _I64, _I64, _P, _P, _P, _I, _P, _SZ, _P, _P]),
     "pq2_linear_workspace_bytes": (_SZ, [_I64, _I64]),
+    "pq2_linear_static": (_I, [_P, _I, _I64, _I64, _I64, _I64, _P, _P, _P, _I, _P, _P]),
     "pq2_mmv_decoder": (_I, [_I64]),
     "pq2_mm": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P]),
     "pq2_debug_group_dots": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P, _P, _P]),
