@@ -44,6 +44,10 @@ METRIC = ("µs/call and HBM GB/s (frac of peak) for ternary×INT8 matmul at "
           "M=1–8; prefill TOPS")
 K_DIM, N_DIM, MS = 5120, 10240, (1, 2, 3, 4)
 PREFILL_K, PREFILL_N, PREFILL_MS = 5120, 17408, (16, 128, 512, 2048, 4096)
+# DRAM bytes (read + write) per pq2_mmv launch on attn_qkv, from the ncu
+# captures in profiles/pq2_mmv_attn_qkv_full.md (mean of M=1 and M=4);
+# None once the kernel changes after that capture.
+MMV_TRAFFIC_BYTES = (13_965_568 + 13_988_608) // 2
 WORKLOAD = ("attn_qkv K=5120 N=10240, M=1,2,3,4 per step (quantise + GEMV each); ternary "
             "codes U{0,1,2}, fp16 group-128 scales U[0.005,0.05]; bf16 x N(0,1) with 1% "
             "channels x20; fp32 accumulate, bf16 out")
@@ -426,7 +430,8 @@ def run_ours(args):
                 "d2h_bytes_per_step": sum(M * N_DIM * 2 for M in MS)},
         "gpu_launches": 2 * len(MS) * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 3), "traffic": None,
+                     "unit": "GB/s", "frac": round(achieved / peak, 3),
+                     "traffic": MMV_TRAFFIC_BYTES,
                      "kernel": "pq2_mmv", "peak_source": peak_kind,
                      "bytes_per_launch": wbytes},
         "per_m": per_m,
