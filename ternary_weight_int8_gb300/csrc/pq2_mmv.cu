@@ -70,6 +70,7 @@ struct MmvParams {
   int overlap;            // 1: stream weights before the grid dependency
                           // resolves; 2: stream every input before it
   int sw_bulk;            // weight-scale slab arrives by one bulk copy (G % 8 == 0)
+  int side16;             // s_x and sum(q) copied in 16-byte pieces (aligned)
 };
 
 // Batched global -> shared copy of `count` 16-bit values by `threads`
@@ -109,9 +110,8 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
-               : "memory");
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
@@ -314,17 +314,26 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
     auto issue_inputs = [&](int i) {
       const int slot = i % p.ring;
       const int g0 = i * Gs, nb = min(Gs, G - g0);
-      uint8_t* st = ring + (size_t)slot * p.stage_bytes + p.q_off;
-      const int chunks = M * nb * 8;
-      for (int idx = lane; idx < chunks; idx += 32) {
-        const int m = idx / (nb * 8), rem = idx - m * nb * 8, l = rem >> 3, c = rem & 7;
-        cp_async16(st + m * p.qbox_stride + l * kGroup + ((c ^ (l & 7)) << 4),
-                   p.q + ((size_t)m * G + g0 + l) * kGroup + c * 16);
-      }
+      const uint32_t dst0 = smem_u32(ring) + slot * p.stage_bytes + p.q_off;
+      const int8_t* src0 = p.q + (size_t)g0 * kGroup;
+      // Lane = 16-byte chunk c of row l of a block of four group rows; no
+      // division in the address arithmetic.
+      const int c = lane & 7;
+      for (int m = 0; m < M; ++m)
+        for (int l = lane >> 3; l < nb; l += 4)
+          cp_async16(dst0 + m * p.qbox_stride + l * kGroup + ((c ^ (l & 7)) << 4),
+                     src0 + ((size_t)m * G + l) * kGroup + c * 16);
       if (i == 0) {
-        for (int idx = lane; idx < M * G; idx += 32) {
-          if (!DOTS) cp_async4(sx_s + idx, p.sx + idx);
-          if (need_qs) cp_async4(qs_s + idx, p.qsum + idx);
+        if (p.side16) {
+          for (int idx = 4 * lane; idx < M * G; idx += 128) {
+            if (!DOTS) cp_async16(smem_u32(sx_s + idx), p.sx + idx);
+            if (need_qs) cp_async16(smem_u32(qs_s + idx), p.qsum + idx);
+          }
+        } else {
+          for (int idx = lane; idx < M * G; idx += 32) {
+            if (!DOTS) cp_async4(sx_s + idx, p.sx + idx);
+            if (need_qs) cp_async4(qs_s + idx, p.qsum + idx);
+          }
         }
       }
       cp_async_mbar_arrive(&full[slot]);
@@ -620,6 +629,8 @@ int launch_mmv(const int8_t* q, const float* sx, const int32_t* qsum, const uint
   p.overlap = overlap;
   p.y_bf16 = y_dtype == PQ2_BF16;
   p.sw_bulk = (K / kGroup) % 8 == 0 && reinterpret_cast<uintptr_t>(scales) % 16 == 0;
+  p.side16 = (M * (K / kGroup)) % 4 == 0 && reinterpret_cast<uintptr_t>(sx) % 16 == 0 &&
+             reinterpret_cast<uintptr_t>(qsum) % 16 == 0;
   const int mi = (int)M, R = geo.rows_max, S = geo.splits, G = p.G;
   const int unit = 4 * S / gcd(4, S);
   p.box_stride = align_up(R * kBoxBytes, 1024);
