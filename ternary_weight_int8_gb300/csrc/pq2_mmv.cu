@@ -61,6 +61,7 @@ struct MmvParams {
   int ctas, splits, rows_max, stages_total, ring;
   int cons_threads;
   int stage_groups;       // Gs: groups per stage (a multiple of 4 and of S)
+  int groups_per_thread;  // Gs / S when that is 1 or 2 (S >= 4), else 0
   int box_stride;         // bytes per box in shared memory (1024-aligned)
   int stage_bytes;        // boxes + q region
   int q_off;              // q region inside a stage
@@ -340,12 +341,15 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[slot]);
     };
+    // Stages that fit the ring go out at once: each stage's weights and then
+    // its inputs (an independent call), or every stage's weights now and the
+    // inputs once the grid dependency resolves (weights-only overlap).
     const int pre = p.overlap ? min(p.ring, p.stages_total) : 0;
-    for (int i = 0; i < pre; ++i) issue_weights(i);
-    if (independent)
-      for (int i = 0; i < pre; ++i) issue_inputs(i);
-    else
-      grid_dep_wait();
+    for (int i = 0; i < pre; ++i) {
+      issue_weights(i);
+      if (independent) issue_inputs(i);
+    }
+    if (!independent) grid_dep_wait();
     for (int i = 0; i < p.stages_total; ++i) {
       if (i < pre) {
         if (!independent) issue_inputs(i);
@@ -423,44 +427,61 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
     }
   };
 
+  // One group of the stage at shared address st_s: its dots for every
+  // column, scaled and accumulated.
+  auto do_group = [&](uint32_t st_s, int l, int g) {
+    const int lo = (l & 3) * 32;  // logical byte offset of the group in the box row
+    uint32_t c0[RP], c1[RP];
+#pragma unroll
+    for (int r = 0; r < RP; ++r) {
+      // 128-byte swizzle of the code boxes: 16-byte chunk ^= row % 8
+      const uint32_t rowa = st_s + (l >> 2) * p.box_stride + rows[r] * kBoxBytes;
+      const int sw = (rows[r] & 7) << 4;
+      c0[r] = rowa + (lo ^ sw);
+      c1[r] = rowa + ((lo + 16) ^ sw);
+    }
+    const uint32_t qz = st_s + p.q_off + l * kGroup;
+    const int qsw = (l & 7) << 4;
+    // Columns in blocks of at most four keep the accumulators in registers.
+    constexpr int MA = M <= 4 ? M : 4;
+    {
+      int dot[RP][MA];
+      group_dot<MA, RP, DEC>(c0, c1, qz, p.qbox_stride, qsw, qs_base + g * 4, G * 4, dot);
+      consume(dot, 0, g);
+    }
+    if constexpr (M > 4) {
+      int dot[RP][M - 4];
+      group_dot<M - 4, RP, DEC>(c0, c1, qz + 4 * p.qbox_stride, p.qbox_stride, qsw,
+                                qs_base + (4 * G + g) * 4, G * 4, dot);
+      consume(dot, 4, g);
+    }
+  };
+
+  // A thread's groups in a stage are z + j*S for j < Gs/S.  The geometry
+  // makes that count 1 or 2 whenever S >= 4, and those cases run as
+  // straight-line code (a run-time loop here measurably slows the latency-
+  // bound stage); smaller S (tiny K) takes the general loop.
+  const int gpt = p.groups_per_thread;
+  const bool recycle = p.stages_total > p.ring;
   for (int i = 0; i < p.stages_total; ++i) {
     const int slot = i % p.ring;
     ok = ok && mbar_wait(&full[slot], (i / p.ring) & 1);
     const uint32_t st_s = ring_s + slot * p.stage_bytes;
     const int g0 = i * Gs;
     if (active && ok) {
-      for (int l = z; l < Gs; l += S) {
-        const int g = g0 + l;
-        if (g >= G) break;
-        const int lo = (l & 3) * 32;  // logical byte offset of the group in the box row
-        uint32_t c0[RP], c1[RP];
-#pragma unroll
-        for (int r = 0; r < RP; ++r) {
-          // 128-byte swizzle of the code boxes: 16-byte chunk ^= row % 8
-          const uint32_t rowa = st_s + (l >> 2) * p.box_stride + rows[r] * kBoxBytes;
-          const int sw = (rows[r] & 7) << 4;
-          c0[r] = rowa + (lo ^ sw);
-          c1[r] = rowa + ((lo + 16) ^ sw);
-        }
-        const uint32_t qz = st_s + p.q_off + l * kGroup;
-        const int qsw = (l & 7) << 4;
-        // Columns in blocks of at most four keep the accumulators in registers.
-        constexpr int MA = M <= 4 ? M : 4;
-        {
-          int dot[RP][MA];
-          group_dot<MA, RP, DEC>(c0, c1, qz, p.qbox_stride, qsw, qs_base + g * 4, G * 4, dot);
-          consume(dot, 0, g);
-        }
-        if constexpr (M > 4) {
-          int dot[RP][M - 4];
-          group_dot<M - 4, RP, DEC>(c0, c1, qz + 4 * p.qbox_stride, p.qbox_stride, qsw,
-                                    qs_base + (4 * G + g) * 4, G * 4, dot);
-          consume(dot, 4, g);
-        }
+      if (gpt == 1) {
+        if (g0 + z < G) do_group(st_s, z, g0 + z);
+      } else if (gpt == 2) {
+        if (g0 + z < G) do_group(st_s, z, g0 + z);
+        if (g0 + z + S < G) do_group(st_s, z + S, g0 + z + S);
+      } else {
+        for (int l = z; l < Gs && g0 + l < G; l += S) do_group(st_s, l, g0 + l);
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
+    if (recycle) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+    }
   }
   if (!ok && lane == 0) report(p.status, PQ2_ERR_TIMEOUT);
   if constexpr (!DOTS) {
@@ -644,10 +665,21 @@ int launch_mmv(const int8_t* q, const float* sx, const int32_t* qsum, const uint
   auto stage_bytes = [&](int gs) {
     return (gs / 4) * p.box_stride + mi * align_up(gs * kGroup, 1024);
   };
-  int gs = unit;
-  while (gs + unit <= std::max(unit, (G + 3) / 4 * 4) && stage_bytes(gs + unit) <= 24 * 1024 &&
-         stage_bytes(gs + unit) * 3 <= room)
-    gs += unit;
+  // Stage: S groups (S >= 8) or 8 groups (S = 4), so that a thread meets one
+  // or two groups per stage; smaller S (tiny K) grows the stage by units of
+  // lcm(4, S) groups towards ~16-24 KB of codes.
+  int gs;
+  if (S >= 4) {
+    gs = S >= 8 ? S : 8;
+    if (stage_bytes(gs) * 3 > room && S == 4) gs = 4;
+    p.groups_per_thread = gs / S;
+  } else {
+    gs = unit;
+    while (gs + unit <= std::max(unit, (G + 3) / 4 * 4) && stage_bytes(gs + unit) <= 24 * 1024 &&
+           stage_bytes(gs + unit) * 3 <= room)
+      gs += unit;
+    p.groups_per_thread = 0;
+  }
   p.stage_groups = gs;
   p.q_off = (gs / 4) * p.box_stride;
   p.qbox_stride = align_up(gs * kGroup, 1024);
