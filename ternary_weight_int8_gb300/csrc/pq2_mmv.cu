@@ -40,7 +40,7 @@
 namespace pq2 {
 namespace {
 
-constexpr int kMaxConsumerThreads = 352;
+constexpr int kMaxConsumerThreads = 288;
 constexpr int kRowsPerThread = 2;         // rows sharing each q load
 constexpr int kMaxBlock = kMaxConsumerThreads + 32;
 constexpr int kMaxSplits = 64;

@@ -143,7 +143,7 @@ def test_mmv_geometry(L, N, K, sms):
     G = K // 128
     assert 1 <= ctas and rows_max == -(-N // ctas)
     assert ctas <= max(sms, -(-N // 256)) and rows_max <= 256
-    assert threads % 32 == 0 and 32 <= threads <= 352
+    assert threads % 32 == 0 and 32 <= threads <= 288
     # each consumer thread owns two rows of one split
     pairs = -(-rows_max // 2)
     assert pairs * splits <= threads < pairs * splits + 32
