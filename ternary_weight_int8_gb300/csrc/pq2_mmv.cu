@@ -46,6 +46,7 @@ constexpr int kMaxBlock = kMaxConsumerThreads + 32;
 constexpr int kMaxSplits = 64;
 constexpr int kMaxBoxRows = 256;          // TMA box height limit
 constexpr int kSmemBudget = 110 * 1024;   // two CTAs per SM
+constexpr int kSoloSmem = 120 * 1024;     // one CTA per SM (dynamic request)
 constexpr int kMaxStages = 48;
 constexpr int kBoxBytes = 128;            // 4 groups of 32 code bytes
 
@@ -558,10 +559,10 @@ int launch_one(const CUtensorMap& hi, const CUtensorMap& lo,
   auto kern = mmv_kernel<M, DEC, DOTS>;
   static int configured = 0;  // largest dynamic smem size set so far
   if (smem > configured) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget + 1024) !=
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSoloSmem) !=
         cudaSuccess)
       return PQ2_ERR_LAUNCH;
-    configured = kSmemBudget + 1024;
+    configured = kSoloSmem;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.ctas);
@@ -687,7 +688,13 @@ int launch_mmv(const int8_t* q, const float* sx, const int32_t* qsum, const uint
   p.stages_total = (G + gs - 1) / gs;
   if (room < p.stage_bytes) return PQ2_ERR_SHAPE;
   p.ring = std::min(std::min(p.stages_total, room / p.stage_bytes), kMaxStages);
-  const int smem = 1024 + p.ring_off + p.ring * p.stage_bytes;  // + alignment slack
+  int smem = 1024 + p.ring_off + p.ring * p.stage_bytes;  // + alignment slack
+  // A call that waits for the kernel before it (weights-only overlap) takes
+  // a whole SM: more than half the shared memory keeps a second CTA of any
+  // grid off it.  Chained calls then fill each SM as its previous CTA
+  // leaves, one per SM, and a call's weights still stream in while the
+  // quantisation and the two grid hand-overs in front of it run.
+  if (overlap == 1) smem = std::max(smem, kSoloSmem);
 
   CUtensorMap hi, lo;
   const int rows_lo = (int)(N / geo.ctas);
