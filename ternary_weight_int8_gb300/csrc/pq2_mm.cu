@@ -54,6 +54,7 @@ constexpr int kThreads = (6 + kEpiWarps) * 32;
 constexpr int kEpiCols = BT / 4;  // tokens per epilogue thread
 constexpr int kDBuf = 2;          // D buffers in flight
 constexpr int kABuf = 4;          // decoded weight (A) buffers in flight
+constexpr int kDone = 8;          // group-completion barriers (> every reuse distance)
 constexpr int kQBytes = BT * kGroup * 2;       // 32 KB: q tile of one group (fp16)
 constexpr int kCBytes = BW * kGroupCodeBytes;  // 4 KB: code bytes of one group
 constexpr int kDCol = 0;                       // D buffers: columns [0, kDBuf*BT)
@@ -80,7 +81,7 @@ constexpr int kSwBytes = BW * kGC * 2;
 constexpr int kSBytes = kSxBytes + kSwBytes;
 constexpr int kOffS = kOffC + kStagesC * kCBytes;
 constexpr int kOffBar = kOffS + 2 * kSBytes;
-constexpr int kNumBars = 2 * kStagesQ + 2 * kStagesC + 2 * kABuf + 2 * kDBuf + 4;
+constexpr int kNumBars = kStagesQ + 2 * kStagesC + kABuf + kDone + kDBuf + 4;
 constexpr int kOffTmemAddr = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffTmemAddr + 16 + 1024;  // + alignment slack
 
@@ -201,13 +202,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* q_full = bars;
-  uint64_t* q_empty = q_full + kStagesQ;
-  uint64_t* c_full = q_empty + kStagesQ;
+  uint64_t* c_full = q_full + kStagesQ;
   uint64_t* c_empty = c_full + kStagesC;
   uint64_t* a_full = c_empty + kStagesC;
-  uint64_t* a_empty = a_full + kABuf;
-  uint64_t* d_full = a_empty + kABuf;
-  uint64_t* d_empty = d_full + kDBuf;
+  uint64_t* g_done = a_full + kABuf;   // kDone: group g's MMAs are complete
+  uint64_t* d_empty = g_done + kDone;
   uint64_t* s_full = d_empty + kDBuf;
   uint64_t* s_empty = s_full + 2;
   uint32_t* tmem_addr_s = reinterpret_cast<uint32_t*>(smem + kOffTmemAddr);
@@ -217,22 +216,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   // (no L2 hot spot) and share a few weight tiles.
   const int m0 = blockIdx.x * BT, n0 = blockIdx.y * BW;
   const int G = p.G;
+  // Wait until group j's MMAs are complete (ring of kDone barriers, one
+  // phase per kDone groups; no waiter lags the MMA by kDone groups).
+  auto done_wait = [&](int j) { return mbar_wait(&g_done[j % kDone], (j / kDone) & 1); };
 
   if (tid == 0) {
-    for (int i = 0; i < kStagesQ; ++i) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
+    for (int i = 0; i < kStagesQ; ++i) mbar_init(&q_full[i], 1);
+    for (int i = 0; i < kDone; ++i) mbar_init(&g_done[i], 1);
     for (int i = 0; i < kStagesC; ++i) { mbar_init(&c_full[i], 1); mbar_init(&c_empty[i], 4); }
-    for (int i = 0; i < kABuf; ++i) {
-      mbar_init(&a_full[i], 4);
-      mbar_init(&a_empty[i], 1);
-    }
+    for (int i = 0; i < kABuf; ++i) mbar_init(&a_full[i], 4);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 32);
       mbar_init(&s_empty[i], kEpiWarps);
     }
-    for (int i = 0; i < kDBuf; ++i) {
-      mbar_init(&d_full[i], 1);
-      mbar_init(&d_empty[i], kEpiWarps);
-    }
+    for (int i = 0; i < kDBuf; ++i) mbar_init(&d_empty[i], kEpiWarps);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -298,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (g >= kStagesC) ok = ok && mbar_wait(&c_empty[sc], ((g / kStagesC) - 1) & 1);
         mbar_arrive_expect_tx(&c_full[sc], kCBytes);
         tma_2d(smem + kOffC + sc * kCBytes, &map_c, g * kGroupCodeBytes, n0, &c_full[sc]);
-        if (g >= kStagesQ) ok = ok && mbar_wait(&q_empty[sq], ((g / kStagesQ) - 1) & 1);
+        if (g >= kStagesQ) ok = ok && done_wait(g - kStagesQ);
         uint8_t* qs = smem + kOffQ + sq * kQBytes;
         mbar_arrive_expect_tx(&q_full[sq], kQBytes);
         tma_2d(qs, &map_q, g * kGroup, m0, &q_full[sq]);
@@ -316,22 +313,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = ok && mbar_wait(&q_full[sq], (g / kStagesQ) & 1);
         if (g >= kDBuf) ok = ok && mbar_wait(&d_empty[db], ((g / kDBuf) - 1) & 1);
         tc_fence_after();
-        const uint32_t q_base = smem_u32(smem + kOffQ + sq * kQBytes);
+        // One thread issues every MMA: between two MMAs of a group it does
+        // only an add, so the tensor pipe never waits on descriptor math;
+        // one commit per group tells the q producer, the decoders and the
+        // epilogue alike (each commit costs the pipe time).
+        const uint64_t qd = smem_desc_sw128(smem_u32(smem + kOffQ + sq * kQBytes));
         const uint32_t d_tmem = tmem_base + kDCol + db * BT;
         const uint32_t a_tmem = tmem_base + kACol + b * 64;  // b = g % kABuf
         if (ok) {
 #pragma unroll
           for (int k = 0; k < kGroup / 16; ++k) {
             // K step k: A columns 8k..8k+7; B 64-column atom k/4, 32-byte
-            // offset (k%4) inside the 128-byte swizzled row.
-            const uint32_t boff = (k >> 2) * (BT * 128) + (k & 3) * 32;
-            mma_f16_ta(d_tmem, a_tmem + 8 * k, smem_desc_sw128(q_base + boff), idesc,
-                       k > 0 ? 1u : 0u);
+            // offset (k%4) inside the 128-byte swizzled row (start-address
+            // field, in 16-byte units, of the descriptor).
+            const uint64_t boff16 = (uint64_t)(((k >> 2) * (BT * 128) + (k & 3) * 32) >> 4);
+            mma_f16_ta(d_tmem, a_tmem + 8 * k, qd + boff16, idesc, k > 0 ? 1u : 0u);
           }
         }
-        mma_commit(&q_empty[sq]);
-        mma_commit(&a_empty[b]);
-        mma_commit(&d_full[db]);
+        mma_commit(&g_done[g % kDone]);
       }
     }
   } else if (warp >= 2 && warp < 6) {
@@ -342,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int g = 0; g < G; ++g) {
       const int sc = g % kStagesC, b = g % kABuf;
       ok = ok && mbar_wait(&c_full[sc], (g / kStagesC) & 1);
-      if (g >= kABuf) ok = ok && mbar_wait(&a_empty[b], ((g / kABuf) - 1) & 1);
+      if (g >= kABuf) ok = ok && done_wait(g - kABuf);
       tc_fence_after();
       const uint8_t* cs = smem + kOffC + sc * kCBytes + row * kGroupCodeBytes;
       const uint4 c0 = *reinterpret_cast<const uint4*>(cs);
@@ -385,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g = ch * kGC + gg;
         if (g >= G) break;
         const int db = g % kDBuf;
-        ok = ok && mbar_wait(&d_full[db], (g / kDBuf) & 1);
+        ok = ok && done_wait(g);
         tc_fence_after();
         const float* sxg = sxs + gg * BT + col0;
         const float sw = __half2float(sws[row * kGC + gg]);
