@@ -50,7 +50,8 @@ constexpr int kStagesQ = 6;      // q tile stages
 constexpr int kStagesC = 4;      // code tile stages
 constexpr int kGC = 4;           // groups per scale chunk
 constexpr int kEpiWarps = 16;     // warps 6-21: four per TMEM lane quarter
-constexpr int kThreads = (6 + kEpiWarps) * 32;
+constexpr int kSchedWarp = 6 + kEpiWarps;  // warp 22: waits on the MMA's inputs
+constexpr int kThreads = (7 + kEpiWarps) * 32;
 constexpr int kEpiCols = BT / 4;  // tokens per epilogue thread
 constexpr int kDBuf = 2;          // D buffers in flight
 constexpr int kABuf = 4;          // decoded weight (A) buffers in flight
@@ -179,18 +180,27 @@ __host__ __device__ constexpr uint32_t instr_desc_f16(int m, int n) {
 
 // Eight fp16x2 words of one code word w, in the operand K order: word
 // j = 2s + pb holds the weights c - 1 of (byte pb, field s) and (byte pb + 2,
-// field s), i.e. weights 4pb + s and 4(pb + 2) + s.  The halves 0x6400 | c
-// are exactly 1024 + c; subtracting 1025 (one HSUB2) is exact.
+// field s), i.e. weights 4pb + s and 4(pb + 2) + s.  Field s masked in place
+// and OR-ed with 0x6400 gives the fp16 value 1024 + c * 4^s exactly (the
+// field sits in the low mantissa bits); one HFMA2 by 4^-s with the bias
+// -(1024 * 4^-s + 1), both exact in fp16, leaves exactly c - 1.  Bytes 1 and
+// 3 come from one shift by 8, so a word costs 1 SHF + 8 LOP3 + 8 HFMA2.
 __device__ __forceinline__ void decode_word(uint32_t w, uint32_t* out) {
-  const __half2 k1025 = __halves2half2(__ushort_as_half(0x6401), __ushort_as_half(0x6401));
+  // fp16 bit patterns: 1, 1/4, 1/16, 1/64 and -1025, -257, -65, -17
+  constexpr uint16_t kScale[4] = {0x3C00, 0x3400, 0x2C00, 0x2400};
+  constexpr uint16_t kBias[4] = {0xE401, 0xDC04, 0xD410, 0xCC40};
+  const uint32_t w8 = w >> 8;
 #pragma unroll
-  for (int s = 0; s < 4; ++s)
+  for (int s = 0; s < 4; ++s) {
+    const __half2 sc = __halves2half2(__ushort_as_half(kScale[s]), __ushort_as_half(kScale[s]));
+    const __half2 bi = __halves2half2(__ushort_as_half(kBias[s]), __ushort_as_half(kBias[s]));
 #pragma unroll
     for (int pb = 0; pb < 2; ++pb) {
-      const uint32_t u = ((w >> (2 * s + 8 * pb)) & 0x00030003u) | 0x64006400u;
-      const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&u), k1025);
+      const uint32_t u = ((pb ? w8 : w) & (0x00030003u << (2 * s))) | 0x64006400u;
+      const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&u), sc, bi);
       out[2 * s + pb] = *reinterpret_cast<const uint32_t*>(&r);
     }
+  }
 }
 
 template <bool DOTS>
@@ -305,33 +315,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
-      constexpr uint32_t idesc = instr_desc_f16(BW, BT);
-      for (int g = 0; g < G; ++g) {
+    // The issuing thread touches no shared memory and no mbarrier while its
+    // MMAs run: such an access waits for the MMAs in flight, which left the
+    // tensor pipe idle between groups.  The scheduler warp does the waiting;
+    // the two warps meet once per group at named barrier 1.
+    constexpr uint32_t idesc = instr_desc_f16(BW, BT);
+    for (int g = 0; g < G; ++g) {
+      named_bar_sync(1, 64);
+      if (lane == 0) {
         const int sq = g % kStagesQ, b = g % kABuf, db = g % kDBuf;
-        ok = ok && mbar_wait(&a_full[b], (g / kABuf) & 1);
-        ok = ok && mbar_wait(&q_full[sq], (g / kStagesQ) & 1);
-        if (g >= kDBuf) ok = ok && mbar_wait(&d_empty[db], ((g / kDBuf) - 1) & 1);
         tc_fence_after();
-        // One thread issues every MMA: between two MMAs of a group it does
-        // only an add, so the tensor pipe never waits on descriptor math;
-        // one commit per group tells the q producer, the decoders and the
-        // epilogue alike (each commit costs the pipe time).
+        // Between two MMAs of a group only an add: the descriptor's start
+        // address field is in 16-byte units.
         const uint64_t qd = smem_desc_sw128(smem_u32(smem + kOffQ + sq * kQBytes));
         const uint32_t d_tmem = tmem_base + kDCol + db * BT;
         const uint32_t a_tmem = tmem_base + kACol + b * 64;  // b = g % kABuf
-        if (ok) {
 #pragma unroll
-          for (int k = 0; k < kGroup / 16; ++k) {
-            // K step k: A columns 8k..8k+7; B 64-column atom k/4, 32-byte
-            // offset (k%4) inside the 128-byte swizzled row (start-address
-            // field, in 16-byte units, of the descriptor).
-            const uint64_t boff16 = (uint64_t)(((k >> 2) * (BT * 128) + (k & 3) * 32) >> 4);
-            mma_f16_ta(d_tmem, a_tmem + 8 * k, qd + boff16, idesc, k > 0 ? 1u : 0u);
-          }
+        for (int k = 0; k < kGroup / 16; ++k) {
+          // K step k: A columns 8k..8k+7; B 64-column atom k/4, 32-byte
+          // offset (k%4) inside the 128-byte swizzled row.
+          const uint64_t boff16 = (uint64_t)(((k >> 2) * (BT * 128) + (k & 3) * 32) >> 4);
+          mma_f16_ta(d_tmem, a_tmem + 8 * k, qd + boff16, idesc, k > 0 ? 1u : 0u);
         }
+        // One commit per group tells the q producer, the decoders and the
+        // epilogue alike.
         mma_commit(&g_done[g % kDone]);
       }
+      __syncwarp();
+    }
+  } else if (warp == kSchedWarp) {
+    // ------------------------------------------------------------ scheduler
+    // Per group: A decoded (lane 0), q tile landed (lane 1), D buffer read
+    // by the epilogue (lane 2); then release the MMA warp.  Both warps run
+    // exactly G rounds of named barrier 1, whatever the waits return, so a
+    // wait that gives up (reported below) cannot leave the MMA warp stuck.
+    for (int g = 0; g < G; ++g) {
+      const int sq = g % kStagesQ, b = g % kABuf, db = g % kDBuf;
+      if (lane == 0) ok = ok && mbar_wait(&a_full[b], (g / kABuf) & 1);
+      if (lane == 1) ok = ok && mbar_wait(&q_full[sq], (g / kStagesQ) & 1);
+      if (lane == 2 && g >= kDBuf) ok = ok && mbar_wait(&d_empty[db], ((g / kDBuf) - 1) & 1);
+      tc_fence_before();
+      __syncwarp();
+      named_bar_sync(1, 64);
     }
   } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------------ decoders
