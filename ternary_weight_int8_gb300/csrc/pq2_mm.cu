@@ -122,6 +122,22 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
           smem_u32(bar))
       : "memory");
 }
+// Packed pairs of fp32 (element 0 in the low half): one instruction, two
+// IEEE round-to-nearest results, the same as two scalar operations.
+__device__ __forceinline__ uint64_t f2_pack(uint32_t lo, uint32_t hi) {
+  return ((uint64_t)hi << 32) | lo;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
@@ -395,9 +411,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = 32 * quarter + lane;
     const int n = n0 + row;
     const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
-    float acc[kEpiCols];
+    // Token pairs (2j, 2j+1) of the thread's columns, as packed fp32 pairs.
+    uint64_t acc2[kEpiCols / 2];
 #pragma unroll
-    for (int j = 0; j < kEpiCols; ++j) acc[j] = 0.0f;
+    for (int j = 0; j < kEpiCols / 2; ++j) acc2[j] = 0ull;
     const int nchunks = (G + kGC - 1) / kGC;
     for (int ch = 0; ch < nchunks; ++ch) {
       const int slot = ch & 1;
@@ -413,6 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const float* sxg = sxs + gg * BT + col0;
         const float sw = __half2float(sws[row * kGC + gg]);
+        const uint64_t sw2 = f2_pack(__float_as_uint(sw), __float_as_uint(sw));
         const uint32_t taddr = tmem_base + lane_base + kDCol + db * BT + col0;
 #pragma unroll
         for (int hh = 0; hh < kEpiCols / 16; ++hh) {
@@ -428,18 +446,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j4 = 0; j4 < 4; ++j4) {
             // four tokens' s_x per 16-byte broadcast load
-            const float4 xv = *reinterpret_cast<const float4*>(sxg + 16 * hh + 4 * j4);
-            const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
+            const uint4 xv = *reinterpret_cast<const uint4*>(sxg + 16 * hh + 4 * j4);
+            if (DOTS) {
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-              const int t = 16 * hh + 4 * j4 + jj;
-              const float dot = __uint_as_float(v[4 * j4 + jj]);  // exact integer group dot
-              if (DOTS) {
-                const int m = m0 + col0 + t;
+              for (int jj = 0; jj < 4; ++jj) {
+                const int m = m0 + col0 + 16 * hh + 4 * j4 + jj;
+                const float dot = __uint_as_float(v[4 * j4 + jj]);  // exact integer group dot
                 if (m < p.M && n < p.N) p.dots[((size_t)m * p.N + n) * G + g] = (int32_t)dot;
-              } else {
-                acc[t] = __fmaf_rn(__fmul_rn(dot, xa[jj]), sw, acc[t]);
               }
+            } else {
+              // acc += (dot * s_x) * s_w for two tokens per instruction
+              const int t2 = (16 * hh + 4 * j4) / 2;
+              const uint64_t x01 = f2_pack(xv.x, xv.y), x23 = f2_pack(xv.z, xv.w);
+              const uint64_t d01 = f2_pack(v[4 * j4], v[4 * j4 + 1]);
+              const uint64_t d23 = f2_pack(v[4 * j4 + 2], v[4 * j4 + 3]);
+              acc2[t2] = f2_fma(f2_mul(d01, x01), sw2, acc2[t2]);
+              acc2[t2 + 1] = f2_fma(f2_mul(d23, x23), sw2, acc2[t2 + 1]);
             }
           }
         }
@@ -451,12 +473,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int t = 0; t < kEpiCols; ++t) {
         const int m = m0 + col0 + t;
+        const float a = __uint_as_float((uint32_t)(acc2[t / 2] >> (32 * (t & 1))));
         if (m < p.M) {
           const size_t o = (size_t)m * p.N + n;
           if (p.y_bf16)
-            static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(acc[t]);
+            static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(a);
           else
-            static_cast<float*>(p.y)[o] = acc[t];
+            static_cast<float*>(p.y)[o] = a;
         }
       }
     }
