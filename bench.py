@@ -47,7 +47,7 @@ PREFILL_K, PREFILL_N, PREFILL_MS = 5120, 17408, (16, 128, 512, 2048, 4096)
 # DRAM bytes (read + write) per pq2_mmv launch on attn_qkv, from the ncu
 # captures in profiles/pq2_mmv_attn_qkv_full.md (mean of M=1 and M=4);
 # None once the kernel changes after that capture.
-MMV_TRAFFIC_BYTES = (13_982_464 + 14_026_752) // 2
+MMV_TRAFFIC_BYTES = (13_982_720 + 14_027_264) // 2
 WORKLOAD = ("attn_qkv K=5120 N=10240, M=1,2,3,4 per step (quantise + GEMV each); ternary "
             "codes U{0,1,2}, fp16 group-128 scales U[0.005,0.05]; bf16 x N(0,1) with 1% "
             "channels x20; fp32 accumulate, bf16 out")

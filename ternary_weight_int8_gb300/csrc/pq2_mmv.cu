@@ -377,18 +377,23 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
   bool ok = true;
   if (!DOTS && p.sw_bulk) ok = ok && mbar_wait(swbar, 0);
 
-  // Thread t owns split z = t % S and the RP rows RP*(t / S) ..; an odd
-  // row count leaves the last thread's second row a duplicate of row R-1,
+  // Thread t owns split z = t % S and the RP rows rb, rb + H, rb + 2H ..
+  // (rb = t / S, H = ceil(R / RP)).  A warp then reads code rows with
+  // consecutive indices, whose 128-byte swizzle keys (row % 8) differ in the
+  // low bit, so its 16-byte code loads spread over all eight chunk slots of
+  // a 128-byte line (rows 2rb, 2rb + 1 would leave half the slots, and the
+  // banks behind them, unused).  A row beyond R is a duplicate of row R-1,
   // computed but never stored.
   constexpr int RP = kRowsPerThread;
   const int z = tid % S;
   const int rb = tid / S;
+  const int H = (R + RP - 1) / RP;
   int rows[RP];
   bool valid[RP];
 #pragma unroll
   for (int r = 0; r < RP; ++r) {
-    valid[r] = rb * RP + r < R;
-    rows[r] = min(rb * RP + r, R - 1);
+    valid[r] = rb < H && rb + r * H < R;
+    rows[r] = min(rb + r * H, R - 1);
   }
   const bool active = valid[0];
   const uint32_t ring_s = smem_u32(ring), sw_base = smem_u32(sw_s);
@@ -666,12 +671,16 @@ int launch_mmv(const int8_t* q, const float* sx, const int32_t* qsum, const uint
   auto stage_bytes = [&](int gs) {
     return (gs / 4) * p.box_stride + mi * align_up(gs * kGroup, 1024);
   };
-  // Stage: S groups (S >= 8) or 8 groups (S = 4), so that a thread meets one
-  // or two groups per stage; smaller S (tiny K) grows the stage by units of
-  // lcm(4, S) groups towards ~16-24 KB of codes.
+  // Stage: 2S groups when two such stages fit the ring, else S (S >= 8), or
+  // 8 groups (S = 4), so that a thread meets one or two groups per stage.
+  // Two independent groups between stage waits keep more loads and dp4a in
+  // flight per warp (the warps of a CTA move through the stages together);
+  // measured 4-13 % faster than one at M = 1-2.  Smaller S (tiny K) grows
+  // the stage by units of lcm(4, S) groups towards ~16-24 KB of codes.
   int gs;
   if (S >= 4) {
     gs = S >= 8 ? S : 8;
+    if (S >= 8 && G >= 2 * S && 2 * stage_bytes(2 * S) <= room) gs = 2 * S;
     if (stage_bytes(gs) * 3 > room && S == 4) gs = 4;
     p.groups_per_thread = gs / S;
   } else {
