@@ -464,9 +464,9 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
   };
 
   // A thread's groups in a stage are z + j*S for j < Gs/S.  The geometry
-  // makes that count 1 or 2 whenever S >= 4, and those cases run as
-  // straight-line code (a run-time loop here measurably slows the latency-
-  // bound stage); smaller S (tiny K) takes the general loop.
+  // makes that count 1 or 2 whenever S >= 4; up to two columns those cases
+  // run as straight-line code (a run-time loop here measurably slows the
+  // latency-bound stage); smaller S (tiny K) takes the general loop.
   const int gpt = p.groups_per_thread;
   const bool recycle = p.stages_total > p.ring;
   for (int i = 0; i < p.stages_total; ++i) {
@@ -475,7 +475,13 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
     const uint32_t st_s = ring_s + slot * p.stage_bytes;
     const int g0 = i * Gs;
     if (active && ok) {
-      if (gpt == 1) {
+      if constexpr (M >= 3) {
+        // One copy of the (large) group code: with three copies, instruction
+        // fetch stalled these kernels, above all when calls of different M
+        // alternate (measured 8-12 % per call).
+#pragma unroll 1
+        for (int l = z; l < Gs && g0 + l < G; l += S) do_group(st_s, l, g0 + l);
+      } else if (gpt == 1) {
         if (g0 + z < G) do_group(st_s, z, g0 + z);
       } else if (gpt == 2) {
         if (g0 + z < G) do_group(st_s, z, g0 + z);
