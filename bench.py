@@ -13,8 +13,10 @@ the L2 size in total) rotate, so weights always stream from HBM.  Steps are
 replayed from CUDA graphs and timed with CUDA events on the launching stream.
 
   value       mean microseconds per complete call over the step (device time)
-  e2e         the same through host buffers: pinned host x -> device, the
-              calls, device -> pinned host y, all inside the timed region
+  e2e         the same through host buffers, all inside the timed region:
+              per step one copy of the step's x (M = 1..4, one pinned host
+              buffer) to the device, the calls, one copy of the step's y
+              back to pinned host memory
   roofline    pq2_mmv alone: packed weight bytes K*N*34/128 per launch over
               its CUDA-event time per launch, against the measured HBM peak
   cpu_baseline the CPU oracle on the host cores, on a bounded sample
@@ -47,7 +49,7 @@ PREFILL_K, PREFILL_N, PREFILL_MS = 5120, 17408, (16, 128, 512, 2048, 4096)
 # DRAM bytes (read + write) per pq2_mmv launch on attn_qkv, from the ncu
 # captures in profiles/pq2_mmv_attn_qkv_full.md (mean of M=1 and M=4);
 # None once the kernel changes after that capture.
-MMV_TRAFFIC_BYTES = (13_982_720 + 14_027_264) // 2
+MMV_TRAFFIC_BYTES = (13_982_720 + 14_014_208) // 2
 WORKLOAD = ("attn_qkv K=5120 N=10240, M=1,2,3,4 per step (quantise + GEMV each); ternary "
             "codes U{0,1,2}, fp16 group-128 scales U[0.005,0.05]; bf16 x N(0,1) with 1% "
             "channels x20; fp32 accumulate, bf16 out")
@@ -289,11 +291,17 @@ def run_ours(args):
     xs = {M: synth.activations(M, K_DIM, seed=77 + M, device=dev, outlier_frac=0.01)
           for M in MS}
     qbuf = {M: pq2.pq2_quantize_act(xs[M], pq2.PQ2_Q_PLANES) for M in MS}
-    ys = {M: torch.empty((M, N_DIM), dtype=torch.bfloat16, device=dev) for M in MS}
-    # host-side buffers for the end-to-end leg
-    hx = {M: xs[M].cpu().pin_memory() for M in MS}
-    hy = {M: torch.empty((M, N_DIM), dtype=torch.bfloat16).pin_memory() for M in MS}
-    dx = {M: torch.empty_like(xs[M]) for M in MS}
+    # The step's outputs (M = 1..4) live in one contiguous buffer, [sum M][N].
+    y_all = torch.empty((sum(MS), N_DIM), dtype=torch.bfloat16, device=dev)
+    row0 = {M: sum(MS[:i]) for i, M in enumerate(MS)}
+    ys = {M: y_all[row0[M]:row0[M] + M] for M in MS}
+    # End-to-end leg: the step's inputs in one pinned host buffer [sum M][K]
+    # (one host->device copy per step) and its outputs read back with one
+    # device->host copy per step.
+    hx_all = torch.cat([xs[M].cpu() for M in MS]).pin_memory()
+    hy_all = torch.empty((sum(MS), N_DIM), dtype=torch.bfloat16).pin_memory()
+    dx_all = torch.empty((sum(MS), K_DIM), dtype=torch.bfloat16, device=dev)
+    dx = {M: dx_all[row0[M]:row0[M] + M] for M in MS}
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     torch.cuda.synchronize()
 
@@ -349,10 +357,10 @@ def run_ours(args):
 
     def e2e_step(j):
         j %= n_graphs
+        dx_all.copy_(hx_all, non_blocking=True)
         for i, M in enumerate(MS):
-            dx[M].copy_(hx[M], non_blocking=True)
             complete(M, 4 * j + i, dx[M], sp)
-            hy[M].copy_(ys[M], non_blocking=True)
+        hy_all.copy_(y_all, non_blocking=True)
 
     n_chunks = n_graphs // math.gcd(n_graphs, chunk)
     step_graphs = [capture(lambda j=j: [step_calls(j * chunk + t) for t in range(chunk)])
