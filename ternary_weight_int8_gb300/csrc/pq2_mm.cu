@@ -25,8 +25,11 @@
 //   warp 1      TMEM allocation; lane 0 issues the MMAs and commits
 //   warps 2-5   decoders: one weight row per thread, codes -> TMEM A tile
 //   warps 6-21  epilogue: one weight row and 32 tokens per thread, reads D
-//               (three buffers in flight), scales it and adds it into fp32
-//               running sums in registers, finally stores y (coalesced)
+//               (two buffers in flight), scales it and adds it into fp32
+//               running sums in registers, finally stores y
+//   warp 22     scheduler: waits until a group's A, q and D buffer are
+//               ready, then releases the MMA warp (named barrier)
+//   warp 23     scales: stages s_x and s_w chunk by chunk for the epilogue
 // A warp may only reach the TMEM lanes 32*(warp % 4) .. +31, so each role
 // spans four consecutive warps (one per lane quarter).
 // Every wait is bounded and fails fast: a wait that gives up records
@@ -51,7 +54,8 @@ constexpr int kStagesC = 4;      // code tile stages
 constexpr int kGC = 4;           // groups per scale chunk
 constexpr int kEpiWarps = 16;     // warps 6-21: four per TMEM lane quarter
 constexpr int kSchedWarp = 6 + kEpiWarps;  // warp 22: waits on the MMA's inputs
-constexpr int kThreads = (7 + kEpiWarps) * 32;
+constexpr int kScaleWarp = 7 + kEpiWarps;  // warp 23: stages the scales
+constexpr int kThreads = (8 + kEpiWarps) * 32;
 constexpr int kEpiCols = BT / 4;  // tokens per epilogue thread
 constexpr int kDBuf = 2;          // D buffers in flight
 constexpr int kABuf = 4;          // decoded weight (A) buffers in flight
@@ -273,16 +277,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool ok = true;
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Lane 0 issues the TMA copies of codes and q group by group.
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&map_q) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&map_c) : "memory");
+      for (int g = 0; g < G; ++g) {
+        const int sq = g % kStagesQ, sc = g % kStagesC;
+        if (g >= kStagesC) ok = ok && mbar_wait(&c_empty[sc], ((g / kStagesC) - 1) & 1);
+        mbar_arrive_expect_tx(&c_full[sc], kCBytes);
+        tma_2d(smem + kOffC + sc * kCBytes, &map_c, g * kGroupCodeBytes, n0, &c_full[sc]);
+        if (g >= kStagesQ) ok = ok && done_wait(g - kStagesQ);
+        uint8_t* qs = smem + kOffQ + sq * kQBytes;
+        mbar_arrive_expect_tx(&q_full[sq], kQBytes);
+        tma_2d(qs, &map_q, g * kGroup, m0, &q_full[sq]);
+        tma_2d(qs + kQBytes / 2, &map_q, g * kGroup + 64, m0, &q_full[sq]);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kScaleWarp) {
+    // ------------------------------------------------------------- scales
     // All 32 lanes stage the scales of each chunk of kGC groups (s_x of the
-    // tile's tokens, s_w of its rows) into the scale ring; lane 0 issues the
-    // TMA copies of q and codes group by group.
+    // tile's tokens, s_w of its rows) into the two-slot scale ring, loading
+    // chunk ch + 1 into registers while chunk ch waits for its slot.  A warp
+    // of its own: the waits for a free slot (the epilogue's pace) never
+    // delay the TMA issue of codes and q.
     const int nchunks = (G + kGC - 1) / kGC;
     constexpr int kPer = kGC * BT / 32;
     float xv[kPer];
     uint16_t wv[kPer];
-    // Scales of chunk ch: loaded into registers one chunk ahead, stored into
-    // the ring slot when the chunk starts, so their latency overlaps the TMA
-    // issue of the previous chunk.
     auto load_scales = [&](int ch) {
 #pragma unroll
       for (int j = 0; j < kPer; ++j) {
@@ -294,7 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              : (uint16_t)0;
       }
     };
-    auto store_scales = [&](int ch) {
+    load_scales(0);
+    for (int ch = 0; ch < nchunks; ++ch) {
       const int slot = ch & 1;
       if (ch >= 2) ok = ok && mbar_wait(&s_empty[slot], ((ch >> 1) - 1) & 1);
       float* sxs = reinterpret_cast<float*>(smem + kOffS + slot * kSBytes);  // [kGC][BT]
@@ -305,29 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         sws[lane + 32 * j] = wv[j];
       }
       mbar_arrive(&s_full[slot]);
-    };
-    if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(&map_q) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(&map_c) : "memory");
-    }
-    load_scales(0);
-    for (int g = 0; g < G; ++g) {
-      if (g % kGC == 0) {
-        store_scales(g / kGC);
-        if (g / kGC + 1 < nchunks) load_scales(g / kGC + 1);
-      }
-      if (lane == 0) {
-        const int sq = g % kStagesQ, sc = g % kStagesC;
-        if (g >= kStagesC) ok = ok && mbar_wait(&c_empty[sc], ((g / kStagesC) - 1) & 1);
-        mbar_arrive_expect_tx(&c_full[sc], kCBytes);
-        tma_2d(smem + kOffC + sc * kCBytes, &map_c, g * kGroupCodeBytes, n0, &c_full[sc]);
-        if (g >= kStagesQ) ok = ok && done_wait(g - kStagesQ);
-        uint8_t* qs = smem + kOffQ + sq * kQBytes;
-        mbar_arrive_expect_tx(&q_full[sq], kQBytes);
-        tma_2d(qs, &map_q, g * kGroup, m0, &q_full[sq]);
-        tma_2d(qs + kQBytes / 2, &map_q, g * kGroup + 64, m0, &q_full[sq]);
-      }
-      __syncwarp();
+      if (ch + 1 < nchunks) load_scales(ch + 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
@@ -404,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&a_full[b]);
       }
     }
-  } else if (warp >= 6) {
+  } else if (warp >= 6 && warp < 6 + kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     const int col0 = ((warp - 6) >> 2) * kEpiCols;
