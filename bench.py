@@ -23,6 +23,10 @@ replayed from CUDA graphs and timed with CUDA events on the launching stream.
   prefill     pq2_mm (and pq2_linear) on ffn_up K=5120 N=17408 at
               M = 16 .. 4096: microseconds, TOPS and the fraction of the
               measured dense 16-bit tensor peak
+  gated       the gated gate/up projection (pq2_mmv_gated, silu(gate) * up
+              in the GEMV's epilogue) on ffn gate/up (K=5120, 2 x 17408
+              rows) at M = 1..4: microseconds, HBM GB/s and fraction, the
+              plain GEMV on the same rows and the complete gated call
 
 `--impl reference` times the CPU oracle on the same workload instead (the
 reference arm of this comparison).
@@ -46,6 +50,7 @@ METRIC = ("µs/call and HBM GB/s (frac of peak) for ternary×INT8 matmul at "
           "M=1–8; prefill TOPS")
 K_DIM, N_DIM, MS = 5120, 10240, (1, 2, 3, 4)
 PREFILL_K, PREFILL_N, PREFILL_MS = 5120, 17408, (16, 128, 512, 2048, 4096)
+GATED_K, GATED_I = 5120, 17408
 # DRAM bytes (read + write) per pq2_mmv launch on attn_qkv, from the ncu
 # captures in profiles/pq2_mmv_attn_qkv_full.md (mean of M=1 and M=4);
 # None once the kernel changes after that capture.
@@ -264,6 +269,78 @@ def prefill_leg(args, dev, stream, timed, capture):
     return out
 
 
+def gated_leg(args, dev, stream, timed, capture):
+    """The gated gate/up projection (silu(gate) * up in the GEMV's epilogue)
+    on the ffn gate/up shape: K=5120, N = 2 x 17408 weight rows, 4 rotated
+    matrices (189 MB, above the L2 size), M = 1..4.  Per call: pq2_mmv_gated
+    alone (back-to-back independent calls on pre-quantised activations),
+    the complete pq2_linear_gated call, and pq2_mmv on the same N rows
+    without the gated epilogue; GB/s of packed weight bytes K*N*34/128."""
+    import torch
+    from ternary_weight_int8_gb300 import pq2, synth
+    lib = pq2.lib()
+    K, N, nm = GATED_K, 2 * GATED_I, 4
+    mats = []
+    for i in range(nm):
+        raw = synth.raw_weights(N, K, seed=7000 + i, device=dev)
+        mats.append(pq2.pq2_prepare(raw, K))
+        del raw
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sp = stream.cuda_stream
+    hbm, hbm_kind = measured_peaks()
+    nbytes = N * K * 34 // 128
+    out = {"workload": f"ffn gate/up K={K} N=2x{GATED_I} (gate rows, then up rows), "
+                       f"bf16 x N(0,1) with 1% outliers, bf16 out, {nm} rotated matrices",
+           "bytes_per_call": nbytes, "peak_gbs": hbm, "peak_source": hbm_kind, "by_m": {}}
+    for M in MS:
+        x = synth.activations(M, K, seed=300 + M, device=dev, outlier_frac=0.01)
+        q, sx, qs = pq2.pq2_quantize_act(x, pq2.PQ2_Q_PLANES)
+        o = torch.empty((M, N // 2), dtype=torch.bfloat16, device=dev)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(pq2.linear_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
+
+        def gated_calls():
+            for c, sc in mats:
+                st = lib.pq2_mmv_gated(q.data_ptr(), sx.data_ptr(), qs.data_ptr(), c.data_ptr(),
+                                       sc.data_ptr(), o.data_ptr(), pq2.PQ2_BF16, M, N, K,
+                                       pq2.PQ2_MMV_INDEPENDENT, status.data_ptr(), sp)
+                if st:
+                    raise RuntimeError(f"pq2_mmv_gated failed ({st})")
+
+        def plain_calls():
+            for c, sc in mats:
+                st = lib.pq2_mmv_ex(q.data_ptr(), sx.data_ptr(), qs.data_ptr(), c.data_ptr(),
+                                    sc.data_ptr(), y.data_ptr(), pq2.PQ2_BF16, M, N, K,
+                                    lib.pq2_mmv_decoder(M), pq2.PQ2_MMV_INDEPENDENT,
+                                    status.data_ptr(), sp)
+                if st:
+                    raise RuntimeError(f"pq2_mmv failed ({st})")
+
+        def complete_calls():
+            for c, sc in mats:
+                st = lib.pq2_linear_gated(x.data_ptr(), pq2.PQ2_BF16, K, M, N, K, c.data_ptr(),
+                                          sc.data_ptr(), o.data_ptr(), pq2.PQ2_BF16,
+                                          ws.data_ptr(), ws.numel(), status.data_ptr(), sp)
+                if st:
+                    raise RuntimeError(f"pq2_linear_gated failed ({st})")
+
+        reps = 50
+        g_ms = timed([capture(gated_calls)], reps, 3) / (reps * nm)
+        p_ms = timed([capture(plain_calls)], reps, 3) / (reps * nm)
+        c_ms = timed([capture(complete_calls)], reps, 3) / (reps * nm)
+        gbs = nbytes / (g_ms * 1e-3) / 1e9
+        out["by_m"][str(M)] = {"gated_us": round(g_ms * 1e3, 3), "gated_gbs": round(gbs, 1),
+                               "gated_frac": round(gbs / hbm, 3),
+                               "mmv_same_rows_us": round(p_ms * 1e3, 3),
+                               "complete_us": round(c_ms * 1e3, 3)}
+        del x, q, sx, qs, o, y, ws
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    del mats
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -417,6 +494,7 @@ def run_ours(args):
             "mmv_frac": round(wbytes / (k_ms * 1e-3) / 1e9 / peak, 3),
         }
     prefill = prefill_leg(args, dev, stream, timed, capture) if not args.no_prefill else None
+    gated = gated_leg(args, dev, stream, timed, capture) if not args.no_gated else None
     # dominant kernel: pq2_mmv over the step's M mix, kernel-only
     mean_k_us = statistics.mean(per_m[str(M)]["mmv_us"] for M in MS)
     achieved = wbytes / (mean_k_us * 1e-6) / 1e9
@@ -444,6 +522,7 @@ def run_ours(args):
                      "bytes_per_launch": wbytes},
         "per_m": per_m,
         "prefill": prefill,
+        "gated": gated,
         "clocks": clocks.summary(),
     }
     if rank == 0 and not args.no_cpu:
@@ -494,6 +573,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill (pq2_mm) leg")
+    ap.add_argument("--no-gated", action="store_true",
+                    help="skip the gated gate/up (pq2_mmv_gated) leg")
     ap.add_argument("--profile-case", choices=["mmv", "mm"], default=None,
                     help="run a short fixed call sequence for an ncu capture and exit")
     ap.add_argument("--profile-m", type=int, default=1, help="columns for --profile-case")

@@ -151,8 +151,8 @@ int pq2_mmv(const int8_t *q_planes, const float *sx, const int32_t *qsum,
 /* Flags of pq2_mmv_ex.  Every libpq2 kernel is launched with programmatic
  * dependent launch: it may start before the kernel enqueued before it on the
  * stream completes, and waits for it before reading anything that kernel may
- * write.  pq2_quantize_act, pq2_mmv and pq2_mmv_ex release the next kernel
- * as soon as they start; pq2_mm releases it only once the kernel before it
+ * write.  pq2_quantize_act, pq2_mmv, pq2_mmv_ex and pq2_mmv_gated release
+ * the next kernel as soon as they start; pq2_mm releases it only once the kernel before it
  * has completed.  So the kernels that may still run when a call starts are
  * those enqueued at or after the latest "ordering point" before it: a
  * pq2_mm call, a host synchronisation, an event wait, a copy, or a kernel
@@ -196,6 +196,42 @@ int pq2_linear(const void *x, int x_dtype, int64_t ldx, int64_t M, int64_t N,
 /* Workspace bytes pq2_linear needs for M columns of K inputs (0 if the
  * shape is invalid). */
 size_t pq2_linear_workspace_bytes(int64_t M, int64_t K);
+
+/* pq2_mmv_gated — the gate/up projection with its gated activation in the
+ * GEMV's epilogue (page "Kernel experiments: recorded evidence", Test 12,
+ * "gated" fusion screen: the projection's output z = x W^T of width N is
+ * split in halves, gate = z[:, :N/2], up = z[:, N/2:], and the result is
+ * silu(gate) * up computed in fp32 and rounded to the output type):
+ *   out[m][n] = silu(y[m][n]) * y[m][n + N/2],  n < N/2,
+ *   silu(v)   = v / (1 + exp(-v)),
+ * each operation in fp32 with round-to-nearest (exp: CUDA's expf, 2 ulp),
+ * where y is the fp32 sum pq2_mmv forms for those rows, with the same
+ * operation order (the split count comes from all N rows), so gate and up
+ * are bit-identical to pq2_mmv's y.  Batch invariant like pq2_mmv.  Gate
+ * row n and up row n + N/2 are streamed by the same CTA; the N/2 x M
+ * intermediate never exists.
+ *   q_planes, sx, qsum, codes, scales, M, K, flags, dev_status as for
+ *            pq2_mmv_ex (masked-plane decoder).  codes/scales hold N rows:
+ *            the gate rows, then the up rows.
+ *   N        even, 2 .. 1<<30.
+ *   out      (device) out_dtype [M][N/2] (PQ2_F32 or PQ2_BF16).
+ * Returns PQ2_ERR_SHAPE for an odd N, else as pq2_mmv_ex. */
+int pq2_mmv_gated(const int8_t *q_planes, const float *sx, const int32_t *qsum,
+                  const uint8_t *codes, const uint16_t *scales, void *out,
+                  int out_dtype, int64_t M, int64_t N, int64_t K, int flags,
+                  int32_t *dev_status, void *stream);
+
+/* pq2_linear_gated — the complete gated call for M = 1..8:
+ * pq2_quantize_act into the workspace, then pq2_mmv_gated with
+ * PQ2_MMV_OVERLAP_WEIGHTS (the stream contract of pq2_linear).  Results are
+ * bit-identical to pq2_quantize_act + pq2_mmv_gated.
+ *   x, x_dtype, ldx, workspace as for pq2_linear (M 1..8 only);
+ *   N, codes, scales, out, out_dtype, dev_status as for pq2_mmv_gated. */
+int pq2_linear_gated(const void *x, int x_dtype, int64_t ldx, int64_t M,
+                     int64_t N, int64_t K, const uint8_t *codes,
+                     const uint16_t *scales, void *out, int out_dtype,
+                     void *workspace, size_t workspace_bytes,
+                     int32_t *dev_status, void *stream);
 
 /* Size of the static device scratch of pq2_linear_static (1 MiB). */
 #define PQ2_STATIC_SCRATCH_BYTES ((size_t)1 << 20)

@@ -7,6 +7,7 @@ acceptance checks (``within_bound`` / ``bf16_within_bound``), which state the
 error bound of the scale-accumulate step:
   |y - y64| <= 1e-5 * B,  B = sum_g |s_x * s_w * dot_g|            (fp32 out)
   |y - y64| <= 1e-5 * B * (1 + 2^-8) + 2^-8 * |y64|                (bf16 out)
+and of the gated output (``gated_within_bound``).
 """
 from __future__ import annotations
 
@@ -69,6 +70,7 @@ def load(path: str | None = None):
             "orc_group_dots": (None, [P, P, I64, I64, I64, P]),
             "orc_scale_accumulate": (None, [P, P, P, I64, I64, I64, P, P, P]),
             "orc_linear": (None, [P, I, I64, I64, I64, I64, P, P, P, P, P, P, P]),
+            "orc_gated": (None, [P, I64, I64, P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -213,6 +215,17 @@ def linear(x_bits: np.ndarray, kind: str, codes: np.ndarray,
     return y
 
 
+def gated(y64: np.ndarray, lib=None) -> np.ndarray:
+    """y64 f64[M][N] (gate columns, then up columns) -> silu(gate) * up,
+    f64[M][N/2]."""
+    lib = lib or load()
+    y64 = np.ascontiguousarray(y64, dtype=np.float64)
+    M, N = y64.shape
+    out = np.empty((M, N // 2), np.float64)
+    lib.orc_gated(_p(y64), M, N, _p(out))
+    return out
+
+
 # --------------------------------------------------------- acceptance rules
 REL_BOUND = 1e-5
 
@@ -234,6 +247,37 @@ def bf16_within_bound(y: np.ndarray, y64: np.ndarray, bound: np.ndarray):
     |y - y64| <= 1e-5*B*(1 + 2^-8) + 2^-8*|y64|."""
     err = np.abs(np.asarray(y, np.float64) - y64)
     lim = REL_BOUND * bound * (1.0 + 2.0 ** -8) + np.abs(y64) * 2.0 ** -8
+    ratio = np.where(lim > 0, err / np.where(lim > 0, lim, 1.0),
+                     np.where(err > 0, np.inf, 0.0))
+    return bool(np.all(err <= lim)), float(ratio.max(initial=0.0))
+
+
+SILU_SLOPE = 1.1  # max |d silu / dx| = 1.09984, at x ~ 2.3994
+GATED_ROUND = 2.0 ** -20  # fp32 expf (2 ulp), add, divide, multiply: <= 1.75 * 2^-22
+
+
+def gated_bound(y64: np.ndarray, bound: np.ndarray) -> np.ndarray:
+    """Error bound of an fp32 gated output silu(g) * u whose g and u obey
+    the fp32 output rule |g - g64| <= Bg = 1e-5 * B_gate, |u - u64| <= Bu:
+      |silu(g) u - silu(g64) u64| <= SILU_SLOPE * Bg * (|u64| + Bu)
+                                     + |silu(g64)| * Bu                  (E)
+    plus the fp32 rounding of silu and the product, relative <= 2^-20 of
+    (|out64| + E).  Returns that bound, f64[M][N/2]."""
+    M, N = y64.shape
+    I = N // 2
+    g, u = y64[:, :I], y64[:, I:]
+    bg, bu = REL_BOUND * bound[:, :I], REL_BOUND * bound[:, I:]
+    silu = g / (1.0 + np.exp(-g))
+    e = SILU_SLOPE * bg * (np.abs(u) + bu) + np.abs(silu) * bu
+    return e + GATED_ROUND * (np.abs(silu * u) + e)
+
+
+def gated_within_bound(out: np.ndarray, out64: np.ndarray, gbound: np.ndarray,
+                       bf16: bool = False):
+    """|out - out64| <= gbound (fp32), or + 2^-8 * (|out64| + gbound) for a
+    bf16 output (round to nearest even).  Returns (ok, worst ratio)."""
+    err = np.abs(np.asarray(out, np.float64) - out64)
+    lim = gbound + (2.0 ** -8 * (np.abs(out64) + gbound) if bf16 else 0.0)
     ratio = np.where(lim > 0, err / np.where(lim > 0, lim, 1.0),
                      np.where(err > 0, np.inf, 0.0))
     return bool(np.all(err <= lim)), float(ratio.max(initial=0.0))

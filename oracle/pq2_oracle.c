@@ -25,6 +25,11 @@
  *     Triton small-batch MMA", Diagram 7 and the plane-order quantisation
  *     listing): element i of a group is stored at (i%4)*32 + i/4, and
  *     T = sum of q removes the -1 offset of the codes once per group.
+ *   - gated output of a gate/up projection: KE Test 12 ("Single-token
+ *     geometry, PRMT, chaining and fusion screens"), the "activated" and
+ *     gated-fusion calls: the projection's output is split in halves along
+ *     the output dimension, gate first, and the result is silu(gate) * up,
+ *     with silu(v) = v * sigmoid(v) = v / (1 + e^-v).
  *
  * Parity pins for every function live in tests/test_oracle_pins.py.
  */
@@ -228,6 +233,19 @@ void orc_scale_accumulate(const int32_t *dots, const float *sx,
       if (y32) y32[m * N + n] = acc;
       if (y64) y64[m * N + n] = acc64;
       if (bound) bound[m * N + n] = b;
+    }
+}
+
+/* Gated output, KE Test 12: y64 [M][N] (N even) holds the projection's
+ * output, gate = columns 0..N/2-1, up = columns N/2..N-1;
+ * out64[m][n] = silu(gate) * up = gate / (1 + exp(-gate)) * up, in double. */
+void orc_gated(const double *y64, int64_t M, int64_t N, double *out64) {
+  int64_t I = N / 2;
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t n = 0; n < I; ++n) {
+      double g = y64[m * N + n];
+      double u = y64[m * N + I + n];
+      out64[m * I + n] = g / (1.0 + exp(-g)) * u;
     }
 }
 

@@ -151,6 +151,22 @@ int pq2_mmv(const int8_t* q, const float* sx, const int32_t* qsum, const uint8_t
                     pq2_mmv_decoder(M < 1 ? 1 : M), 0, dev_status, stream);
 }
 
+int pq2_mmv_gated(const int8_t* q, const float* sx, const int32_t* qsum, const uint8_t* codes,
+                  const uint16_t* scales, void* out, int out_dtype, int64_t M, int64_t N,
+                  int64_t K, int flags, int32_t* dev_status, void* stream) {
+  if (int st = check_mmv_args(q, sx, qsum, codes, scales, out, out_dtype, M, N, K,
+                              PQ2_DECODE_PLANES))
+    return st;
+  if (N % 2) return PQ2_ERR_SHAPE;
+  if (flags & ~(PQ2_MMV_OVERLAP_WEIGHTS | PQ2_MMV_INDEPENDENT)) return PQ2_ERR_DTYPE;
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  const int overlap = (flags & PQ2_MMV_INDEPENDENT) ? 2 : (flags & PQ2_MMV_OVERLAP_WEIGHTS) ? 1 : 0;
+  return pq2::launch_mmv_gated(q, sx, qsum, codes, scales, out, out_dtype, M, N, K,
+                               pq2::kDecodeMaskPlanes, overlap, sms, dev_status,
+                               static_cast<cudaStream_t>(stream));
+}
+
 size_t pq2_linear_workspace_bytes(int64_t M, int64_t K) {
   if (M < 1 || M > kMaxM || !valid_k(K)) return 0;
   const size_t G = (size_t)(K / 128);
@@ -192,6 +208,37 @@ int pq2_linear(const void* x, int x_dtype, int64_t ldx, int64_t M, int64_t N, in
                           y_dtype, nullptr, M, N, K, sms, dev_status, s);
   return pq2::launch_mmv(reinterpret_cast<const int8_t*>(ws), sx, qs, codes, scales, y,
                          y_dtype, nullptr, M, N, K, pq2_mmv_decoder(M), 1, sms, dev_status, s);
+}
+
+int pq2_linear_gated(const void* x, int x_dtype, int64_t ldx, int64_t M, int64_t N, int64_t K,
+                     const uint8_t* codes, const uint16_t* scales, void* out, int out_dtype,
+                     void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                     void* stream) {
+  if (!x || !codes || !scales || !out || !workspace) return PQ2_ERR_NULL;
+  if (x_dtype != PQ2_BF16 && x_dtype != PQ2_F16 && x_dtype != PQ2_F32) return PQ2_ERR_DTYPE;
+  if (out_dtype != PQ2_F32 && out_dtype != PQ2_BF16) return PQ2_ERR_DTYPE;
+  if (M < 1 || M > 8 || !valid_n(N) || N % 2 || !valid_k(K) || ldx < K ||
+      ldx > ((int64_t)1 << 40))
+    return PQ2_ERR_SHAPE;
+  if (workspace_bytes < pq2_linear_workspace_bytes(M, K)) return PQ2_ERR_SHAPE;
+  if (!aligned(x, elem_bytes(x_dtype)) || !aligned(workspace, 256) || !aligned(codes, 16) ||
+      !aligned(scales, 2) || !aligned(out, elem_bytes(out_dtype)))
+    return PQ2_ERR_ALIGN;
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  const size_t G = (size_t)(K / 128);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t q_bytes = (size_t)M * (size_t)K;
+  const size_t sx_off = (q_bytes + 255) / 256 * 256;
+  const size_t qs_off = (sx_off + (size_t)M * G * 4 + 255) / 256 * 256;
+  float* sx = reinterpret_cast<float*>(ws + sx_off);
+  int32_t* qs = reinterpret_cast<int32_t*>(ws + qs_off);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (int st = pq2::launch_quantize(x, x_dtype, ldx, M, K, ws, PQ2_Q_PLANES, sx, qs, s))
+    return st;
+  return pq2::launch_mmv_gated(reinterpret_cast<const int8_t*>(ws), sx, qs, codes, scales, out,
+                               out_dtype, M, N, K, pq2::kDecodeMaskPlanes, 1, sms, dev_status,
+                               s);
 }
 
 int pq2_mm(const uint16_t* q_f16, const float* sx, const int32_t* qsum, const uint8_t* codes,

@@ -43,6 +43,13 @@ int launch_mmv(const int8_t* q, const float* sx, const int32_t* qsum,
                int decode, int overlap, int sm_count, int32_t* status,
                cudaStream_t stream);
 
+// Gated gate/up output: out[m][n] = silu(y[m][n]) * y[m][n + N/2] for
+// n < N/2, y as launch_mmv computes it (N even, dots not supported).
+int launch_mmv_gated(const int8_t* q, const float* sx, const int32_t* qsum,
+                     const uint8_t* codes, const uint16_t* scales, void* out, int out_dtype,
+                     int64_t M, int64_t N, int64_t K, int decode, int overlap, int sm_count,
+                     int32_t* status, cudaStream_t stream);
+
 int launch_mm(const uint16_t* q_f16, const float* sx, const int32_t* qsum,
               const uint8_t* codes, const uint16_t* scales, void* y, int y_dtype,
               int32_t* dots, int64_t M, int64_t N, int64_t K, int sm_count,

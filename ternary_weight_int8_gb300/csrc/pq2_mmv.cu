@@ -73,6 +73,13 @@ struct MmvParams {
                           // resolves; 2: stream every input before it
   int sw_bulk;            // weight-scale slab arrives by one bulk copy (G % 8 == 0)
   int side16;             // s_x and sum(q) copied in 16-byte pieces (aligned)
+  // Gated output (gate/up): CTA rows n0.. are outputs; gate rows n0.. and up
+  // rows up_row + n0.. of the weights, the up boxes up_smem rows after the
+  // gate boxes (a multiple of 8, so both keep the 128-byte swizzle keys).
+  int gated;
+  int up_row;             // I = N / 2: first up row of the weights
+  int up_smem;            // rows between a gate box and its up box in smem
+  int y_ld;               // output row stride (N, or I when gated)
 };
 
 // Batched global -> shared copy of `count` 16-bit values by `threads`
@@ -101,6 +108,12 @@ __device__ __forceinline__ void grid_dep_wait() {
 }
 __device__ __forceinline__ void grid_dep_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Gated output of the gate/up projection: silu(g) * u = g / (1 + e^-g) * u
+// in fp32, each operation rounded to nearest (expf is CUDA's, 2 ulp).
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
 }
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
@@ -294,8 +307,11 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
     if (!DOTS && p.sw_bulk && lane == 0) {
       if (!p.overlap) grid_dep_wait();
       const uint32_t bytes = (uint32_t)(R * G * 2);
-      mbar_arrive_expect_tx(swbar, bytes);
+      mbar_arrive_expect_tx(swbar, p.gated ? 2 * bytes : bytes);
       bulk_g2s(sw_s, p.scales + (size_t)n0 * G, bytes, swbar);
+      if (p.gated)
+        bulk_g2s(sw_s + (size_t)p.up_smem * G, p.scales + (size_t)(p.up_row + n0) * G, bytes,
+                 swbar);
     }
     // Weights of stage i: TMA boxes announced on the stage barrier without
     // arriving, so the stage completes only once its inputs are issued too.
@@ -304,9 +320,13 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
       const int slot = i % p.ring;
       const int g0 = i * Gs, boxes = (min(Gs, G - g0) + 3) / 4;
       uint8_t* st = ring + (size_t)slot * p.stage_bytes;
-      mbar_expect_tx(&full[slot], (uint32_t)(boxes * R * kBoxBytes));
-      for (int b = 0; b < boxes; ++b)
+      mbar_expect_tx(&full[slot], (uint32_t)(boxes * R * kBoxBytes * (p.gated ? 2 : 1)));
+      for (int b = 0; b < boxes; ++b) {
         tma_load_2d(st + b * p.box_stride, map, (g0 + 4 * b) * kGroupCodeBytes, n0, &full[slot]);
+        if (p.gated)
+          tma_load_2d(st + b * p.box_stride + p.up_smem * kBoxBytes, map,
+                      (g0 + 4 * b) * kGroupCodeBytes, p.up_row + n0, &full[slot]);
+      }
     };
     // Inputs of stage i (and with stage 0 s_x and sum(q)), copied by the
     // whole warp with cp.async rather than TMA: the SM's TMA unit serves its
@@ -372,6 +392,9 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
   if (!DOTS && !p.sw_bulk) {
     preload_u16(reinterpret_cast<uint16_t*>(sw_s), p.scales + (size_t)n0 * G, R * G, tid,
                 p.cons_threads);
+    if (p.gated)
+      preload_u16(reinterpret_cast<uint16_t*>(sw_s) + (size_t)p.up_smem * G,
+                  p.scales + (size_t)(p.up_row + n0) * G, R * G, tid, p.cons_threads);
     named_bar_sync(1, p.cons_threads);
   }
   bool ok = true;
@@ -383,17 +406,20 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
   // low bit, so its 16-byte code loads spread over all eight chunk slots of
   // a 128-byte line (rows 2rb, 2rb + 1 would leave half the slots, and the
   // banks behind them, unused).  A row beyond R is a duplicate of row R-1,
-  // computed but never stored.
+  // computed but never stored.  Gated: the two rows are gate row rb and
+  // up row rb (up_smem rows further in shared memory), for output rb.
   constexpr int RP = kRowsPerThread;
+  static_assert(RP == 2, "the gated output pairs a thread's two rows");
   const int z = tid % S;
   const int rb = tid / S;
-  const int H = (R + RP - 1) / RP;
+  const int H = p.gated ? p.up_smem : (R + RP - 1) / RP;
+  const int Rv = p.gated ? H + R : R;  // rows beyond Rv - 1 do not exist
   int rows[RP];
   bool valid[RP];
 #pragma unroll
   for (int r = 0; r < RP; ++r) {
-    valid[r] = rb < H && rb + r * H < R;
-    rows[r] = min(rb + r * H, R - 1);
+    valid[r] = (p.gated ? rb < R : rb < H) && rb + r * H < Rv;
+    rows[r] = min(rb + r * H, Rv - 1);
   }
   const bool active = valid[0];
   const uint32_t ring_s = smem_u32(ring), sw_base = smem_u32(sw_s);
@@ -506,13 +532,25 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
         for (int off = S >> 1; off > 0; off >>= 1)
           yacc[r][m] = __fadd_rn(yacc[r][m], __shfl_xor_sync(0xffffffffu, yacc[r][m], off));
     grid_dep_wait();  // earlier kernels may still read or write y
-    if (z == 0) {
+    if (z == 0 && p.gated) {
+      if (valid[0]) {
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          const size_t o = (size_t)m * p.y_ld + n0 + rb;
+          const float v = silu_mul(yacc[0][m], yacc[1][m]);
+          if (p.y_bf16)
+            static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(v);
+          else
+            static_cast<float*>(p.y)[o] = v;
+        }
+      }
+    } else if (z == 0) {
 #pragma unroll
       for (int r = 0; r < RP; ++r) {
         if (!valid[r]) continue;
 #pragma unroll
         for (int m = 0; m < M; ++m) {
-          const size_t o = (size_t)m * p.N + n0 + rows[r];
+          const size_t o = (size_t)m * p.y_ld + n0 + rows[r];
           if (p.y_bf16)
             static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(yacc[r][m]);
           else
@@ -647,29 +685,53 @@ bool mmv_geometry(int64_t N, int64_t K, int sm_count, MmvGeometry* out) {
   return true;
 }
 
-int launch_mmv(const int8_t* q, const float* sx, const int32_t* qsum, const uint8_t* codes,
-               const uint16_t* scales, void* y, int y_dtype, int32_t* dots, int64_t M,
-               int64_t N, int64_t K, int decode, int overlap, int sm_count, int32_t* status,
-               cudaStream_t stream) {
+namespace {
+
+// pq2_mmv over N weight rows, or (gated) the gate/up form: outputs
+// n < I = N / 2 from weight rows n and I + n.  The split count S comes from
+// the geometry of all N rows either way, so a row's fp32 sum is the same.
+int launch_mmv_impl(const int8_t* q, const float* sx, const int32_t* qsum,
+                    const uint8_t* codes, const uint16_t* scales, void* y, int y_dtype,
+                    int32_t* dots, int64_t M, int64_t N, int64_t K, int decode, int overlap,
+                    bool gated, int sm_count, int32_t* status, cudaStream_t stream) {
   MmvGeometry geo;
   if (!mmv_geometry(N, K, sm_count, &geo)) return PQ2_ERR_SHAPE;
+  if (gated && (N % 2 || dots)) return PQ2_ERR_SHAPE;
+  int64_t rows_out = N, ctas = geo.ctas;
+  int rows_max = geo.rows_max, threads = geo.threads;
+  if (gated) {
+    // One output (a gate row and an up row) per thread and split: at most
+    // 288 / S outputs and 256 box rows per CTA.
+    const int64_t I = N / 2;
+    const int64_t per = std::min<int64_t>(kMaxBoxRows, kMaxConsumerThreads / geo.splits);
+    ctas = std::max<int64_t>(std::min<int64_t>(I, sm_count), (I + per - 1) / per);
+    rows_max = (int)((I + ctas - 1) / ctas);
+    threads = align_up(rows_max * geo.splits, 32);
+    rows_out = I;
+  }
   MmvParams p{};
   p.q = q; p.sx = sx; p.qsum = qsum; p.scales = scales;
   p.y = y; p.dots = dots; p.status = status;
-  p.N = (int)N; p.K = (int)K; p.G = (int)(K / kGroup);
-  p.ctas = geo.ctas; p.splits = geo.splits; p.rows_max = geo.rows_max;
-  p.cons_threads = geo.threads;
+  p.N = (int)rows_out; p.K = (int)K; p.G = (int)(K / kGroup);
+  p.ctas = (int)ctas; p.splits = geo.splits; p.rows_max = rows_max;
+  p.cons_threads = threads;
+  p.gated = gated;
+  p.up_row = gated ? (int)(N / 2) : 0;
+  p.up_smem = gated ? align_up(rows_max, 8) : 0;
+  p.y_ld = (int)rows_out;
   p.overlap = overlap;
   p.y_bf16 = y_dtype == PQ2_BF16;
   p.sw_bulk = (K / kGroup) % 8 == 0 && reinterpret_cast<uintptr_t>(scales) % 16 == 0;
   p.side16 = (M * (K / kGroup)) % 4 == 0 && reinterpret_cast<uintptr_t>(sx) % 16 == 0 &&
              reinterpret_cast<uintptr_t>(qsum) % 16 == 0;
-  const int mi = (int)M, R = geo.rows_max, S = geo.splits, G = p.G;
+  const int mi = (int)M, R = rows_max, S = geo.splits, G = p.G;
   const int unit = 4 * S / gcd(4, S);
-  p.box_stride = align_up(R * kBoxBytes, 1024);
+  // rows of weights (and of their scales) a CTA keeps per 4-group box chunk
+  const int slab = gated ? 2 * p.up_smem : R;
+  p.box_stride = align_up(slab * kBoxBytes, 1024);
   // fixed region: barriers, weight scales, s_x, sum(q)
   p.sw_off = align_up(2 * 8 * kMaxStages + 8, 128);
-  p.sx_off = align_up(p.sw_off + G * R * 2, 16);
+  p.sx_off = align_up(p.sw_off + G * slab * 2, 16);
   p.qs_off = align_up(p.sx_off + mi * G * 4, 16);
   p.ring_off = align_up(p.qs_off + mi * G * 4, 1024);
   const int room = kSmemBudget - p.ring_off;
@@ -712,7 +774,7 @@ int launch_mmv(const int8_t* q, const float* sx, const int32_t* qsum, const uint
   if (overlap == 1) smem = std::max(smem, kSoloSmem);
 
   CUtensorMap hi, lo;
-  const int rows_lo = (int)(N / geo.ctas);
+  const int rows_lo = (int)(rows_out / ctas);
   if (!encode_map(&hi, codes, N, K / 4, R) ||
       !encode_map(&lo, codes, N, K / 4, rows_lo > 0 ? rows_lo : R))
     return PQ2_ERR_LAUNCH;
@@ -723,6 +785,24 @@ int launch_mmv(const int8_t* q, const float* sx, const int32_t* qsum, const uint
   return decode == kDecodeMaskPlanes
              ? launch_m<kDecodeMaskPlanes, false>(mi, hi, lo, p, smem, stream)
              : launch_m<kDecodeAddXor, false>(mi, hi, lo, p, smem, stream);
+}
+
+}  // namespace
+
+int launch_mmv(const int8_t* q, const float* sx, const int32_t* qsum, const uint8_t* codes,
+               const uint16_t* scales, void* y, int y_dtype, int32_t* dots, int64_t M,
+               int64_t N, int64_t K, int decode, int overlap, int sm_count, int32_t* status,
+               cudaStream_t stream) {
+  return launch_mmv_impl(q, sx, qsum, codes, scales, y, y_dtype, dots, M, N, K, decode,
+                         overlap, false, sm_count, status, stream);
+}
+
+int launch_mmv_gated(const int8_t* q, const float* sx, const int32_t* qsum,
+                     const uint8_t* codes, const uint16_t* scales, void* out, int out_dtype,
+                     int64_t M, int64_t N, int64_t K, int decode, int overlap, int sm_count,
+                     int32_t* status, cudaStream_t stream) {
+  return launch_mmv_impl(q, sx, qsum, codes, scales, out, out_dtype, nullptr, M, N, K, decode,
+                         overlap, true, sm_count, status, stream);
 }
 
 }  // namespace pq2

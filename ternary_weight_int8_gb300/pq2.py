@@ -44,6 +44,8 @@ SIGNATURES = {
     "pq2_linear": (_I, [_P, _I, _I64, _I64, _I64, _I64, _P, _P, _P, _I, _P, _SZ, _P, _P]),
     "pq2_linear_workspace_bytes": (_SZ, [_I64, _I64]),
     "pq2_linear_static": (_I, [_P, _I, _I64, _I64, _I64, _I64, _P, _P, _P, _I, _P, _P]),
+    "pq2_mmv_gated": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _P, _P]),
+    "pq2_linear_gated": (_I, [_P, _I, _I64, _I64, _I64, _I64, _P, _P, _P, _I, _P, _SZ, _P, _P]),
     "pq2_mmv_decoder": (_I, [_I64]),
     "pq2_mm": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P]),
     "pq2_debug_group_dots": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P, _P, _P]),
@@ -177,6 +179,39 @@ def pq2_linear(x, codes, scales, y=None, out_dtype=torch.float32, workspace=None
         _DT[y.dtype], _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(status), _stream(stream)))
     return y
+
+
+def pq2_mmv_gated(q_planes, sx, qsum, codes, scales, out=None, out_dtype=torch.float32,
+                  flags=0, status=None, stream=None):
+    """Gate/up GEMV with its gated activation, M = 1..8: codes/scales hold N
+    rows (gate rows, then up rows); out[M][N/2] = silu(gate) * up."""
+    M, K = q_planes.shape
+    N = codes.shape[0]
+    if out is None:
+        out = torch.empty((M, N // 2), dtype=out_dtype, device=q_planes.device)
+    _check("pq2_mmv_gated", lib().pq2_mmv_gated(
+        _ptr(q_planes), _ptr(sx), _ptr(qsum), _ptr(codes), _ptr(scales), _ptr(out),
+        _DT[out.dtype], M, N, K, flags, _ptr(status), _stream(stream)))
+    return out
+
+
+def pq2_linear_gated(x, codes, scales, out=None, out_dtype=torch.float32, workspace=None,
+                     status=None, stream=None):
+    """Complete gated call for M = 1..8: quantise x, then pq2_mmv_gated."""
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit column stride")
+    M, K = x.shape
+    N = codes.shape[0]
+    if out is None:
+        out = torch.empty((M, N // 2), dtype=out_dtype, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(linear_workspace_bytes(M, K), dtype=torch.uint8,
+                                device=x.device)
+    _check("pq2_linear_gated", lib().pq2_linear_gated(
+        _ptr(x), _DT[x.dtype], x.stride(0), M, N, K, _ptr(codes), _ptr(scales), _ptr(out),
+        _DT[out.dtype], _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(status), _stream(stream)))
+    return out
 
 
 def pq2_mm(q_f16, sx, qsum, codes, scales, y=None, out_dtype=torch.float32, status=None,

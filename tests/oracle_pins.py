@@ -333,4 +333,53 @@ def pin_prepare(lib):
                                   (np.arange(32) + 40 * n + 7 * g) & 0xFF)
 
 
+# ------------------------------------------------------------------ gated
+# KE Test 12: the gate/up projection's output is split in halves, gate
+# first, and the gated result is silu(gate) * up, silu(v) = v * sigmoid(v).
+# Logistic values (sigmoid(v) = 1 / (1 + e^-v)) to double precision:
+SIGMOID = {1.0: 0.7310585786300049, 1.5: 0.8175744761936437, -2.0: 0.11920292202211755}
+
+
+def pin_gated_values(lib):
+    """Known logistic values, gate columns before up columns."""
+    y = np.array([[1.0, 1.5, -2.0, 2.0, 3.0, 0.5]])
+    out = O.gated(y, lib=lib)
+    want = [1.0 * SIGMOID[1.0] * 2.0, 1.5 * SIGMOID[1.5] * 3.0, -2.0 * SIGMOID[-2.0] * 0.5]
+    assert out.shape == (1, 3)
+    assert np.allclose(out[0], want, rtol=1e-15, atol=0), (out, want)
+
+
+def pin_gated_identities(lib):
+    """silu(0) = 0; silu(v) - silu(-v) = v (sigmoid(v) + sigmoid(-v) = 1);
+    silu(40) = 40 and |silu(-40)| < 1e-15 to double precision."""
+    vs = np.array([0.0, 0.25, 1.0, 3.0, 7.5, 40.0])
+    y = np.concatenate([vs, -vs, np.ones(12)])[None, :]
+    out = O.gated(y, lib=lib)[0]
+    n = len(vs)
+    assert out[0] == 0.0 and out[n] == 0.0
+    assert np.allclose(out[:n] - out[n:], vs, rtol=1e-14, atol=1e-300), out
+    assert out[n - 1] == 40.0 and abs(out[2 * n - 1]) < 1e-15
+
+
+def pin_gated_end_to_end(lib):
+    """Two weight rows through the whole oracle: x = the worked example plus a
+    127 (so s_x = 1, q = x), gate row codes [0,1,2,2] (dot 30), up row codes
+    [2,2,2,2] (dot 20+30+40+10 = 100), weight scale 0.5: gate = 15, up = 50,
+    gated = 15 * sigmoid(15) * 50 with sigmoid(15) = 1 / (1 + 3.059023205018258e-7)."""
+    ex = _golden("worked_example.json")
+    x = np.zeros((1, G), np.float32)
+    x[0, :4] = ex["q"]
+    x[0, 4] = 127.0
+    q, sx = O.quantize(x, lib=lib)
+    codes = np.ones((2, G), np.uint8)
+    codes[0, :4] = ex["codes"]
+    codes[1, :4] = 2
+    dots = O.group_dots(q, _pack(codes), lib=lib)
+    _, y64, _ = O.scale_accumulate(dots, sx, np.full((2, 1), _f16_bits(0.5), np.uint16), lib=lib)
+    assert list(y64[0]) == [15.0, 50.0], y64
+    out = O.gated(y64, lib=lib)
+    want = 15.0 / (1.0 + 3.059023205018258e-7) * 50.0
+    assert abs(out[0, 0] - want) <= 1e-13, (out, want)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

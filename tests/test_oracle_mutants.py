@@ -36,6 +36,10 @@ MUTANTS = [
      "if (kind == 1)\n        a[m * K + k] = orc_bf16_to_float"),
     ("fp64_term_sign", "acc64 += term;", "acc64 -= term;"),
     ("qsum_off_by_one", "for (int i = 0; i < ORC_GROUP; ++i) t +=", "for (int i = 1; i < ORC_GROUP; ++i) t +="),
+    ("gated_halves_swapped", "double g = y64[m * N + n];\n      double u = y64[m * N + I + n];",
+     "double u = y64[m * N + n];\n      double g = y64[m * N + I + n];"),
+    ("gated_exp_sign", "g / (1.0 + exp(-g)) * u", "g / (1.0 + exp(g)) * u"),
+    ("gated_sigmoid_only", "g / (1.0 + exp(-g)) * u", "1.0 / (1.0 + exp(-g)) * u"),
 ]
 
 
