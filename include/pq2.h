@@ -260,6 +260,43 @@ int pq2_linear_static(const void *x, int x_dtype, int64_t ldx, int64_t M,
 /* The decoder pq2_mmv uses for M columns (host only). */
 int pq2_mmv_decoder(int64_t M);
 
+/* Largest K pq2_norm_hadamard_quantize takes (a row's fp32 copy stays in
+ * shared memory). */
+#define PQ2_PREP_MAX_K 32768
+
+/* pq2_norm_hadamard_quantize — the activations' preparation fused into one
+ * kernel (page "Kernel experiments: recorded evidence", Test 18, "RMSNorm +
+ * Hadamard + Q8 fusion"), per row m of K columns:
+ *   h    = x (+ residual), fp32
+ *   S    = sum of h^2: partial i (0..2047) sums h[j]^2 for j = i mod 2048 in
+ *          increasing j, then p[i] += p[i + len] for len = 1024, 512, .., 1
+ *          (fp32; S = p[0])
+ *   inv  = 1 / sqrt(S / K + eps)            (IEEE square root and division)
+ *   n    = bf16((h * inv) * (w + 1))         (norm weight w, applied as w + 1)
+ *   v    = n * sign                          (sign +1 / -1 per column)
+ *   v    = bf16(WHT(v)) per 1024-column block, WHT the orthonormal
+ *          Walsh-Hadamard transform (butterfly passes of half-width 1, 2, ..,
+ *          512 in fp32, then the exact factor 1/32)
+ *   q, sx, qsum = pq2_quantize_act of v (group 128, same rounding)
+ * Every fp32 operation rounds to nearest; the codes are therefore a function
+ * of the inputs alone (bit-exact against the CPU oracle).
+ *   x            (device) bf16 [M][K].
+ *   residual     (device, may be NULL) bf16 [M][K], added to x first.
+ *   residual_out (device, may be NULL) bf16 [M][K] <- bf16(h).
+ *   w            (device) bf16 [K]; sign (device) int8 [K], each +1 or -1.
+ *   eps          0 <= eps <= 1.
+ *   M            1 .. 1<<20;  K a multiple of 1024, 1024 .. PQ2_PREP_MAX_K.
+ *   norm_out     (device, may be NULL) bf16 [M][K] <- n.
+ *   q, q_layout, sx, qsum as for pq2_quantize_act.
+ * Returns PQ2_ERR_SHAPE for K or eps out of range, else as
+ * pq2_quantize_act; launched with programmatic dependent launch like it. */
+int pq2_norm_hadamard_quantize(const uint16_t *x, const uint16_t *residual,
+                               uint16_t *residual_out, const uint16_t *w,
+                               const int8_t *sign, float eps, int64_t M,
+                               int64_t K, uint16_t *norm_out, void *q,
+                               int q_layout, float *sx, int32_t *qsum,
+                               void *stream);
+
 /* pq2_mm — prefill (M >= 16) ternary x INT8 matmul as a dense tensor-core
  * contraction (KE Test 7 "INT8 tensor-core MMQ prefill"; BIB "Use matrix
  * hardware for prefill"): per 128-group the exact dot of q and the decoded

@@ -71,6 +71,10 @@ def load(path: str | None = None):
             "orc_scale_accumulate": (None, [P, P, P, I64, I64, I64, P, P, P]),
             "orc_linear": (None, [P, I, I64, I64, I64, I64, P, P, P, P, P, P, P]),
             "orc_gated": (None, [P, I64, I64, P]),
+            "orc_fwht1024": (None, [P]),
+            "orc_sumsq2048": (ctypes.c_float, [P, I64]),
+            "orc_norm_hadamard_quantize": (None, [P, P, P, P, ctypes.c_float, I64, I64,
+                                                  P, P, P, P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -224,6 +228,44 @@ def gated(y64: np.ndarray, lib=None) -> np.ndarray:
     out = np.empty((M, N // 2), np.float64)
     lib.orc_gated(_p(y64), M, N, _p(out))
     return out
+
+
+def fwht1024(v: np.ndarray, lib=None) -> np.ndarray:
+    """Orthonormal 1024-point Walsh-Hadamard transform (fp32), a copy."""
+    lib = lib or load()
+    out = np.ascontiguousarray(v, dtype=np.float32).copy()
+    assert out.shape == (1024,)
+    lib.orc_fwht1024(_p(out))
+    return out
+
+
+def sumsq2048(h: np.ndarray, lib=None) -> float:
+    """Sum of squares in the 2048-partial reduction structure (fp32)."""
+    lib = lib or load()
+    h = np.ascontiguousarray(h, dtype=np.float32)
+    return float(lib.orc_sumsq2048(_p(h), h.shape[0]))
+
+
+def norm_hadamard_quantize(x_bits: np.ndarray, residual_bits, w_bits: np.ndarray,
+                           sign: np.ndarray, eps: float, lib=None):
+    """bf16 x [M][K] (bits), optional bf16 residual (bits), bf16 norm weight
+    w [K] (bits, applied as w + 1), sign [K] (+1/-1), eps ->
+    (q i8[M][K], sx f32[M][K/128], norm bits u16[M][K], residual-out bits
+    u16[M][K] or None)."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, K = x.shape
+    r = None if residual_bits is None else np.ascontiguousarray(residual_bits, dtype=np.uint16)
+    w = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    sg = np.ascontiguousarray(sign, dtype=np.int8)
+    q = np.empty((M, K), np.int8)
+    sx = np.empty((M, K // GROUP), np.float32)
+    nb = np.empty((M, K), np.uint16)
+    rb = np.empty((M, K), np.uint16) if r is not None else None
+    lib.orc_norm_hadamard_quantize(_p(x), None if r is None else _p(r), _p(w), _p(sg),
+                                   ctypes.c_float(eps), M, K, _p(nb),
+                                   None if rb is None else _p(rb), _p(q), _p(sx))
+    return q, sx, nb, rb
 
 
 # --------------------------------------------------------- acceptance rules

@@ -30,6 +30,12 @@
  *     gated-fusion calls: the projection's output is split in halves along
  *     the output dimension, gate first, and the result is silu(gate) * up,
  *     with silu(v) = v * sigmoid(v) = v / (1 + e^-v).
+ *   - fused preparation of the activations: KE Test 18 ("RMSNorm + Hadamard
+ *     + Q8 fusion"): h = x (+ residual) in fp32; the sum of h^2 over the row
+ *     kept in 2048 strided partial sums, then summed; inv = 1/sqrt(mean +
+ *     eps); normalised = bf16((h * inv) * (w + 1)); v = normalised * sign;
+ *     a 1024-point Walsh-Hadamard transform; bf16; then the group-128 INT8
+ *     quantiser above.
  *
  * Parity pins for every function live in tests/test_oracle_pins.py.
  */
@@ -247,6 +253,78 @@ void orc_gated(const double *y64, int64_t M, int64_t N, double *out64) {
       double u = y64[m * N + I + n];
       out64[m * I + n] = g / (1.0 + exp(-g)) * u;
     }
+}
+
+/* Orthonormal Walsh-Hadamard transform of 1024 values in place, fp32:
+ * butterfly passes with half-width 1, 2, 4, .., 512 (pairs j, j + h inside
+ * blocks of 2h become a + b, a - b), then the factor 1/32 = 1/sqrt(1024),
+ * exact.  (KE Test 18 applies it to each 1024-element block of a row.) */
+void orc_fwht1024(float *v) {
+  for (int h = 1; h < 1024; h *= 2)
+    for (int b = 0; b < 1024; b += 2 * h)
+      for (int j = b; j < b + h; ++j) {
+        float a = v[j], c = v[j + h];
+        v[j] = a + c;
+        v[j + h] = a - c;
+      }
+  for (int j = 0; j < 1024; ++j) v[j] = v[j] * 0.03125f;
+}
+
+/* Sum of squares of one row in the reduction structure of KE Test 18:
+ * partial p[i] = sum of h[j]^2 over j = i, i + 2048, i + 4096, .. (in that
+ * order, fp32), then the 2048 partials summed pairwise: p[i] += p[i + len]
+ * for len = 1024, 512, .., 1; the result is p[0]. */
+float orc_sumsq2048(const float *h, int64_t K) {
+  static float p[2048];
+  for (int i = 0; i < 2048; ++i) p[i] = 0.0f;
+  for (int64_t j = 0; j < K; ++j) {
+    float t = h[j] * h[j];
+    p[j % 2048] = p[j % 2048] + t;
+  }
+  for (int len = 1024; len >= 1; len /= 2)
+    for (int i = 0; i < len; ++i) p[i] = p[i] + p[i + len];
+  return p[0];
+}
+
+/* Fused preparation, KE Test 18, for M rows of K (K % 1024 == 0) bf16
+ * activations x (bits), optional bf16 residual (bits, NULL if none):
+ *   h      = x + residual (fp32; x alone without residual)
+ *   inv    = 1 / sqrt(sumsq2048(h) / K + eps)     (IEEE sqrt and division)
+ *   n      = bf16_rne((h * inv) * (w + 1))        (w: bf16 bits, per column)
+ *   v      = float(n) * sign                       (sign: +1 / -1 per column)
+ *   v      = bf16_rne(fwht1024(v)) per 1024-column block
+ *   q, sx  = orc_quantize(v)                       (group 128)
+ * Optional outputs (NULL to skip): norm_out (bits of n), res_out (bits of
+ * bf16_rne(h)). */
+void orc_norm_hadamard_quantize(const uint16_t *x, const uint16_t *residual,
+                                const uint16_t *w, const int8_t *sign, float eps,
+                                int64_t M, int64_t K, uint16_t *norm_out,
+                                uint16_t *res_out, int8_t *q, float *sx) {
+  int saved = fegetround();
+  fesetround(FE_TONEAREST);
+  static float h[1 << 20], v[1 << 20];
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t j = 0; j < K; ++j) {
+      float a = orc_bf16_to_float(x[m * K + j]);
+      if (residual) a = a + orc_bf16_to_float(residual[m * K + j]);
+      h[j] = a;
+      if (res_out) res_out[m * K + j] = orc_float_to_bf16_rne(a);
+    }
+    float mean = orc_sumsq2048(h, K) / (float)K;
+    float inv = 1.0f / sqrtf(mean + eps);
+    for (int64_t j = 0; j < K; ++j) {
+      float t = (h[j] * inv) * (orc_bf16_to_float(w[j]) + 1.0f);
+      uint16_t nb = orc_float_to_bf16_rne(t);
+      if (norm_out) norm_out[m * K + j] = nb;
+      v[j] = orc_bf16_to_float(nb) * (float)sign[j];
+    }
+    for (int64_t b = 0; b < K; b += 1024) {
+      orc_fwht1024(v + b);
+      for (int j = 0; j < 1024; ++j) v[b + j] = orc_bf16_to_float(orc_float_to_bf16_rne(v[b + j]));
+    }
+    orc_quantize(v, 1, K, q + m * K, sx + m * (K / ORC_GROUP));
+  }
+  fesetround(saved);
 }
 
 /* Whole path on already-prepared planes: y32 for an activation matrix x.

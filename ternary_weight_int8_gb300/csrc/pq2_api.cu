@@ -241,6 +241,26 @@ int pq2_linear_gated(const void* x, int x_dtype, int64_t ldx, int64_t M, int64_t
                                s);
 }
 
+int pq2_norm_hadamard_quantize(const uint16_t* x, const uint16_t* residual,
+                               uint16_t* residual_out, const uint16_t* w, const int8_t* sign,
+                               float eps, int64_t M, int64_t K, uint16_t* norm_out, void* q,
+                               int q_layout, float* sx, int32_t* qsum, void* stream) {
+  if (!x || !w || !sign || !q || !sx) return PQ2_ERR_NULL;
+  if (q_layout != PQ2_Q_ROWS && q_layout != PQ2_Q_PLANES && q_layout != PQ2_Q_F16)
+    return PQ2_ERR_DTYPE;
+  if (M < 1 || M > kMaxM || K < 1024 || K > PQ2_PREP_MAX_K || K % 1024) return PQ2_ERR_SHAPE;
+  if (!(eps >= 0.0f) || eps > 1.0f) return PQ2_ERR_SHAPE;
+  if (!aligned(x, 2) || (residual && !aligned(residual, 2)) || (residual_out && !aligned(residual_out, 2)) ||
+      !aligned(w, 2) || (norm_out && !aligned(norm_out, 2)) || !aligned(q, 16) ||
+      !aligned(sx, 4) || (qsum && !aligned(qsum, 4)))
+    return PQ2_ERR_ALIGN;
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  return pq2::launch_norm_hadamard_quantize(x, residual, residual_out, w, sign, eps, M, K,
+                                            norm_out, q, q_layout, sx, qsum,
+                                            static_cast<cudaStream_t>(stream));
+}
+
 int pq2_mm(const uint16_t* q_f16, const float* sx, const int32_t* qsum, const uint8_t* codes,
            const uint16_t* scales, void* y, int y_dtype, int64_t M, int64_t N, int64_t K,
            int32_t* dev_status, void* stream) {

@@ -50,6 +50,13 @@ int launch_mmv_gated(const int8_t* q, const float* sx, const int32_t* qsum,
                      int64_t M, int64_t N, int64_t K, int decode, int overlap, int sm_count,
                      int32_t* status, cudaStream_t stream);
 
+// Fused RMSNorm + signs + 1024-point Walsh-Hadamard + group-128 INT8
+// quantisation of M rows of K bf16 activations (pq2_norm_hadamard_quantize).
+int launch_norm_hadamard_quantize(const uint16_t* x, const uint16_t* residual,
+                                  uint16_t* residual_out, const uint16_t* w, const int8_t* sign,
+                                  float eps, int64_t M, int64_t K, uint16_t* norm_out, void* q,
+                                  int q_layout, float* sx, int32_t* qsum, cudaStream_t stream);
+
 int launch_mm(const uint16_t* q_f16, const float* sx, const int32_t* qsum,
               const uint8_t* codes, const uint16_t* scales, void* y, int y_dtype,
               int32_t* dots, int64_t M, int64_t N, int64_t K, int sm_count,

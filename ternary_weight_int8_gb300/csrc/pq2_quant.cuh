@@ -1,0 +1,89 @@
+// pq2_quant.cuh — the per-group INT8 activation quantisation as warp-level
+// device functions, shared by the stand-alone quantisation kernel and the
+// fused norm / Hadamard / quantisation kernel, so both produce the same bytes
+// by construction.
+//
+// Method: page "Kernel experiments: recorded evidence" (KE), Test 6
+// (_quantize) and page "Baseline and the integer breakthrough" (BIB),
+// "Calculate with small integers", step 1: per group of 128 activations
+// s = max|a| / 127, q = clamp(round_half_even(a / s), -127, 127), with
+// s = 0 (an all-zero group) dividing by 1.  Layouts: KE Test 21 (plane
+// order) and the prefill MMA operand order (include/pq2.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "pq2.h"
+
+namespace pq2 {
+
+// One group held by a full warp, lane L owning elements 4L..4L+3, with IEEE
+// round-to-nearest divisions.  Returns s (the same in every lane) and the
+// lane's four q.
+__device__ __forceinline__ float quantize_group4(const float a[4], int qi[4]) {
+  float amax = fmaxf(fmaxf(fabsf(a[0]), fabsf(a[1])), fmaxf(fabsf(a[2]), fabsf(a[3])));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const float s = __fdiv_rn(amax, 127.0f);
+  const float d = s > 0.0f ? s : 1.0f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float r = rintf(__fdiv_rn(a[j], d));
+    r = fminf(fmaxf(r, -127.0f), 127.0f);
+    qi[j] = (int)r;
+  }
+  return s;
+}
+
+// Store one group's q (lane L holding elements 4L..4L+3 of the group that
+// starts at element `base` of q) in the requested layout, and its sum of q
+// (to *qsum when non-null).  Every lane of the warp must call it.
+__device__ __forceinline__ void store_group4(const int qi[4], int lane, void* q, int layout,
+                                             int64_t base, int32_t* qsum) {
+  const uint32_t packed = (uint32_t)(qi[0] & 0xff) | ((uint32_t)(qi[1] & 0xff) << 8) |
+                          ((uint32_t)(qi[2] & 0xff) << 16) | ((uint32_t)(qi[3] & 0xff) << 24);
+  if (layout == PQ2_Q_ROWS) {
+    reinterpret_cast<uint32_t*>(static_cast<int8_t*>(q) + base)[lane] = packed;
+  } else if (layout == PQ2_Q_PLANES) {
+    // Plane word (s, w) = q[16w + 4b + s] for b = 0..3: byte s of the packed
+    // words of lanes 4w..4w+3.  Lane L = 8s + w assembles it, so the warp
+    // writes the group's 128 bytes as one coalesced line.
+    const int s_out = lane >> 3, w_out = lane & 7;
+    uint32_t out = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t v = __shfl_sync(0xffffffffu, packed, 4 * w_out + b);
+      out |= ((v >> (8 * s_out)) & 0xffu) << (8 * b);
+    }
+    reinterpret_cast<uint32_t*>(static_cast<int8_t*>(q) + base)[lane] = out;
+  } else {
+    // Operand order of the prefill MMA: inside each 16-element chunk (lanes
+    // 4c..4c+3, element 4b + s held by lane 4c + b), element 4b + s goes to
+    // position 4s + 2(b & 1) + (b >> 1).  Lane L = 4c + s' writes positions
+    // 4s'..4s'+3, i.e. element s' of lanes 4c + 0, 2, 1, 3.
+    const int c = lane >> 2, s_out = lane & 3;
+    int o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int b = (j >> 1) | ((j & 1) << 1);  // 0, 2, 1, 3
+      const uint32_t v = __shfl_sync(0xffffffffu, packed, 4 * c + b);
+      o[j] = (int)(int8_t)((v >> (8 * s_out)) & 0xffu);
+    }
+    __half2 h01 = __halves2half2(__int2half_rn(o[0]), __int2half_rn(o[1]));
+    __half2 h23 = __halves2half2(__int2half_rn(o[2]), __int2half_rn(o[3]));
+    uint2 v;
+    v.x = *reinterpret_cast<uint32_t*>(&h01);
+    v.y = *reinterpret_cast<uint32_t*>(&h23);
+    reinterpret_cast<uint2*>(static_cast<__half*>(q) + base)[lane] = v;
+  }
+  int t = qi[0] + qi[1] + qi[2] + qi[3];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+  if (qsum && lane == 0) *qsum = t;
+}
+
+}  // namespace pq2

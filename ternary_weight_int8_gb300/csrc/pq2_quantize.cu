@@ -11,6 +11,7 @@
 
 #include "pq2_device.cuh"
 #include "pq2_internal.h"
+#include "pq2_quant.cuh"
 
 namespace pq2 {
 namespace {
@@ -85,9 +86,8 @@ __device__ __forceinline__ void load4(const void* x, int64_t i, bool vec,
   }
 }
 
-// One warp per (row m, group g); lane L owns elements 4L..4L+3 of the group.
-//   s = max|a| / 127, d = s > 0 ? s : 1, q = clamp(rne(a / d), -127, 127)
-// with IEEE round-to-nearest divisions, exactly as the definition states.
+// One warp per (row m, group g); lane L owns elements 4L..4L+3 of the group
+// (quantize_group4 / store_group4).
 template <int XT>
 __global__ void __launch_bounds__(256) quantize_kernel(
     const void* __restrict__ x, int64_t ldx, int64_t M, int G, bool vec,
@@ -107,64 +107,9 @@ __global__ void __launch_bounds__(256) quantize_kernel(
 
   float a[4];
   load4<XT>(x, m * ldx + (int64_t)g * kGroup + 4 * lane, vec, a);
-  float amax = fmaxf(fmaxf(fabsf(a[0]), fabsf(a[1])),
-                     fmaxf(fabsf(a[2]), fabsf(a[3])));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1)
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  const float s = __fdiv_rn(amax, 127.0f);
-  const float d = s > 0.0f ? s : 1.0f;
   int qi[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    float r = rintf(__fdiv_rn(a[j], d));
-    r = fminf(fmaxf(r, -127.0f), 127.0f);
-    qi[j] = (int)r;
-  }
-  const uint32_t packed = (uint32_t)(qi[0] & 0xff) | ((uint32_t)(qi[1] & 0xff) << 8) |
-                          ((uint32_t)(qi[2] & 0xff) << 16) | ((uint32_t)(qi[3] & 0xff) << 24);
-  const int64_t base = m * K + (int64_t)g * kGroup;
-  if (layout == PQ2_Q_ROWS) {
-    reinterpret_cast<uint32_t*>(static_cast<int8_t*>(q) + base)[lane] = packed;
-  } else if (layout == PQ2_Q_PLANES) {
-    // Plane word (s, w) = q[16w + 4b + s] for b = 0..3: byte s of the packed
-    // words of lanes 4w..4w+3.  Lane L = 8s + w assembles it, so the warp
-    // writes the group's 128 bytes as one coalesced line.
-    const int s_out = lane >> 3, w_out = lane & 7;
-    uint32_t out = 0;
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const uint32_t v = __shfl_sync(0xffffffffu, packed, 4 * w_out + b);
-      out |= ((v >> (8 * s_out)) & 0xffu) << (8 * b);
-    }
-    reinterpret_cast<uint32_t*>(static_cast<int8_t*>(q) + base)[lane] = out;
-  } else {
-    // Operand order of the prefill MMA: inside each 16-element chunk (lanes
-    // 4c..4c+3, element 4b + s held by lane 4c + b), element 4b + s goes to
-    // position 4s + 2(b & 1) + (b >> 1).  Lane L = 4c + s' writes positions
-    // 4s'..4s'+3, i.e. element s' of lanes 4c + 0, 2, 1, 3.
-    const int c = lane >> 2, s_out = lane & 3;
-    int o[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int b = (j >> 1) | ((j & 1) << 1);  // 0, 2, 1, 3
-      const uint32_t v = __shfl_sync(0xffffffffu, packed, 4 * c + b);
-      o[j] = (int)(int8_t)((v >> (8 * s_out)) & 0xffu);
-    }
-    __half2 h01 = __halves2half2(__int2half_rn(o[0]), __int2half_rn(o[1]));
-    __half2 h23 = __halves2half2(__int2half_rn(o[2]), __int2half_rn(o[3]));
-    uint2 v;
-    v.x = *reinterpret_cast<uint32_t*>(&h01);
-    v.y = *reinterpret_cast<uint32_t*>(&h23);
-    reinterpret_cast<uint2*>(static_cast<__half*>(q) + base)[lane] = v;
-  }
-  if (qsum) {
-    int t = qi[0] + qi[1] + qi[2] + qi[3];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-      t += __shfl_xor_sync(0xffffffffu, t, off);
-    if (lane == 0) qsum[m * G + g] = t;
-  }
+  const float s = quantize_group4(a, qi);
+  store_group4(qi, lane, q, layout, m * K + (int64_t)g * kGroup, qsum ? qsum + m * G + g : nullptr);
   if (lane == 0) sx[m * G + g] = s;
 }
 

@@ -45,6 +45,8 @@ SIGNATURES = {
     "pq2_linear_workspace_bytes": (_SZ, [_I64, _I64]),
     "pq2_linear_static": (_I, [_P, _I, _I64, _I64, _I64, _I64, _P, _P, _P, _I, _P, _P]),
     "pq2_mmv_gated": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _P, _P]),
+    "pq2_norm_hadamard_quantize": (_I, [_P, _P, _P, _P, _P, ctypes.c_float, _I64, _I64, _P,
+                                        _P, _I, _P, _P, _P]),
     "pq2_linear_gated": (_I, [_P, _I, _I64, _I64, _I64, _I64, _P, _P, _P, _I, _P, _SZ, _P, _P]),
     "pq2_mmv_decoder": (_I, [_I64]),
     "pq2_mm": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P]),
@@ -212,6 +214,26 @@ def pq2_linear_gated(x, codes, scales, out=None, out_dtype=torch.float32, worksp
         _DT[out.dtype], _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(status), _stream(stream)))
     return out
+
+
+def pq2_norm_hadamard_quantize(x, w, sign, eps, residual=None, layout: int = PQ2_Q_PLANES,
+                               want_norm=False, want_residual=False, stream=None):
+    """x bf16 [M][K] (CUDA), norm weight w bf16 [K], sign int8 [K] (+-1) ->
+    (q, sx, qsum, norm_out or None, residual_out or None): RMSNorm, signs,
+    1024-point Walsh-Hadamard and group-128 quantisation in one kernel."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D bf16 tensor")
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.float16 if layout == PQ2_Q_F16 else torch.int8,
+                    device=x.device)
+    sx = torch.empty((M, K // GROUP), dtype=torch.float32, device=x.device)
+    qsum = torch.empty((M, K // GROUP), dtype=torch.int32, device=x.device)
+    norm = torch.empty_like(x) if want_norm else None
+    rout = torch.empty_like(x) if want_residual else None
+    _check("pq2_norm_hadamard_quantize", lib().pq2_norm_hadamard_quantize(
+        _ptr(x), _ptr(residual), _ptr(rout), _ptr(w), _ptr(sign), float(eps), M, K,
+        _ptr(norm), _ptr(q), layout, _ptr(sx), _ptr(qsum), _stream(stream)))
+    return q, sx, qsum, norm, rout
 
 
 def pq2_mm(q_f16, sx, qsum, codes, scales, y=None, out_dtype=torch.float32, status=None,

@@ -382,4 +382,95 @@ def pin_gated_end_to_end(lib):
     assert abs(out[0, 0] - want) <= 1e-13, (out, want)
 
 
+# ------------------------------------------- fused preparation (KE Test 18)
+def _walsh(k: int) -> np.ndarray:
+    """Column k of the Sylvester Hadamard matrix of order 1024: entry j is
+    (-1)^popcount(j & k)."""
+    j = np.arange(1024)
+    bits = np.array([bin(v).count("1") for v in (j & k)])
+    return np.where(bits % 2 == 0, 1.0, -1.0)
+
+
+def _bf16_bits(values) -> np.ndarray:
+    return synth_bits(np.asarray(values, np.float32))
+
+
+def synth_bits(a: np.ndarray) -> np.ndarray:
+    """bf16 bits of fp32 values that bf16 represents exactly."""
+    b = np.ascontiguousarray(a, np.float32).view(np.uint32)
+    assert np.all((b & 0xFFFF) == 0), "not exact in bf16"
+    return (b >> 16).astype(np.uint16)
+
+
+def pin_fwht_columns(lib):
+    """H e_k = column k of the Sylvester matrix / 32 (closed form)."""
+    for k in (0, 1, 5, 513, 1023):
+        e = np.zeros(1024, np.float32)
+        e[k] = 1.0
+        assert np.array_equal(O.fwht1024(e, lib=lib), (_walsh(k) / 32.0).astype(np.float32)), k
+
+
+def pin_fwht_involution(lib):
+    """The orthonormal transform is its own inverse; for small integers every
+    partial sum is exact, so H(H(v)) == v bit for bit."""
+    v = (np.arange(1024) * 37 % 201 - 100).astype(np.float32)
+    assert np.array_equal(O.fwht1024(O.fwht1024(v, lib=lib), lib=lib), v)
+
+
+def pin_sumsq_structure(lib):
+    """2048 strided fp32 partials, then a tree: with h[0]^2 = 2^24 and
+    h[1], h[2], h[3] = 1 the tree adds 1 + 1 before meeting 2^24 and keeps
+    2^24 + 2; a sequential fp32 sum would round each +1 away (2^24).  The
+    squares of small integers sum exactly otherwise."""
+    h = np.zeros(4096, np.float32)
+    h[0], h[1], h[2], h[3] = 4096.0, 1.0, 1.0, 1.0
+    assert O.sumsq2048(h, lib=lib) == 16777218.0
+    g = (np.arange(5120) % 7).astype(np.float32)
+    assert O.sumsq2048(g, lib=lib) == float(np.sum((np.arange(5120) % 7) ** 2))
+
+
+def pin_norm_hadamard_constant_row(lib):
+    """x = 3, residual = -1 (h = 2), w = 0, signs +1, eps = 0, K = 2048:
+    mean h^2 = 4, inv = 1/2, n = 1; the transform of a constant block is
+    32 e_0, so each 1024-block quantises to q = 127 at its first element
+    (s_x = 32/127) and zeros elsewhere (s_x = 0); the residual output is 2."""
+    K = 2048
+    x = _bf16_bits(np.full((1, K), 3.0))
+    r = _bf16_bits(np.full((1, K), -1.0))
+    w = _bf16_bits(np.zeros(K))
+    q, sx, nb, rb = O.norm_hadamard_quantize(x, r, w, np.ones(K, np.int8), 0.0, lib=lib)
+    assert np.all(nb == _bf16_bits([1.0])[0]) and np.all(rb == _bf16_bits([2.0])[0])
+    want = np.zeros((1, K), np.int8)
+    want[0, 0] = want[0, 1024] = 127
+    assert np.array_equal(q, want), np.nonzero(q)
+    s = np.zeros((1, K // G), np.float32)
+    s[0, 0] = s[0, 8] = np.float32(32.0) / np.float32(127.0)
+    assert np.array_equal(sx, s), sx
+
+
+def pin_norm_hadamard_sign_pattern(lib):
+    """Signs equal to Walsh function k and a constant row: v = column k, and
+    its transform is 32 e_k, so q = 127 exactly at element k; the norm
+    weight enters as w + 1 (w = 0.5 gives n = 1.5 for h * inv = 1)."""
+    K, k = 1024, 300
+    x = _bf16_bits(np.full((1, K), 1.0))
+    w = _bf16_bits(np.full(K, 0.5))
+    sign = _walsh(k).astype(np.int8)
+    q, sx, nb, _ = O.norm_hadamard_quantize(x, None, w, sign, 0.0, lib=lib)
+    assert np.all(nb == _bf16_bits([1.5])[0])
+    want = np.zeros((1, K), np.int8)
+    want[0, k] = 127
+    assert np.array_equal(q, want), np.nonzero(q)
+    assert sx[0, k // G] == np.float32(48.0) / np.float32(127.0)
+
+
+def pin_norm_eps(lib):
+    """eps enters under the root: x = 1, eps = 3 gives inv = 1/2, n = 0.5."""
+    K = 1024
+    x = _bf16_bits(np.full((1, K), 1.0))
+    w = _bf16_bits(np.zeros(K))
+    _, _, nb, _ = O.norm_hadamard_quantize(x, None, w, np.ones(K, np.int8), 3.0, lib=lib)
+    assert np.all(nb == _bf16_bits([0.5])[0])
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

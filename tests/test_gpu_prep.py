@@ -1,0 +1,115 @@
+"""pq2_norm_hadamard_quantize (RMSNorm + signs + 1024-point Walsh-Hadamard +
+group-128 INT8 in one kernel) against the CPU oracle, bit for bit: q in every
+layout, s_x, sum(q), the normalised row and the residual output."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from ternary_weight_int8_gb300 import pq2, synth
+import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pq2.lib()
+    yield
+    torch.cuda.synchronize()
+
+
+def _inputs(M, K, seed, residual):
+    g = torch.Generator().manual_seed(seed)
+    x = synth.activations(M, K, seed=seed, outlier_frac=0.01).to(torch.bfloat16)
+    r = (torch.randn((M, K), generator=g) * 0.5).to(torch.bfloat16) if residual else None
+    w = (torch.randn(K, generator=g) * 0.1).to(torch.bfloat16)
+    sign = (torch.randint(0, 2, (K,), generator=g) * 2 - 1).to(torch.int8)
+    return x, r, w, sign
+
+
+def _oracle(x, r, w, sign, eps, rows=None):
+    xb = synth.bits_u16(x)
+    rb = None if r is None else synth.bits_u16(r)
+    if rows is not None:
+        xb = xb[rows]
+        rb = None if rb is None else rb[rows]
+    return O.norm_hadamard_quantize(xb, rb, synth.bits_u16(w), sign.numpy(), eps)
+
+
+@pytest.mark.parametrize("M,K", [(1, 1024), (3, 5120), (8, 17408), (64, 2048), (2, 32768)])
+@pytest.mark.parametrize("residual", [False, True])
+def test_prep_bitexact(M, K, residual):
+    eps = 1e-6
+    x, r, w, sign = _inputs(M, K, seed=M * 31 + K, residual=residual)
+    q_o, sx_o, nb_o, rb_o = _oracle(x, r, w, sign, eps)
+    dev = lambda t: None if t is None else t.cuda()
+    for layout in (pq2.PQ2_Q_ROWS, pq2.PQ2_Q_PLANES, pq2.PQ2_Q_F16):
+        q, sx, qs, nb, rb = pq2.pq2_norm_hadamard_quantize(
+            dev(x), dev(w), dev(sign), eps, residual=dev(r), layout=layout,
+            want_norm=True, want_residual=residual)
+        torch.cuda.synchronize()
+        if layout == pq2.PQ2_Q_ROWS:
+            assert np.array_equal(q.cpu().numpy(), q_o)
+        elif layout == pq2.PQ2_Q_PLANES:
+            assert np.array_equal(q.cpu().numpy(), O.q_planes(q_o))
+        else:
+            assert np.array_equal(q.cpu().float().numpy(),
+                                  U.mm_operand_order(q_o).astype(np.float32))
+        assert np.array_equal(sx.cpu().numpy().view(np.uint32), sx_o.view(np.uint32))
+        assert np.array_equal(qs.cpu().numpy(), O.qsum(q_o))
+        assert np.array_equal(synth.bits_u16(nb.cpu()), nb_o)
+        if residual:
+            assert np.array_equal(synth.bits_u16(rb.cpu()), rb_o)
+
+
+def test_prep_prefill_rows_sampled():
+    """M = 4096, K = 5120 (the prefill shape): sampled rows bit-exact."""
+    M, K, eps = 4096, 5120, 1e-5
+    x, r, w, sign = _inputs(M, K, seed=11, residual=True)
+    q, sx, qs, _, _ = pq2.pq2_norm_hadamard_quantize(
+        x.cuda(), w.cuda(), sign.cuda(), eps, residual=r.cuda(), layout=pq2.PQ2_Q_F16)
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, 777, 2048, 4095])
+    q_o, sx_o, _, _ = _oracle(x, r, w, sign, eps, rows=rows)
+    assert np.array_equal(q.cpu().float().numpy()[rows], U.mm_operand_order(q_o).astype(np.float32))
+    assert np.array_equal(sx.cpu().numpy()[rows].view(np.uint32), sx_o.view(np.uint32))
+
+
+def test_prep_rows_are_independent():
+    """Row j of an 8-row call equals the same row prepared alone."""
+    K, eps = 5120, 1e-6
+    x, r, w, sign = _inputs(8, K, seed=5, residual=False)
+    xc, wc, sc = x.cuda(), w.cuda(), sign.cuda()
+    q8, sx8, _, _, _ = pq2.pq2_norm_hadamard_quantize(xc, wc, sc, eps)
+    for j in range(8):
+        q1, sx1, _, _, _ = pq2.pq2_norm_hadamard_quantize(xc[j:j + 1].contiguous(), wc, sc, eps)
+        torch.cuda.synchronize()
+        assert torch.equal(q1[0], q8[j]) and torch.equal(sx1[0].view(torch.int32), sx8[j].view(torch.int32))
+
+
+def test_prep_rejects_bad_arguments():
+    lib = pq2.lib()
+    M, K = 2, 1024
+    x = torch.zeros((M, 4 * K), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(4 * K, dtype=torch.bfloat16, device="cuda")
+    sign = torch.ones(4 * K, dtype=torch.int8, device="cuda")
+    q = torch.empty((M, 4 * K), dtype=torch.int8, device="cuda")
+    sx = torch.empty((M, 32), dtype=torch.float32, device="cuda")
+
+    def call(K_, eps=0.0, layout=pq2.PQ2_Q_PLANES, xp=x.data_ptr(), qp=q.data_ptr()):
+        return lib.pq2_norm_hadamard_quantize(xp, None, None, w.data_ptr(), sign.data_ptr(),
+                                              eps, M, K_, None, qp, layout, sx.data_ptr(),
+                                              None, None)
+    assert call(1536) == pq2.PQ2_ERR_SHAPE
+    assert call(512) == pq2.PQ2_ERR_SHAPE
+    assert call(40960) == pq2.PQ2_ERR_SHAPE
+    assert call(1024, eps=-1.0) == pq2.PQ2_ERR_SHAPE
+    assert call(1024, eps=float("nan")) == pq2.PQ2_ERR_SHAPE
+    assert call(1024, layout=7) == pq2.PQ2_ERR_DTYPE
+    assert call(1024, xp=None) == pq2.PQ2_ERR_NULL
+    assert call(1024, qp=q.data_ptr() + 4) == pq2.PQ2_ERR_ALIGN
+    assert call(1024) == pq2.PQ2_OK
+    torch.cuda.synchronize()

@@ -40,6 +40,15 @@ MUTANTS = [
      "double u = y64[m * N + n];\n      double g = y64[m * N + I + n];"),
     ("gated_exp_sign", "g / (1.0 + exp(-g)) * u", "g / (1.0 + exp(g)) * u"),
     ("gated_sigmoid_only", "g / (1.0 + exp(-g)) * u", "1.0 / (1.0 + exp(-g)) * u"),
+    ("fwht_unnormalised", "v[j] = v[j] * 0.03125f;", "v[j] = v[j] * 1.0f;"),
+    ("fwht_butterfly_swapped", "v[j] = a + c;\n        v[j + h] = a - c;",
+     "v[j] = a - c;\n        v[j + h] = a + c;"),
+    ("sumsq_sequential", "for (int i = 0; i < len; ++i) p[i] = p[i] + p[i + len];",
+     "for (int i = 1; i < 2 * len; ++i) if (len == 1024) p[0] = p[0] + p[i];"),
+    ("norm_weight_no_offset", "(orc_bf16_to_float(w[j]) + 1.0f)", "(orc_bf16_to_float(w[j]) + 0.0f)"),
+    ("norm_eps_dropped", "1.0f / sqrtf(mean + eps)", "1.0f / sqrtf(mean)"),
+    ("norm_sign_dropped", "* (float)sign[j];", "* 1.0f;"),
+    ("norm_residual_dropped", "if (residual) a = a + orc_bf16_to_float", "if (0) a = a + orc_bf16_to_float"),
 ]
 
 
