@@ -23,6 +23,8 @@ replayed from CUDA graphs and timed with CUDA events on the launching stream.
   prefill     pq2_mm (and pq2_linear) on ffn_up K=5120 N=17408 at
               M = 16 .. 4096: microseconds, TOPS and the fraction of the
               measured dense 16-bit tensor peak
+  prep        the fused preparation (pq2_norm_hadamard_quantize) at K=5120,
+              M = 1..4 and 4096, with the stand-alone quantisation beside it
   gated       the gated gate/up projection (pq2_mmv_gated, silu(gate) * up
               in the GEMV's epilogue) on ffn gate/up (K=5120, 2 x 17408
               rows) at M = 1..4: microseconds, HBM GB/s and fraction, the
@@ -341,6 +343,64 @@ def gated_leg(args, dev, stream, timed, capture):
     return out
 
 
+def prep_leg(args, dev, stream, timed, capture):
+    """The fused preparation (pq2_norm_hadamard_quantize: RMSNorm with a
+    residual, signs, 1024-point Walsh-Hadamard, group-128 INT8 in the plane
+    layout) at K=5120 for M = 1..4 and 4096, against the stand-alone
+    quantisation of the same rows; HBM bytes per call: x and residual in
+    (2 x 2MK), w and signs (3K), q out (MK), s_x and sum(q) (8MK/128)."""
+    import torch
+    from ternary_weight_int8_gb300 import pq2, synth
+    lib = pq2.lib()
+    K = K_DIM
+    hbm, hbm_kind = measured_peaks()
+    g = torch.Generator().manual_seed(17)
+    w = (torch.randn(K, generator=g) * 0.1).to(torch.bfloat16).to(dev)
+    sign = (torch.randint(0, 2, (K,), generator=g) * 2 - 1).to(torch.int8).to(dev)
+    sp = stream.cuda_stream
+    out = {"workload": f"K={K}, bf16 x and residual, eps 1e-6, q in plane order",
+           "peak_gbs": hbm, "peak_source": hbm_kind, "by_m": {}}
+    for M in tuple(MS) + (4096,):
+        n_in = 8 if M < 64 else 1  # rotate inputs of small calls
+        xs = [synth.activations(M, K, seed=40 + i, device=dev).to(torch.bfloat16)
+              for i in range(n_in)]
+        rs = [synth.activations(M, K, seed=80 + i, device=dev).to(torch.bfloat16)
+              for i in range(n_in)]
+        q = torch.empty((M, K), dtype=torch.int8, device=dev)
+        sx = torch.empty((M, K // 128), dtype=torch.float32, device=dev)
+        qs = torch.empty((M, K // 128), dtype=torch.int32, device=dev)
+        calls = 8
+
+        def fused():
+            for i in range(calls):
+                st = lib.pq2_norm_hadamard_quantize(
+                    xs[i % n_in].data_ptr(), rs[i % n_in].data_ptr(), None, w.data_ptr(),
+                    sign.data_ptr(), 1e-6, M, K, None, q.data_ptr(), pq2.PQ2_Q_PLANES,
+                    sx.data_ptr(), qs.data_ptr(), sp)
+                if st:
+                    raise RuntimeError(f"pq2_norm_hadamard_quantize failed ({st})")
+
+        def quant_only():
+            for i in range(calls):
+                st = lib.pq2_quantize_act(xs[i % n_in].data_ptr(), pq2.PQ2_BF16, K, M, K,
+                                          q.data_ptr(), pq2.PQ2_Q_PLANES, sx.data_ptr(),
+                                          qs.data_ptr(), sp)
+                if st:
+                    raise RuntimeError(f"pq2_quantize_act failed ({st})")
+
+        reps = 20 if M >= 64 else 100
+        f_ms = timed([capture(fused)], reps, 3) / (reps * calls)
+        q_ms = timed([capture(quant_only)], reps, 3) / (reps * calls)
+        nbytes = 4 * M * K + 3 * K + M * K + 8 * M * K // 128
+        out["by_m"][str(M)] = {"fused_us": round(f_ms * 1e3, 3),
+                               "gbs": round(nbytes / (f_ms * 1e-3) / 1e9, 1),
+                               "frac": round(nbytes / (f_ms * 1e-3) / 1e9 / hbm, 3),
+                               "quantize_only_us": round(q_ms * 1e3, 3)}
+        del xs, rs, q, sx, qs
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -495,6 +555,7 @@ def run_ours(args):
         }
     prefill = prefill_leg(args, dev, stream, timed, capture) if not args.no_prefill else None
     gated = gated_leg(args, dev, stream, timed, capture) if not args.no_gated else None
+    prep = prep_leg(args, dev, stream, timed, capture) if not args.no_prep else None
     # dominant kernel: pq2_mmv over the step's M mix, kernel-only
     mean_k_us = statistics.mean(per_m[str(M)]["mmv_us"] for M in MS)
     achieved = wbytes / (mean_k_us * 1e-6) / 1e9
@@ -523,6 +584,7 @@ def run_ours(args):
         "per_m": per_m,
         "prefill": prefill,
         "gated": gated,
+        "prep": prep,
         "clocks": clocks.summary(),
     }
     if rank == 0 and not args.no_cpu:
@@ -575,6 +637,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill (pq2_mm) leg")
     ap.add_argument("--no-gated", action="store_true",
                     help="skip the gated gate/up (pq2_mmv_gated) leg")
+    ap.add_argument("--no-prep", action="store_true",
+                    help="skip the fused preparation (pq2_norm_hadamard_quantize) leg")
     ap.add_argument("--profile-case", choices=["mmv", "mm"], default=None,
                     help="run a short fixed call sequence for an ncu capture and exit")
     ap.add_argument("--profile-m", type=int, default=1, help="columns for --profile-case")

@@ -16,9 +16,15 @@
 // orthonormal one (butterfly passes of half-width 1, 2, .., 512, then the
 // exact factor 1/32).
 //
-// One CTA (512 threads) per row: the row's h sits in shared memory between
-// the two passes; each 1024-block is transformed in shared memory (ten
-// butterfly passes) and quantised by eight warps, one 128-group each.
+// One CTA (256 threads; four fit on an SM) per row: the row's h sits in
+// shared memory between
+// the two passes.  In the second pass each warp owns whole 1024-blocks: lane
+// l holds elements 32i + l (i = 0..31) in registers, so the passes of
+// half-width 1..16 are shuffles between lanes and those of 32..512 are
+// butterflies inside a lane, with no block-wide barrier; the rounded block
+// is written back over its h.  Then all the warps share the row's
+// 128-groups (each a latency chain of shuffles), in the quantiser's lane
+// layout (elements 4l..4l+3 of a group per lane).
 #include <cuda_bf16.h>
 
 #include "pq2_device.cuh"
@@ -28,7 +34,6 @@
 namespace pq2 {
 namespace {
 
-constexpr int kPrepThreads = 512;
 constexpr int kLanes = 2048;  // strided partial sums of h^2
 constexpr int kHad = 1024;    // transform block
 
@@ -39,16 +44,21 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-__global__ void __launch_bounds__(kPrepThreads, 1)
+// kPrepThreads threads per row: 1024 when few rows run (the latency of one
+// row: more warps share its 128-groups), 256 for many rows (four CTAs per
+// SM).  The thread count changes which thread holds which of the 2048 lanes,
+// never the order of an operation.
+template <int kPrepThreads>
+__global__ void __launch_bounds__(kPrepThreads, kPrepThreads == 256 ? 4 : 1)
     prep_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ res,
                 uint16_t* __restrict__ res_out, const uint16_t* __restrict__ w,
-                const int8_t* __restrict__ sign, float eps, int K,
+                const int8_t* __restrict__ sign, float eps, int K, int vec,
                 uint16_t* __restrict__ norm_out, void* __restrict__ q, int layout,
                 float* __restrict__ sx, int32_t* __restrict__ qsum) {
   extern __shared__ float sh[];
-  float* hs = sh;            // [K]     h = x (+ residual), fp32
-  float* vb = sh + K;        // [1024]  the block being transformed
-  float* tree = vb + kHad;   // [512]   cross-thread levels of the sum
+  float* hs = sh;          // [K]    h = x (+ residual), then the transformed row
+  float* tree = sh + K;    // [512]  cross-thread levels of the sum
+  constexpr int kPrepWarps = kPrepThreads / 32;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int64_t m = blockIdx.x;
   const int G = K / kGroup;
@@ -56,31 +66,84 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // Pass 1: h, the optional residual output, and lanes t + 512k (k = 0..3)
-  // of the 2048 strided partial sums of h^2, in increasing j.
+  // Pass 1a: h = x (+ residual) into shared memory, and the optional
+  // residual output.  With 16-byte aligned rows the loads (eight bf16 each)
+  // go out four per thread at a time before any is used (all of them for
+  // K <= 8192); else element by element.
   const uint16_t* xr = x + m * K;
-  float p[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  for (int base = 0; base < K; base += kLanes) {
+  if (vec) {
+    constexpr int kBatch = 4;
+    const int chunks = K / 8;
+    for (int c0 = 0; c0 < chunks; c0 += kBatch * kPrepThreads) {
+      uint4 xv[kBatch], rv[kBatch];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int j = base + t + kPrepThreads * k;
-      if (j < K) {
-        float a = bf16_bits_to_float(xr[j]);
-        if (res) a = __fadd_rn(a, bf16_bits_to_float(res[m * K + j]));
-        hs[j] = a;
-        if (res_out) res_out[m * K + j] = float_to_bf16_bits(a);
-        p[k] = __fadd_rn(p[k], __fmul_rn(a, a));
+      for (int u = 0; u < kBatch; ++u) {
+        const int c = c0 + t + kPrepThreads * u;
+        if (c < chunks) {
+          xv[u] = reinterpret_cast<const uint4*>(xr)[c];
+          if (res) rv[u] = reinterpret_cast<const uint4*>(res + m * K)[c];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int c = c0 + t + kPrepThreads * u;
+        if (c < chunks) {
+          const uint32_t xw[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+          const uint32_t rw[4] = {rv[u].x, rv[u].y, rv[u].z, rv[u].w};
+          float h8[8];
+          uint32_t ob[4];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const uint16_t xb = (uint16_t)(xw[e >> 1] >> (16 * (e & 1)));
+            float a = bf16_bits_to_float(xb);
+            if (res) a = __fadd_rn(a, bf16_bits_to_float((uint16_t)(rw[e >> 1] >> (16 * (e & 1)))));
+            h8[e] = a;
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            ob[e] = (uint32_t)float_to_bf16_bits(h8[2 * e]) |
+                    ((uint32_t)float_to_bf16_bits(h8[2 * e + 1]) << 16);
+          reinterpret_cast<float4*>(hs)[2 * c] = make_float4(h8[0], h8[1], h8[2], h8[3]);
+          reinterpret_cast<float4*>(hs)[2 * c + 1] = make_float4(h8[4], h8[5], h8[6], h8[7]);
+          if (res_out)
+            reinterpret_cast<uint4*>(res_out + m * K)[c] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+        }
       }
     }
+  } else {
+    for (int j = t; j < K; j += kPrepThreads) {
+      float a = bf16_bits_to_float(xr[j]);
+      if (res) a = __fadd_rn(a, bf16_bits_to_float(res[m * K + j]));
+      hs[j] = a;
+      if (res_out) res_out[m * K + j] = float_to_bf16_bits(a);
+    }
   }
-  // p[i] += p[i + len]: len 1024 and 512 inside the thread (lanes t + 512k),
-  // 256 .. 32 through shared memory, 16 .. 1 by shuffles in warp 0.
-  p[0] = __fadd_rn(p[0], p[2]);
-  p[1] = __fadd_rn(p[1], p[3]);
-  p[0] = __fadd_rn(p[0], p[1]);
+  __syncthreads();
+  // Pass 1b: lanes t + kPrepThreads * k of the 2048 strided partial sums of
+  // h^2, each in increasing j (slices of 2048 outside, the thread's lanes
+  // inside, so a slice's loads go out together).
+  constexpr int kPer = kLanes / kPrepThreads;
+  float p[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) p[k] = 0.0f;
+  for (int base = 0; base < K; base += kLanes) {
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int j = base + t + kPrepThreads * k;
+      if (j < K) p[k] = __fadd_rn(p[k], __fmul_rn(hs[j], hs[j]));
+    }
+  }
+  // p[i] += p[i + len]: len 1024 .. kPrepThreads inside the thread (lane
+  // t + kPrepThreads * k pairs with k + kPer/2, then k + kPer/4, ..), the
+  // levels below kPrepThreads down to 32 through shared memory, 16 .. 1 by
+  // shuffles in warp 0.
+#pragma unroll
+  for (int step = kPer / 2; step >= 1; step >>= 1)
+#pragma unroll
+    for (int k = 0; k < step; ++k) p[k] = __fadd_rn(p[k], p[k + step]);
   tree[t] = p[0];
   __syncthreads();
-  for (int len = 256; len >= 32; len >>= 1) {
+  for (int len = kPrepThreads / 2; len >= 32; len >>= 1) {
     if (t < len) tree[t] = __fadd_rn(tree[t], tree[t + len]);
     __syncthreads();
   }
@@ -97,56 +160,68 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   const float mean = __fdiv_rn(tree[0], (float)K);
   const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
 
-  // Pass 2, block by block: normalise, round to bf16, apply the signs,
-  // transform, round to bf16, quantise.
-  for (int b = 0; b < K; b += kHad) {
+  // Pass 2, one 1024-block per warp at a time: normalise, round to bf16,
+  // apply the signs, transform, round to bf16, and store the block back.
+  for (int b = warp * kHad; b < K; b += kPrepWarps * kHad) {
+    float r[32];
 #pragma unroll
-    for (int e = t; e < kHad; e += kPrepThreads) {
-      const int j = b + e;
+    for (int i = 0; i < 32; ++i) {
+      const int j = b + 32 * i + lane;
       const float tn =
           __fmul_rn(__fmul_rn(hs[j], inv), __fadd_rn(bf16_bits_to_float(w[j]), 1.0f));
       const uint16_t nb = float_to_bf16_bits(tn);
       if (norm_out) norm_out[m * K + j] = nb;
-      vb[e] = bf16_bits_to_float(nb) * (float)sign[j];  // exact: the sign is +-1
+      r[i] = bf16_bits_to_float(nb) * (float)sign[j];  // exact: the sign is +-1
     }
-    __syncthreads();
-    for (int h = 1; h < kHad; h <<= 1) {
-      const int j = (t / h) * 2 * h + (t % h);  // pair t of this pass
-      const float a = vb[j], c = vb[j + h];
-      vb[j] = __fadd_rn(a, c);
-      vb[j + h] = __fsub_rn(a, c);
-      __syncthreads();
+    // Passes of half-width 1..16 pair lanes l and l ^ h (the lower lane of a
+    // pair keeps a + c, the upper a - c) ...
+#pragma unroll
+    for (int h = 1; h < 32; h <<= 1) {
+      const bool upper = (lane & h) != 0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float o = __shfl_xor_sync(0xffffffffu, r[i], h);
+        r[i] = upper ? __fsub_rn(o, r[i]) : __fadd_rn(r[i], o);
+      }
+    }
+    // ... those of 32..512 pair registers i and i + h/32 of one lane.
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if (i & d) continue;
+        const float a = r[i], c = r[i + d];
+        r[i] = __fadd_rn(a, c);
+        r[i + d] = __fsub_rn(a, c);
+      }
     }
 #pragma unroll
-    for (int e = t; e < kHad; e += kPrepThreads)
-      vb[e] = bf16_bits_to_float(float_to_bf16_bits(vb[e] * 0.03125f));  // 1/32: exact
-    __syncthreads();
-    if (warp < kHad / kGroup) {
-      const int gi = b / kGroup + warp;
-      float a[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = vb[warp * kGroup + 4 * lane + i];
-      int qi[4];
-      const float s = quantize_group4(a, qi);
-      store_group4(qi, lane, q, layout, m * K + (int64_t)gi * kGroup,
-                   qsum ? qsum + m * G + gi : nullptr);
-      if (lane == 0) sx[m * G + gi] = s;
-    }
-    __syncthreads();
+    for (int i = 0; i < 32; ++i)  // 1/32 is exact; the warp has read all of its h
+      hs[b + 32 * i + lane] = bf16_bits_to_float(float_to_bf16_bits(r[i] * 0.03125f));
+  }
+  __syncthreads();
+  // Pass 3: the row's 128-groups shared by all warps.
+  for (int gi = warp; gi < G; gi += kPrepWarps) {
+    const float4 v4 = *reinterpret_cast<const float4*>(hs + gi * kGroup + 4 * lane);
+    const float a[4] = {v4.x, v4.y, v4.z, v4.w};
+    int qi[4];
+    const float s = quantize_group4(a, qi);
+    store_group4(qi, lane, q, layout, m * K + (int64_t)gi * kGroup,
+                 qsum ? qsum + m * G + gi : nullptr);
+    if (lane == 0) sx[m * G + gi] = s;
   }
 }
 
-}  // namespace
-
-int launch_norm_hadamard_quantize(const uint16_t* x, const uint16_t* residual,
-                                  uint16_t* residual_out, const uint16_t* w, const int8_t* sign,
-                                  float eps, int64_t M, int64_t K, uint16_t* norm_out, void* q,
-                                  int q_layout, float* sx, int32_t* qsum, cudaStream_t stream) {
-  const int smem = (int)((K + kHad + kPrepThreads) * sizeof(float));
+template <int kPrepThreads>
+int launch_prep(const uint16_t* x, const uint16_t* residual, uint16_t* residual_out,
+                const uint16_t* w, const int8_t* sign, float eps, int64_t M, int64_t K,
+                uint16_t* norm_out, void* q, int q_layout, float* sx, int32_t* qsum,
+                cudaStream_t stream) {
+  const int smem = (int)((K + kPrepThreads) * sizeof(float));
   static int configured = 0;
   if (smem > configured) {
-    if (cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess) {
+    if (cudaFuncSetAttribute(prep_kernel<kPrepThreads>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
       cudaGetLastError();
       return PQ2_ERR_LAUNCH;
     }
@@ -162,12 +237,29 @@ int launch_norm_hadamard_quantize(const uint16_t* x, const uint16_t* residual,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, prep_kernel, x, residual, residual_out, w, sign, eps, (int)K,
+  auto a16 = [](const void* ptr) { return reinterpret_cast<uintptr_t>(ptr) % 16 == 0; };
+  const int vec = a16(x) && (!residual || a16(residual)) && (!residual_out || a16(residual_out));
+  if (cudaLaunchKernelEx(&cfg, prep_kernel<kPrepThreads>, x, residual, residual_out, w, sign,
+                         eps, (int)K, vec,
                          norm_out, q, q_layout, sx, qsum) != cudaSuccess) {
     cudaGetLastError();
     return PQ2_ERR_LAUNCH;
   }
   return PQ2_OK;
+}
+
+}  // namespace
+
+int launch_norm_hadamard_quantize(const uint16_t* x, const uint16_t* residual,
+                                  uint16_t* residual_out, const uint16_t* w, const int8_t* sign,
+                                  float eps, int64_t M, int64_t K, uint16_t* norm_out, void* q,
+                                  int q_layout, float* sx, int32_t* qsum, cudaStream_t stream) {
+  // Rows resident at once with 256 threads: four per SM on 152 SMs.
+  if (M < 4 * 152)
+    return launch_prep<1024>(x, residual, residual_out, w, sign, eps, M, K, norm_out, q,
+                             q_layout, sx, qsum, stream);
+  return launch_prep<256>(x, residual, residual_out, w, sign, eps, M, K, norm_out, q, q_layout,
+                          sx, qsum, stream);
 }
 
 }  // namespace pq2

@@ -20,9 +20,16 @@
 
 namespace pq2 {
 
-// One group held by a full warp, lane L owning elements 4L..4L+3, with IEEE
-// round-to-nearest divisions.  Returns s (the same in every lane) and the
-// lane's four q.
+// One group held by a full warp, lane L owning elements 4L..4L+3.  Returns
+// s (the same in every lane) and the lane's four q, equal to
+// clamp(rint(a / d)) with the IEEE round-to-nearest quotient a / d.
+// The quotient is first formed as t = a * rcp(d) (rcp correctly rounded):
+// t differs from the rounded quotient by at most |a / d| * 2^-23 + 2^-24
+// relative, i.e. 2.3e-5 for |a / d| <= 127.01, so rint(t) is rint(a / d)
+// unless t lies within 1e-4 of a half-integer (t - rint(t) is exact).  If any
+// element of the group is that close (or d < 2^-120, where rcp(d) may
+// overflow), the whole group takes the IEEE divisions: one uniform branch,
+// rarely taken.
 __device__ __forceinline__ float quantize_group4(const float a[4], int qi[4]) {
   float amax = fmaxf(fmaxf(fabsf(a[0]), fabsf(a[1])), fmaxf(fabsf(a[2]), fabsf(a[3])));
 #pragma unroll
@@ -30,12 +37,21 @@ __device__ __forceinline__ float quantize_group4(const float a[4], int qi[4]) {
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
   const float s = __fdiv_rn(amax, 127.0f);
   const float d = s > 0.0f ? s : 1.0f;
+  const float inv = __frcp_rn(d);
+  bool near_tie = d < 7.52316385e-37f;  // 2^-120
+  float r[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    float r = rintf(__fdiv_rn(a[j], d));
-    r = fminf(fmaxf(r, -127.0f), 127.0f);
-    qi[j] = (int)r;
+    const float t = __fmul_rn(a[j], inv);
+    r[j] = rintf(t);
+    near_tie |= fabsf(t - r[j]) > 0.4999f;
   }
+  if (__any_sync(0xffffffffu, near_tie)) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) r[j] = rintf(__fdiv_rn(a[j], d));
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) qi[j] = (int)fminf(fmaxf(r[j], -127.0f), 127.0f);
   return s;
 }
 
