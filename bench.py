@@ -12,7 +12,8 @@ every call on a different weight matrix; the distinct matrices (more than 4x
 the L2 size in total) rotate, so weights always stream from HBM.  Steps are
 replayed from CUDA graphs and timed with CUDA events on the launching stream.
 
-  value       mean microseconds per complete call over the step (device time)
+  value       microseconds per complete call (device time) for the whole job:
+              the slowest rank's step time over all ranks' calls (N replicas)
   e2e         the same through host buffers, all inside the timed region:
               per step one copy of the step's x (M = 1..4, one pinned host
               buffer) to the device, the calls, one copy of the step's y
@@ -60,6 +61,25 @@ MMV_TRAFFIC_BYTES = (13_982_720 + 14_014_208) // 2
 WORKLOAD = ("attn_qkv K=5120 N=10240, M=1,2,3,4 per step (quantise + GEMV each); ternary "
             "codes U{0,1,2}, fp16 group-128 scales U[0.005,0.05]; bf16 x N(0,1) with 1% "
             "channels x20; fp32 accumulate, bf16 out")
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest value over the ranks of the process group (an all-reduce
+    MAX), or the value itself without one: the job's time is its slowest
+    rank's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_us_per_call(ms: float, calls_per_rank: int, world: int) -> float:
+    """Whole-job microseconds per call: `world` replicas each made
+    `calls_per_rank` calls in `ms` (the slowest rank's time)."""
+    return ms * 1e3 / (calls_per_rank * world)
 
 
 def measured_peaks():
@@ -518,12 +538,7 @@ def run_ours(args):
                 graphs[i % len(graphs)].replay()
             e1.record(stream)
             torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(e0.elapsed_time(e1), dev)
 
     warm_replays = -(-args.warmup // chunk)
     # soak (untimed) while the clock sampler runs, then the timed region
@@ -534,8 +549,8 @@ def run_ours(args):
         total_ms = timed(step_graphs, args.steps // chunk, warm_replays)
         e2e_ms = timed(e2e_graphs, args.steps // chunk, warm_replays)
     ms_step = total_ms / args.steps
-    us_call = ms_step * 1e3 / len(MS)
-    e2e_us = e2e_ms / args.steps * 1e3 / len(MS)
+    us_call = job_us_per_call(ms_step, len(MS), world)
+    e2e_us = job_us_per_call(e2e_ms / args.steps, len(MS), world)
 
     # ------------------------------------------- per-M and kernel-only legs
     per_m = {}
