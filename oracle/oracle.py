@@ -71,6 +71,10 @@ def load(path: str | None = None):
             "orc_scale_accumulate": (None, [P, P, P, I64, I64, I64, P, P, P]),
             "orc_linear": (None, [P, I, I64, I64, I64, I64, P, P, P, P, P, P, P]),
             "orc_gated": (None, [P, I64, I64, P]),
+            "orc_quantize_grouped": (None, [P, I64, I64, I, P, P]),
+            "orc_qsum_grouped": (None, [P, I64, I64, I, P]),
+            "orc_group_dots_grouped": (None, [P, P, I64, I64, I64, I, P]),
+            "orc_scale_accumulate_grouped": (None, [P, P, P, I64, I64, I64, I, P, P, P]),
             "orc_fwht1024": (None, [P]),
             "orc_sumsq2048": (ctypes.c_float, [P, I64]),
             "orc_norm_hadamard_quantize": (None, [P, P, P, P, ctypes.c_float, I64, I64,
@@ -217,6 +221,57 @@ def linear(x_bits: np.ndarray, kind: str, codes: np.ndarray,
                    _p(np.ascontiguousarray(scales)), _p(a), _p(q), _p(sx),
                    _p(dots), _p(y))
     return y
+
+
+def quantize_grouped(a: np.ndarray, A: int, lib=None):
+    """f32 a[M][K], activation group A (128, 64, 32) -> (q i8[M][K],
+    sx f32[M][K/A])."""
+    lib = lib or load()
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    M, K = a.shape
+    q = np.empty((M, K), np.int8)
+    sx = np.empty((M, K // A), np.float32)
+    lib.orc_quantize_grouped(_p(a), M, K, A, _p(q), _p(sx))
+    return q, sx
+
+
+def group_dots_grouped(q: np.ndarray, codes: np.ndarray, A: int, lib=None) -> np.ndarray:
+    """q i8[M][K], codes u8[N][K/4] -> int32 partial dots [M][N][K/A]."""
+    lib = lib or load()
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    M, K = q.shape
+    N = codes.shape[0]
+    dots = np.empty((M, N, K // A), np.int32)
+    lib.orc_group_dots_grouped(_p(q), _p(codes), M, N, K, A, _p(dots))
+    return dots
+
+
+def scale_accumulate_grouped(dots: np.ndarray, sx: np.ndarray, scales: np.ndarray, A: int,
+                             lib=None):
+    """-> (y32 f32[M][N], y64 f64[M][N], bound f64[M][N])."""
+    lib = lib or load()
+    dots = np.ascontiguousarray(dots, dtype=np.int32)
+    sx = np.ascontiguousarray(sx, dtype=np.float32)
+    scales = np.ascontiguousarray(scales, dtype=np.uint16)
+    M, N, GA = dots.shape
+    K = GA * A
+    y32 = np.empty((M, N), np.float32)
+    y64 = np.empty((M, N), np.float64)
+    bound = np.empty((M, N), np.float64)
+    lib.orc_scale_accumulate_grouped(_p(dots), _p(sx), _p(scales), M, N, K, A, _p(y32),
+                                     _p(y64), _p(bound))
+    return y32, y64, bound
+
+
+def qsum_grouped(q: np.ndarray, A: int, lib=None) -> np.ndarray:
+    """Sum of q over each A-group, int32 [M][K/A]."""
+    lib = lib or load()
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    M, K = q.shape
+    T = np.empty((M, K // A), np.int32)
+    lib.orc_qsum_grouped(_p(q), M, K, A, _p(T))
+    return T
 
 
 def gated(y64: np.ndarray, lib=None) -> np.ndarray:

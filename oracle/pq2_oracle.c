@@ -30,6 +30,10 @@
  *     gated-fusion calls: the projection's output is split in halves along
  *     the output dimension, gate first, and the result is silu(gate) * up,
  *     with silu(v) = v * sigmoid(v) = v / (1 + e^-v).
+ *   - smaller activation groups: KE Test 9 ("Smaller Q8 activation groups"):
+ *     the activations get one scale per A = 64 or 32 elements, the weights
+ *     keep their 128-groups and scales; each 128-group's dot splits into
+ *     128/A partial dots, each scaled by its own activation scale.
  *   - fused preparation of the activations: KE Test 18 ("RMSNorm + Hadamard
  *     + Q8 fusion"): h = x (+ residual) in fp32; the sum of h^2 over the row
  *     kept in 2048 strided partial sums, then summed; inv = 1/sqrt(mean +
@@ -235,6 +239,96 @@ void orc_scale_accumulate(const int32_t *dots, const float *sx,
         double term = (double)dot * (double)xs * (double)ws;
         acc64 += term;
         b += fabs(term);
+      }
+      if (y32) y32[m * N + n] = acc;
+      if (y64) y64[m * N + n] = acc64;
+      if (bound) bound[m * N + n] = b;
+    }
+}
+
+/* Quantiser with activation groups of A elements (A = 128, 64 or 32; KE
+ * Test 9): per A-group s = max|x| / 127, q = clamp(rne(x / d)) as
+ * orc_quantize; sx is [M][K/A]. */
+void orc_quantize_grouped(const float *a, int64_t M, int64_t K, int A, int8_t *q, float *sx) {
+  int saved = fegetround();
+  fesetround(FE_TONEAREST);
+  int64_t GA = K / A;
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t g = 0; g < GA; ++g) {
+      const float *x = a + m * K + g * A;
+      float amax = 0.0f;
+      for (int i = 0; i < A; ++i) {
+        float v = fabsf(x[i]);
+        if (v > amax) amax = v;
+      }
+      float s = amax / 127.0f;
+      float d = (s > 0.0f) ? s : 1.0f;
+      for (int i = 0; i < A; ++i) {
+        float r = nearbyintf(x[i] / d);
+        if (r > 127.0f) r = 127.0f;
+        if (r < -127.0f) r = -127.0f;
+        q[m * K + g * A + i] = (int8_t)r;
+      }
+      sx[m * GA + g] = s;
+    }
+  }
+  fesetround(saved);
+}
+
+/* Sum of q over each A-group: T[m][j], j = 0..K/A-1 (the masked-plane
+ * decoder's offset term, KE Test 21, per activation group). */
+void orc_qsum_grouped(const int8_t *q, int64_t M, int64_t K, int A, int32_t *T) {
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t j = 0; j < K / A; ++j) {
+      int32_t t = 0;
+      for (int i = 0; i < A; ++i) t += q[m * K + j * A + i];
+      T[m * (K / A) + j] = t;
+    }
+}
+
+/* Partial dots over each A-group: dots[m][n][j] = sum over k in
+ * [jA, jA + A) of (c_{n,k} - 1) q_{m,k}, j = 0..K/A-1. */
+void orc_group_dots_grouped(const int8_t *q, const uint8_t *codes, int64_t M, int64_t N,
+                            int64_t K, int A, int32_t *dots) {
+  int64_t GA = K / A;
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t n = 0; n < N; ++n)
+      for (int64_t j = 0; j < GA; ++j) {
+        int32_t acc = 0;
+        for (int i = 0; i < A; ++i) {
+          int64_t k = j * A + i;
+          int w = orc_decode_field(codes[n * (K / 4) + k / 4], (int)(k % 4));
+          acc += w * (int32_t)q[m * K + k];
+        }
+        dots[(m * N + n) * GA + j] = acc;
+      }
+}
+
+/* Scale and accumulate with activation groups of A elements (KE Test 9):
+ * y32[m][n] = sum over the weight groups g, then over their activation
+ * groups h = 0..128/A-1, of ((float)dot_{gh} * s_x[m][g*128/A + h]) *
+ * s_w[n][g], in sequential fp32; y64 the same in double; bound B = the sum
+ * of |s_x * s_w * dot| (double). */
+void orc_scale_accumulate_grouped(const int32_t *dots, const float *sx, const uint16_t *scales,
+                                  int64_t M, int64_t N, int64_t K, int A, float *y32,
+                                  double *y64, double *bound) {
+  int64_t G = K / ORC_GROUP, GA = K / A, H = ORC_GROUP / A;
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t n = 0; n < N; ++n) {
+      float acc = 0.0f;
+      double acc64 = 0.0, b = 0.0;
+      for (int64_t g = 0; g < G; ++g) {
+        float ws = orc_half_to_float(scales[n * G + g]);
+        for (int64_t h = 0; h < H; ++h) {
+          int32_t dot = dots[(m * N + n) * GA + g * H + h];
+          float xs = sx[m * GA + g * H + h];
+          float t = (float)dot * xs;
+          t = t * ws;
+          acc = acc + t;
+          double term = (double)dot * (double)xs * (double)ws;
+          acc64 += term;
+          b += fabs(term);
+        }
       }
       if (y32) y32[m * N + n] = acc;
       if (y64) y64[m * N + n] = acc64;

@@ -382,6 +382,94 @@ def pin_gated_end_to_end(lib):
     assert abs(out[0, 0] - want) <= 1e-13, (out, want)
 
 
+# ------------------------------------------ activation groups (KE Test 9)
+def pin_grouped_quantize_scales(lib):
+    """A = 64 and 32: each activation group gets its own max|x| / 127.  Group
+    maxima 127, 63.5, 31.75 and 100 (a later group larger than an earlier one)
+    give s = 1, 1/2, 1/4 and 100/127, and q = x / s."""
+    x = np.zeros((1, 128), np.float32)
+    x[0, 0:4] = [127.0, 10.0, -3.0, 0.0]
+    x[0, 32:35] = [63.5, 5.0, -2.5]
+    x[0, 64:66] = [31.75, 1.25]
+    x[0, 96:98] = [100.0, 40.0]
+    s100 = np.float32(100.0) / np.float32(127.0)
+    q64, s64 = O.quantize_grouped(x, 64, lib=lib)
+    assert list(s64[0]) == [1.0, s100], s64
+    q32, s32 = O.quantize_grouped(x, 32, lib=lib)
+    assert list(s32[0]) == [1.0, 0.5, 0.25, s100], s32
+    assert list(q32[0, 0:4]) == [127, 10, -3, 0]
+    assert list(q32[0, 32:35]) == [127, 10, -5]
+    assert list(q32[0, 64:66]) == [127, 5]
+    assert list(q32[0, 96:98]) == [127, 51]          # 40 * 127 / 100 = 50.8
+    assert list(O.qsum_grouped(q32, 32, lib=lib)[0]) == [134, 132, 132, 178]
+
+
+def pin_grouped_128_is_the_plain_path(lib):
+    """A = 128 reproduces the (separately pinned) ungrouped functions."""
+    rng = np.random.default_rng(9)
+    M, N, K = 2, 5, 384
+    a = (rng.standard_normal((M, K)) * 3).astype(np.float32)
+    q1, s1 = O.quantize(a, lib=lib)
+    q2, s2 = O.quantize_grouped(a, 128, lib=lib)
+    assert np.array_equal(q1, q2) and np.array_equal(s1.view(np.uint32), s2.view(np.uint32))
+    plane = _pack(rng.integers(0, 3, (N, K)).astype(np.uint8))
+    d1 = O.group_dots(q1, plane, lib=lib)
+    d2 = O.group_dots_grouped(q1, plane, 128, lib=lib)
+    assert np.array_equal(d1, d2)
+    sw = rng.uniform(0.005, 0.05, (N, K // G)).astype(np.float16).view(np.uint16)
+    y1 = O.scale_accumulate(d1, s1, sw, lib=lib)
+    y2 = O.scale_accumulate_grouped(d2, s2, sw, 128, lib=lib)
+    assert all(np.array_equal(u, v) for u, v in zip(y1, y2))
+
+
+def pin_grouped_dots_brute_force(lib):
+    """Partial dots against numpy's own decode (int64), and summed over a
+    128-group's partials they give the group's dot."""
+    rng = np.random.default_rng(4)
+    M, N, K = 3, 4, 256
+    q = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    plane = _pack(rng.integers(0, 3, (N, K)).astype(np.uint8))
+    w = _unpack_numpy(plane)
+    for A in (64, 32):
+        d = O.group_dots_grouped(q, plane, A, lib=lib)
+        ref = np.einsum("nk,mk->mnk", w, q.astype(np.int64)).reshape(M, N, K // A, A).sum(-1)
+        assert np.array_equal(d, ref), A
+        full = O.group_dots(q, plane, lib=lib)
+        assert np.array_equal(d.reshape(M, N, K // G, G // A).sum(-1), full), A
+        # fp64 scale-accumulate against a dense numpy evaluation: activation
+        # group j belongs to weight group j // (128 / A)
+        sx = rng.uniform(0.01, 0.1, (M, K // A)).astype(np.float32)
+        sw = rng.uniform(0.005, 0.05, (N, K // G)).astype(np.float16)
+        _, y64, _ = O.scale_accumulate_grouped(d, sx, sw.view(np.uint16), A, lib=lib)
+        wg = sw.astype(np.float64)[:, np.arange(K // A) // (G // A)]
+        ref = np.einsum("mnj,mj,nj->mn", d.astype(np.float64), sx.astype(np.float64), wg)
+        assert np.allclose(y64, ref, rtol=1e-12, atol=1e-12), A
+
+
+def pin_grouped_worked_example(lib):
+    """The worked example in both halves of a 128-group at A = 64: half 0
+    holds x = [20,30,40,10] with a 127 (s = 1, q = x), half 1 holds
+    [10,15,20,5] with a 63.5 (s = 1/2, q = [20,30,40,10]); codes [0,1,2,2]
+    in both halves give partial dots 30 and 30, and at weight scale 0.5
+    y = (30 * 1) * 0.5 + (30 * 0.5) * 0.5 = 22.5."""
+    ex = _golden("worked_example.json")
+    x = np.zeros((1, G), np.float32)
+    x[0, 0:4] = ex["q"]
+    x[0, 4] = 127.0
+    x[0, 64:68] = np.array(ex["q"], np.float32) / 2
+    x[0, 68] = 63.5
+    q, sx = O.quantize_grouped(x, 64, lib=lib)
+    assert list(sx[0]) == [1.0, 0.5]
+    codes = np.ones((1, G), np.uint8)
+    codes[0, 0:4] = ex["codes"]
+    codes[0, 64:68] = ex["codes"]
+    d = O.group_dots_grouped(q, _pack(codes), 64, lib=lib)
+    assert list(d[0, 0]) == [ex["dot"], ex["dot"]]
+    y32, y64, b = O.scale_accumulate_grouped(d, sx, np.array([[_f16_bits(0.5)]], np.uint16), 64,
+                                             lib=lib)
+    assert y32[0, 0] == np.float32(22.5) and y64[0, 0] == 22.5 and b[0, 0] == 22.5
+
+
 # ------------------------------------------- fused preparation (KE Test 18)
 def _walsh(k: int) -> np.ndarray:
     """Column k of the Sylvester Hadamard matrix of order 1024: entry j is

@@ -48,6 +48,12 @@ MUTANTS = [
     ("norm_weight_no_offset", "(orc_bf16_to_float(w[j]) + 1.0f)", "(orc_bf16_to_float(w[j]) + 0.0f)"),
     ("norm_eps_dropped", "1.0f / sqrtf(mean + eps)", "1.0f / sqrtf(mean)"),
     ("norm_sign_dropped", "* (float)sign[j];", "* 1.0f;"),
+    ("grouped_scale_index", "float xs = sx[m * GA + g * H + h];", "float xs = sx[m * GA + g * H];"),
+    ("grouped_quant_range", "for (int i = 0; i < A; ++i) {\n        float v = fabsf(x[i]);",
+     "for (int i = 0; i < ORC_GROUP && g * A + i < K; ++i) {\n        float v = fabsf(x[i]);"),
+    ("grouped_dot_offset", "int64_t k = j * A + i;", "int64_t k = j * A + i + 1 - (i + 1) / A;"),
+    ("grouped_weight_group", "float ws = orc_half_to_float(scales[n * G + g]);\n        for (int64_t h",
+     "float ws = orc_half_to_float(scales[n * G + (g * H) % G]);\n        for (int64_t h"),
     ("norm_residual_dropped", "if (residual) a = a + orc_bf16_to_float", "if (0) a = a + orc_bf16_to_float"),
 ]
 
