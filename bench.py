@@ -363,6 +363,57 @@ def gated_leg(args, dev, stream, timed, capture):
     return out
 
 
+def grouped_leg(args, dev, stream, timed, capture, mats, wbytes):
+    """Activation groups of 64 and 32 on the step's attn_qkv shape and its
+    rotated weight matrices (inputs larger than L2): pq2_mmv_grouped alone
+    (back-to-back independent calls on pre-quantised activations) and
+    pq2_quantize_act_grouped, M = 1..4; GB/s of packed weight bytes."""
+    import torch
+    from ternary_weight_int8_gb300 import pq2, synth
+    lib = pq2.lib()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sp = stream.cuda_stream
+    hbm, hbm_kind = measured_peaks()
+    out = {"workload": f"attn_qkv K={K_DIM} N={N_DIM}, bf16 x N(0,1) with 1% outliers, "
+                       f"bf16 out, {len(mats)} rotated matrices",
+           "bytes_per_call": wbytes, "peak_gbs": hbm, "peak_source": hbm_kind, "by_a": {}}
+    for A in (64, 32):
+        by_m = {}
+        for M in MS:
+            x = synth.activations(M, K_DIM, seed=500 + M + A, device=dev, outlier_frac=0.01)
+            q, sx, qs = pq2.pq2_quantize_act_grouped(x, A, pq2.PQ2_Q_PLANES)
+            y = torch.empty((M, N_DIM), dtype=torch.bfloat16, device=dev)
+
+            def mmv_calls():
+                for c, sc in mats:
+                    st = lib.pq2_mmv_grouped(q.data_ptr(), sx.data_ptr(), qs.data_ptr(),
+                                             c.data_ptr(), sc.data_ptr(), y.data_ptr(),
+                                             pq2.PQ2_BF16, M, N_DIM, K_DIM, A,
+                                             pq2.PQ2_MMV_INDEPENDENT, status.data_ptr(), sp)
+                    if st:
+                        raise RuntimeError(f"pq2_mmv_grouped failed ({st})")
+
+            def quant_calls():
+                for _ in mats:
+                    st = lib.pq2_quantize_act_grouped(x.data_ptr(), pq2.PQ2_BF16, K_DIM, M,
+                                                      K_DIM, A, q.data_ptr(), pq2.PQ2_Q_PLANES,
+                                                      sx.data_ptr(), qs.data_ptr(), sp)
+                    if st:
+                        raise RuntimeError(f"pq2_quantize_act_grouped failed ({st})")
+
+            reps = 30
+            k_ms = timed([capture(mmv_calls)], reps, 3) / (reps * len(mats))
+            q_ms = timed([capture(quant_calls)], reps, 3) / (reps * len(mats))
+            gbs = wbytes / (k_ms * 1e-3) / 1e9
+            by_m[str(M)] = {"mmv_us": round(k_ms * 1e3, 3), "mmv_gbs": round(gbs, 1),
+                            "mmv_frac": round(gbs / hbm, 3), "quant_us": round(q_ms * 1e3, 3)}
+            del x, q, sx, qs, y
+        out["by_a"][str(A)] = by_m
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    return out
+
+
 def prep_leg(args, dev, stream, timed, capture):
     """The fused preparation (pq2_norm_hadamard_quantize: RMSNorm with a
     residual, signs, 1024-point Walsh-Hadamard, group-128 INT8 in the plane
@@ -571,6 +622,8 @@ def run_ours(args):
     prefill = prefill_leg(args, dev, stream, timed, capture) if not args.no_prefill else None
     gated = gated_leg(args, dev, stream, timed, capture) if not args.no_gated else None
     prep = prep_leg(args, dev, stream, timed, capture) if not args.no_prep else None
+    grouped = (grouped_leg(args, dev, stream, timed, capture, mats, wbytes)
+               if not args.no_grouped else None)
     # dominant kernel: pq2_mmv over the step's M mix, kernel-only
     mean_k_us = statistics.mean(per_m[str(M)]["mmv_us"] for M in MS)
     achieved = wbytes / (mean_k_us * 1e-6) / 1e9
@@ -600,6 +653,7 @@ def run_ours(args):
         "prefill": prefill,
         "gated": gated,
         "prep": prep,
+        "grouped": grouped,
         "clocks": clocks.summary(),
     }
     if rank == 0 and not args.no_cpu:
@@ -654,6 +708,8 @@ def main():
                     help="skip the gated gate/up (pq2_mmv_gated) leg")
     ap.add_argument("--no-prep", action="store_true",
                     help="skip the fused preparation (pq2_norm_hadamard_quantize) leg")
+    ap.add_argument("--no-grouped", action="store_true",
+                    help="skip the activation-group 64/32 (pq2_mmv_grouped) leg")
     ap.add_argument("--profile-case", choices=["mmv", "mm"], default=None,
                     help="run a short fixed call sequence for an ncu capture and exit")
     ap.add_argument("--profile-m", type=int, default=1, help="columns for --profile-case")

@@ -197,6 +197,42 @@ int pq2_linear(const void *x, int x_dtype, int64_t ldx, int64_t M, int64_t N,
  * shape is invalid). */
 size_t pq2_linear_workspace_bytes(int64_t M, int64_t K);
 
+/* Activation groups of 64 or 32 (page "Kernel experiments: recorded
+ * evidence", Test 9, "Smaller Q8 activation groups"): the activations get
+ * one scale per act_group elements, the weights keep their 128-groups and
+ * scales, and each 128-group's dot splits into 128 / act_group partial dots,
+ * each scaled by its own activation scale:
+ *   y[m][n] = sum_g sum_{h < 128/A} (float(dot_gh) * s_x[m][g*128/A + h])
+ *             * s_w[n][g]        (fp32, each operation rounded to nearest)
+ * act_group = 128 is exactly pq2_quantize_act / pq2_mmv.
+ *
+ * pq2_quantize_act_grouped — pq2_quantize_act with activation groups of
+ * act_group (128, 64, 32) elements; sx and qsum are [M][K / act_group].
+ * q keeps the layouts of pq2_quantize_act. */
+int pq2_quantize_act_grouped(const void *x, int x_dtype, int64_t ldx,
+                             int64_t M, int64_t K, int act_group, void *q,
+                             int q_layout, float *sx, int32_t *qsum,
+                             void *stream);
+
+/* pq2_mmv_grouped — pq2_mmv_ex (masked-plane decoder, flags) on activations
+ * quantised by pq2_quantize_act_grouped with the same act_group; M 1..4.
+ * Batch invariant like pq2_mmv.  Returns PQ2_ERR_SHAPE for M > 4 or another
+ * act_group, else as pq2_mmv_ex. */
+int pq2_mmv_grouped(const int8_t *q_planes, const float *sx,
+                    const int32_t *qsum, const uint8_t *codes,
+                    const uint16_t *scales, void *y, int y_dtype, int64_t M,
+                    int64_t N, int64_t K, int act_group, int flags,
+                    int32_t *dev_status, void *stream);
+
+/* The exact partial dots of pq2_mmv_grouped, dots[m][n][j] = sum over k in
+ * [j*A, j*A + A) of (c_{n,k} - 1) q_{m,k}, from the same device code, for
+ * parity checks (M 1..4, q in PQ2_Q_PLANES order, qsum from
+ * pq2_quantize_act_grouped).  dots (device) int32 [M][N][K / A]. */
+int pq2_debug_group_dots_grouped(const int8_t *q_planes, const int32_t *qsum,
+                                 const uint8_t *codes, int64_t M, int64_t N,
+                                 int64_t K, int act_group, int32_t *dots,
+                                 int32_t *dev_status, void *stream);
+
 /* pq2_mmv_gated — the gate/up projection with its gated activation in the
  * GEMV's epilogue (page "Kernel experiments: recorded evidence", Test 12,
  * "gated" fusion screen: the projection's output z = x W^T of width N is

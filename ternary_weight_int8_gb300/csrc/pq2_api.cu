@@ -151,6 +151,57 @@ int pq2_mmv(const int8_t* q, const float* sx, const int32_t* qsum, const uint8_t
                     pq2_mmv_decoder(M < 1 ? 1 : M), 0, dev_status, stream);
 }
 
+int pq2_quantize_act_grouped(const void* x, int x_dtype, int64_t ldx, int64_t M, int64_t K,
+                             int act_group, void* q, int q_layout, float* sx, int32_t* qsum,
+                             void* stream) {
+  if (act_group != 128 && act_group != 64 && act_group != 32) return PQ2_ERR_SHAPE;
+  if (!x || !q || !sx) return PQ2_ERR_NULL;
+  if (x_dtype != PQ2_BF16 && x_dtype != PQ2_F16 && x_dtype != PQ2_F32) return PQ2_ERR_DTYPE;
+  if (q_layout != PQ2_Q_ROWS && q_layout != PQ2_Q_PLANES && q_layout != PQ2_Q_F16)
+    return PQ2_ERR_DTYPE;
+  if (M < 1 || M > kMaxM || !valid_k(K) || ldx < K || ldx > ((int64_t)1 << 40))
+    return PQ2_ERR_SHAPE;
+  if (!aligned(x, elem_bytes(x_dtype)) || !aligned(q, 16) || !aligned(sx, 4) ||
+      (qsum && !aligned(qsum, 4)))
+    return PQ2_ERR_ALIGN;
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  return pq2::launch_quantize(x, x_dtype, ldx, M, K, q, q_layout, sx, qsum,
+                              static_cast<cudaStream_t>(stream), act_group);
+}
+
+int pq2_mmv_grouped(const int8_t* q, const float* sx, const int32_t* qsum, const uint8_t* codes,
+                    const uint16_t* scales, void* y, int y_dtype, int64_t M, int64_t N,
+                    int64_t K, int act_group, int flags, int32_t* dev_status, void* stream) {
+  if (int st = check_mmv_args(q, sx, qsum, codes, scales, y, y_dtype, M, N, K,
+                              PQ2_DECODE_PLANES))
+    return st;
+  if (M > 4 || (act_group != 128 && act_group != 64 && act_group != 32)) return PQ2_ERR_SHAPE;
+  if (flags & ~(PQ2_MMV_OVERLAP_WEIGHTS | PQ2_MMV_INDEPENDENT)) return PQ2_ERR_DTYPE;
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  const int overlap = (flags & PQ2_MMV_INDEPENDENT) ? 2 : (flags & PQ2_MMV_OVERLAP_WEIGHTS) ? 1 : 0;
+  return pq2::launch_mmv_grouped(q, sx, qsum, codes, scales, y, y_dtype, nullptr, M, N, K,
+                                 act_group, overlap, sms, dev_status,
+                                 static_cast<cudaStream_t>(stream));
+}
+
+int pq2_debug_group_dots_grouped(const int8_t* q, const int32_t* qsum, const uint8_t* codes,
+                                 int64_t M, int64_t N, int64_t K, int act_group, int32_t* dots,
+                                 int32_t* dev_status, void* stream) {
+  if (!q || !qsum || !codes || !dots) return PQ2_ERR_NULL;
+  if (M < 1 || M > 4 || !valid_n(N) || !valid_k(K) ||
+      (act_group != 128 && act_group != 64 && act_group != 32))
+    return PQ2_ERR_SHAPE;
+  if (!aligned(q, 16) || !aligned(codes, 16) || !aligned(dots, 4) || !aligned(qsum, 4))
+    return PQ2_ERR_ALIGN;
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  return pq2::launch_mmv_grouped(q, nullptr, qsum, codes, nullptr, nullptr, PQ2_F32, dots, M, N,
+                                 K, act_group, 0, sms, dev_status,
+                                 static_cast<cudaStream_t>(stream));
+}
+
 int pq2_mmv_gated(const int8_t* q, const float* sx, const int32_t* qsum, const uint8_t* codes,
                   const uint16_t* scales, void* out, int out_dtype, int64_t M, int64_t N,
                   int64_t K, int flags, int32_t* dev_status, void* stream) {

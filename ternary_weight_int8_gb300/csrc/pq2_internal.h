@@ -30,9 +30,11 @@ int launch_prepare(const uint8_t* raw, int64_t raw_stride, int64_t N,
                    int64_t K, uint8_t* codes, uint16_t* scales,
                    cudaStream_t stream);
 
+// act_group: activation group of 128 (default), 64 or 32 elements; sx and
+// qsum are [M][K / act_group].
 int launch_quantize(const void* x, int x_dtype, int64_t ldx, int64_t M,
                     int64_t K, void* q, int q_layout, float* sx, int32_t* qsum,
-                    cudaStream_t stream);
+                    cudaStream_t stream, int act_group = 128);
 
 // overlap 1: the CTAs may stream the weight planes before the preceding
 // kernels on the stream have completed (programmatic dependent launch);
@@ -42,6 +44,13 @@ int launch_mmv(const int8_t* q, const float* sx, const int32_t* qsum,
                int y_dtype, int32_t* dots, int64_t M, int64_t N, int64_t K,
                int decode, int overlap, int sm_count, int32_t* status,
                cudaStream_t stream);
+
+// pq2_mmv with activation groups of act_group (128, 64, 32) elements: sx and
+// qsum are [M][K/act_group]; dots (debug) [M][N][K/act_group].  M <= 4.
+int launch_mmv_grouped(const int8_t* q, const float* sx, const int32_t* qsum,
+                       const uint8_t* codes, const uint16_t* scales, void* y, int y_dtype,
+                       int32_t* dots, int64_t M, int64_t N, int64_t K, int act_group,
+                       int overlap, int sm_count, int32_t* status, cudaStream_t stream);
 
 // Gated gate/up output: out[m][n] = silu(y[m][n]) * y[m][n + N/2] for
 // n < N/2, y as launch_mmv computes it (N even, dots not supported).

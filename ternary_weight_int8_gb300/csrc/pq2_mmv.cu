@@ -254,9 +254,84 @@ __device__ __forceinline__ void group_dot(const uint32_t (&c0)[RP], const uint32
   }
 }
 
+// Partial dots of one 128-group over its NSUB activation groups of
+// A = 128 / NSUB elements (KE Test 9), masked-plane decoder: activation group
+// u covers weights [uA, uA + A), i.e. half h = u / (NSUB / 2) of the group's
+// code bytes and, for A = 32, code words 2v, 2v + 1 of that half
+// (v = u % 2).  Each partial is finished as in group_dot with its own
+// sum(q) and handed to emit(u, dot[RP][MB]) in increasing u.
+//   qs : shared address of sum(q) of activation group 0 of this 128-group
+//        for column 0; group u of column m at qs + (m * qs_mstride) + 4u
+template <int MB, int RP, int NSUB, typename Emit>
+__device__ __forceinline__ void group_dot_sub(const uint32_t (&c0)[RP], const uint32_t (&c1)[RP],
+                                              uint32_t qz, int q_mstride, int qsw, uint32_t qs,
+                                              int qs_mstride, Emit&& emit) {
+  static_assert(NSUB == 2 || NSUB == 4, "activation groups of 64 or 32");
+  constexpr int HS = NSUB / 2;  // activation groups per half
+  constexpr int WPS = 4 / HS;   // code words of a half per activation group
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t cw[RP][4];
+#pragma unroll
+    for (int r = 0; r < RP; ++r) {
+      const uint4 c = lds128(h ? c1[r] : c0[r]);
+      cw[r][0] = c.x; cw[r][1] = c.y; cw[r][2] = c.z; cw[r][3] = c.w;
+    }
+    // even planes accumulate code * q, odd planes 4 * code * q
+    int acc[HS][RP][2][MB];
+#pragma unroll
+    for (int v = 0; v < HS; ++v)
+#pragma unroll
+      for (int r = 0; r < RP; ++r)
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int m = 0; m < MB; ++m) acc[v][r][a][m] = 0;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      if (s == 2) {
+#pragma unroll
+        for (int r = 0; r < RP; ++r)
+#pragma unroll
+          for (int w = 0; w < 4; ++w) cw[r][w] >>= 4;
+      }
+      uint4 qv[MB];
+#pragma unroll
+      for (int m = 0; m < MB; ++m)
+        qv[m] = lds128(qz + m * q_mstride + ((s * 32 + 16 * h) ^ qsw));
+#pragma unroll
+      for (int r = 0; r < RP; ++r)
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t wv = cw[r][w] & ((s & 1) ? 0x0C0C0C0Cu : 0x03030303u);
+#pragma unroll
+          for (int m = 0; m < MB; ++m) {
+            const int qw =
+                (int)(w == 0 ? qv[m].x : w == 1 ? qv[m].y : w == 2 ? qv[m].z : qv[m].w);
+            int& a = acc[w / WPS][r][s & 1][m];
+            a = dp4a_us(wv, qw, a);
+          }
+        }
+    }
+#pragma unroll
+    for (int v = 0; v < HS; ++v) {
+      const int u = h * HS + v;
+      int dot[RP][MB];
+#pragma unroll
+      for (int m = 0; m < MB; ++m) {
+        const int qsm = (int)lds32(qs + m * qs_mstride + 4 * u);
+#pragma unroll
+        for (int r = 0; r < RP; ++r)
+          dot[r][m] = acc[v][r][0][m] + (acc[v][r][1][m] >> 2) - qsm;
+      }
+      emit(u, dot);
+    }
+  }
+}
+
 // Up to four columns two CTAs fit on an SM (a call overlaps the next one);
 // more columns need the registers of one CTA per SM.
-template <int M, int DEC, bool DOTS>
+template <int M, int DEC, bool DOTS, int NSUB = 1>
 __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
     mmv_kernel(const __grid_constant__ CUtensorMap map_hi,
                const __grid_constant__ CUtensorMap map_lo,
@@ -347,12 +422,12 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
                      src0 + ((size_t)m * G + l) * kGroup + c * 16);
       if (i == 0) {
         if (p.side16) {
-          for (int idx = 4 * lane; idx < M * G; idx += 128) {
+          for (int idx = 4 * lane; idx < M * G * NSUB; idx += 128) {
             if (!DOTS) cp_async16(smem_u32(sx_s + idx), p.sx + idx);
             if (need_qs) cp_async16(smem_u32(qs_s + idx), p.qsum + idx);
           }
         } else {
-          for (int idx = lane; idx < M * G; idx += 32) {
+          for (int idx = lane; idx < M * G * NSUB; idx += 32) {
             if (!DOTS) cp_async4(sx_s + idx, p.sx + idx);
             if (need_qs) cp_async4(qs_s + idx, p.qsum + idx);
           }
@@ -431,8 +506,10 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
     for (int m = 0; m < M; ++m) yacc[r][m] = 0.0f;
 
   // Scale and accumulate the dots of columns m0 .. m0+MB-1 in the method's
-  // order: t = (float(dot) * s_x) * s_w, y += t.
-  auto consume = [&](auto& dot, int m0, int g) {
+  // order: t = (float(dot) * s_x) * s_w, y += t (activation group u of the
+  // 128-group g when NSUB > 1).
+  constexpr int GA_PER_G = NSUB;
+  auto consume = [&](auto& dot, int m0, int g, int u) {
     constexpr int MB = sizeof(dot[0]) / sizeof(int);
     if constexpr (DOTS) {
 #pragma unroll
@@ -440,7 +517,8 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
         if (valid[r])
 #pragma unroll
           for (int m = 0; m < MB; ++m)
-            p.dots[((size_t)(m0 + m) * p.N + n0 + rows[r]) * G + g] = dot[r][m];
+            p.dots[((size_t)(m0 + m) * p.N + n0 + rows[r]) * G * NSUB + g * NSUB + u] =
+                dot[r][m];
     } else {
       float ws[RP];
 #pragma unroll
@@ -448,7 +526,8 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
         ws[r] = __half2float(__ushort_as_half((uint16_t)lds16(sw_base + (rows[r] * G + g) * 2)));
 #pragma unroll
       for (int m = 0; m < MB; ++m) {
-        const float xs = __uint_as_float(lds32(sx_base + ((m0 + m) * G + g) * 4));
+        const float xs =
+            __uint_as_float(lds32(sx_base + (((m0 + m) * G + g) * GA_PER_G + u) * 4));
 #pragma unroll
         for (int r = 0; r < RP; ++r) {
           float t = __fmul_rn(__int2float_rn(dot[r][m]), xs);
@@ -476,16 +555,23 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
     const int qsw = (l & 7) << 4;
     // Columns in blocks of at most four keep the accumulators in registers.
     constexpr int MA = M <= 4 ? M : 4;
-    {
-      int dot[RP][MA];
-      group_dot<MA, RP, DEC>(c0, c1, qz, p.qbox_stride, qsw, qs_base + g * 4, G * 4, dot);
-      consume(dot, 0, g);
-    }
-    if constexpr (M > 4) {
-      int dot[RP][M - 4];
-      group_dot<M - 4, RP, DEC>(c0, c1, qz + 4 * p.qbox_stride, p.qbox_stride, qsw,
-                                qs_base + (4 * G + g) * 4, G * 4, dot);
-      consume(dot, 4, g);
+    if constexpr (NSUB > 1) {
+      static_assert(M <= 4 && DEC == kDecodeMaskPlanes, "activation groups: M <= 4, planes");
+      group_dot_sub<M, RP, NSUB>(c0, c1, qz, p.qbox_stride, qsw, qs_base + g * NSUB * 4,
+                                 G * NSUB * 4,
+                                 [&](int u, auto& dot) { consume(dot, 0, g, u); });
+    } else {
+      {
+        int dot[RP][MA];
+        group_dot<MA, RP, DEC>(c0, c1, qz, p.qbox_stride, qsw, qs_base + g * 4, G * 4, dot);
+        consume(dot, 0, g, 0);
+      }
+      if constexpr (M > 4) {
+        int dot[RP][M - 4];
+        group_dot<M - 4, RP, DEC>(c0, c1, qz + 4 * p.qbox_stride, p.qbox_stride, qsw,
+                                  qs_base + (4 * G + g) * 4, G * 4, dot);
+        consume(dot, 4, g, 0);
+      }
     }
   };
 
@@ -602,10 +688,10 @@ bool encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_by
 int align_up(int v, int a) { return (v + a - 1) / a * a; }
 int gcd(int a, int b) { return b ? gcd(b, a % b) : a; }
 
-template <int M, int DEC, bool DOTS>
+template <int M, int DEC, bool DOTS, int NSUB = 1>
 int launch_one(const CUtensorMap& hi, const CUtensorMap& lo,
                const MmvParams& p, int smem, cudaStream_t stream) {
-  auto kern = mmv_kernel<M, DEC, DOTS>;
+  auto kern = mmv_kernel<M, DEC, DOTS, NSUB>;
   static int configured = 0;  // largest dynamic smem size set so far
   if (smem > configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSoloSmem) !=
@@ -642,6 +728,29 @@ int launch_m(int M, const CUtensorMap& hi, const CUtensorMap& lo,
     case 6: return launch_one<6, DEC, DOTS>(hi, lo, p, smem, s);
     case 7: return launch_one<7, DEC, DOTS>(hi, lo, p, smem, s);
     case 8: return launch_one<8, DEC, DOTS>(hi, lo, p, smem, s);
+    default: return PQ2_ERR_SHAPE;
+  }
+}
+
+// Activation groups of 128 / NSUB (NSUB = 2, 4), masked planes, M <= 4.
+template <bool DOTS>
+int launch_m_sub(int nsub, int M, const CUtensorMap& hi, const CUtensorMap& lo,
+                 const MmvParams& p, int smem, cudaStream_t s) {
+  constexpr int D = kDecodeMaskPlanes;
+  if (nsub == 2) {
+    switch (M) {
+      case 1: return launch_one<1, D, DOTS, 2>(hi, lo, p, smem, s);
+      case 2: return launch_one<2, D, DOTS, 2>(hi, lo, p, smem, s);
+      case 3: return launch_one<3, D, DOTS, 2>(hi, lo, p, smem, s);
+      case 4: return launch_one<4, D, DOTS, 2>(hi, lo, p, smem, s);
+      default: return PQ2_ERR_SHAPE;
+    }
+  }
+  switch (M) {
+    case 1: return launch_one<1, D, DOTS, 4>(hi, lo, p, smem, s);
+    case 2: return launch_one<2, D, DOTS, 4>(hi, lo, p, smem, s);
+    case 3: return launch_one<3, D, DOTS, 4>(hi, lo, p, smem, s);
+    case 4: return launch_one<4, D, DOTS, 4>(hi, lo, p, smem, s);
     default: return PQ2_ERR_SHAPE;
   }
 }
@@ -693,7 +802,10 @@ namespace {
 int launch_mmv_impl(const int8_t* q, const float* sx, const int32_t* qsum,
                     const uint8_t* codes, const uint16_t* scales, void* y, int y_dtype,
                     int32_t* dots, int64_t M, int64_t N, int64_t K, int decode, int overlap,
-                    bool gated, int sm_count, int32_t* status, cudaStream_t stream) {
+                    bool gated, int sm_count, int32_t* status, cudaStream_t stream,
+                    int nsub = 1) {
+  if (nsub != 1 && ((nsub != 2 && nsub != 4) || M > 4 || gated || decode != kDecodeMaskPlanes))
+    return PQ2_ERR_SHAPE;
   MmvGeometry geo;
   if (!mmv_geometry(N, K, sm_count, &geo)) return PQ2_ERR_SHAPE;
   if (gated && (N % 2 || dots)) return PQ2_ERR_SHAPE;
@@ -722,7 +834,7 @@ int launch_mmv_impl(const int8_t* q, const float* sx, const int32_t* qsum,
   p.overlap = overlap;
   p.y_bf16 = y_dtype == PQ2_BF16;
   p.sw_bulk = (K / kGroup) % 8 == 0 && reinterpret_cast<uintptr_t>(scales) % 16 == 0;
-  p.side16 = (M * (K / kGroup)) % 4 == 0 && reinterpret_cast<uintptr_t>(sx) % 16 == 0 &&
+  p.side16 = (M * (K / kGroup) * nsub) % 4 == 0 && reinterpret_cast<uintptr_t>(sx) % 16 == 0 &&
              reinterpret_cast<uintptr_t>(qsum) % 16 == 0;
   const int mi = (int)M, R = rows_max, S = geo.splits, G = p.G;
   const int unit = 4 * S / gcd(4, S);
@@ -732,8 +844,8 @@ int launch_mmv_impl(const int8_t* q, const float* sx, const int32_t* qsum,
   // fixed region: barriers, weight scales, s_x, sum(q)
   p.sw_off = align_up(2 * 8 * kMaxStages + 8, 128);
   p.sx_off = align_up(p.sw_off + G * slab * 2, 16);
-  p.qs_off = align_up(p.sx_off + mi * G * 4, 16);
-  p.ring_off = align_up(p.qs_off + mi * G * 4, 1024);
+  p.qs_off = align_up(p.sx_off + mi * G * nsub * 4, 16);
+  p.ring_off = align_up(p.qs_off + mi * G * nsub * 4, 1024);
   const int room = kSmemBudget - p.ring_off;
   // Stage: k units of lcm(4, S) groups, aiming at ~16-24 KB of codes.
   auto stage_bytes = [&](int gs) {
@@ -778,6 +890,9 @@ int launch_mmv_impl(const int8_t* q, const float* sx, const int32_t* qsum,
   if (!encode_map(&hi, codes, N, K / 4, R) ||
       !encode_map(&lo, codes, N, K / 4, rows_lo > 0 ? rows_lo : R))
     return PQ2_ERR_LAUNCH;
+  if (nsub > 1)
+    return dots ? launch_m_sub<true>(nsub, mi, hi, lo, p, smem, stream)
+                : launch_m_sub<false>(nsub, mi, hi, lo, p, smem, stream);
   if (dots)
     return decode == kDecodeMaskPlanes
                ? launch_m<kDecodeMaskPlanes, true>(mi, hi, lo, p, smem, stream)
@@ -795,6 +910,16 @@ int launch_mmv(const int8_t* q, const float* sx, const int32_t* qsum, const uint
                cudaStream_t stream) {
   return launch_mmv_impl(q, sx, qsum, codes, scales, y, y_dtype, dots, M, N, K, decode,
                          overlap, false, sm_count, status, stream);
+}
+
+int launch_mmv_grouped(const int8_t* q, const float* sx, const int32_t* qsum,
+                       const uint8_t* codes, const uint16_t* scales, void* y, int y_dtype,
+                       int32_t* dots, int64_t M, int64_t N, int64_t K, int act_group,
+                       int overlap, int sm_count, int32_t* status, cudaStream_t stream) {
+  if (act_group != 128 && act_group != 64 && act_group != 32) return PQ2_ERR_SHAPE;
+  return launch_mmv_impl(q, sx, qsum, codes, scales, y, y_dtype, dots, M, N, K,
+                         kDecodeMaskPlanes, overlap, false, sm_count, status, stream,
+                         128 / act_group);
 }
 
 int launch_mmv_gated(const int8_t* q, const float* sx, const int32_t* qsum,

@@ -20,8 +20,11 @@
 
 namespace pq2 {
 
-// One group held by a full warp, lane L owning elements 4L..4L+3.  Returns
-// s (the same in every lane) and the lane's four q, equal to
+// One 128-group held by a full warp, lane L owning elements 4L..4L+3, in
+// activation groups of 4 * LANES elements (LANES = 32: the whole 128-group;
+// 16 or 8: groups of 64 or 32, KE Test 9).  Returns the scale s of the
+// lane's activation group (the same in all its lanes) and the lane's four q,
+// equal to
 // clamp(rint(a / d)) with the IEEE round-to-nearest quotient a / d.
 // The quotient is first formed as t = a * rcp(d) (rcp correctly rounded):
 // t differs from the rounded quotient by at most |a / d| * 2^-23 + 2^-24
@@ -30,10 +33,11 @@ namespace pq2 {
 // element of the group is that close (or d < 2^-120, where rcp(d) may
 // overflow), the whole group takes the IEEE divisions: one uniform branch,
 // rarely taken.
+template <int LANES = 32>
 __device__ __forceinline__ float quantize_group4(const float a[4], int qi[4]) {
   float amax = fmaxf(fmaxf(fabsf(a[0]), fabsf(a[1])), fmaxf(fabsf(a[2]), fabsf(a[3])));
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1)
+  for (int off = LANES / 2; off > 0; off >>= 1)
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
   const float s = __fdiv_rn(amax, 127.0f);
   const float d = s > 0.0f ? s : 1.0f;
@@ -55,9 +59,11 @@ __device__ __forceinline__ float quantize_group4(const float a[4], int qi[4]) {
   return s;
 }
 
-// Store one group's q (lane L holding elements 4L..4L+3 of the group that
-// starts at element `base` of q) in the requested layout, and its sum of q
-// (to *qsum when non-null).  Every lane of the warp must call it.
+// Store one 128-group's q (lane L holding elements 4L..4L+3 of the group
+// that starts at element `base` of q) in the requested layout, and the sum of
+// q of each of its activation groups of 4 * LANES elements (to qsum[0 ..
+// 32 / LANES - 1] when non-null).  Every lane of the warp must call it.
+template <int LANES = 32>
 __device__ __forceinline__ void store_group4(const int qi[4], int lane, void* q, int layout,
                                              int64_t base, int32_t* qsum) {
   const uint32_t packed = (uint32_t)(qi[0] & 0xff) | ((uint32_t)(qi[1] & 0xff) << 8) |
@@ -98,8 +104,8 @@ __device__ __forceinline__ void store_group4(const int qi[4], int lane, void* q,
   }
   int t = qi[0] + qi[1] + qi[2] + qi[3];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
-  if (qsum && lane == 0) *qsum = t;
+  for (int off = LANES / 2; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+  if (qsum && lane % LANES == 0) qsum[lane / LANES] = t;
 }
 
 }  // namespace pq2

@@ -86,9 +86,10 @@ __device__ __forceinline__ void load4(const void* x, int64_t i, bool vec,
   }
 }
 
-// One warp per (row m, group g); lane L owns elements 4L..4L+3 of the group
-// (quantize_group4 / store_group4).
-template <int XT>
+// One warp per (row m, 128-group g); lane L owns elements 4L..4L+3 of the
+// group (quantize_group4 / store_group4), in activation groups of 4 * LANES
+// elements: sx and qsum are [M][K / (4 * LANES)].
+template <int XT, int LANES>
 __global__ void __launch_bounds__(256) quantize_kernel(
     const void* __restrict__ x, int64_t ldx, int64_t M, int G, bool vec,
     void* __restrict__ q, int layout, float* __restrict__ sx,
@@ -107,10 +108,12 @@ __global__ void __launch_bounds__(256) quantize_kernel(
 
   float a[4];
   load4<XT>(x, m * ldx + (int64_t)g * kGroup + 4 * lane, vec, a);
+  constexpr int NSUB = 32 / LANES;  // activation groups per 128-group
   int qi[4];
-  const float s = quantize_group4(a, qi);
-  store_group4(qi, lane, q, layout, m * K + (int64_t)g * kGroup, qsum ? qsum + m * G + g : nullptr);
-  if (lane == 0) sx[m * G + g] = s;
+  const float s = quantize_group4<LANES>(a, qi);
+  store_group4<LANES>(qi, lane, q, layout, m * K + (int64_t)g * kGroup,
+                      qsum ? qsum + (m * G + g) * NSUB : nullptr);
+  if (lane % LANES == 0) sx[(m * G + g) * NSUB + lane / LANES] = s;
 }
 
 }  // namespace
@@ -125,9 +128,30 @@ int launch_prepare(const uint8_t* raw, int64_t raw_stride, int64_t N,
   return cudaGetLastError() == cudaSuccess ? PQ2_OK : PQ2_ERR_LAUNCH;
 }
 
+namespace {
+
+template <int XT>
+cudaError_t launch_quantize_xt(const cudaLaunchConfig_t& cfg, int act_group, const void* x,
+                               int64_t ldx, int64_t M, int G, bool vec, void* q, int q_layout,
+                               float* sx, int32_t* qsum) {
+  switch (act_group) {
+    case 64:
+      return cudaLaunchKernelEx(&cfg, quantize_kernel<XT, 16>, x, ldx, M, G, vec, q, q_layout, sx,
+                                qsum);
+    case 32:
+      return cudaLaunchKernelEx(&cfg, quantize_kernel<XT, 8>, x, ldx, M, G, vec, q, q_layout, sx,
+                                qsum);
+    default:
+      return cudaLaunchKernelEx(&cfg, quantize_kernel<XT, 32>, x, ldx, M, G, vec, q, q_layout, sx,
+                                qsum);
+  }
+}
+
+}  // namespace
+
 int launch_quantize(const void* x, int x_dtype, int64_t ldx, int64_t M,
                     int64_t K, void* q, int q_layout, float* sx, int32_t* qsum,
-                    cudaStream_t stream) {
+                    cudaStream_t stream, int act_group) {
   const int G = (int)(K / kGroup);
   const int elem = x_dtype == PQ2_F32 ? 4 : 2;
   const uintptr_t addr = reinterpret_cast<uintptr_t>(x);
@@ -146,13 +170,13 @@ int launch_quantize(const void* x, int x_dtype, int64_t ldx, int64_t M,
   cudaError_t e;
   switch (x_dtype) {
     case PQ2_BF16:
-      e = cudaLaunchKernelEx(&cfg, quantize_kernel<PQ2_BF16>, x, ldx, M, G, vec, q, q_layout, sx, qsum);
+      e = launch_quantize_xt<PQ2_BF16>(cfg, act_group, x, ldx, M, G, vec, q, q_layout, sx, qsum);
       break;
     case PQ2_F16:
-      e = cudaLaunchKernelEx(&cfg, quantize_kernel<PQ2_F16>, x, ldx, M, G, vec, q, q_layout, sx, qsum);
+      e = launch_quantize_xt<PQ2_F16>(cfg, act_group, x, ldx, M, G, vec, q, q_layout, sx, qsum);
       break;
     default:
-      e = cudaLaunchKernelEx(&cfg, quantize_kernel<PQ2_F32>, x, ldx, M, G, vec, q, q_layout, sx, qsum);
+      e = launch_quantize_xt<PQ2_F32>(cfg, act_group, x, ldx, M, G, vec, q, q_layout, sx, qsum);
       break;
   }
   if (e != cudaSuccess) {

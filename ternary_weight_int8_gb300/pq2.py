@@ -45,6 +45,9 @@ SIGNATURES = {
     "pq2_linear_workspace_bytes": (_SZ, [_I64, _I64]),
     "pq2_linear_static": (_I, [_P, _I, _I64, _I64, _I64, _I64, _P, _P, _P, _I, _P, _P]),
     "pq2_mmv_gated": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _P, _P]),
+    "pq2_quantize_act_grouped": (_I, [_P, _I, _I64, _I64, _I64, _I, _P, _I, _P, _P, _P]),
+    "pq2_mmv_grouped": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _I, _P, _P]),
+    "pq2_debug_group_dots_grouped": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P, _P, _P]),
     "pq2_norm_hadamard_quantize": (_I, [_P, _P, _P, _P, _P, ctypes.c_float, _I64, _I64, _P,
                                         _P, _I, _P, _P, _P]),
     "pq2_linear_gated": (_I, [_P, _I, _I64, _I64, _I64, _I64, _P, _P, _P, _I, _P, _SZ, _P, _P]),
@@ -181,6 +184,46 @@ def pq2_linear(x, codes, scales, y=None, out_dtype=torch.float32, workspace=None
         _DT[y.dtype], _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(status), _stream(stream)))
     return y
+
+
+def pq2_quantize_act_grouped(x: torch.Tensor, act_group: int, layout: int = PQ2_Q_PLANES,
+                             stream=None):
+    """x[M][K] -> (q, sx [M][K/A], qsum [M][K/A]) with activation groups of A."""
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit column stride")
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.float16 if layout == PQ2_Q_F16 else torch.int8,
+                    device=x.device)
+    sx = torch.empty((M, K // act_group), dtype=torch.float32, device=x.device)
+    qsum = torch.empty((M, K // act_group), dtype=torch.int32, device=x.device)
+    _check("pq2_quantize_act_grouped", lib().pq2_quantize_act_grouped(
+        _ptr(x), _DT[x.dtype], x.stride(0), M, K, act_group, _ptr(q), layout, _ptr(sx),
+        _ptr(qsum), _stream(stream)))
+    return q, sx, qsum
+
+
+def pq2_mmv_grouped(q_planes, sx, qsum, codes, scales, act_group: int, y=None,
+                    out_dtype=torch.float32, flags=0, status=None, stream=None):
+    """GEMV with activation groups of A (M = 1..4)."""
+    M, K = q_planes.shape
+    N = codes.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=q_planes.device)
+    _check("pq2_mmv_grouped", lib().pq2_mmv_grouped(
+        _ptr(q_planes), _ptr(sx), _ptr(qsum), _ptr(codes), _ptr(scales), _ptr(y), _DT[y.dtype],
+        M, N, K, act_group, flags, _ptr(status), _stream(stream)))
+    return y
+
+
+def pq2_debug_group_dots_grouped(q_planes, qsum, codes, act_group: int, stream=None):
+    """Exact partial dots [M][N][K/A] of the grouped GEMV's device code."""
+    M, K = q_planes.shape
+    N = codes.shape[0]
+    dots = torch.empty((M, N, K // act_group), dtype=torch.int32, device=q_planes.device)
+    _check("pq2_debug_group_dots_grouped", lib().pq2_debug_group_dots_grouped(
+        _ptr(q_planes), _ptr(qsum), _ptr(codes), M, N, K, act_group, _ptr(dots), None,
+        _stream(stream)))
+    return dots
 
 
 def pq2_mmv_gated(q_planes, sx, qsum, codes, scales, out=None, out_dtype=torch.float32,
