@@ -62,6 +62,8 @@ def load(path: str | None = None):
             "orc_bf16_to_float": (ctypes.c_float, [ctypes.c_uint16]),
             "orc_float_to_bf16_rne": (ctypes.c_uint16, [ctypes.c_float]),
             "orc_prepare": (None, [P, I64, I64, I64, P, P]),
+            "orc_ptq_trit": (I, [ctypes.c_uint8, I]),
+            "orc_ptq_unpack": (None, [P, I64, I64, I64, P, P]),
             "orc_decode_matrix": (None, [P, I64, I64, P]),
             "orc_quantize": (None, [P, I64, I64, P, P]),
             "orc_widen": (None, [P, I, I64, I64, I64, P]),
@@ -136,6 +138,23 @@ def decode_matrix(codes: np.ndarray, K: int, lib=None) -> np.ndarray:
     w = np.empty((codes.shape[0], K), np.int8)
     lib.orc_decode_matrix(_p(codes), codes.shape[0], K, _p(w))
     return w
+
+
+def ptq_trit(byte: int, level: int, lib=None) -> int:
+    lib = lib or load()
+    return int(lib.orc_ptq_trit(byte, level))
+
+
+def ptq_unpack(raw: np.ndarray, K: int, lib=None):
+    """PTQ1_0 rows u8[N][>= K/128*28] -> (code plane u8[N][K/4] with code =
+    trit, fp16 scale bits u16[N][K/128])."""
+    lib = lib or load()
+    raw = np.ascontiguousarray(raw, dtype=np.uint8)
+    N = raw.shape[0]
+    codes = np.empty((N, K // 4), np.uint8)
+    scales = np.empty((N, K // GROUP), np.uint16)
+    lib.orc_ptq_unpack(_p(raw), raw.shape[1], N, K, _p(codes), _p(scales))
+    return codes, scales
 
 
 # ------------------------------------------------------------ quantisation

@@ -40,6 +40,15 @@
  *     eps); normalised = bf16((h * inv) * (w + 1)); v = normalised * sign;
  *     a 1024-point Walsh-Hadamard transform; bf16; then the group-128 INT8
  *     quantiser above.
+ *   - PTQ1_0 weights: page "KERNEL_REPORT: PTQ1_0 small-batch decoding on the
+ *     PrismML fork, RTX 3060 12GB" (abbreviated KR), "What the source said":
+ *     a 28-byte block per 128 weights; 24 qs bytes of five trits each,
+ *     unpacked by repeatedly multiplying by 3 (a 16-bit lane) and taking the
+ *     part above the low byte; qh, two bytes holding the other 8 trits; the
+ *     fp16 scale d in the last two bytes; trit t means weight t - 1.  The
+ *     page does not say which trit is which weight; the reading taken here:
+ *     trit n of qs byte j is weight 24n + j, trit n (n < 4) of qh byte j is
+ *     weight 120 + 2n + j.
  *
  * Parity pins for every function live in tests/test_oracle_pins.py.
  */
@@ -123,6 +132,52 @@ void orc_decode_matrix(const uint8_t *codes, int64_t N, int64_t K, int8_t *w) {
     for (int64_t k = 0; k < K; ++k)
       w[n * K + k] =
           (int8_t)orc_decode_field(codes[n * (K / 4) + k / 4], (int)(k % 4));
+}
+
+/* ------------------------------------------------------------------ PTQ1_0 */
+
+#define ORC_PTQ_BLOCK_BYTES 28
+
+/* Trit `level` (0 first) of a five-trit byte, KR: v <- 3v in a 16-bit lane,
+ * the trit is the part above the low byte, the low byte carries on. */
+int orc_ptq_trit(uint8_t byte, int level) {
+  unsigned v = byte, t = 0;
+  for (int n = 0; n <= level; ++n) {
+    unsigned w = 3u * v;
+    t = w >> 8;
+    v = w & 0xFFu;
+  }
+  return (int)t;
+}
+
+/* PTQ1_0 rows -> the code plane used everywhere in this file (code = trit, so
+ * the weight is code - 1) and the fp16 scale bits.
+ *   raw    : N rows, row stride raw_stride bytes, K/128 blocks of 28 bytes:
+ *            qs bytes 0-23, qh bytes 24-25, d bytes 26-27 (little-endian)
+ *   codes  : [N][K/4], weight k of a group in bits 2(k%4).. of byte k/4
+ *   scales : [N][K/128] */
+void orc_ptq_unpack(const uint8_t *raw, int64_t raw_stride, int64_t N, int64_t K,
+                    uint8_t *codes, uint16_t *scales) {
+  int64_t G = K / ORC_GROUP;
+  for (int64_t n = 0; n < N; ++n) {
+    uint8_t *crow = codes + n * (K / 4);
+    memset(crow, 0, (size_t)(K / 4));
+    for (int64_t g = 0; g < G; ++g) {
+      const uint8_t *blk = raw + n * raw_stride + g * ORC_PTQ_BLOCK_BYTES;
+      uint8_t *cg = crow + g * 32;
+      for (int j = 0; j < 24; ++j)
+        for (int lv = 0; lv < 5; ++lv) {
+          int k = 24 * lv + j;
+          cg[k / 4] |= (uint8_t)(orc_ptq_trit(blk[j], lv) << (2 * (k % 4)));
+        }
+      for (int j = 0; j < 2; ++j)
+        for (int lv = 0; lv < 4; ++lv) {
+          int k = 120 + 2 * lv + j;
+          cg[k / 4] |= (uint8_t)(orc_ptq_trit(blk[24 + j], lv) << (2 * (k % 4)));
+        }
+      scales[n * G + g] = (uint16_t)(blk[26] | (blk[27] << 8));
+    }
+  }
 }
 
 /* ------------------------------------------------------------ quantisation */

@@ -561,4 +561,102 @@ def pin_norm_eps(lib):
     assert np.all(nb == _bf16_bits([0.5])[0])
 
 
+# -------------------------------------------------- PTQ1_0 weights (KR)
+# Page "KERNEL_REPORT: PTQ1_0 small-batch decoding on the PrismML fork, RTX
+# 3060 12GB" (KR), "What the source said": 28-byte blocks of 128 weights,
+# 24 qs bytes of five trits, 2 qh bytes with 8 more trits, fp16 d last.
+
+def _ptq_byte(trits) -> int:
+    """The byte whose repeated x3 expansion gives `trits` (first trit most
+    significant): the base-3 fraction 0.t0t1t2t3t4 rounded up to 1/256ths,
+    ceil(256 V / 243) with V the base-3 value of the five trits."""
+    t = list(trits) + [0] * (5 - len(trits))
+    V = sum(d * 3 ** (4 - i) for i, d in enumerate(t))
+    return (256 * V + 242) // 243
+
+
+def _ptq_position(k: int):
+    """Reading taken for the weight order: trit n of qs byte j is weight
+    24n + j; trit n of qh byte j is weight 120 + 2n + j.  -> (byte, trit)."""
+    if k < 120:
+        return k % 24, k // 24
+    return 24 + (k - 120) % 2, (k - 120) // 2
+
+
+def _ptq_block(trits128, d_bits: int) -> np.ndarray:
+    """28 bytes for one block from 128 trits (0..2) and an fp16 bit pattern."""
+    per_byte = [[0] * 5 for _ in range(26)]
+    for k in range(G):
+        b, n = _ptq_position(k)
+        per_byte[b][n] = int(trits128[k])
+    blk = np.zeros(28, np.uint8)
+    for b in range(26):
+        blk[b] = _ptq_byte(per_byte[b])
+    blk[26], blk[27] = d_bits & 0xFF, d_bits >> 8
+    return blk
+
+
+def pin_ptq_trit_closed_form(lib):
+    """Trit n of byte b is the (n+1)-th base-3 digit of the fraction b/256,
+    floor(b * 3^(n+1) / 256) mod 3, for every byte and level; and every
+    five-trit value V comes back from its byte ceil(256 V / 243)."""
+    for b in range(256):
+        for n in range(5):
+            assert O.ptq_trit(b, n, lib=lib) == (b * 3 ** (n + 1) // 256) % 3, (b, n)
+    for V in range(243):
+        digits = [(V // 3 ** (4 - i)) % 3 for i in range(5)]
+        b = _ptq_byte(digits)
+        assert [O.ptq_trit(b, n, lib=lib) for n in range(5)] == digits, V
+
+
+def pin_ptq_weight_positions(lib):
+    """A block with one +1 weight (trit 2) at k and 0 (trit 1) elsewhere
+    unpacks to the unit vector e_k, for every k; the scale is bytes 26-27."""
+    raw = np.stack([_ptq_block(np.where(np.arange(G) == k, 2, 1), 0x3C00 + k) for k in range(G)])
+    codes, scales = O.ptq_unpack(raw, G, lib=lib)
+    w = _unpack_numpy(codes)
+    assert np.array_equal(w, np.eye(G, dtype=np.int64)), np.argwhere(w != np.eye(G))[:4]
+    assert list(scales[:, 0]) == [0x3C00 + k for k in range(G)]
+
+
+def pin_ptq_random_blocks(lib):
+    """Random trits through independently built blocks (three rows of three
+    blocks, rows padded to a longer stride) come back as code = trit."""
+    rng = np.random.default_rng(21)
+    N, K = 3, 384
+    trits = rng.integers(0, 3, (N, K))
+    dbits = rng.integers(0, 0x7C00, (N, K // G))
+    raw = np.zeros((N, 3 * 28 + 5), np.uint8)
+    for n in range(N):
+        for g in range(K // G):
+            raw[n, 28 * g:28 * g + 28] = _ptq_block(trits[n, g * G:(g + 1) * G], int(dbits[n, g]))
+    codes, scales = O.ptq_unpack(raw, K, lib=lib)
+    assert np.array_equal(_unpack_numpy(codes), trits - 1)
+    assert np.array_equal(scales, dbits.astype(np.uint16))
+
+
+def pin_ptq_worked_example(lib):
+    """BIB 'Calculate with small integers' in PTQ1_0 form: weights
+    [-1, 0, +1, +1] at k = 0..3, d = 0.5, x = [20, 30, 40, 10, 127, 0...]:
+    y = 15 with activation groups of 128 and of 32; all-(+1) and all-(-1)
+    blocks give +sum(q) and -sum(q)."""
+    ex = _golden("worked_example.json")
+    trits = np.ones(G, np.int64)
+    trits[:4] = ex["codes"]
+    raw = _ptq_block(trits, _f16_bits(0.5))[None, :]
+    codes, scales = O.ptq_unpack(raw, G, lib=lib)
+    x = np.zeros((1, G), np.float32)
+    x[0, :4] = ex["q"]
+    x[0, 4] = 127.0
+    for A in (128, 32):
+        q, sx = O.quantize_grouped(x, A, lib=lib)
+        d = O.group_dots_grouped(q, codes, A, lib=lib)
+        _, y64, _ = O.scale_accumulate_grouped(d, sx, scales, A, lib=lib)
+        assert y64[0, 0] == 15.0, (A, y64)
+    q = np.random.default_rng(2).integers(-127, 128, (1, G)).astype(np.int8)
+    for t, sign in ((2, 1), (0, -1)):
+        c, _ = O.ptq_unpack(_ptq_block(np.full(G, t), 0)[None, :], G, lib=lib)
+        assert O.group_dots(q, c, lib=lib)[0, 0, 0] == sign * int(q.astype(np.int64).sum())
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

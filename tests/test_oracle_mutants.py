@@ -54,6 +54,12 @@ MUTANTS = [
     ("grouped_dot_offset", "int64_t k = j * A + i;", "int64_t k = j * A + i + 1 - (i + 1) / A;"),
     ("grouped_weight_group", "float ws = orc_half_to_float(scales[n * G + g]);\n        for (int64_t h",
      "float ws = orc_half_to_float(scales[n * G + (g * H) % G]);\n        for (int64_t h"),
+    ("ptq_trit_carry", "v = w & 0xFFu;", "v = w & 0x7Fu;"),
+    ("ptq_trit_low_digit", "t = w >> 8;", "t = v % 3u;"),
+    ("ptq_weight_order", "int k = 24 * lv + j;", "int k = 5 * j + lv;"),
+    ("ptq_qh_order", "int k = 120 + 2 * lv + j;", "int k = 120 + 4 * j + lv;"),
+    ("ptq_scale_first", "(uint16_t)(blk[26] | (blk[27] << 8))", "(uint16_t)(blk[0] | (blk[1] << 8))"),
+    ("ptq_scale_big_endian", "(uint16_t)(blk[26] | (blk[27] << 8))", "(uint16_t)(blk[27] | (blk[26] << 8))"),
     ("norm_residual_dropped", "if (residual) a = a + orc_bf16_to_float", "if (0) a = a + orc_bf16_to_float"),
 ]
 
