@@ -414,6 +414,62 @@ def grouped_leg(args, dev, stream, timed, capture, mats, wbytes):
     return out
 
 
+def ptq_leg(args, dev, stream, timed, capture):
+    """PTQ1_0 weights (28 bytes per 128 weights) on the attn_qkv shape, 48
+    rotated matrices (550 MB, above L2), activation groups of 32 (the pages'
+    PTQ1_0 path) and 128, M = 1..4: pq2_ptq_mmv alone (back-to-back
+    independent calls) and the complete call (grouped quantisation, then the
+    GEMV streaming its weights while the quantisation runs)."""
+    import torch
+    from ternary_weight_int8_gb300 import pq2, synth
+    lib = pq2.lib()
+    K, N, nm = K_DIM, N_DIM, 48
+    mats = []
+    for i in range(nm):
+        raw = synth.ptq_raw_weights(N, K, seed=9000 + i, device=dev)
+        mats.append(pq2.pq2_ptq_prepare(raw, K))
+        del raw
+    sp = stream.cuda_stream
+    hbm, hbm_kind = measured_peaks()
+    nbytes = N * K * 28 // 128
+    out = {"workload": f"attn_qkv K={K} N={N} PTQ1_0 (bytes uniform, fp16 d in [0.005, 0.05]), "
+                       f"bf16 x N(0,1) with 1% outliers, bf16 out, {nm} rotated matrices",
+           "bytes_per_call": nbytes, "peak_gbs": hbm, "peak_source": hbm_kind, "by_a": {}}
+    for A in (32, 128):
+        by_m = {}
+        for M in MS:
+            x = synth.activations(M, K, seed=700 + M + A, device=dev, outlier_frac=0.01)
+            q, sx, qs = pq2.pq2_quantize_act_grouped(x, A, pq2.PQ2_Q_ROWS)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+            def mmv_calls(flags=pq2.PQ2_MMV_INDEPENDENT, quant=False):
+                for wq, ws in mats:
+                    if quant:
+                        st = lib.pq2_quantize_act_grouped(x.data_ptr(), pq2.PQ2_BF16, K, M, K, A,
+                                                          q.data_ptr(), pq2.PQ2_Q_ROWS,
+                                                          sx.data_ptr(), qs.data_ptr(), sp)
+                        if st:
+                            raise RuntimeError(f"pq2_quantize_act_grouped failed ({st})")
+                    st = lib.pq2_ptq_mmv(q.data_ptr(), sx.data_ptr(), qs.data_ptr(), wq.data_ptr(),
+                                         ws.data_ptr(), y.data_ptr(), pq2.PQ2_BF16, M, N, K, A,
+                                         flags, sp)
+                    if st:
+                        raise RuntimeError(f"pq2_ptq_mmv failed ({st})")
+
+            reps = 30
+            k_ms = timed([capture(mmv_calls)], reps, 3) / (reps * nm)
+            c_ms = timed([capture(lambda: mmv_calls(pq2.PQ2_MMV_OVERLAP_WEIGHTS, True))],
+                         reps, 3) / (reps * nm)
+            gbs = nbytes / (k_ms * 1e-3) / 1e9
+            by_m[str(M)] = {"mmv_us": round(k_ms * 1e3, 3), "mmv_gbs": round(gbs, 1),
+                            "mmv_frac": round(gbs / hbm, 3), "complete_us": round(c_ms * 1e3, 3)}
+            del x, q, sx, qs, y
+        out["by_a"][str(A)] = by_m
+    del mats
+    torch.cuda.empty_cache()
+    return out
+
+
 def prep_leg(args, dev, stream, timed, capture):
     """The fused preparation (pq2_norm_hadamard_quantize: RMSNorm with a
     residual, signs, 1024-point Walsh-Hadamard, group-128 INT8 in the plane
@@ -624,6 +680,7 @@ def run_ours(args):
     prep = prep_leg(args, dev, stream, timed, capture) if not args.no_prep else None
     grouped = (grouped_leg(args, dev, stream, timed, capture, mats, wbytes)
                if not args.no_grouped else None)
+    ptq = ptq_leg(args, dev, stream, timed, capture) if not args.no_ptq else None
     # dominant kernel: pq2_mmv over the step's M mix, kernel-only
     mean_k_us = statistics.mean(per_m[str(M)]["mmv_us"] for M in MS)
     achieved = wbytes / (mean_k_us * 1e-6) / 1e9
@@ -654,6 +711,7 @@ def run_ours(args):
         "gated": gated,
         "prep": prep,
         "grouped": grouped,
+        "ptq": ptq,
         "clocks": clocks.summary(),
     }
     if rank == 0 and not args.no_cpu:
@@ -710,6 +768,8 @@ def main():
                     help="skip the fused preparation (pq2_norm_hadamard_quantize) leg")
     ap.add_argument("--no-grouped", action="store_true",
                     help="skip the activation-group 64/32 (pq2_mmv_grouped) leg")
+    ap.add_argument("--no-ptq", action="store_true",
+                    help="skip the PTQ1_0 weight-format (pq2_ptq_mmv) leg")
     ap.add_argument("--profile-case", choices=["mmv", "mm"], default=None,
                     help="run a short fixed call sequence for an ncu capture and exit")
     ap.add_argument("--profile-m", type=int, default=1, help="columns for --profile-case")

@@ -233,6 +233,45 @@ int pq2_debug_group_dots_grouped(const int8_t *q_planes, const int32_t *qsum,
                                  int64_t K, int act_group, int32_t *dots,
                                  int32_t *dev_status, void *stream);
 
+/* PTQ1_0 weights (page "KERNEL_REPORT: PTQ1_0 small-batch decoding on the
+ * PrismML fork, RTX 3060 12GB", "What the source said"): each row of K
+ * weights is K/128 blocks of 28 bytes: qs (bytes 0-23, five trits per byte),
+ * qh (bytes 24-25, four trits per byte), the fp16 scale d (bytes 26-27,
+ * little-endian).  Trit n (0 first) of a byte b is floor(b * 3^(n+1) / 256)
+ * mod 3, the digit left above the low byte after n + 1 multiplications by 3;
+ * trit t means weight t - 1.  Weight order inside a block (the page does
+ * not fix it; this library's reading): trit n of qs byte j is weight 24n + j,
+ * trit n of qh byte j is weight 120 + 2n + j.
+ *
+ * pq2_ptq_prepare — raw blocks (device, N rows, row stride raw_row_stride
+ * bytes >= 28 K/128) -> qs plane u8[N][24 K/128] (16-byte aligned) and side
+ * plane u32[N][K/128] (8-byte aligned): bits 0-15 qh (byte 24 low), bits
+ * 16-31 d.  A byte move; K % 256 == 0. */
+int pq2_ptq_prepare(const uint8_t *raw, int64_t raw_row_stride, int64_t N,
+                    int64_t K, uint8_t *qs, uint32_t *side, void *stream);
+
+/* pq2_ptq_mmv — y[m][n] = sum_g d_g * sum_h float(dot_gh) * s_x[m][g*128/A+h]
+ * for M = 1..4 columns of activations quantised by pq2_quantize_act_grouped
+ * with the same act_group A (128, 64 or 32; PQ2_Q_ROWS layout, sum(q)
+ * required), dot_gh the exact integer dot of activation group h of block g:
+ * fp32, each operation rounded to nearest, a fixed order that depends on
+ * (N, K, SM count) only, so column m is bit-identical for every M.
+ * y fp32 or bf16 (RNE of the fp32 result) [M][N].  flags as pq2_mmv_ex
+ * (PQ2_MMV_OVERLAP_WEIGHTS, PQ2_MMV_INDEPENDENT, same stream contract).
+ * K % 256 == 0; the kernel has no waits that can time out. */
+int pq2_ptq_mmv(const int8_t *q_rows, const float *sx, const int32_t *qsum,
+                const uint8_t *qs, const uint32_t *side, void *y, int y_dtype,
+                int64_t M, int64_t N, int64_t K, int act_group, int flags,
+                void *stream);
+
+/* The exact partial dots of pq2_ptq_mmv, dots[m][n][j] = sum over k in
+ * [jA, jA + A) of (t_{n,k} - 1) q_{m,k}, from the same device code (parity
+ * checks).  dots (device) int32 [M][N][K / A]. */
+int pq2_debug_ptq_dots(const int8_t *q_rows, const int32_t *qsum,
+                       const uint8_t *qs, const uint32_t *side, int64_t M,
+                       int64_t N, int64_t K, int act_group, int32_t *dots,
+                       void *stream);
+
 /* pq2_mmv_gated — the gate/up projection with its gated activation in the
  * GEMV's epilogue (page "Kernel experiments: recorded evidence", Test 12,
  * "gated" fusion screen: the projection's output z = x W^T of width N is

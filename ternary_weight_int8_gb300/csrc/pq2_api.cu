@@ -202,6 +202,58 @@ int pq2_debug_group_dots_grouped(const int8_t* q, const int32_t* qsum, const uin
                                  static_cast<cudaStream_t>(stream));
 }
 
+int pq2_ptq_prepare(const uint8_t* raw, int64_t raw_row_stride, int64_t N, int64_t K,
+                    uint8_t* qs, uint32_t* side, void* stream) {
+  if (!raw || !qs || !side) return PQ2_ERR_NULL;
+  if (!valid_n(N) || !valid_k(K) || K % 256 || raw_row_stride < K / 128 * 28)
+    return PQ2_ERR_SHAPE;
+  if (!aligned(qs, 16) || !aligned(side, 8)) return PQ2_ERR_ALIGN;
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  return pq2::launch_ptq_prepare(raw, raw_row_stride, N, K, qs, side,
+                                 static_cast<cudaStream_t>(stream));
+}
+
+namespace {
+int check_ptq_args(const int8_t* q, const int32_t* qsum, const uint8_t* qs, const uint32_t* side,
+                   int64_t M, int64_t N, int64_t K, int act_group) {
+  if (!q || !qsum || !qs || !side) return PQ2_ERR_NULL;
+  if (M < 1 || M > 4 || !valid_n(N) || !valid_k(K) || K % 256 ||
+      (act_group != 128 && act_group != 64 && act_group != 32))
+    return PQ2_ERR_SHAPE;
+  if (!aligned(q, 16) || !aligned(qsum, 4) || !aligned(qs, 16) || !aligned(side, 8))
+    return PQ2_ERR_ALIGN;
+  return PQ2_OK;
+}
+}  // namespace
+
+int pq2_ptq_mmv(const int8_t* q_rows, const float* sx, const int32_t* qsum, const uint8_t* qs,
+                const uint32_t* side, void* y, int y_dtype, int64_t M, int64_t N, int64_t K,
+                int act_group, int flags, void* stream) {
+  if (int st = check_ptq_args(q_rows, qsum, qs, side, M, N, K, act_group)) return st;
+  if (!sx || !y) return PQ2_ERR_NULL;
+  if (y_dtype != PQ2_F32 && y_dtype != PQ2_BF16) return PQ2_ERR_DTYPE;
+  if (flags & ~(PQ2_MMV_OVERLAP_WEIGHTS | PQ2_MMV_INDEPENDENT)) return PQ2_ERR_DTYPE;
+  if (!aligned(sx, 4) || !aligned(y, elem_bytes(y_dtype))) return PQ2_ERR_ALIGN;
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  const int overlap = (flags & PQ2_MMV_INDEPENDENT) ? 2 : (flags & PQ2_MMV_OVERLAP_WEIGHTS) ? 1 : 0;
+  return pq2::launch_ptq_mmv(q_rows, sx, qsum, qs, side, y, y_dtype, nullptr, M, N, K, act_group,
+                             overlap, sms, static_cast<cudaStream_t>(stream));
+}
+
+int pq2_debug_ptq_dots(const int8_t* q_rows, const int32_t* qsum, const uint8_t* qs,
+                       const uint32_t* side, int64_t M, int64_t N, int64_t K, int act_group,
+                       int32_t* dots, void* stream) {
+  if (int st = check_ptq_args(q_rows, qsum, qs, side, M, N, K, act_group)) return st;
+  if (!dots) return PQ2_ERR_NULL;
+  if (!aligned(dots, 4)) return PQ2_ERR_ALIGN;
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  return pq2::launch_ptq_mmv(q_rows, nullptr, qsum, qs, side, nullptr, PQ2_F32, dots, M, N, K,
+                             act_group, 0, sms, static_cast<cudaStream_t>(stream));
+}
+
 int pq2_mmv_gated(const int8_t* q, const float* sx, const int32_t* qsum, const uint8_t* codes,
                   const uint16_t* scales, void* out, int out_dtype, int64_t M, int64_t N,
                   int64_t K, int flags, int32_t* dev_status, void* stream) {

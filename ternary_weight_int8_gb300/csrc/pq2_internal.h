@@ -66,6 +66,17 @@ int launch_norm_hadamard_quantize(const uint16_t* x, const uint16_t* residual,
                                   float eps, int64_t M, int64_t K, uint16_t* norm_out, void* q,
                                   int q_layout, float* sx, int32_t* qsum, cudaStream_t stream);
 
+// PTQ1_0: raw 28-byte blocks -> qs plane u8[N][24 K/128] + side plane
+// u32[N][K/128] (qh | d << 16); GEMV on row-layout q with activation groups
+// of act_group (128, 64, 32), M 1..4, K % 256 == 0.
+int launch_ptq_prepare(const uint8_t* raw, int64_t raw_stride, int64_t N, int64_t K, uint8_t* qs,
+                       uint32_t* side, cudaStream_t stream);
+bool ptq_geometry(int64_t N, int64_t K, int sm_count, int* ctas, int* rows, int* splits);
+int launch_ptq_mmv(const int8_t* q, const float* sx, const int32_t* qsum, const uint8_t* qs,
+                   const uint32_t* side, void* y, int y_dtype, int32_t* dots, int64_t M,
+                   int64_t N, int64_t K, int act_group, int overlap, int sm_count,
+                   cudaStream_t stream);
+
 int launch_mm(const uint16_t* q_f16, const float* sx, const int32_t* qsum,
               const uint8_t* codes, const uint16_t* scales, void* y, int y_dtype,
               int32_t* dots, int64_t M, int64_t N, int64_t K, int sm_count,

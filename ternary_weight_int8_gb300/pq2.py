@@ -46,6 +46,9 @@ SIGNATURES = {
     "pq2_linear_static": (_I, [_P, _I, _I64, _I64, _I64, _I64, _P, _P, _P, _I, _P, _P]),
     "pq2_mmv_gated": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _P, _P]),
     "pq2_quantize_act_grouped": (_I, [_P, _I, _I64, _I64, _I64, _I, _P, _I, _P, _P, _P]),
+    "pq2_ptq_prepare": (_I, [_P, _I64, _I64, _I64, _P, _P, _P]),
+    "pq2_ptq_mmv": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _I, _P]),
+    "pq2_debug_ptq_dots": (_I, [_P, _P, _P, _P, _I64, _I64, _I64, _I, _P, _P]),
     "pq2_mmv_grouped": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _I, _P, _P]),
     "pq2_debug_group_dots_grouped": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P, _P, _P]),
     "pq2_norm_hadamard_quantize": (_I, [_P, _P, _P, _P, _P, ctypes.c_float, _I64, _I64, _P,
@@ -222,6 +225,43 @@ def pq2_debug_group_dots_grouped(q_planes, qsum, codes, act_group: int, stream=N
     dots = torch.empty((M, N, K // act_group), dtype=torch.int32, device=q_planes.device)
     _check("pq2_debug_group_dots_grouped", lib().pq2_debug_group_dots_grouped(
         _ptr(q_planes), _ptr(qsum), _ptr(codes), M, N, K, act_group, _ptr(dots), None,
+        _stream(stream)))
+    return dots
+
+
+def pq2_ptq_prepare(raw: torch.Tensor, K: int, stream=None):
+    """Raw PTQ1_0 rows u8[N][>= 28 K/128] (CUDA, unit column stride) ->
+    (qs u8[N][24 K/128], side i32[N][K/128]: qh | d << 16)."""
+    if raw.dim() != 2 or raw.stride(1) != 1 or raw.dtype != torch.uint8:
+        raise ValueError("Expected a CUDA uint8 PTQ1_0 matrix")
+    N = raw.shape[0]
+    qs = torch.empty((N, K // GROUP * 24), dtype=torch.uint8, device=raw.device)
+    side = torch.empty((N, K // GROUP), dtype=torch.int32, device=raw.device)
+    _check("pq2_ptq_prepare", lib().pq2_ptq_prepare(_ptr(raw), raw.stride(0), N, K, _ptr(qs),
+                                                     _ptr(side), _stream(stream)))
+    return qs, side
+
+
+def pq2_ptq_mmv(q_rows, sx, qsum, qs, side, act_group: int, y=None, out_dtype=torch.float32,
+                flags=0, stream=None):
+    """PTQ1_0 GEMV (M = 1..4) on row-layout grouped activations."""
+    M, K = q_rows.shape
+    N = qs.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=q_rows.device)
+    _check("pq2_ptq_mmv", lib().pq2_ptq_mmv(
+        _ptr(q_rows), _ptr(sx), _ptr(qsum), _ptr(qs), _ptr(side), _ptr(y), _DT[y.dtype], M, N,
+        K, act_group, flags, _stream(stream)))
+    return y
+
+
+def pq2_debug_ptq_dots(q_rows, qsum, qs, side, act_group: int, stream=None):
+    """Exact partial dots [M][N][K/A] of the PTQ1_0 GEMV's device code."""
+    M, K = q_rows.shape
+    N = qs.shape[0]
+    dots = torch.empty((M, N, K // act_group), dtype=torch.int32, device=q_rows.device)
+    _check("pq2_debug_ptq_dots", lib().pq2_debug_ptq_dots(
+        _ptr(q_rows), _ptr(qsum), _ptr(qs), _ptr(side), M, N, K, act_group, _ptr(dots),
         _stream(stream)))
     return dots
 

@@ -55,6 +55,30 @@ def raw_weights(N: int, K: int, seed: int, device="cpu", *,
     return raw.view(N, G * BLOCK_BYTES)
 
 
+PTQ_BLOCK_BYTES = 28
+
+
+def ptq_raw_weights(N: int, K: int, seed: int, device="cpu", *,
+                    scale_lo: float = 0.005, scale_hi: float = 0.05) -> torch.Tensor:
+    """Raw PTQ1_0 matrix u8[N][K/128*28] (page "KERNEL_REPORT: PTQ1_0
+    small-batch decoding on the PrismML fork, RTX 3060 12GB"): per block, 26
+    trit bytes (24 qs, 2 qh) drawn uniformly over 0..255, then the fp16
+    scale in bytes 26-27.  Every byte value is a valid five-trit word, so
+    uniform bytes give each trit value with probability about 1/3."""
+    if K % GROUP:
+        raise ValueError("K must be a multiple of 128")
+    G = K // GROUP
+    g = _gen(seed, device)
+    trit_bytes = torch.randint(0, 256, (N, G, 26), generator=g, device=device,
+                               dtype=torch.int32).to(torch.uint8)
+    scales = (torch.rand((N, G), generator=g, device=device, dtype=torch.float32)
+              * (scale_hi - scale_lo) + scale_lo).to(torch.float16)
+    raw = torch.empty((N, G, PTQ_BLOCK_BYTES), dtype=torch.uint8, device=device)
+    raw[:, :, :26] = trit_bytes
+    raw[:, :, 26:] = scales.view(torch.uint8).view(N, G, 2)
+    return raw.view(N, G * PTQ_BLOCK_BYTES)
+
+
 def activations(M: int, K: int, seed: int, device="cpu", *,
                 dtype=torch.bfloat16, outlier_frac: float = 0.0,
                 outlier_scale: float = 20.0) -> torch.Tensor:
