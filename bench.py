@@ -731,6 +731,20 @@ def run_profile_case(args):
     from ternary_weight_int8_gb300 import pq2, synth
     dev = torch.device("cuda", 0)
     M = args.profile_m
+    if args.profile_case == "ptq":
+        K, N, nm, A = K_DIM, N_DIM, 8, args.profile_act_group
+        mats = [pq2.pq2_ptq_prepare(synth.ptq_raw_weights(N, K, seed=9000 + i, device=dev), K)
+                for i in range(nm)]
+        x = synth.activations(M, K, seed=11, device=dev, outlier_frac=0.01)
+        q, sx, qs = pq2.pq2_quantize_act_grouped(x, A, pq2.PQ2_Q_ROWS)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        for i in range(6):
+            wq, ws = mats[i % nm]
+            pq2.pq2_ptq_mmv(q, sx, qs, wq, ws, A, y=y, flags=pq2.PQ2_MMV_INDEPENDENT)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_case": "ptq", "M": M, "N": N, "K": K, "act_group": A,
+                          "launches": 6, "ok": True}))
+        return 0
     if args.profile_case == "mmv":
         K, N, nm = K_DIM, N_DIM, 8
         layout = pq2.PQ2_Q_PLANES
@@ -770,9 +784,11 @@ def main():
                     help="skip the activation-group 64/32 (pq2_mmv_grouped) leg")
     ap.add_argument("--no-ptq", action="store_true",
                     help="skip the PTQ1_0 weight-format (pq2_ptq_mmv) leg")
-    ap.add_argument("--profile-case", choices=["mmv", "mm"], default=None,
+    ap.add_argument("--profile-case", choices=["mmv", "mm", "ptq"], default=None,
                     help="run a short fixed call sequence for an ncu capture and exit")
     ap.add_argument("--profile-m", type=int, default=1, help="columns for --profile-case")
+    ap.add_argument("--profile-act-group", type=int, default=32,
+                    help="activation group for --profile-case ptq")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -32,10 +32,13 @@
 //    (255 * 243 < 2^16), and H_n, the byte above each lane's low byte, is
 //    floor(b * 3^(n+1) / 256); the trits are T_n = H_n - 3 H_(n-1) bytewise
 //    (no borrow: floor(3x) >= 3 floor(x)), the same digits as the repeated
-//    x3-and-carry of the format, with five independent products instead of a
+//    x3-and-carry of the format, with independent products instead of a
 //    chain.  T_n holds the trits of weights 24n + 4w .. +3, which meet the
 //    q word 6n + w in one dp4a.u32.s32; the -1 offset is removed with
-//    sum(q) once per activation group.
+//    sum(q) once per activation group.  The decode runs level by level over
+//    a block's six qs words, so a level's six trit words meet 24
+//    consecutive q bytes (three 8-byte shared loads per column) and the
+//    live state stays small enough for three CTAs per SM.
 //  * y = sum over blocks g of d_g * (sum over activation groups h of
 //    float(dot_gh) * s_x_gh), fp32, every operation rounded to nearest, h
 //    ascending, the blocks of a split in order, then a fixed xor butterfly
@@ -56,8 +59,10 @@ constexpr int kRawBlock = 28;
 constexpr int kQsBytes = 24;
 constexpr int kPairBytes = 48;
 constexpr int kSlotChunks = 4;          // 3 x 16 qs bytes + 8 side bytes
+// q of a block pair (256 bytes) sits at a pitch of 272 bytes: the splits of a
+// warp read consecutive pairs, 17 16-byte units apart, in different banks.
+constexpr int kQPitch = 272;
 constexpr int kMaxThreads = 288;
-constexpr int kTwoPerSm = 110 * 1024;   // two CTAs per SM
 constexpr int kSoloSmem = 120 * 1024;  // one CTA per SM
 constexpr int kMaxSmem = 227 * 1024;
 
@@ -98,21 +103,6 @@ __device__ __forceinline__ void cp_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Trits of the four bytes of w, level n = 0..4, as four byte lanes each.
-__device__ __forceinline__ void decode_qs_word(uint32_t w, uint32_t t[5]) {
-  const uint32_t lo = __byte_perm(w, 0u, 0x4240);  // b0, b2 in 16-bit lanes
-  const uint32_t hi = __byte_perm(w, 0u, 0x4341);  // b1, b3
-  uint32_t prev = 0;
-  uint32_t f = 3;
-#pragma unroll
-  for (int n = 0; n < 5; ++n) {
-    const uint32_t h = __byte_perm(lo * f, hi * f, 0x7351);
-    t[n] = h - 3u * prev;
-    prev = h;
-    f *= 3;
-  }
-}
-
 // Trits of the two qh bytes (bits 0-15 of side): weights 120..123 and
 // 124..127 of the block, as two words in weight order.
 __device__ __forceinline__ void decode_qh(uint32_t side, uint32_t& t01, uint32_t& t23) {
@@ -124,7 +114,7 @@ __device__ __forceinline__ void decode_qh(uint32_t side, uint32_t& t01, uint32_t
 }
 
 template <int M, int NSUB, bool DOTS>
-__global__ void __launch_bounds__(kMaxThreads, 2) ptq_mmv_kernel(const PtqParams p) {
+__global__ void __launch_bounds__(kMaxThreads, 3) ptq_mmv_kernel(const PtqParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   grid_dep_launch();
   constexpr int A = 128 / NSUB;
@@ -153,14 +143,14 @@ __global__ void __launch_bounds__(kMaxThreads, 2) ptq_mmv_kernel(const PtqParams
     cp_async16(slot_addr(slot, 2), src + 32);
     cp_async8(slot_addr(slot, 3), side_row + 2 * pp);
   };
-  // q (swizzled by pair), s_x and sum(q) of every column: all threads.
+  // q (pairs at a pitch of kQPitch bytes), s_x and sum(q): all threads.
+  const int QP = p.G2 * kQPitch;  // bytes of one column's q in shared memory
   auto load_inputs = [&]() {
     const uint32_t qb = smem_u32(smem);
     const int chunks = M * (K / 16);
     for (int i = tid; i < chunks; i += T) {
       const int m = i / (K / 16), k16 = i % (K / 16);
-      const int pr = k16 >> 4, cc = k16 & 15;
-      const uint32_t dst = qb + (uint32_t)(m * K + pr * 256 + 16 * (cc ^ (pr & 7)));
+      const uint32_t dst = qb + (uint32_t)(m * QP + (k16 >> 4) * kQPitch + 16 * (k16 & 15));
       cp_async16(dst, p.q + (size_t)m * K + 16 * k16);
     }
     const uint32_t sb = smem_u32(smem + p.sx_off), tb = smem_u32(smem + p.qs_off);
@@ -180,7 +170,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) ptq_mmv_kernel(const PtqParams
     if (s < n_it) load_pair(s);
     cp_commit();
   }
-  if (D == 8) cp_wait<6>(); else cp_wait<2>();
+  if (D == 8) cp_wait<6>(); else if (D == 4) cp_wait<2>(); else cp_wait<0>();
   __syncthreads();
 
   const int8_t* qsm = reinterpret_cast<const int8_t*>(smem);
@@ -194,7 +184,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) ptq_mmv_kernel(const PtqParams
   for (int it = 0; it < n_it; ++it) {
     if (it + D - 1 < n_it) load_pair(it + D - 1);
     cp_commit();
-    if (D == 8) cp_wait<7>(); else cp_wait<3>();
+    if (D == 8) cp_wait<7>(); else if (D == 4) cp_wait<3>(); else cp_wait<1>();
     const int slot = it & (D - 1);
     const int pp = z + S * it;
     const uint8_t* sl = smem + p.ring_off + (size_t)((slot * kSlotChunks) * T + tid) * 16;
@@ -208,43 +198,78 @@ __global__ void __launch_bounds__(kMaxThreads, 2) ptq_mmv_kernel(const PtqParams
     for (int b = 0; b < 2; ++b) {
       const int g = 2 * pp + b;
       const uint32_t side = b ? sd.y : sd.x;
-      uint32_t t[6][5];
+      // Level-major: the trits of level lv of all six qs words meet the q
+      // words 6 lv .. 6 lv + 5 (24 consecutive bytes), so the decode state
+      // is the split bytes and the previous H of each word.
+      uint32_t lo[6], hi[6], prev[6];
 #pragma unroll
-      for (int wi = 0; wi < 6; ++wi) decode_qs_word(words[6 * b + wi], t[wi]);
+      for (int wi = 0; wi < 6; ++wi) {
+        lo[wi] = __byte_perm(words[6 * b + wi], 0u, 0x4240);  // b0, b2 in 16-bit lanes
+        hi[wi] = __byte_perm(words[6 * b + wi], 0u, 0x4341);  // b1, b3
+        prev[wi] = 0u;
+      }
+      const int8_t* qblk = qsm + pp * kQPitch + 128 * b;
+      int acc[M][NSUB];
+#pragma unroll
+      for (int m = 0; m < M; ++m)
+#pragma unroll
+        for (int h = 0; h < NSUB; ++h) acc[m][h] = 0;
+      uint32_t f = 3;
+#pragma unroll
+      for (int lv = 0; lv < 5; ++lv) {
+        uint32_t t[6];
+#pragma unroll
+        for (int wi = 0; wi < 6; ++wi) {
+          const uint32_t hv = __byte_perm(lo[wi] * f, hi[wi] * f, 0x7351);
+          t[wi] = hv - 3u * prev[wi];
+          prev[wi] = hv;
+        }
+        f *= 3;
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          const uint2* qv = reinterpret_cast<const uint2*>(qblk + m * QP + 24 * lv);
+          const uint2 q0 = qv[0], q1 = qv[1], q2 = qv[2];
+          const uint32_t qw[6] = {q0.x, q0.y, q1.x, q1.y, q2.x, q2.y};
+#pragma unroll
+          for (int wi = 0; wi < 6; ++wi) {
+            const int h = (24 * lv + 4 * wi) / A;
+            acc[m][h] = dp4a_us(t[wi], (int)qw[wi], acc[m][h]);
+          }
+        }
+      }
       uint32_t th01, th23;
       decode_qh(side, th01, th23);
       const float d = __half2float(__ushort_as_half((unsigned short)(side >> 16)));
 #pragma unroll
       for (int m = 0; m < M; ++m) {
-        // the block's 128 q bytes: chunk cc of pair pp sits at cc ^ (pp & 7)
-        const int8_t* qp = qsm + (size_t)m * K + (size_t)pp * 256;
-        uint32_t qw[32];
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const uint4 v = *reinterpret_cast<const uint4*>(qp + 16 * ((8 * b + ch) ^ (pp & 7)));
-          qw[4 * ch] = v.x; qw[4 * ch + 1] = v.y; qw[4 * ch + 2] = v.z; qw[4 * ch + 3] = v.w;
+        const uint2 qh = *reinterpret_cast<const uint2*>(qblk + m * QP + 120);
+        acc[m][NSUB - 1] = dp4a_us(th01, (int)qh.x, acc[m][NSUB - 1]);
+        acc[m][NSUB - 1] = dp4a_us(th23, (int)qh.y, acc[m][NSUB - 1]);
+        const int j0 = m * GA + g * NSUB;
+        float xs[NSUB];
+        int ts[NSUB];
+        if constexpr (NSUB == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(sxs + j0);
+          const int4 u = *reinterpret_cast<const int4*>(tss + j0);
+          xs[0] = v.x; xs[1] = v.y; xs[2] = v.z; xs[3] = v.w;
+          ts[0] = u.x; ts[1] = u.y; ts[2] = u.z; ts[3] = u.w;
+        } else if constexpr (NSUB == 2) {
+          const float2 v = *reinterpret_cast<const float2*>(sxs + j0);
+          const int2 u = *reinterpret_cast<const int2*>(tss + j0);
+          xs[0] = v.x; xs[1] = v.y;
+          ts[0] = u.x; ts[1] = u.y;
+        } else {
+          xs[0] = sxs[j0];
+          ts[0] = tss[j0];
         }
-        int acc[NSUB];
-#pragma unroll
-        for (int h = 0; h < NSUB; ++h) acc[h] = 0;
-#pragma unroll
-        for (int lv = 0; lv < 5; ++lv)
-#pragma unroll
-          for (int wi = 0; wi < 6; ++wi) {
-            const int k = 24 * lv + 4 * wi;
-            acc[k / A] = dp4a_us(t[wi][lv], (int)qw[k / 4], acc[k / A]);
-          }
-        acc[NSUB - 1] = dp4a_us(th01, (int)qw[30], acc[NSUB - 1]);
-        acc[NSUB - 1] = dp4a_us(th23, (int)qw[31], acc[NSUB - 1]);
         float inner = 0.0f;
 #pragma unroll
         for (int h = 0; h < NSUB; ++h) {
-          const int j = m * GA + g * NSUB + h;
-          const int dot = acc[h] - tss[j];
+          const int dot = acc[m][h] - ts[h];
           if (DOTS) {
             p.dots[((size_t)m * p.N + n) * GA + g * NSUB + h] = dot;
           } else {
-            const float x = __fmul_rn((float)dot, sxs[j]);
+            const float x = __fmul_rn((float)dot, xs[h]);
             inner = h == 0 ? x : __fadd_rn(inner, x);
           }
         }
@@ -386,14 +411,21 @@ int launch_ptq_mmv(const int8_t* q, const float* sx, const int32_t* qsum, const 
   p.y_bf16 = y_dtype == PQ2_BF16;
   p.overlap = overlap;
   const int GA = p.G * nsub;
-  p.sx_off = align16((int)(M * K));
+  p.sx_off = align16((int)M * p.G2 * kQPitch);
   p.qs_off = align16(p.sx_off + (int)M * GA * 4);
   p.ring_off = align16(p.qs_off + (int)M * GA * 4);
   const int slot_bytes = p.threads * kSlotChunks * 16;
-  // Ring depth: eight slots where they fit the budget (two CTAs per SM, or
-  // the whole SM for a call that waits for the kernel before it), else four.
-  const int budget = overlap == 1 ? kMaxSmem : kTwoPerSm;
-  p.depth = p.ring_off + 8 * slot_bytes <= budget ? 8 : 4;
+  // Ring depth: the deepest of 8, 4, 2 slots that keeps three CTAs (the
+  // register budget of the kernel) within an SM's shared memory; a call that
+  // waits for the kernel before it takes the whole SM.
+  const int per_sm = 3;
+  const int budget = overlap == 1 ? kMaxSmem : (228 * 1024) / per_sm - 1024;
+  p.depth = 2;
+  for (int d : {8, 4})
+    if (p.ring_off + d * slot_bytes <= budget) {
+      p.depth = d;
+      break;
+    }
   int smem = p.ring_off + p.depth * slot_bytes;
   if (smem > kMaxSmem) return PQ2_ERR_SHAPE;
   // A call that waits for the kernel before it takes a whole SM (more than
