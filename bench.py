@@ -256,8 +256,17 @@ def prefill_leg(args, dev, stream, timed, capture):
     for M in PREFILL_MS:
         x = synth.activations(M, K, seed=900 + M, device=dev)
         q, sx, qs = pq2.pq2_quantize_act(x, pq2.PQ2_Q_F16)
+        q8, _, _ = pq2.pq2_quantize_act(x, pq2.PQ2_Q_F8)
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         ws = torch.empty(pq2.linear_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
+
+        def mm_f8_calls():
+            for c, sc in mats:
+                st = lib.pq2_mm_f8(q8.data_ptr(), sx.data_ptr(), qs.data_ptr(), c.data_ptr(),
+                                   sc.data_ptr(), y.data_ptr(), pq2.PQ2_BF16, M, N, K,
+                                   status.data_ptr(), sp)
+                if st:
+                    raise RuntimeError(f"pq2_mm_f8 failed ({st})")
 
         def mm_calls():
             for c, sc in mats:
@@ -277,13 +286,16 @@ def prefill_leg(args, dev, stream, timed, capture):
 
         reps = max(3, min(50, 20000 // M))
         k_ms = timed([capture(mm_calls)], reps, 3) / (reps * nm)
+        k8_ms = timed([capture(mm_f8_calls)], reps, 3) / (reps * nm)
         c_ms = timed([capture(linear_calls)], reps, 3) / (reps * nm)
         tops = 2.0 * M * N * K / (k_ms * 1e-3) / 1e12
         out["by_m"][str(M)] = {"mm_us": round(k_ms * 1e3, 2), "mm_tflops": round(tops, 1),
                                "frac": round(tops / peak, 3),
+                               "mm_f8_us": round(k8_ms * 1e3, 2),
+                               "f8_frac": round(2.0 * M * N * K / (k8_ms * 1e-3) / 1e12 / peak, 3),
                                "complete_us": round(c_ms * 1e3, 2),
                                "complete_tflops": round(2.0 * M * N * K / (c_ms * 1e-3) / 1e12, 1)}
-        del x, q, sx, qs, y, ws
+        del x, q, q8, sx, qs, y, ws
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
     del mats

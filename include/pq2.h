@@ -70,8 +70,16 @@ enum { PQ2_BF16 = 0, PQ2_F16 = 1, PQ2_F32 = 2 };
  *               position 4s + 2(b & 1) + (b >> 1).  Operand of pq2_mm: sm_103a
  *               has no 8-bit integer tcgen05 MMA, so the prefill contraction
  *               runs on the fp16 tensor path, whose fp32 sums of integer
- *               products below 2^24 are exact. */
-enum { PQ2_Q_ROWS = 0, PQ2_Q_PLANES = 1, PQ2_Q_F16 = 2 };
+ *               products below 2^24 are exact.
+ *  PQ2_Q_F8     two e4m3 planes per 128-group (2 bytes per element, the size
+ *               of PQ2_Q_F16): q = 16a + b with a = q >> 4 in [-8, 7] and
+ *               b = q & 15 in [0, 15], both exact in e4m3; bytes 0..127 of a
+ *               group hold e4m3(16a), bytes 128..255 hold e4m3(b), each in
+ *               the K order of pq2_mm_f8's weight decode: inside every 16
+ *               consecutive elements, element 8h + 2e + o (h, o in {0, 1},
+ *               e = 0..3) is stored at position 4(2h + o) + e.  Operand of
+ *               pq2_mm_f8 (the 8-bit tensor path, two MMAs per K step). */
+enum { PQ2_Q_ROWS = 0, PQ2_Q_PLANES = 1, PQ2_Q_F16 = 2, PQ2_Q_F8 = 3 };
 
 /* Version of the prepared plane layout; bump whenever what a kernel reads
  * changes, so callers can key caches on it (BIB: a layout switch must change
@@ -180,10 +188,11 @@ int pq2_mmv_ex(const int8_t *q_planes, const float *sx, const int32_t *qsum,
  * as the pages time it ("complete call", KE Tests 3, 6): pq2_quantize_act
  * into the caller's workspace, then pq2_mmv (M = 1..8) with
  * PQ2_MMV_OVERLAP_WEIGHTS, so that it streams the weights while the
- * quantisation and the kernel before it finish, or pq2_mm (M >= 16).  Hence
+ * quantisation and the kernel before it finish, or pq2_mm_f8 on PQ2_Q_F8
+ * (M >= 16; bit-identical to pq2_mm, faster).  Hence
  * codes and scales must not be written by a kernel that may still run when
  * the call starts (see the flags of pq2_mmv_ex).
- * Results are bit-identical to pq2_quantize_act + pq2_mmv / pq2_mm.
+ * Results are bit-identical to pq2_quantize_act + pq2_mmv / pq2_mm_f8.
  *   x         (device) x_dtype [M][ldx], ldx >= K; M 1..8 or 16 .. 1<<20.
  *   workspace (device) pq2_linear_workspace_bytes(M, K) bytes, 256-byte
  *             aligned, holding q, s_x and sum(q); contents are scratch.
@@ -390,14 +399,28 @@ int pq2_mm(const uint16_t *q_f16, const float *sx, const int32_t *qsum,
            const uint8_t *codes, const uint16_t *scales, void *y, int y_dtype,
            int64_t M, int64_t N, int64_t K, int32_t *dev_status, void *stream);
 
+/* pq2_mm_f8 — pq2_mm on the 8-bit tensor path: the weights decode to e4m3
+ * (-1, 0, +1; code 3 gives +2) and q comes as the two exact e4m3 planes of
+ * PQ2_Q_F8; each K step is two kind::f8f6f4 MMAs (16a and b) accumulating
+ * into the same fp32 group tile, whose integer sums stay below 2^24, so the
+ * group dot is exact and y is bit-identical to pq2_mm's.
+ *   q_f8     (device) [M][2K] bytes from pq2_quantize_act(PQ2_Q_F8);
+ *            16-byte aligned.  Other arguments as for pq2_mm. */
+int pq2_mm_f8(const uint8_t *q_f8, const float *sx, const int32_t *qsum,
+              const uint8_t *codes, const uint16_t *scales, void *y,
+              int y_dtype, int64_t M, int64_t N, int64_t K,
+              int32_t *dev_status, void *stream);
+
 /* Paths of pq2_debug_group_dots. */
-enum { PQ2_PATH_MMV_ADDXOR = 0, PQ2_PATH_MM = 1, PQ2_PATH_MMV_PLANES = 2 };
+enum { PQ2_PATH_MMV_ADDXOR = 0, PQ2_PATH_MM = 1, PQ2_PATH_MMV_PLANES = 2,
+       PQ2_PATH_MM_F8 = 3 };
 
 /* pq2_debug_group_dots — the exact per-group int32 dots
  * dots[m][n][g] = sum_{k in g} (c_{n,k} - 1) q_{m,k} computed by the SAME
  * device decode and dot code as pq2_mmv with either decoder (paths 0 and 2,
  * q int8 in PQ2_Q_PLANES order, qsum required for path 2, M 1..8) or as
- * pq2_mm (path 1, q fp16 PQ2_Q_F16 and qsum, M >= 16), for parity checks.
+ * pq2_mm (path 1, q fp16 PQ2_Q_F16 and qsum, M >= 16) or pq2_mm_f8 (path 3,
+ * q PQ2_Q_F8 and qsum, M >= 16), for parity checks.
  *   dots (device) int32 [M][N][K/128]. */
 int pq2_debug_group_dots(const void *q, const int32_t *qsum,
                          const uint8_t *codes, int64_t M, int64_t N, int64_t K,

@@ -110,7 +110,8 @@ int pq2_quantize_act(const void* x, int x_dtype, int64_t ldx, int64_t M, int64_t
                      void* q, int q_layout, float* sx, int32_t* qsum, void* stream) {
   if (!x || !q || !sx) return PQ2_ERR_NULL;
   if (x_dtype != PQ2_BF16 && x_dtype != PQ2_F16 && x_dtype != PQ2_F32) return PQ2_ERR_DTYPE;
-  if (q_layout != PQ2_Q_ROWS && q_layout != PQ2_Q_PLANES && q_layout != PQ2_Q_F16)
+  if (q_layout != PQ2_Q_ROWS && q_layout != PQ2_Q_PLANES && q_layout != PQ2_Q_F16 &&
+      q_layout != PQ2_Q_F8)
     return PQ2_ERR_DTYPE;
   if (M < 1 || M > kMaxM || !valid_k(K) || ldx < K || ldx > ((int64_t)1 << 40))
     return PQ2_ERR_SHAPE;
@@ -157,7 +158,8 @@ int pq2_quantize_act_grouped(const void* x, int x_dtype, int64_t ldx, int64_t M,
   if (act_group != 128 && act_group != 64 && act_group != 32) return PQ2_ERR_SHAPE;
   if (!x || !q || !sx) return PQ2_ERR_NULL;
   if (x_dtype != PQ2_BF16 && x_dtype != PQ2_F16 && x_dtype != PQ2_F32) return PQ2_ERR_DTYPE;
-  if (q_layout != PQ2_Q_ROWS && q_layout != PQ2_Q_PLANES && q_layout != PQ2_Q_F16)
+  if (q_layout != PQ2_Q_ROWS && q_layout != PQ2_Q_PLANES && q_layout != PQ2_Q_F16 &&
+      q_layout != PQ2_Q_F8)
     return PQ2_ERR_DTYPE;
   if (M < 1 || M > kMaxM || !valid_k(K) || ldx < K || ldx > ((int64_t)1 << 40))
     return PQ2_ERR_SHAPE;
@@ -304,11 +306,12 @@ int pq2_linear(const void* x, int x_dtype, int64_t ldx, int64_t M, int64_t N, in
   int32_t* qs = reinterpret_cast<int32_t*>(ws + qs_off);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (int st = pq2::launch_quantize(x, x_dtype, ldx, M, K, ws,
-                                    small ? PQ2_Q_PLANES : PQ2_Q_F16, sx, qs, s))
+                                    small ? PQ2_Q_PLANES : PQ2_Q_F8, sx, qs, s))
     return st;
+  // Prefill on the 8-bit tensor path: bit-identical to the fp16 one, faster.
   if (!small)
-    return pq2::launch_mm(reinterpret_cast<const uint16_t*>(ws), sx, qs, codes, scales, y,
-                          y_dtype, nullptr, M, N, K, sms, dev_status, s);
+    return pq2::launch_mm(ws, true, sx, qs, codes, scales, y, y_dtype, nullptr, M, N, K, sms,
+                          dev_status, s);
   return pq2::launch_mmv(reinterpret_cast<const int8_t*>(ws), sx, qs, codes, scales, y,
                          y_dtype, nullptr, M, N, K, pq2_mmv_decoder(M), 1, sms, dev_status, s);
 }
@@ -349,7 +352,8 @@ int pq2_norm_hadamard_quantize(const uint16_t* x, const uint16_t* residual,
                                float eps, int64_t M, int64_t K, uint16_t* norm_out, void* q,
                                int q_layout, float* sx, int32_t* qsum, void* stream) {
   if (!x || !w || !sign || !q || !sx) return PQ2_ERR_NULL;
-  if (q_layout != PQ2_Q_ROWS && q_layout != PQ2_Q_PLANES && q_layout != PQ2_Q_F16)
+  if (q_layout != PQ2_Q_ROWS && q_layout != PQ2_Q_PLANES && q_layout != PQ2_Q_F16 &&
+      q_layout != PQ2_Q_F8)
     return PQ2_ERR_DTYPE;
   if (M < 1 || M > kMaxM || K < 1024 || K > PQ2_PREP_MAX_K || K % 1024) return PQ2_ERR_SHAPE;
   if (!(eps >= 0.0f) || eps > 1.0f) return PQ2_ERR_SHAPE;
@@ -375,7 +379,22 @@ int pq2_mm(const uint16_t* q_f16, const float* sx, const int32_t* qsum, const ui
     return PQ2_ERR_ALIGN;
   int sms = 0;
   if (int st = device_check(&sms)) return st;
-  return pq2::launch_mm(q_f16, sx, qsum, codes, scales, y, y_dtype, nullptr, M, N, K, sms,
+  return pq2::launch_mm(q_f16, false, sx, qsum, codes, scales, y, y_dtype, nullptr, M, N, K, sms,
+                        dev_status, static_cast<cudaStream_t>(stream));
+}
+
+int pq2_mm_f8(const uint8_t* q_f8, const float* sx, const int32_t* qsum, const uint8_t* codes,
+              const uint16_t* scales, void* y, int y_dtype, int64_t M, int64_t N, int64_t K,
+              int32_t* dev_status, void* stream) {
+  if (!q_f8 || !sx || !qsum || !codes || !scales || !y) return PQ2_ERR_NULL;
+  if (M < 16 || M > kMaxM || !valid_n(N) || !valid_k(K)) return PQ2_ERR_SHAPE;
+  if (y_dtype != PQ2_F32 && y_dtype != PQ2_BF16) return PQ2_ERR_DTYPE;
+  if (!aligned(q_f8, 16) || !aligned(codes, 16) || !aligned(sx, 4) || !aligned(qsum, 4) ||
+      !aligned(scales, 2) || !aligned(y, elem_bytes(y_dtype)))
+    return PQ2_ERR_ALIGN;
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  return pq2::launch_mm(q_f8, true, sx, qsum, codes, scales, y, y_dtype, nullptr, M, N, K, sms,
                         dev_status, static_cast<cudaStream_t>(stream));
 }
 
@@ -383,20 +402,22 @@ int pq2_debug_group_dots(const void* q, const int32_t* qsum, const uint8_t* code
                          int64_t M, int64_t N, int64_t K, int path, int32_t* dots,
                          int32_t* dev_status, void* stream) {
   if (!q || !codes || !dots) return PQ2_ERR_NULL;
-  if (path != PQ2_PATH_MMV_ADDXOR && path != PQ2_PATH_MM && path != PQ2_PATH_MMV_PLANES)
+  if (path != PQ2_PATH_MMV_ADDXOR && path != PQ2_PATH_MM && path != PQ2_PATH_MMV_PLANES &&
+      path != PQ2_PATH_MM_F8)
     return PQ2_ERR_DTYPE;
-  if ((path == PQ2_PATH_MMV_PLANES || path == PQ2_PATH_MM) && !qsum) return PQ2_ERR_NULL;
+  const bool mm = path == PQ2_PATH_MM || path == PQ2_PATH_MM_F8;
+  if ((path == PQ2_PATH_MMV_PLANES || mm) && !qsum) return PQ2_ERR_NULL;
   if (!valid_n(N) || !valid_k(K)) return PQ2_ERR_SHAPE;
-  if (path == PQ2_PATH_MM ? (M < 16 || M > kMaxM) : (M < 1 || M > 8)) return PQ2_ERR_SHAPE;
+  if (mm ? (M < 16 || M > kMaxM) : (M < 1 || M > 8)) return PQ2_ERR_SHAPE;
   if (!aligned(q, 16) || !aligned(codes, 16) || !aligned(dots, 4) ||
       (qsum && !aligned(qsum, 4)))
     return PQ2_ERR_ALIGN;
   int sms = 0;
   if (int st = device_check(&sms)) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (path == PQ2_PATH_MM)
-    return pq2::launch_mm(static_cast<const uint16_t*>(q), nullptr, qsum, codes, nullptr,
-                          nullptr, PQ2_F32, dots, M, N, K, sms, dev_status, s);
+  if (mm)
+    return pq2::launch_mm(q, path == PQ2_PATH_MM_F8, nullptr, qsum, codes, nullptr, nullptr,
+                          PQ2_F32, dots, M, N, K, sms, dev_status, s);
   // The dot-only variant reads neither scales nor y; sx is unused as well.
   return pq2::launch_mmv(static_cast<const int8_t*>(q), nullptr, qsum, codes, nullptr, nullptr,
                          PQ2_F32, dots, M, N, K,

@@ -77,7 +77,8 @@ int launch_ptq_mmv(const int8_t* q, const float* sx, const int32_t* qsum, const 
                    int64_t N, int64_t K, int act_group, int overlap, int sm_count,
                    cudaStream_t stream);
 
-int launch_mm(const uint16_t* q_f16, const float* sx, const int32_t* qsum,
+// q_op: fp16 PQ2_Q_F16 (f8 false) or the e4m3 planes of PQ2_Q_F8 (f8 true).
+int launch_mm(const void* q_op, bool f8, const float* sx, const int32_t* qsum,
               const uint8_t* codes, const uint16_t* scales, void* y, int y_dtype,
               int32_t* dots, int64_t M, int64_t N, int64_t K, int sm_count,
               int32_t* status, cudaStream_t stream);

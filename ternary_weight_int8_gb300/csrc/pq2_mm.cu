@@ -19,6 +19,13 @@
 // integer of magnitude <= 32512 < 2^24, so D is the exact int32 per-group
 // partial of the method.  The epilogue scales it by s_x * s_w into fp32.
 //
+// An 8-bit variant (pq2_mm_f8) decodes the weights to e4m3 with one byte
+// permute per four weights and takes q as two exact e4m3 planes (16a and b,
+// q = 16a + b, PQ2_Q_F8); each K step is two kind::f8f6f4 MMAs into the same
+// group tile, at twice the fp16 rate, so the tensor time is unchanged while
+// the decode costs 11 instead of 17 instructions per 16 weights and A takes
+// half the tensor memory, leaving room for a third D buffer.
+//
 // One CTA computes a tile of 128 output rows x 128 tokens:
 //   warp 0      TMA producer: q tiles (two 64-column boxes per group, 128-byte
 //               swizzle, the canonical K-major layout) and code tiles
@@ -57,15 +64,21 @@ constexpr int kSchedWarp = 6 + kEpiWarps;  // warp 22: waits on the MMA's inputs
 constexpr int kScaleWarp = 7 + kEpiWarps;  // warp 23: stages the scales
 constexpr int kThreads = (8 + kEpiWarps) * 32;
 constexpr int kEpiCols = BT / 4;  // tokens per epilogue thread
-constexpr int kDBuf = 2;          // D buffers in flight
+// Tensor-memory budget (512 columns): fp16 A takes 64 columns per group, so
+// two D buffers (128 columns each) fit beside four A buffers; e4m3 A takes 32,
+// which leaves room for a third D buffer.
+template <bool F8> constexpr int kDBufT = F8 ? 3 : 2;  // D buffers in flight
+template <bool F8> constexpr int kAColsT = F8 ? 32 : 64;  // A columns per group
+constexpr int kDBufMax = 3;
 constexpr int kABuf = 4;          // decoded weight (A) buffers in flight
 constexpr int kDone = 8;          // group-completion barriers (> every reuse distance)
 constexpr int kQBytes = BT * kGroup * 2;       // 32 KB: q tile of one group (fp16)
 constexpr int kCBytes = BW * kGroupCodeBytes;  // 4 KB: code bytes of one group
 constexpr int kDCol = 0;                       // D buffers: columns [0, kDBuf*BT)
-constexpr int kACol = kDBuf * BT;              // A buffers: 64 columns each
+template <bool F8> constexpr int kAColT = kDBufT<F8> * BT;  // A buffers after them
 constexpr int kTmemCols = 512;
-static_assert(kACol + kABuf * 64 <= kTmemCols, "tensor memory budget");
+static_assert(kAColT<false> + kABuf * kAColsT<false> <= kTmemCols, "tensor memory budget");
+static_assert(kAColT<true> + kABuf * kAColsT<true> <= kTmemCols, "tensor memory budget");
 
 struct MmParams {
   const float* sx;         // [M][G]
@@ -86,7 +99,7 @@ constexpr int kSwBytes = BW * kGC * 2;
 constexpr int kSBytes = kSxBytes + kSwBytes;
 constexpr int kOffS = kOffC + kStagesC * kCBytes;
 constexpr int kOffBar = kOffS + 2 * kSBytes;
-constexpr int kNumBars = kStagesQ + 2 * kStagesC + kABuf + kDone + kDBuf + 4;
+constexpr int kNumBars = kStagesQ + 2 * kStagesC + kABuf + kDone + kDBufMax + 4;
 constexpr int kOffTmemAddr = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffTmemAddr + 16 + 1024;  // + alignment slack
 
@@ -116,6 +129,15 @@ __device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uin
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem]^T, e4m3 inputs, fp32 accumulation.
+__device__ __forceinline__ void mma_f8_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -188,8 +210,9 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
   return d;
 }
 
-// Instruction descriptor: kind::f16, D fp32, A and B fp16, both K-major
-// (A may come from tensor memory).
+// Instruction descriptor: D fp32, A and B format code 0 (fp16 under
+// kind::f16, e4m3 under kind::f8f6f4), both K-major (A may come from tensor
+// memory).
 __host__ __device__ constexpr uint32_t instr_desc_f16(int m, int n) {
   return (1u << 4)                      // D format: f32
          | (0u << 7) | (0u << 10)       // A, B format: f16
@@ -223,10 +246,26 @@ __device__ __forceinline__ void decode_word(uint32_t w, uint32_t* out) {
   }
 }
 
-template <bool DOTS>
+// Four e4m3 words of one code word w in the operand K order of PQ2_Q_F8:
+// word 0 holds the weights 0, 2, 4, 6 of the code word (weight 4j + s is
+// field s of byte j, bits 8j + 2s), word 1 the weights 1, 3, 5, 7, word 2
+// 8, 10, 12, 14 and word 3 9, 11, 13, 15.  Masked with 0x3333, four fields
+// sit in the four selector nibbles of a byte permute that picks from the
+// table {-1, 0, +1, +2} in e4m3: 1 SHF + ... = 3 SHF + 4 LOP3 + 4 PRMT.
+__device__ __forceinline__ void decode_word_f8(uint32_t w, uint32_t* out) {
+  constexpr uint32_t kTable = 0x403800B8u;  // bytes: e4m3 -1, 0, +1, +2
+  const uint32_t w2 = w >> 2;
+  out[0] = __byte_perm(kTable, 0u, w & 0x3333u);
+  out[1] = __byte_perm(kTable, 0u, w2 & 0x3333u);
+  out[2] = __byte_perm(kTable, 0u, (w >> 16) & 0x3333u);
+  out[3] = __byte_perm(kTable, 0u, (w2 >> 16) & 0x3333u);
+}
+
+template <bool DOTS, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     mm_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_c,
               const MmParams p) {
+  constexpr int kDBuf = kDBufT<F8>, kACol = kAColT<F8>, kACols = kAColsT<F8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
@@ -237,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* a_full = c_empty + kStagesC;
   uint64_t* g_done = a_full + kABuf;   // kDone: group g's MMAs are complete
   uint64_t* d_empty = g_done + kDone;
-  uint64_t* s_full = d_empty + kDBuf;
+  uint64_t* s_full = d_empty + kDBufMax;
   uint64_t* s_empty = s_full + 2;
   uint32_t* tmem_addr_s = reinterpret_cast<uint32_t*>(smem + kOffTmemAddr);
 
@@ -346,13 +385,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // address field is in 16-byte units.
         const uint64_t qd = smem_desc_sw128(smem_u32(smem + kOffQ + sq * kQBytes));
         const uint32_t d_tmem = tmem_base + kDCol + db * BT;
-        const uint32_t a_tmem = tmem_base + kACol + b * 64;  // b = g % kABuf
+        const uint32_t a_tmem = tmem_base + kACol + b * kACols;  // b = g % kABuf
 #pragma unroll
         for (int k = 0; k < kGroup / 16; ++k) {
-          // K step k: A columns 8k..8k+7; B 64-column atom k/4, 32-byte
-          // offset (k%4) inside the 128-byte swizzled row.
+          // Step k reads B at atom k/4 (128 rows x 128 bytes), 32-byte offset
+          // (k%4) inside the swizzled row.  fp16: K step k, A columns
+          // 8k..8k+7.  e4m3: atom 0 is the 16a plane and atom 1 the b plane,
+          // K step k%4 of 32 elements, A columns 8(k%4)..+7 for both.
           const uint64_t boff16 = (uint64_t)(((k >> 2) * (BT * 128) + (k & 3) * 32) >> 4);
-          mma_f16_ta(d_tmem, a_tmem + 8 * k, qd + boff16, idesc, k > 0 ? 1u : 0u);
+          if constexpr (F8)
+            mma_f8_ta(d_tmem, a_tmem + 8 * (k & 3), qd + boff16, idesc, k > 0 ? 1u : 0u);
+          else
+            mma_f16_ta(d_tmem, a_tmem + 8 * k, qd + boff16, idesc, k > 0 ? 1u : 0u);
         }
         // One commit per group tells the q producer, the decoders and the
         // epilogue alike.
@@ -389,13 +433,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint4 c0 = *reinterpret_cast<const uint4*>(cs);
       const uint4 c1 = *reinterpret_cast<const uint4*>(cs + 16);
       const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-      const uint32_t taddr = tmem_base + lane_base + kACol + b * 64;
+      const uint32_t taddr = tmem_base + lane_base + kACol + b * kACols;
+      if constexpr (F8) {
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        uint32_t v[16];
-        decode_word(cw[2 * h], v);
-        decode_word(cw[2 * h + 1], v + 8);
-        tmem_st16(taddr + 16 * h, v);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t v[16];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) decode_word_f8(cw[4 * h + i], v + 4 * i);
+          tmem_st16(taddr + 16 * h, v);
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          uint32_t v[16];
+          decode_word(cw[2 * h], v);
+          decode_word(cw[2 * h + 1], v + 8);
+          tmem_st16(taddr + 16 * h, v);
+        }
       }
       tmem_st_wait();
       tc_fence_before();
@@ -516,10 +570,10 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-template <bool DOTS>
+template <bool DOTS, bool F8>
 int launch_mm_t(const CUtensorMap& mq, const CUtensorMap& mc, const MmParams& p,
                 cudaStream_t stream) {
-  auto kern = mm_kernel<DOTS>;
+  auto kern = mm_kernel<DOTS, F8>;
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
@@ -546,9 +600,10 @@ int launch_mm_t(const CUtensorMap& mq, const CUtensorMap& mc, const MmParams& p,
 
 }  // namespace
 
-int launch_mm(const uint16_t* q_f16, const float* sx, const int32_t* qsum, const uint8_t* codes,
-              const uint16_t* scales, void* y, int y_dtype, int32_t* dots, int64_t M,
-              int64_t N, int64_t K, int sm_count, int32_t* status, cudaStream_t stream) {
+int launch_mm(const void* q_op, bool f8, const float* sx, const int32_t* qsum,
+              const uint8_t* codes, const uint16_t* scales, void* y, int y_dtype, int32_t* dots,
+              int64_t M, int64_t N, int64_t K, int sm_count, int32_t* status,
+              cudaStream_t stream) {
   (void)sm_count;
   if (M > (int64_t)1 << 20 || N > (int64_t)1 << 30) return PQ2_ERR_SHAPE;
   if ((M + BT - 1) / BT > 0x7fffffff || (N + BW - 1) / BW > 65535) return PQ2_ERR_SHAPE;
@@ -556,12 +611,13 @@ int launch_mm(const uint16_t* q_f16, const float* sx, const int32_t* qsum, const
   if (!enc) return PQ2_ERR_LAUNCH;
   CUtensorMap mq, mc;
   {
-    // q: fp16 [M][K], box 64 x 128 (128-byte rows), 128-byte swizzle.
+    // q: fp16 [M][K] (or its e4m3 planes, the same 2 bytes per element),
+    // box 64 x 128 (128-byte rows), 128-byte swizzle.
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
     const cuuint32_t box[2] = {64, (cuuint32_t)BT};
     const cuuint32_t es[2] = {1, 1};
-    if (enc(&mq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(q_f16), dims, strides,
+    if (enc(&mq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(q_op), dims, strides,
             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return PQ2_ERR_LAUNCH;
@@ -582,7 +638,11 @@ int launch_mm(const uint16_t* q_f16, const float* sx, const int32_t* qsum, const
   p.sx = sx; p.scales = scales; p.y = y; p.dots = dots; p.status = status;
   p.M = (int)M; p.N = (int)N; p.K = (int)K; p.G = (int)(K / kGroup);
   p.y_bf16 = y_dtype == PQ2_BF16;
-  return dots ? launch_mm_t<true>(mq, mc, p, stream) : launch_mm_t<false>(mq, mc, p, stream);
+  if (f8)
+    return dots ? launch_mm_t<true, true>(mq, mc, p, stream)
+                : launch_mm_t<false, true>(mq, mc, p, stream);
+  return dots ? launch_mm_t<true, false>(mq, mc, p, stream)
+              : launch_mm_t<false, false>(mq, mc, p, stream);
 }
 
 }  // namespace pq2

@@ -13,6 +13,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <cstdint>
 
@@ -82,6 +83,31 @@ __device__ __forceinline__ void store_group4(const int qi[4], int lane, void* q,
       out |= ((v >> (8 * s_out)) & 0xffu) << (8 * b);
     }
     reinterpret_cast<uint32_t*>(static_cast<int8_t*>(q) + base)[lane] = out;
+  } else if (layout == PQ2_Q_F8) {
+    // Two e4m3 planes of the 8-bit prefill MMA, q = 16 a + b with
+    // a = q >> 4 in [-8, 7] and b = q & 15 in [0, 15], both exact in e4m3:
+    // bytes 0..127 of the group hold 16 a, bytes 128..255 hold b, each in the
+    // operand K order.  Word W = 4i + c of a plane holds the elements
+    // 16i + 8(c >> 1) + (c & 1) + 2e, e = 0..3: bytes (c & 1) and (c & 1) + 2
+    // of lanes 4i + 2(c >> 1) and 4i + 2(c >> 1) + 1.
+    uint32_t hi = 0, lo = 0;
+#pragma unroll
+    for (int j = 0; j < 4; j += 2) {
+      const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(
+          make_float2((float)(16 * (qi[j] >> 4)), (float)(16 * (qi[j + 1] >> 4))),
+          __NV_SATFINITE, __NV_E4M3);
+      const __nv_fp8x2_storage_t l2 = __nv_cvt_float2_to_fp8x2(
+          make_float2((float)(qi[j] & 15), (float)(qi[j + 1] & 15)), __NV_SATFINITE, __NV_E4M3);
+      hi |= (uint32_t)h2 << (8 * j);
+      lo |= (uint32_t)l2 << (8 * j);
+    }
+    const int src = 4 * (lane >> 2) + 2 * ((lane & 3) >> 1);
+    const uint32_t sel = (lane & 1) ? 0x7531u : 0x6420u;
+    const uint32_t ha = __shfl_sync(0xffffffffu, hi, src), hb = __shfl_sync(0xffffffffu, hi, src + 1);
+    const uint32_t la = __shfl_sync(0xffffffffu, lo, src), lb = __shfl_sync(0xffffffffu, lo, src + 1);
+    uint32_t* out = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(q) + 2 * base);
+    out[lane] = __byte_perm(ha, hb, sel);
+    out[32 + lane] = __byte_perm(la, lb, sel);
   } else {
     // Operand order of the prefill MMA: inside each 16-element chunk (lanes
     // 4c..4c+3, element 4b + s held by lane 4c + b), element 4b + s goes to

@@ -24,9 +24,9 @@ LIB_PATH = os.path.join(_PKG, "libpq2.so")
 PQ2_OK, PQ2_ERR_NULL, PQ2_ERR_SHAPE, PQ2_ERR_ALIGN, PQ2_ERR_DTYPE = 0, 1, 2, 3, 4
 PQ2_ERR_ARCH, PQ2_ERR_LAUNCH, PQ2_ERR_TIMEOUT, PQ2_ERR_CUDA = 5, 6, 7, 8
 PQ2_BF16, PQ2_F16, PQ2_F32 = 0, 1, 2
-PQ2_Q_ROWS, PQ2_Q_PLANES, PQ2_Q_F16 = 0, 1, 2
+PQ2_Q_ROWS, PQ2_Q_PLANES, PQ2_Q_F16, PQ2_Q_F8 = 0, 1, 2, 3
 PQ2_DECODE_ADDXOR, PQ2_DECODE_PLANES = 0, 1
-PQ2_PATH_MMV_ADDXOR, PQ2_PATH_MM, PQ2_PATH_MMV_PLANES = 0, 1, 2
+PQ2_PATH_MMV_ADDXOR, PQ2_PATH_MM, PQ2_PATH_MMV_PLANES, PQ2_PATH_MM_F8 = 0, 1, 2, 3
 PQ2_MMV_OVERLAP_WEIGHTS, PQ2_MMV_INDEPENDENT = 1, 2
 PQ2_STATIC_SCRATCH_BYTES = 1 << 20
 GROUP = 128
@@ -56,6 +56,7 @@ SIGNATURES = {
     "pq2_linear_gated": (_I, [_P, _I, _I64, _I64, _I64, _I64, _P, _P, _P, _I, _P, _SZ, _P, _P]),
     "pq2_mmv_decoder": (_I, [_I64]),
     "pq2_mm": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P]),
+    "pq2_mm_f8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P]),
     "pq2_debug_group_dots": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P, _P, _P]),
     "pq2_mmv_geometry": (_I, [_I64, _I64, _I, _P, _P, _P, _P]),
 }
@@ -134,8 +135,7 @@ def pq2_quantize_act(x: torch.Tensor, layout: int = PQ2_Q_PLANES, q=None, sx=Non
         raise ValueError("x must be 2-D with unit column stride")
     M, K = x.shape
     if q is None:
-        q = torch.empty((M, K), dtype=torch.float16 if layout == PQ2_Q_F16 else torch.int8,
-                        device=x.device)
+        q = q_buffer(M, K, layout, x.device)
     if sx is None:
         sx = torch.empty((M, K // GROUP), dtype=torch.float32, device=x.device)
     if qsum is None and want_qsum:
@@ -195,8 +195,7 @@ def pq2_quantize_act_grouped(x: torch.Tensor, act_group: int, layout: int = PQ2_
     if x.dim() != 2 or x.stride(1) != 1:
         raise ValueError("x must be 2-D with unit column stride")
     M, K = x.shape
-    q = torch.empty((M, K), dtype=torch.float16 if layout == PQ2_Q_F16 else torch.int8,
-                    device=x.device)
+    q = q_buffer(M, K, layout, x.device)
     sx = torch.empty((M, K // act_group), dtype=torch.float32, device=x.device)
     qsum = torch.empty((M, K // act_group), dtype=torch.int32, device=x.device)
     _check("pq2_quantize_act_grouped", lib().pq2_quantize_act_grouped(
@@ -307,8 +306,7 @@ def pq2_norm_hadamard_quantize(x, w, sign, eps, residual=None, layout: int = PQ2
     if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
         raise ValueError("x must be a contiguous 2-D bf16 tensor")
     M, K = x.shape
-    q = torch.empty((M, K), dtype=torch.float16 if layout == PQ2_Q_F16 else torch.int8,
-                    device=x.device)
+    q = q_buffer(M, K, layout, x.device)
     sx = torch.empty((M, K // GROUP), dtype=torch.float32, device=x.device)
     qsum = torch.empty((M, K // GROUP), dtype=torch.int32, device=x.device)
     norm = torch.empty_like(x) if want_norm else None
@@ -317,6 +315,29 @@ def pq2_norm_hadamard_quantize(x, w, sign, eps, residual=None, layout: int = PQ2
         _ptr(x), _ptr(residual), _ptr(rout), _ptr(w), _ptr(sign), float(eps), M, K,
         _ptr(norm), _ptr(q), layout, _ptr(sx), _ptr(qsum), _stream(stream)))
     return q, sx, qsum, norm, rout
+
+
+def q_buffer(M: int, K: int, layout: int, device):
+    """Output buffer of the quantiser for `layout`: fp16 [M][K] (PQ2_Q_F16),
+    uint8 [M][2K] (the two e4m3 planes of PQ2_Q_F8) or int8 [M][K]."""
+    if layout == PQ2_Q_F16:
+        return torch.empty((M, K), dtype=torch.float16, device=device)
+    if layout == PQ2_Q_F8:
+        return torch.empty((M, 2 * K), dtype=torch.uint8, device=device)
+    return torch.empty((M, K), dtype=torch.int8, device=device)
+
+
+def pq2_mm_f8(q_f8, sx, qsum, codes, scales, y=None, out_dtype=torch.float32, status=None,
+              stream=None):
+    """Prefill matmul, M >= 16, on the 8-bit tcgen05 path (q from PQ2_Q_F8)."""
+    M, K = q_f8.shape[0], q_f8.shape[1] // 2
+    N = codes.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=q_f8.device)
+    _check("pq2_mm_f8", lib().pq2_mm_f8(_ptr(q_f8), _ptr(sx), _ptr(qsum), _ptr(codes),
+                                        _ptr(scales), _ptr(y), _DT[y.dtype], M, N, K,
+                                        _ptr(status), _stream(stream)))
+    return y
 
 
 def pq2_mm(q_f16, sx, qsum, codes, scales, y=None, out_dtype=torch.float32, status=None,
@@ -336,6 +357,8 @@ def pq2_debug_group_dots(q, codes, path: int, qsum=None, dots=None, status=None,
                          stream=None):
     """Exact int32 group dots [M][N][K/128] from the kernels' own decode/dot code."""
     M, K = q.shape
+    if path == PQ2_PATH_MM_F8:
+        K //= 2
     N = codes.shape[0]
     if dots is None:
         dots = torch.empty((M, N, K // GROUP), dtype=torch.int32, device=q.device)

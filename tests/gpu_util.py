@@ -75,3 +75,23 @@ def mm_operand_order(q: np.ndarray) -> np.ndarray:
         p = 4 * s + 2 * (b & 1) + (b >> 1)
         out[:, p::16] = q[:, i::16]
     return out
+
+
+def mm_operand_order_f8(q: np.ndarray) -> np.ndarray:
+    """The PQ2_Q_F8 layout (include/pq2.h) as bytes [M][2K]: per 128-group the
+    e4m3 plane of 16a, then the e4m3 plane of b (q = 16a + b, b = q & 15);
+    inside every 16 elements, element 8h + 2e + o sits at 4(2h + o) + e.
+    The e4m3 bytes come from torch's float8_e4m3fn conversion."""
+    M, K = q.shape
+    qi = q.astype(np.int64)
+    planes = [(qi >> 4) * 16, qi & 15]
+    i = np.arange(16)
+    pos = 4 * (2 * (i // 8) + (i % 2)) + (i % 8) // 2
+    out = np.empty((M, K // G, 2, G), np.uint8)
+    for p, v in enumerate(planes):
+        b = torch.from_numpy(v.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        b = b.reshape(M, K // 16, 16)
+        r = np.empty_like(b)
+        r[:, :, pos] = b
+        out[:, :, p, :] = r.reshape(M, K // G, G)
+    return out.reshape(M, 2 * K)

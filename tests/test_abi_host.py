@@ -66,7 +66,7 @@ def test_quantize_validation(L):
     f = L.pq2_quantize_act
     assert f(None, 0, 128, 1, 128, A, 1, A, A, None) == pq2.PQ2_ERR_NULL
     assert f(A, 3, 128, 1, 128, A, 1, A, A, None) == pq2.PQ2_ERR_DTYPE
-    assert f(A, 0, 128, 1, 128, A, 3, A, A, None) == pq2.PQ2_ERR_DTYPE
+    assert f(A, 0, 128, 1, 128, A, 4, A, A, None) == pq2.PQ2_ERR_DTYPE
     assert f(A, 0, 127, 1, 128, A, 1, A, A, None) == pq2.PQ2_ERR_SHAPE
     assert f(A, 0, 128, 0, 128, A, 1, A, A, None) == pq2.PQ2_ERR_SHAPE
     assert f(A, 0, 256, 1, 192, A, 1, A, A, None) == pq2.PQ2_ERR_SHAPE
