@@ -738,7 +738,8 @@ def run_ours(args):
 def run_profile_case(args):
     """A short fixed sequence for an ncu capture: the attn_qkv GEMV
     (pq2_mmv, INDEPENDENT calls over 8 rotated matrices) or the ffn_up prefill
-    GEMM (pq2_mm), at --profile-m columns; 3 warm-up calls then 3 calls."""
+    GEMM (pq2_mm, or pq2_mm_f8 for "mm8"), at --profile-m columns; 3 warm-up
+    calls then 3 calls."""
     import torch
     from ternary_weight_int8_gb300 import pq2, synth
     dev = torch.device("cuda", 0)
@@ -762,7 +763,7 @@ def run_profile_case(args):
         layout = pq2.PQ2_Q_PLANES
     else:
         K, N, nm = PREFILL_K, PREFILL_N, 2
-        layout = pq2.PQ2_Q_F16
+        layout = pq2.PQ2_Q_F8 if args.profile_case == "mm8" else pq2.PQ2_Q_F16
     mats = [pq2.pq2_prepare(synth.raw_weights(N, K, seed=7000 + i, device=dev), K)
             for i in range(nm)]
     x = synth.activations(M, K, seed=11, device=dev, outlier_frac=0.01)
@@ -772,6 +773,8 @@ def run_profile_case(args):
         c, sc = mats[i % nm]
         if args.profile_case == "mmv":
             pq2.pq2_mmv(q, sx, qs, c, sc, y=y, flags=pq2.PQ2_MMV_INDEPENDENT)
+        elif args.profile_case == "mm8":
+            pq2.pq2_mm_f8(q, sx, qs, c, sc, y=y)
         else:
             pq2.pq2_mm(q, sx, qs, c, sc, y=y)
     torch.cuda.synchronize()
@@ -796,7 +799,7 @@ def main():
                     help="skip the activation-group 64/32 (pq2_mmv_grouped) leg")
     ap.add_argument("--no-ptq", action="store_true",
                     help="skip the PTQ1_0 weight-format (pq2_ptq_mmv) leg")
-    ap.add_argument("--profile-case", choices=["mmv", "mm", "ptq"], default=None,
+    ap.add_argument("--profile-case", choices=["mmv", "mm", "mm8", "ptq"], default=None,
                     help="run a short fixed call sequence for an ncu capture and exit")
     ap.add_argument("--profile-m", type=int, default=1, help="columns for --profile-case")
     ap.add_argument("--profile-act-group", type=int, default=32,
