@@ -209,6 +209,30 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------- ours
+def host_mapped(t) -> bool:
+    """True when the pinned host tensor `t` is addressable by the device at
+    its own address (unified addressing): then kernels can read and write it
+    directly, over NVLink-C2C on a Grace-Blackwell node.  Asked of the CUDA
+    runtime (cudaPointerGetAttributes), never by touching it from the GPU."""
+    import ctypes
+
+    class Attr(ctypes.Structure):
+        _fields_ = [("type", ctypes.c_int), ("device", ctypes.c_int),
+                    ("devicePointer", ctypes.c_void_p), ("hostPointer", ctypes.c_void_p),
+                    ("reserved", ctypes.c_long * 16)]
+    for name in ("libcudart.so", "libcudart.so.13", "/usr/local/cuda/lib64/libcudart.so"):
+        try:
+            rt = ctypes.CDLL(name)
+            break
+        except OSError:
+            rt = None
+    if rt is None:
+        return False
+    a = Attr()
+    rc = rt.cudaPointerGetAttributes(ctypes.byref(a), ctypes.c_void_p(t.data_ptr()))
+    return rc == 0 and a.type == 1 and a.devicePointer == t.data_ptr()
+
+
 def cpu_baseline_sample(budget_s=12.0):
     """The oracle as it stands on one host core: complete calls for M = 1..4
     on the full attn_qkv shape, repeated for about budget_s seconds."""
@@ -587,11 +611,12 @@ def run_ours(args):
     wss = {M: torch.empty(pq2.linear_workspace_bytes(M, K_DIM), dtype=torch.uint8, device=dev)
            for M in MS}
 
-    def complete(M, mat, x, s):
+    def complete(M, mat, x, s, y=None):
         """One complete call through the public entry point: quantise + GEMV."""
         c, sc = mats[mat]
+        y = ys[M] if y is None else y
         st = lib.pq2_linear(x.data_ptr(), pq2.PQ2_BF16, K_DIM, M, N_DIM, K_DIM, c.data_ptr(),
-                            sc.data_ptr(), ys[M].data_ptr(), pq2.PQ2_BF16, wss[M].data_ptr(),
+                            sc.data_ptr(), y.data_ptr(), pq2.PQ2_BF16, wss[M].data_ptr(),
                             wss[M].numel(), status.data_ptr(), s)
         if st:
             raise RuntimeError(f"pq2_linear failed ({st})")
@@ -631,18 +656,34 @@ def run_ours(args):
         for i, M in enumerate(MS):
             complete(M, 4 * j + i, xs[M], sp)
 
-    def e2e_step(j):
+    def e2e_staged_step(j):
         j %= n_graphs
         dx_all.copy_(hx_all, non_blocking=True)
         for i, M in enumerate(MS):
             complete(M, 4 * j + i, dx[M], sp)
         hy_all.copy_(y_all, non_blocking=True)
 
+    # Mapped end to end: the calls read x from the pinned host buffer and
+    # write y into the pinned host buffer themselves (unified addressing over
+    # NVLink-C2C), so the step has no staging copies between its kernels.
+    mapped = host_mapped(hx_all) and host_mapped(hy_all)
+    hx = {M: hx_all[row0[M]:row0[M] + M] for M in MS}
+    hy = {M: hy_all[row0[M]:row0[M] + M] for M in MS}
+
+    def e2e_mapped_step(j):
+        j %= n_graphs
+        for i, M in enumerate(MS):
+            complete(M, 4 * j + i, hx[M], sp, y=hy[M])
+
+    e2e_step = e2e_mapped_step if mapped else e2e_staged_step
+
     n_chunks = n_graphs // math.gcd(n_graphs, chunk)
     step_graphs = [capture(lambda j=j: [step_calls(j * chunk + t) for t in range(chunk)])
                    for j in range(n_chunks)]
     e2e_graphs = [capture(lambda j=j: [e2e_step(j * chunk + t) for t in range(chunk)])
                   for j in range(n_chunks)]
+    staged_graphs = ([capture(lambda j=j: [e2e_staged_step(j * chunk + t) for t in range(chunk)])
+                      for j in range(n_chunks)] if mapped else e2e_graphs)
 
     def timed(graphs, replays, warmup):
         with torch.cuda.stream(stream):
@@ -667,9 +708,19 @@ def run_ours(args):
             timed(step_graphs, 20, 0)
         total_ms = timed(step_graphs, args.steps // chunk, warm_replays)
         e2e_ms = timed(e2e_graphs, args.steps // chunk, warm_replays)
+        staged_ms = timed(staged_graphs, args.steps // chunk, warm_replays)
     ms_step = total_ms / args.steps
     us_call = job_us_per_call(ms_step, len(MS), world)
     e2e_us = job_us_per_call(e2e_ms / args.steps, len(MS), world)
+    staged_us = job_us_per_call(staged_ms / args.steps, len(MS), world)
+    if mapped:
+        # the mapped outputs equal the device path's, bit for bit
+        with torch.cuda.stream(stream):
+            e2e_mapped_step(0)
+            step_calls(0)
+        torch.cuda.synchronize()
+        if not torch.equal(hy_all.view(torch.int16), y_all.cpu().view(torch.int16)):
+            raise RuntimeError("mapped end-to-end outputs differ from the device path")
 
     # ------------------------------------------- per-M and kernel-only legs
     per_m = {}
@@ -711,7 +762,14 @@ def run_ours(args):
                              "replayed, CUDA events on the launching stream"},
         "e2e": {"value": round(e2e_us, 3), "unit": "us/call",
                 "h2d_bytes_per_step": sum(M * K_DIM * 2 for M in MS),
-                "d2h_bytes_per_step": sum(M * N_DIM * 2 for M in MS)},
+                "d2h_bytes_per_step": sum(M * N_DIM * 2 for M in MS),
+                "transfer": ("x read and y written by the calls in mapped pinned host memory "
+                             "(unified addressing, NVLink-C2C)" if mapped else
+                             "one pinned host-to-device copy of x and one device-to-host copy "
+                             "of y per step"),
+                "staged_value": round(staged_us, 3),
+                "staged_transfer": "one pinned host-to-device copy of x and one "
+                                   "device-to-host copy of y per step"},
         "gpu_launches": 2 * len(MS) * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 3),
