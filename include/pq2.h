@@ -19,7 +19,12 @@
  * Conventions shared by every entry point:
  *   * Pointers marked (device) are CUDA device pointers owned by the caller;
  *     the library never allocates, frees or keeps them.  Buffers passed to
- *     one call must not overlap unless stated.
+ *     one call must not overlap unless stated.  The activations x and the
+ *     output y of pq2_quantize_act, pq2_mmv and pq2_linear are read and
+ *     written with plain loads and stores, so they may also be pinned host
+ *     memory that the device addresses at its own address (unified
+ *     addressing, e.g. over NVLink-C2C); weights and q must be device
+ *     memory (tensor-memory-access copies).
  *   * `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
  *     enqueued on it; no call synchronises the host with the device.
  *   * Shapes: K > 0 and K % 128 == 0, N >= 1, M in the entry point's range.

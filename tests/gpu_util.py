@@ -95,3 +95,26 @@ def mm_operand_order_f8(q: np.ndarray) -> np.ndarray:
         r[:, :, pos] = b
         out[:, :, p, :] = r.reshape(M, K // G, G)
     return out.reshape(M, 2 * K)
+
+
+def host_mapped(t) -> bool:
+    """True when the pinned host tensor `t` is addressable by the device at
+    its own address (asked of the CUDA runtime, not by touching it)."""
+    import ctypes
+
+    class Attr(ctypes.Structure):
+        _fields_ = [("type", ctypes.c_int), ("device", ctypes.c_int),
+                    ("devicePointer", ctypes.c_void_p), ("hostPointer", ctypes.c_void_p),
+                    ("reserved", ctypes.c_long * 16)]
+    rt = None
+    for name in ("libcudart.so", "libcudart.so.13", "/usr/local/cuda/lib64/libcudart.so"):
+        try:
+            rt = ctypes.CDLL(name)
+            break
+        except OSError:
+            continue
+    if rt is None:
+        return False
+    a = Attr()
+    rc = rt.cudaPointerGetAttributes(ctypes.byref(a), ctypes.c_void_p(t.data_ptr()))
+    return rc == 0 and a.type == 1 and a.devicePointer == t.data_ptr()

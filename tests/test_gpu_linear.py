@@ -133,3 +133,29 @@ def test_quotients_at_and_near_half_integers(dtype):
     assert np.array_equal(q.cpu().numpy(), q_o)
     assert np.array_equal(sx.cpu().numpy().view(np.uint32), sx_o.view(np.uint32))
     assert np.array_equal(qs.cpu().numpy(), O.qsum(q_o))
+
+
+@pytest.mark.parametrize("M", [1, 3, 8, 48])
+def test_linear_on_mapped_host_buffers(M):
+    """pq2_linear reading x from, and writing y to, pinned host memory the
+    device addresses directly: bit-identical to the same call on device
+    buffers (GEMV for M <= 8, the 8-bit prefill path above)."""
+    N, K = 1000, 2048
+    raw = synth.raw_weights(N, K, seed=M + 1, device="cuda")
+    codes, scales = pq2.pq2_prepare(raw, K)
+    x = synth.activations(M, K, seed=M, outlier_frac=0.01)
+    hx = x.pin_memory()
+    hy = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    if not (U.host_mapped(hx) and U.host_mapped(hy)):
+        pytest.skip("pinned host memory is not device-addressable here")
+    lib = pq2.lib()
+    ws = torch.empty(pq2.linear_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st = lib.pq2_linear(hx.data_ptr(), pq2.PQ2_BF16, K, M, N, K, codes.data_ptr(),
+                        scales.data_ptr(), hy.data_ptr(), pq2.PQ2_BF16, ws.data_ptr(), ws.numel(),
+                        status.data_ptr(), None)
+    assert st == pq2.PQ2_OK
+    yd = pq2.linear(x.cuda(), codes, scales, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(hy.view(torch.int16), yd.cpu().view(torch.int16))
