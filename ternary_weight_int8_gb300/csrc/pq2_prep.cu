@@ -16,13 +16,15 @@
 // orthonormal one (butterfly passes of half-width 1, 2, .., 512, then the
 // exact factor 1/32).
 //
-// One CTA (256 threads; four fit on an SM) per row: the row's h sits in
-// shared memory between
-// the two passes.  In the second pass each warp owns whole 1024-blocks: lane
-// l holds elements 32i + l (i = 0..31) in registers, so the passes of
-// half-width 1..16 are shuffles between lanes and those of 32..512 are
-// butterflies inside a lane, with no block-wide barrier; the rounded block
-// is written back over its h.  Then all the warps share the row's
+// One CTA per row (256 threads, four per SM, for many rows; 1024 threads for
+// few rows, where one row's latency counts): the row's h sits in shared
+// memory between the passes.  With 1024 threads, 64 threads form the sum of
+// squares (levels 1024..64 of its tree inside a thread) and up to four warps
+// share each 1024-block of the transform; otherwise each warp owns whole
+// 1024-blocks: lane l holds elements 32i + l (i = 0..31) in registers, so
+// the passes of half-width 1..16 are shuffles between lanes and those of
+// 32..512 are butterflies inside a lane, with no block-wide barrier; the
+// rounded block is written back over its h.  Then all the warps share the row's
 // 128-groups (each a latency chain of shuffles), in the quantiser's lane
 // layout (elements 4l..4l+3 of a group per lane).
 #include <cuda_bf16.h>
@@ -42,6 +44,108 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
 }
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// The transform of every 1024-block of a row by W warps per block (W = 2 or
+// 4): warp u of block b holds the elements b + (1024/W) u + 32 i + l,
+// i < 32/W, of lane l.  Passes of half-width 1..16 are shuffles, those up to
+// 512/W pair registers of a lane, and the last log2(W) passes pair elements
+// of two warps through shared memory (the block's h, already read), in the
+// order 1, 2, .., 512 of the single-warp transform, so the bits are the
+// same.  Every warp of the CTA reaches the same barriers.
+// The norm weights (bf16 bits, two per word) and signs (bytes, four per
+// word) of a lane's elements in the transform_shared layout for W = 2 or 4,
+// loaded at kernel entry so that their latency overlaps the first pass.
+struct TransformOperands {
+  uint32_t wb[8];
+  uint32_t sb[4];
+};
+
+template <int W>
+__device__ __forceinline__ void load_transform_operands(const uint16_t* __restrict__ w,
+                                                        const int8_t* __restrict__ sign, int nblk,
+                                                        int warp, int lane, TransformOperands& o) {
+  constexpr int E = 32 / W, kSpan = kHad / W;
+  if (warp >= nblk * W) return;
+  const int base = (warp / W) * kHad + kSpan * (warp % W);
+#pragma unroll
+  for (int i = 0; i < E; i += 2)
+    o.wb[i / 2] = (uint32_t)w[base + 32 * i + lane] | ((uint32_t)w[base + 32 * (i + 1) + lane] << 16);
+#pragma unroll
+  for (int i = 0; i < E; i += 4) {
+    uint32_t v = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v |= (uint32_t)(uint8_t)sign[base + 32 * (i + e) + lane] << (8 * e);
+    o.sb[i / 4] = v;
+  }
+}
+
+template <int W, int kWarps>
+__device__ __forceinline__ void transform_shared(float* hs, const TransformOperands& o,
+                                                 float inv, uint16_t* __restrict__ norm_out,
+                                                 int64_t m, int K, int nblk, int warp, int lane) {
+  constexpr int E = 32 / W;           // registers per lane
+  constexpr int kSpan = kHad / W;     // elements per warp
+  const bool busy = warp < nblk * W;  // nblk * W <= kWarps
+  const int b = (warp / W) * kHad, u = warp % W;
+  const int base = b + kSpan * u;
+  float r[E];
+  if (busy) {
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      const int j = base + 32 * i + lane;
+      const float w1 = __fadd_rn(bf16_bits_to_float((uint16_t)(o.wb[i / 2] >> (16 * (i & 1)))), 1.0f);
+      const float sg = (float)(int8_t)(uint8_t)(o.sb[i / 4] >> (8 * (i & 3)));
+      const float tn = __fmul_rn(__fmul_rn(hs[j], inv), w1);
+      const uint16_t nb = float_to_bf16_bits(tn);
+      if (norm_out) norm_out[m * K + j] = nb;
+      r[i] = bf16_bits_to_float(nb) * sg;  // exact: the sign is +-1
+    }
+#pragma unroll
+    for (int h = 1; h < 32; h <<= 1) {
+      const bool upper = (lane & h) != 0;
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
+        const float o = __shfl_xor_sync(0xffffffffu, r[i], h);
+        r[i] = upper ? __fsub_rn(o, r[i]) : __fadd_rn(r[i], o);
+      }
+    }
+#pragma unroll
+    for (int d = 1; d < E; d <<= 1) {
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
+        if (i & d) continue;
+        const float a = r[i], c = r[i + d];
+        r[i] = __fadd_rn(a, c);
+        r[i + d] = __fsub_rn(a, c);
+      }
+    }
+  }
+  // half-widths kSpan .. 512: warp u pairs with warp u ^ (h / kSpan)
+#pragma unroll
+  for (int hw = 1; hw < W; hw <<= 1) {
+    __syncthreads();  // every warp has read its h (first round) or its partner's values
+    if (busy) {
+#pragma unroll
+      for (int i = 0; i < E; ++i) hs[base + 32 * i + lane] = r[i];
+    }
+    __syncthreads();
+    if (busy) {
+      const bool upper = (u & hw) != 0;
+      const int pbase = b + kSpan * (u ^ hw);
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
+        const float o = hs[pbase + 32 * i + lane];
+        r[i] = upper ? __fsub_rn(o, r[i]) : __fadd_rn(r[i], o);
+      }
+    }
+  }
+  __syncthreads();  // partners have read the exchanged values
+  if (busy) {
+#pragma unroll
+    for (int i = 0; i < E; ++i)  // 1/32 is exact
+      hs[base + 32 * i + lane] = bf16_bits_to_float(float_to_bf16_bits(r[i] * 0.03125f));
+  }
 }
 
 // kPrepThreads threads per row: 1024 when few rows run (the latency of one
@@ -65,6 +169,12 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepThreads == 256 ? 4 : 1)
   // Programmatic dependent launch, as the stand-alone quantiser.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Latency variant: the transform's norm weights and signs go out first.
+  const int nblk = K / kHad;
+  const int W = kPrepThreads == 1024 ? (nblk <= 8 ? 4 : nblk <= 16 ? 2 : 1) : 1;
+  TransformOperands ops;
+  if (W == 4) load_transform_operands<4>(w, sign, nblk, warp, lane, ops);
+  if (W == 2) load_transform_operands<2>(w, sign, nblk, warp, lane, ops);
 
   // Pass 1a: h = x (+ residual) into shared memory, and the optional
   // residual output.  With 16-byte aligned rows the loads (eight bf16 each)
@@ -119,87 +229,138 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepThreads == 256 ? 4 : 1)
     }
   }
   __syncthreads();
-  // Pass 1b: lanes t + kPrepThreads * k of the 2048 strided partial sums of
-  // h^2, each in increasing j (slices of 2048 outside, the thread's lanes
-  // inside, so a slice's loads go out together).
-  constexpr int kPer = kLanes / kPrepThreads;
-  float p[kPer];
+  if constexpr (kPrepThreads == 1024) {
+    // Pass 1b, latency variant: 64 threads own the lanes i, i + 64, ..,
+    // i + 1984 of the 2048 strided partial sums (i = t), so the levels
+    // len = 1024 .. 64 of the tree pair two lanes of one thread; level 32
+    // goes through shared memory and 16 .. 1 by shuffles in warp 0.
+    if (t < 64) {
+      float p[32];
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) p[k] = 0.0f;
-  for (int base = 0; base < K; base += kLanes) {
+      for (int k = 0; k < 32; ++k) p[k] = 0.0f;
+      for (int base = 0; base < K; base += kLanes) {
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int j = base + t + kPrepThreads * k;
-      if (j < K) p[k] = __fadd_rn(p[k], __fmul_rn(hs[j], hs[j]));
+        for (int k = 0; k < 32; ++k) {
+          const int j = base + t + 64 * k;
+          if (j < K) p[k] = __fadd_rn(p[k], __fmul_rn(hs[j], hs[j]));
+        }
+      }
+      // lane t + 64k pairs with lane t + 64(k + step) at level 64 * step
+#pragma unroll
+      for (int step = 16; step >= 1; step >>= 1)
+#pragma unroll
+        for (int k = 0; k < step; ++k) p[k] = __fadd_rn(p[k], p[k + step]);
+      if (t >= 32) tree[t] = p[0];
+      tree[64 + t] = p[0];
     }
-  }
-  // p[i] += p[i + len]: len 1024 .. kPrepThreads inside the thread (lane
-  // t + kPrepThreads * k pairs with k + kPer/2, then k + kPer/4, ..), the
-  // levels below kPrepThreads down to 32 through shared memory, 16 .. 1 by
-  // shuffles in warp 0.
+    __syncthreads();
+    if (warp == 0) {
+      float v = __fadd_rn(tree[64 + lane], tree[lane + 32]);  // level 32
 #pragma unroll
-  for (int step = kPer / 2; step >= 1; step >>= 1)
+      for (int len = 16; len >= 1; len >>= 1) {
+        const float o = __shfl_down_sync(0xffffffffu, v, len);
+        if (lane < len) v = __fadd_rn(v, o);
+      }
+      if (lane == 0) tree[0] = v;
+    }
+    __syncthreads();
+  } else {
+    // Pass 1b: lanes t + kPrepThreads * k of the 2048 strided partial sums of
+    // h^2, each in increasing j (slices of 2048 outside, the thread's lanes
+    // inside, so a slice's loads go out together).
+    constexpr int kPer = kLanes / kPrepThreads;
+    float p[kPer];
 #pragma unroll
-    for (int k = 0; k < step; ++k) p[k] = __fadd_rn(p[k], p[k + step]);
-  tree[t] = p[0];
-  __syncthreads();
-  for (int len = kPrepThreads / 2; len >= 32; len >>= 1) {
-    if (t < len) tree[t] = __fadd_rn(tree[t], tree[t + len]);
+    for (int k = 0; k < kPer; ++k) p[k] = 0.0f;
+    for (int base = 0; base < K; base += kLanes) {
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int j = base + t + kPrepThreads * k;
+        if (j < K) p[k] = __fadd_rn(p[k], __fmul_rn(hs[j], hs[j]));
+      }
+    }
+    // p[i] += p[i + len]: len 1024 .. kPrepThreads inside the thread (lane
+    // t + kPrepThreads * k pairs with k + kPer/2, then k + kPer/4, ..), the
+    // levels below kPrepThreads down to 32 through shared memory, 16 .. 1 by
+    // shuffles in warp 0.
+#pragma unroll
+    for (int step = kPer / 2; step >= 1; step >>= 1)
+#pragma unroll
+      for (int k = 0; k < step; ++k) p[k] = __fadd_rn(p[k], p[k + step]);
+    tree[t] = p[0];
+    __syncthreads();
+    for (int len = kPrepThreads / 2; len >= 32; len >>= 1) {
+      if (t < len) tree[t] = __fadd_rn(tree[t], tree[t + len]);
+      __syncthreads();
+    }
+    if (warp == 0) {
+      float v = tree[lane];
+#pragma unroll
+      for (int len = 16; len >= 1; len >>= 1) {
+        const float o = __shfl_down_sync(0xffffffffu, v, len);
+        if (lane < len) v = __fadd_rn(v, o);
+      }
+      if (lane == 0) tree[0] = v;
+    }
     __syncthreads();
   }
-  if (warp == 0) {
-    float v = tree[lane];
-#pragma unroll
-    for (int len = 16; len >= 1; len >>= 1) {
-      const float o = __shfl_down_sync(0xffffffffu, v, len);
-      if (lane < len) v = __fadd_rn(v, o);
-    }
-    if (lane == 0) tree[0] = v;
-  }
-  __syncthreads();
   const float mean = __fdiv_rn(tree[0], (float)K);
   const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
 
-  // Pass 2, one 1024-block per warp at a time: normalise, round to bf16,
-  // apply the signs, transform, round to bf16, and store the block back.
-  for (int b = warp * kHad; b < K; b += kPrepWarps * kHad) {
-    float r[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int j = b + 32 * i + lane;
-      const float tn =
-          __fmul_rn(__fmul_rn(hs[j], inv), __fadd_rn(bf16_bits_to_float(w[j]), 1.0f));
-      const uint16_t nb = float_to_bf16_bits(tn);
-      if (norm_out) norm_out[m * K + j] = nb;
-      r[i] = bf16_bits_to_float(nb) * (float)sign[j];  // exact: the sign is +-1
-    }
-    // Passes of half-width 1..16 pair lanes l and l ^ h (the lower lane of a
-    // pair keeps a + c, the upper a - c) ...
-#pragma unroll
-    for (int h = 1; h < 32; h <<= 1) {
-      const bool upper = (lane & h) != 0;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float o = __shfl_xor_sync(0xffffffffu, r[i], h);
-        r[i] = upper ? __fsub_rn(o, r[i]) : __fadd_rn(r[i], o);
-      }
-    }
-    // ... those of 32..512 pair registers i and i + h/32 of one lane.
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
+  // Pass 2: normalise, round to bf16, apply the signs, transform, round to
+  // bf16, and store the block back.
+  // Warps per 1024-block (W, chosen at entry): up to four in the latency
+  // variant (each lane then holds 8 of the block's values, and the passes of
+  // half-width 256 and 512 exchange halves through shared memory), one
+  // otherwise.
+  if (W == 4) {
+    transform_shared<4, kPrepWarps>(hs, ops, inv, norm_out, m, K, nblk, warp, lane);
+    __syncthreads();
+  } else if (W == 2) {
+    transform_shared<2, kPrepWarps>(hs, ops, inv, norm_out, m, K, nblk, warp, lane);
+    __syncthreads();
+  } else {
+    // Pass 2, one 1024-block per warp at a time: normalise, round to bf16,
+    // apply the signs, transform, round to bf16, and store the block back.
+    for (int b = warp * kHad; b < K; b += kPrepWarps * kHad) {
+      float r[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        if (i & d) continue;
-        const float a = r[i], c = r[i + d];
-        r[i] = __fadd_rn(a, c);
-        r[i + d] = __fsub_rn(a, c);
+        const int j = b + 32 * i + lane;
+        const float tn =
+            __fmul_rn(__fmul_rn(hs[j], inv), __fadd_rn(bf16_bits_to_float(w[j]), 1.0f));
+        const uint16_t nb = float_to_bf16_bits(tn);
+        if (norm_out) norm_out[m * K + j] = nb;
+        r[i] = bf16_bits_to_float(nb) * (float)sign[j];  // exact: the sign is +-1
       }
-    }
+      // Passes of half-width 1..16 pair lanes l and l ^ h (the lower lane of a
+      // pair keeps a + c, the upper a - c) ...
 #pragma unroll
-    for (int i = 0; i < 32; ++i)  // 1/32 is exact; the warp has read all of its h
-      hs[b + 32 * i + lane] = bf16_bits_to_float(float_to_bf16_bits(r[i] * 0.03125f));
+      for (int h = 1; h < 32; h <<= 1) {
+        const bool upper = (lane & h) != 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float o = __shfl_xor_sync(0xffffffffu, r[i], h);
+          r[i] = upper ? __fsub_rn(o, r[i]) : __fadd_rn(r[i], o);
+        }
+      }
+      // ... those of 32..512 pair registers i and i + h/32 of one lane.
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (i & d) continue;
+          const float a = r[i], c = r[i + d];
+          r[i] = __fadd_rn(a, c);
+          r[i + d] = __fsub_rn(a, c);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i)  // 1/32 is exact; the warp has read all of its h
+        hs[b + 32 * i + lane] = bf16_bits_to_float(float_to_bf16_bits(r[i] * 0.03125f));
+    }
+    __syncthreads();
   }
-  __syncthreads();
   // Pass 3: the row's 128-groups shared by all warps.
   for (int gi = warp; gi < G; gi += kPrepWarps) {
     const float4 v4 = *reinterpret_cast<const float4*>(hs + gi * kGroup + 4 * lane);
