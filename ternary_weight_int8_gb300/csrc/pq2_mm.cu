@@ -10,9 +10,10 @@
 // GB300 design.  sm_103a has no 8-bit integer tcgen05 MMA, so the contraction
 // runs as kind::f16.  The weights are the MMA's A operand and live in tensor
 // memory: decoder threads (one weight row each) turn a 4-byte code word into
-// eight fp16x2 words of c - 1 with a shift, a LOP3 and one exact HSUB2 each
-// (the fp16 value of 0x6400 | c is 1024 + c) and store them with tcgen05.st,
-// so decoded weights never touch shared memory.  q (B operand, fp16, exact)
+// eight fp16x2 words of c - 1 (one shift, then a LOP3 and one exact HFMA2
+// per word: field s masked in place and OR-ed with 0x6400 is the fp16 value
+// 1024 + c * 4^s) and store them with tcgen05.st, so decoded weights never
+// touch shared memory.  q (B operand, fp16, exact)
 // streams into shared memory by TMA in the matching K order
 // (pq2_quantize_act's PQ2_Q_F16 layout).  Each 128-group is one accumulation
 // of eight K=16 MMAs into a fresh fp32 TMEM tile: every partial sum is an
@@ -32,8 +33,9 @@
 //   warp 1      TMEM allocation; lane 0 issues the MMAs and commits
 //   warps 2-5   decoders: one weight row per thread, codes -> TMEM A tile
 //   warps 6-21  epilogue: one weight row and 32 tokens per thread, reads D
-//               (two buffers in flight), scales it and adds it into fp32
-//               running sums in registers, finally stores y
+//               (two buffers in flight, three on the 8-bit path), scales it
+//               and adds it into fp32 running sums in registers, finally
+//               stores y
 //   warp 22     scheduler: waits until a group's A, q and D buffer are
 //               ready, then releases the MMA warp (named barrier)
 //   warp 23     scales: stages s_x and s_w chunk by chunk for the epilogue
