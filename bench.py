@@ -454,8 +454,9 @@ def ptq_leg(args, dev, stream, timed, capture):
     """PTQ1_0 weights (28 bytes per 128 weights) on the attn_qkv shape, 48
     rotated matrices (550 MB, above L2), activation groups of 32 (the pages'
     PTQ1_0 path) and 128, M = 1..4: pq2_ptq_mmv alone (back-to-back
-    independent calls) and the complete call (grouped quantisation, then the
-    GEMV streaming its weights while the quantisation runs)."""
+    independent calls) and the complete call pq2_ptq_linear (grouped
+    quantisation, then the GEMV streaming its weights while the quantisation
+    runs)."""
     import torch
     from ternary_weight_int8_gb300 import pq2, synth
     lib = pq2.lib()
@@ -478,28 +479,32 @@ def ptq_leg(args, dev, stream, timed, capture):
             q, sx, qs = pq2.pq2_quantize_act_grouped(x, A, pq2.PQ2_Q_ROWS)
             y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
 
-            def mmv_calls(flags=pq2.PQ2_MMV_INDEPENDENT, quant=False):
+            wsb = torch.empty(lib.pq2_ptq_linear_workspace_bytes(M, K, A), dtype=torch.uint8,
+                              device=dev)
+
+            def mmv_calls():
                 for wq, ws in mats:
-                    if quant:
-                        st = lib.pq2_quantize_act_grouped(x.data_ptr(), pq2.PQ2_BF16, K, M, K, A,
-                                                          q.data_ptr(), pq2.PQ2_Q_ROWS,
-                                                          sx.data_ptr(), qs.data_ptr(), sp)
-                        if st:
-                            raise RuntimeError(f"pq2_quantize_act_grouped failed ({st})")
                     st = lib.pq2_ptq_mmv(q.data_ptr(), sx.data_ptr(), qs.data_ptr(), wq.data_ptr(),
                                          ws.data_ptr(), y.data_ptr(), pq2.PQ2_BF16, M, N, K, A,
-                                         flags, sp)
+                                         pq2.PQ2_MMV_INDEPENDENT, sp)
                     if st:
                         raise RuntimeError(f"pq2_ptq_mmv failed ({st})")
 
+            def complete_calls():
+                for wq, ws in mats:
+                    st = lib.pq2_ptq_linear(x.data_ptr(), pq2.PQ2_BF16, K, M, N, K, wq.data_ptr(),
+                                            ws.data_ptr(), A, y.data_ptr(), pq2.PQ2_BF16,
+                                            wsb.data_ptr(), wsb.numel(), sp)
+                    if st:
+                        raise RuntimeError(f"pq2_ptq_linear failed ({st})")
+
             reps = 30
             k_ms = timed([capture(mmv_calls)], reps, 3) / (reps * nm)
-            c_ms = timed([capture(lambda: mmv_calls(pq2.PQ2_MMV_OVERLAP_WEIGHTS, True))],
-                         reps, 3) / (reps * nm)
+            c_ms = timed([capture(complete_calls)], reps, 3) / (reps * nm)
             gbs = nbytes / (k_ms * 1e-3) / 1e9
             by_m[str(M)] = {"mmv_us": round(k_ms * 1e3, 3), "mmv_gbs": round(gbs, 1),
                             "mmv_frac": round(gbs / hbm, 3), "complete_us": round(c_ms * 1e3, 3)}
-            del x, q, sx, qs, y
+            del x, q, sx, qs, y, wsb
         out["by_a"][str(A)] = by_m
     del mats
     torch.cuda.empty_cache()

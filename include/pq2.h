@@ -278,6 +278,22 @@ int pq2_ptq_mmv(const int8_t *q_rows, const float *sx, const int32_t *qsum,
                 int64_t M, int64_t N, int64_t K, int act_group, int flags,
                 void *stream);
 
+/* pq2_ptq_linear — the complete PTQ1_0 projection: pq2_quantize_act_grouped
+ * (PQ2_Q_ROWS, act_group) into the caller's workspace, then pq2_ptq_mmv with
+ * PQ2_MMV_OVERLAP_WEIGHTS (the GEMV streams its weights while the
+ * quantisation runs; qs and side must not be written by a kernel that may
+ * still run).  Bit-identical to the two calls.
+ *   x         (device or device-addressable host) x_dtype [M][ldx], M 1..4.
+ *   workspace (device) pq2_ptq_linear_workspace_bytes(M, K, act_group)
+ *             bytes, 256-byte aligned; contents are scratch.
+ * Returns PQ2_ERR_SHAPE for a workspace that is too small, else as the two
+ * calls. */
+size_t pq2_ptq_linear_workspace_bytes(int64_t M, int64_t K, int act_group);
+int pq2_ptq_linear(const void *x, int x_dtype, int64_t ldx, int64_t M,
+                   int64_t N, int64_t K, const uint8_t *qs, const uint32_t *side,
+                   int act_group, void *y, int y_dtype, void *workspace,
+                   size_t workspace_bytes, void *stream);
+
 /* The exact partial dots of pq2_ptq_mmv, dots[m][n][j] = sum over k in
  * [jA, jA + A) of (t_{n,k} - 1) q_{m,k}, from the same device code (parity
  * checks).  dots (device) int32 [M][N][K / A]. */

@@ -244,6 +244,46 @@ int pq2_ptq_mmv(const int8_t* q_rows, const float* sx, const int32_t* qsum, cons
                              overlap, sms, static_cast<cudaStream_t>(stream));
 }
 
+size_t pq2_ptq_linear_workspace_bytes(int64_t M, int64_t K, int act_group) {
+  if (M < 1 || M > 4 || !valid_k(K) || K % 256 ||
+      (act_group != 128 && act_group != 64 && act_group != 32))
+    return 0;
+  const size_t GA = (size_t)(K / act_group);
+  const size_t q_bytes = (size_t)M * (size_t)K;
+  const size_t sx_off = (q_bytes + 255) / 256 * 256;
+  const size_t qs_off = (sx_off + (size_t)M * GA * 4 + 255) / 256 * 256;
+  return qs_off + (size_t)M * GA * 4;
+}
+
+int pq2_ptq_linear(const void* x, int x_dtype, int64_t ldx, int64_t M, int64_t N, int64_t K,
+                   const uint8_t* qs, const uint32_t* side, int act_group, void* y, int y_dtype,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  if (!x || !qs || !side || !y || !workspace) return PQ2_ERR_NULL;
+  if (x_dtype != PQ2_BF16 && x_dtype != PQ2_F16 && x_dtype != PQ2_F32) return PQ2_ERR_DTYPE;
+  if (y_dtype != PQ2_F32 && y_dtype != PQ2_BF16) return PQ2_ERR_DTYPE;
+  const size_t need = pq2_ptq_linear_workspace_bytes(M, K, act_group);
+  if (need == 0 || !valid_n(N) || ldx < K || ldx > ((int64_t)1 << 40)) return PQ2_ERR_SHAPE;
+  if (workspace_bytes < need) return PQ2_ERR_SHAPE;
+  if (!aligned(x, elem_bytes(x_dtype)) || !aligned(workspace, 256) || !aligned(qs, 16) ||
+      !aligned(side, 8) || !aligned(y, elem_bytes(y_dtype)))
+    return PQ2_ERR_ALIGN;
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  const size_t GA = (size_t)(K / act_group);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t sx_off = ((size_t)M * (size_t)K + 255) / 256 * 256;
+  const size_t qs_off = (sx_off + (size_t)M * GA * 4 + 255) / 256 * 256;
+  float* sx = reinterpret_cast<float*>(ws + sx_off);
+  int32_t* qsum = reinterpret_cast<int32_t*>(ws + qs_off);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (int st = pq2::launch_quantize(x, x_dtype, ldx, M, K, ws, PQ2_Q_ROWS, sx, qsum, s,
+                                    act_group))
+    return st;
+  // The GEMV streams its weights while the quantisation runs.
+  return pq2::launch_ptq_mmv(reinterpret_cast<const int8_t*>(ws), sx, qsum, qs, side, y, y_dtype,
+                             nullptr, M, N, K, act_group, 1, sms, s);
+}
+
 int pq2_debug_ptq_dots(const int8_t* q_rows, const int32_t* qsum, const uint8_t* qs,
                        const uint32_t* side, int64_t M, int64_t N, int64_t K, int act_group,
                        int32_t* dots, void* stream) {

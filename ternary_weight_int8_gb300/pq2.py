@@ -47,6 +47,8 @@ SIGNATURES = {
     "pq2_mmv_gated": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _P, _P]),
     "pq2_quantize_act_grouped": (_I, [_P, _I, _I64, _I64, _I64, _I, _P, _I, _P, _P, _P]),
     "pq2_ptq_prepare": (_I, [_P, _I64, _I64, _I64, _P, _P, _P]),
+    "pq2_ptq_linear_workspace_bytes": (_SZ, [_I64, _I64, _I]),
+    "pq2_ptq_linear": (_I, [_P, _I, _I64, _I64, _I64, _I64, _P, _P, _I, _P, _I, _P, _SZ, _P]),
     "pq2_ptq_mmv": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _I, _P]),
     "pq2_debug_ptq_dots": (_I, [_P, _P, _P, _P, _I64, _I64, _I64, _I, _P, _P]),
     "pq2_mmv_grouped": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _I, _P, _P]),
@@ -251,6 +253,22 @@ def pq2_ptq_mmv(q_rows, sx, qsum, qs, side, act_group: int, y=None, out_dtype=to
     _check("pq2_ptq_mmv", lib().pq2_ptq_mmv(
         _ptr(q_rows), _ptr(sx), _ptr(qsum), _ptr(qs), _ptr(side), _ptr(y), _DT[y.dtype], M, N,
         K, act_group, flags, _stream(stream)))
+    return y
+
+
+def pq2_ptq_linear(x, qs, side, act_group: int, y=None, out_dtype=torch.float32, stream=None):
+    """Complete PTQ1_0 projection (M = 1..4): grouped quantisation + GEMV."""
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit column stride")
+    M, K = x.shape
+    N = qs.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    nbytes = lib().pq2_ptq_linear_workspace_bytes(M, K, act_group)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=x.device)
+    _check("pq2_ptq_linear", lib().pq2_ptq_linear(
+        _ptr(x), _DT[x.dtype], x.stride(0), M, N, K, _ptr(qs), _ptr(side), act_group, _ptr(y),
+        _DT[y.dtype], _ptr(ws), ws.numel(), _stream(stream)))
     return y
 
 

@@ -173,3 +173,38 @@ def test_ptq_rejects_bad_arguments():
     assert mmv(M, K, 32, qs_p=qs.data_ptr() + 4) == pq2.PQ2_ERR_ALIGN
     assert mmv(M, K, 32) == pq2.PQ2_OK
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("M", [1, 2, 4])
+@pytest.mark.parametrize("A", [128, 32])
+def test_ptq_linear_matches_two_calls(M, A):
+    """pq2_ptq_linear is bit-identical to pq2_quantize_act_grouped (rows)
+    followed by pq2_ptq_mmv, for fp32 and bf16 outputs."""
+    N, K = 3000, 5120
+    raw = synth.ptq_raw_weights(N, K, seed=M + A, device="cuda")
+    qs, side = pq2.pq2_ptq_prepare(raw, K)
+    x = synth.activations(M, K, seed=A + 3 * M, device="cuda", outlier_frac=0.01)
+    for out_dtype in (torch.float32, torch.bfloat16):
+        a = pq2.pq2_ptq_linear(x, qs, side, A, out_dtype=out_dtype)
+        q, sx, qsum = pq2.pq2_quantize_act_grouped(x, A, pq2.PQ2_Q_ROWS)
+        b = pq2.pq2_ptq_mmv(q, sx, qsum, qs, side, A, out_dtype=out_dtype)
+        torch.cuda.synchronize()
+        iv = torch.int32 if out_dtype == torch.float32 else torch.int16
+        assert torch.equal(a.view(iv), b.view(iv))
+
+
+def test_ptq_linear_rejects_small_workspace():
+    lib = pq2.lib()
+    M, N, K = 2, 8, 512
+    x = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+    qs = torch.zeros((N, 24 * K // 128), dtype=torch.uint8, device="cuda")
+    side = torch.zeros((N, K // 128), dtype=torch.int32, device="cuda")
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    need = lib.pq2_ptq_linear_workspace_bytes(M, K, 32)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    args = (x.data_ptr(), pq2.PQ2_BF16, K, M, N, K, qs.data_ptr(), side.data_ptr(), 32,
+            y.data_ptr(), pq2.PQ2_F32, ws.data_ptr())
+    assert lib.pq2_ptq_linear(*args, need - 1, None) == pq2.PQ2_ERR_SHAPE
+    assert lib.pq2_ptq_linear_workspace_bytes(5, K, 32) == 0
+    assert lib.pq2_ptq_linear(*args, need, None) == pq2.PQ2_OK
+    torch.cuda.synchronize()
