@@ -54,10 +54,10 @@ METRIC = ("µs/call and HBM GB/s (frac of peak) for ternary×INT8 matmul at "
 K_DIM, N_DIM, MS = 5120, 10240, (1, 2, 3, 4)
 PREFILL_K, PREFILL_N, PREFILL_MS = 5120, 17408, (16, 128, 512, 2048, 4096)
 GATED_K, GATED_I = 5120, 17408
-# DRAM bytes (read + write) per pq2_mmv launch on attn_qkv, from the ncu
-# captures in profiles/pq2_mmv_attn_qkv_full.md (mean of M=1 and M=4);
-# None once the kernel changes after that capture.
-MMV_TRAFFIC_BYTES = (13_982_720 + 14_014_208) // 2
+# DRAM bytes (read + write) per pq2_mmv launch on attn_qkv, from ncu
+# captures of the current kernel at M=1 and M=4 (their mean); to be set to
+# None when the kernel changes after that capture.
+MMV_TRAFFIC_BYTES = (13_992_704 + 14_018_304) // 2
 WORKLOAD = ("attn_qkv K=5120 N=10240, M=1,2,3,4 per step (quantise + GEMV each); ternary "
             "codes U{0,1,2}, fp16 group-128 scales U[0.005,0.05]; bf16 x N(0,1) with 1% "
             "channels x20; fp32 accumulate, bf16 out")
