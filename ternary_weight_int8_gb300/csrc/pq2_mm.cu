@@ -473,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int j = 0; j < kEpiCols / 2; ++j) acc2[j] = 0ull;
     const int nchunks = (G + kGC - 1) / kGC;
+    const bool live = m0 + col0 < p.M;  // some token of the warp's columns is real
     for (int ch = 0; ch < nchunks; ++ch) {
       const int slot = ch & 1;
       ok = ok && mbar_wait(&s_full[slot], (ch >> 1) & 1);
@@ -485,6 +486,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int db = g % kDBuf;
         ok = ok && done_wait(g);
         tc_fence_after();
+        if (!live) {
+          // No valid token in this warp's columns (a partial last tile, as
+          // for M = 16): release D without reading it.  The wait above keeps
+          // the warp in step: its arrival for group g + kDBuf cannot come
+          // before every warp has released group g's buffer.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&d_empty[db]);
+          continue;
+        }
         const float* sxg = sxs + gg * BT + col0;
         const float sw = __half2float(sws[row * kGC + gg]);
         const uint64_t sw2 = f2_pack(__float_as_uint(sw), __float_as_uint(sw));
