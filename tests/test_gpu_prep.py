@@ -39,7 +39,8 @@ def _oracle(x, r, w, sign, eps, rows=None):
     return O.norm_hadamard_quantize(xb, rb, synth.bits_u16(w), sign.numpy(), eps)
 
 
-@pytest.mark.parametrize("M,K", [(1, 1024), (3, 5120), (8, 17408), (64, 2048), (2, 32768)])
+@pytest.mark.parametrize("M,K", [(1, 1024), (3, 5120), (8, 17408), (64, 2048), (2, 32768),
+                                 (2, 10240), (1, 16384), (5, 9216)])
 @pytest.mark.parametrize("residual", [False, True])
 def test_prep_bitexact(M, K, residual):
     eps = 1e-6
