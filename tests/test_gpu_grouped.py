@@ -45,13 +45,15 @@ def test_quantize_grouped_bitexact(dtype, M, K, A):
     a = O.widen(U.x_bits(x), U.kind(x))
     q_o, sx_o = O.quantize_grouped(a, A)
     qs_o = O.qsum_grouped(q_o, A)
-    for layout in (pq2.PQ2_Q_ROWS, pq2.PQ2_Q_PLANES, pq2.PQ2_Q_F16):
+    for layout in (pq2.PQ2_Q_ROWS, pq2.PQ2_Q_PLANES, pq2.PQ2_Q_F16, pq2.PQ2_Q_F8):
         q, sx, qs = pq2.pq2_quantize_act_grouped(x.cuda(), A, layout)
         torch.cuda.synchronize()
         if layout == pq2.PQ2_Q_ROWS:
             assert np.array_equal(q.cpu().numpy(), q_o)
         elif layout == pq2.PQ2_Q_PLANES:
             assert np.array_equal(q.cpu().numpy(), O.q_planes(q_o))
+        elif layout == pq2.PQ2_Q_F8:
+            assert np.array_equal(q.cpu().numpy(), U.mm_operand_order_f8(q_o))
         else:
             assert np.array_equal(q.cpu().float().numpy(),
                                   U.mm_operand_order(q_o).astype(np.float32))
