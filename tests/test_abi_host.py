@@ -164,3 +164,67 @@ def test_mmv_geometry_fills_the_gb300_shapes(L):
         steps = -(-G // splits)
         eff = (-(-R // 2) * splits / threads) * (G / (splits * steps))
         assert ctas == 152 and eff >= 0.87, (N, K, eff)
+
+
+def test_mm_f8_validation(L):
+    f = L.pq2_mm_f8
+    assert f(A, A, A, A, A, A, 2, 15, 10, 128, None, None) == pq2.PQ2_ERR_SHAPE
+    assert f(None, A, A, A, A, A, 2, 16, 10, 128, None, None) == pq2.PQ2_ERR_NULL
+    assert f(A, A, None, A, A, A, 2, 16, 10, 128, None, None) == pq2.PQ2_ERR_NULL
+    assert f(A, A, A, A, A, A, 1, 16, 10, 128, None, None) == pq2.PQ2_ERR_DTYPE
+    assert f(A + 8, A, A, A, A, A, 2, 16, 10, 128, None, None) == pq2.PQ2_ERR_ALIGN
+    assert f(A, A, A, A, A, A, 2, 16, 10, 200, None, None) == pq2.PQ2_ERR_SHAPE
+    d = L.pq2_debug_group_dots
+    assert d(A, None, A, 16, 10, 128, pq2.PQ2_PATH_MM_F8, A, None, None) == pq2.PQ2_ERR_NULL
+    assert d(A, A, A, 8, 10, 128, pq2.PQ2_PATH_MM_F8, A, None, None) == pq2.PQ2_ERR_SHAPE
+    assert d(A, A, A, 16, 10, 128, 4, A, None, None) == pq2.PQ2_ERR_DTYPE
+
+
+def test_grouped_validation(L):
+    q = L.pq2_quantize_act_grouped
+    ok = [A, pq2.PQ2_BF16, 256, 2, 256, 32, A, pq2.PQ2_Q_PLANES, A, A, None]
+    for idx, val, err in [(5, 16, pq2.PQ2_ERR_SHAPE), (5, 96, pq2.PQ2_ERR_SHAPE),
+                          (7, 4, pq2.PQ2_ERR_DTYPE), (1, 9, pq2.PQ2_ERR_DTYPE),
+                          (6, None, pq2.PQ2_ERR_NULL), (0, None, pq2.PQ2_ERR_NULL),
+                          (6, A + 4, pq2.PQ2_ERR_ALIGN), (4, 200, pq2.PQ2_ERR_SHAPE)]:
+        bad = list(ok); bad[idx] = val
+        assert q(*bad) == err, (idx, val)
+    m = L.pq2_mmv_grouped
+    ok = [A, A, A, A, A, A, pq2.PQ2_F32, 4, 10, 256, 32, 0, None, None]
+    for idx, val, err in [(7, 5, pq2.PQ2_ERR_SHAPE), (10, 16, pq2.PQ2_ERR_SHAPE),
+                          (11, 8, pq2.PQ2_ERR_DTYPE), (2, None, pq2.PQ2_ERR_NULL),
+                          (3, A + 8, pq2.PQ2_ERR_ALIGN)]:
+        bad = list(ok); bad[idx] = val
+        assert m(*bad) == err, (idx, val)
+
+
+def test_ptq_validation(L):
+    p = L.pq2_ptq_prepare
+    assert p(A, 56, 1, 384, A, A, None) == pq2.PQ2_ERR_SHAPE       # K % 256
+    assert p(A, 55, 1, 256, A, A, None) == pq2.PQ2_ERR_SHAPE       # row stride < 28 K/128
+    assert p(None, 56, 1, 256, A, A, None) == pq2.PQ2_ERR_NULL
+    assert p(A, 56, 1, 256, A + 8, A, None) == pq2.PQ2_ERR_ALIGN
+    assert p(A, 56, 1, 256, A, A + 4, None) == pq2.PQ2_ERR_ALIGN
+    m = L.pq2_ptq_mmv
+    ok = [A, A, A, A, A, A, pq2.PQ2_F32, 4, 10, 512, 32, 0, None]
+    for idx, val, err in [(7, 5, pq2.PQ2_ERR_SHAPE), (9, 384, pq2.PQ2_ERR_SHAPE),
+                          (10, 16, pq2.PQ2_ERR_SHAPE), (11, 8, pq2.PQ2_ERR_DTYPE),
+                          (6, pq2.PQ2_F16, pq2.PQ2_ERR_DTYPE), (2, None, pq2.PQ2_ERR_NULL),
+                          (1, None, pq2.PQ2_ERR_NULL), (3, A + 8, pq2.PQ2_ERR_ALIGN),
+                          (4, A + 4, pq2.PQ2_ERR_ALIGN)]:
+        bad = list(ok); bad[idx] = val
+        assert m(*bad) == err, (idx, val)
+    wsb = L.pq2_ptq_linear_workspace_bytes
+    n = wsb(4, 512, 32)
+    assert n >= 4 * 512 + 2 * 4 * 16 * 4
+    assert wsb(5, 512, 32) == 0 and wsb(4, 384, 32) == 0 and wsb(4, 512, 16) == 0
+    lin = L.pq2_ptq_linear
+    ok = [A, pq2.PQ2_BF16, 512, 4, 10, 512, A, A, 32, A, pq2.PQ2_F32, A, n, None]
+    for idx, val, err in [(12, n - 1, pq2.PQ2_ERR_SHAPE), (3, 5, pq2.PQ2_ERR_SHAPE),
+                          (2, 500, pq2.PQ2_ERR_SHAPE), (1, 9, pq2.PQ2_ERR_DTYPE),
+                          (11, A + 64, pq2.PQ2_ERR_ALIGN), (0, None, pq2.PQ2_ERR_NULL)]:
+        bad = list(ok); bad[idx] = val
+        assert lin(*bad) == err, (idx, val)
+    d = L.pq2_debug_ptq_dots
+    assert d(A, A, A, A, 5, 10, 512, 32, A, None) == pq2.PQ2_ERR_SHAPE
+    assert d(A, A, A, A, 4, 10, 512, 32, None, None) == pq2.PQ2_ERR_NULL
