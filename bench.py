@@ -21,9 +21,15 @@ replayed from CUDA graphs and timed with CUDA events on the launching stream.
   roofline    pq2_mmv alone: packed weight bytes K*N*34/128 per launch over
               its CUDA-event time per launch, against the measured HBM peak
   cpu_baseline the CPU oracle on the host cores, on a bounded sample
-  prefill     pq2_mm (and pq2_linear) on ffn_up K=5120 N=17408 at
+  per_m       attn_qkv per M: pq2_mmv in independent calls and in a
+              dependent chain, and the complete call, with HBM fractions
+  sweep       the GEMV on every configured shape (4096x14336 at M = 1; the
+              layer shapes 5120x10240, 5120x6144, 5120x17408, 17408x5120 at
+              M = 1..8, with the batch-invariance check): microseconds, GB/s
+              and fraction, independent, dependent and complete calls
+  prefill     pq2_mm, pq2_mm_f8 and pq2_linear on ffn_up K=5120 N=17408 at
               M = 16 .. 4096: microseconds, TOPS and the fraction of the
-              measured dense 16-bit tensor peak
+              measured dense tensor peak of the kernel's own operand type
   prep        the fused preparation (pq2_norm_hadamard_quantize) at K=5120,
               M = 1..4 and 4096, with the stand-alone quantisation beside it
   gated       the gated gate/up projection (pq2_mmv_gated, silu(gate) * up
@@ -54,10 +60,16 @@ METRIC = ("µs/call and HBM GB/s (frac of peak) for ternary×INT8 matmul at "
 K_DIM, N_DIM, MS = 5120, 10240, (1, 2, 3, 4)
 PREFILL_K, PREFILL_N, PREFILL_MS = 5120, 17408, (16, 128, 512, 2048, 4096)
 GATED_K, GATED_I = 5120, 17408
-# DRAM bytes (read + write) per pq2_mmv launch on attn_qkv, from ncu
-# captures of the current kernel at M=1 and M=4 (their mean); to be set to
-# None when the kernel changes after that capture.
-MMV_TRAFFIC_BYTES = (13_992_704 + 14_018_304) // 2
+# The GEMV sweep: the layer shapes at every M in 1..8 (with the batch
+# invariance check) and the 4096 x 14336 shape at M = 1, as (K, N, Ms, name).
+SWEEP = ((4096, 14336, (1,), "4096x14336"),
+         (5120, 10240, tuple(range(1, 9)), "attn_qkv"),
+         (5120, 6144, tuple(range(1, 9)), "5120x6144"),
+         (5120, 17408, tuple(range(1, 9)), "ffn_up"),
+         (17408, 5120, tuple(range(1, 9)), "ffn_down"))
+MMV_PROFILE = os.path.join(ROOT, "profiles", "pq2_mmv_attn_qkv_full.md")
+MMV_SOURCES = ("ternary_weight_int8_gb300/csrc/pq2_mmv.cu",
+               "ternary_weight_int8_gb300/csrc/pq2_device.cuh")
 WORKLOAD = ("attn_qkv K=5120 N=10240, M=1,2,3,4 per step (quantise + GEMV each); ternary "
             "codes U{0,1,2}, fp16 group-128 scales U[0.005,0.05]; bf16 x N(0,1) with 1% "
             "channels x20; fp32 accumulate, bf16 out")
@@ -90,6 +102,26 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def recorded_traffic():
+    """DRAM bytes (read + write) per pq2_mmv launch on attn_qkv from the
+    committed ncu summary, or None when the kernel's sources have changed
+    since that capture (the summary records their hash) or no record exists."""
+    import hashlib
+    try:
+        with open(MMV_PROFILE) as f:
+            line = next(ln for ln in f if ln.startswith("traffic-record:"))
+        fields = dict(kv.split("=", 1) for kv in line.split()[1:])
+        h = hashlib.sha256()
+        for rel in MMV_SOURCES:
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest()[:16] != fields["sources_sha256_16"]:
+            return None
+        return int(fields["dram_bytes_per_launch"])
+    except (OSError, StopIteration, KeyError, ValueError):
+        return None
 
 
 def measured_tensor_peak():
@@ -160,46 +192,71 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- reference
+def oracle_linear_threads(O, x_bits, codes, scales, threads):
+    """The oracle's complete call (widen, quantise, group dots, scale) with
+    the output rows split into `threads` contiguous slices, one host thread
+    each.  Every slice runs the unchanged oracle on its rows (quantising x
+    itself), so the result equals the single-threaded call bit for bit; the
+    oracle is a C library and its calls release the interpreter lock, so the
+    slices run on separate cores."""
+    import numpy as np
+    from concurrent.futures import ThreadPoolExecutor
+    N = codes.shape[0]
+    if threads <= 1:
+        return O.linear(x_bits, "bf16", codes, scales)
+    cuts = [N * i // threads for i in range(threads + 1)]
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        parts = list(ex.map(lambda i: O.linear(x_bits, "bf16", codes[cuts[i]:cuts[i + 1]],
+                                               scales[cuts[i]:cuts[i + 1]]),
+                            range(threads)))
+    return np.concatenate(parts, axis=1)
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
 def run_reference(args):
-    """The CPU oracle on the same workload.  Each step is one complete call
-    for M = 1..4 restricted to a fixed sample of REF_ROWS of the N output
-    rows (quantisation of the whole x included), single-threaded; the time
-    is scaled by N / REF_ROWS to a full call."""
+    """The CPU oracle on the same workload: each step is one complete call
+    for M = 1..4 on the full attn_qkv shape, the output rows split over every
+    host core (oracle_linear_threads)."""
     from oracle import oracle as O
     from ternary_weight_int8_gb300 import synth
 
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    ref_rows = 1024
+    cores = host_cores()
     raw = synth.raw_weights(N_DIM, K_DIM, seed=1234)
     codes, scales = O.prepare(raw.numpy(), K_DIM)
-    codes, scales = codes[:ref_rows].copy(), scales[:ref_rows].copy()
     xs = {M: synth.bits_u16(synth.activations(M, K_DIM, seed=77 + M, outlier_frac=0.01))
           for M in MS}
     O.load()
 
     def step():
         for M in MS:
-            O.linear(xs[M], "bf16", codes, scales)
+            oracle_linear_threads(O, xs[M], codes, scales, cores)
 
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         step()
-    dt = (time.perf_counter() - t0) * (N_DIM / ref_rows)
+    dt = time.perf_counter() - t0
     us = dt / (args.steps * len(MS)) * 1e6
-    sample = (f"{args.steps} steps of M=1..4 calls on {ref_rows} of {N_DIM} output rows, "
-              f"time scaled by {N_DIM / ref_rows:g}")
+    sample = (f"{args.steps} steps of complete M=1..4 calls on the full {K_DIM}x{N_DIM} shape, "
+              f"output rows split over {cores} host threads")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(us, 3), "unit": "us/call",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "i8", "data": "synthetic",
         "config": {"workload": WORKLOAD,
-                   "runs": "CPU oracle (plain C, IEEE fp32/fp64, one thread)"},
-        "cpu_baseline": {"value": round(us, 3), "unit": "us/call", "cores": 1,
+                   "runs": f"CPU oracle (plain C, IEEE fp32/fp64), {cores} host threads"},
+        "cpu_baseline": {"value": round(us, 3), "unit": "us/call", "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(us, 3), "unit": "us/call", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -233,10 +290,11 @@ def host_mapped(t) -> bool:
     return rc == 0 and a.type == 1 and a.devicePointer == t.data_ptr()
 
 
-def cpu_baseline_sample(budget_s=12.0):
-    """The oracle as it stands on one host core: complete calls for M = 1..4
-    on the full attn_qkv shape, repeated for about budget_s seconds."""
-    import torch
+def cpu_baseline_sample(budget_s=8.0):
+    """The oracle as it stands on the host cores: complete calls for M = 1..4
+    on the full attn_qkv shape, repeated for about budget_s seconds on every
+    core (output rows split over one thread per core), then for about
+    budget_s / 2 seconds on one core."""
     from oracle import oracle as O
     from ternary_weight_int8_gb300 import synth
     raw = synth.raw_weights(N_DIM, K_DIM, seed=4321)
@@ -244,17 +302,26 @@ def cpu_baseline_sample(budget_s=12.0):
     xs = {M: synth.bits_u16(synth.activations(M, K_DIM, seed=5 + M, outlier_frac=0.01))
           for M in MS}
     O.load()
-    calls, t0 = 0, time.perf_counter()
-    while True:
-        for M in MS:
-            O.linear(xs[M], "bf16", codes, scales)
-            calls += 1
-        if time.perf_counter() - t0 > budget_s:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": round(dt / calls * 1e6, 3), "unit": "us/call", "cores": 1,
+    cores = host_cores()
+
+    def run(threads, budget):
+        calls, t0 = 0, time.perf_counter()
+        while True:
+            for M in MS:
+                oracle_linear_threads(O, xs[M], codes, scales, threads)
+                calls += 1
+            if time.perf_counter() - t0 > budget:
+                break
+        return calls, time.perf_counter() - t0
+
+    calls, dt = run(cores, budget_s)
+    calls1, dt1 = run(1, budget_s / 2)
+    return {"value": round(dt / calls * 1e6, 3), "unit": "us/call", "cores": cores,
             "kind": "oracle",
-            "sample": f"{calls} complete attn_qkv calls (M=1..4 cycled) in {dt:.1f} s"}
+            "sample": f"{calls} complete attn_qkv calls (M=1..4 cycled) in {dt:.1f} s, output "
+                      f"rows split over {cores} host threads",
+            "single_core_value": round(dt1 / calls1 * 1e6, 3),
+            "single_core_sample": f"{calls1} calls in {dt1:.1f} s on one thread"}
 
 
 def prefill_leg(args, dev, stream, timed, capture):
@@ -316,7 +383,13 @@ def prefill_leg(args, dev, stream, timed, capture):
         out["by_m"][str(M)] = {"mm_us": round(k_ms * 1e3, 2), "mm_tflops": round(tops, 1),
                                "frac": round(tops / peak, 3),
                                "mm_f8_us": round(k8_ms * 1e3, 2),
-                               "f8_frac": round(2.0 * M * N * K / (k8_ms * 1e-3) / 1e12 / peak, 3),
+                               # pq2_mm_f8 runs 2 e4m3 MMAs per K step (the two
+                               # planes of q): 4MNK executed operations at the
+                               # e4m3 rate, twice the 16-bit one
+                               "f8_pipe_frac": round(4.0 * M * N * K / (k8_ms * 1e-3) / 1e12
+                                                     / (2 * peak), 3),
+                               "f8_e4m3_frac": round(2.0 * M * N * K / (k8_ms * 1e-3) / 1e12
+                                                     / (2 * peak), 3),
                                "complete_us": round(c_ms * 1e3, 2),
                                "complete_tflops": round(2.0 * M * N * K / (c_ms * 1e-3) / 1e12, 1)}
         del x, q, q8, sx, qs, y, ws
@@ -329,15 +402,17 @@ def prefill_leg(args, dev, stream, timed, capture):
 
 def gated_leg(args, dev, stream, timed, capture):
     """The gated gate/up projection (silu(gate) * up in the GEMV's epilogue)
-    on the ffn gate/up shape: K=5120, N = 2 x 17408 weight rows, 4 rotated
-    matrices (189 MB, above the L2 size), M = 1..4.  Per call: pq2_mmv_gated
+    on the ffn gate/up shape: K=5120, N = 2 x 17408 weight rows,
+    max(16, ceil(4 L2 / B)) rotated matrices (above 4x the L2 size), M = 1..4.
+    Per call: pq2_mmv_gated
     alone (back-to-back independent calls on pre-quantised activations),
     the complete pq2_linear_gated call, and pq2_mmv on the same N rows
     without the gated epilogue; GB/s of packed weight bytes K*N*34/128."""
     import torch
     from ternary_weight_int8_gb300 import pq2, synth
     lib = pq2.lib()
-    K, N, nm = GATED_K, 2 * GATED_I, 4
+    K, N = GATED_K, 2 * GATED_I
+    nm = rotation_count(torch.cuda.get_device_properties(dev).L2_cache_size, N * K * 34 // 128)
     mats = []
     for i in range(nm):
         raw = synth.raw_weights(N, K, seed=7000 + i, device=dev)
@@ -569,6 +644,114 @@ def prep_leg(args, dev, stream, timed, capture):
     return out
 
 
+def rotation_count(l2_bytes: int, matrix_bytes: int) -> int:
+    """Distinct weight matrices to rotate so that a call never finds its
+    weights in L2: max(16, ceil(4 L2 / B))."""
+    return max(16, math.ceil(4 * l2_bytes / matrix_bytes))
+
+
+def compact(by_m: dict, key: str, frac_key: str | None = None) -> str:
+    """'M:us/frac' pairs in one short string (the summary keys)."""
+    out = []
+    for M, d in by_m.items():
+        s = f"{M}:{d[key]:.2f}"
+        if frac_key:
+            s += f"/{d[frac_key]:.2f}"
+        out.append(s)
+    return " ".join(out)
+
+
+def sweep_leg(args, dev, stream, timed, capture):
+    """The GEMV on every configured shape (SWEEP), each rotating
+    rotation_count() distinct weight matrices, per M:
+      mmv_us   pq2_mmv alone, back-to-back PQ2_MMV_INDEPENDENT calls (each
+               call may read its inputs and compute while the previous call
+               finishes)
+      dep_us   pq2_mmv in a dependent chain: PQ2_MMV_OVERLAP_WEIGHTS calls,
+               each waiting for the previous call to complete before it
+               reads its activations (the position of a GEMV in a decode
+               step; the weights still stream early)
+      complete_us  pq2_linear (quantise + GEMV), chained
+    with GB/s of packed weight bytes K*N*34/128 and the fraction of the
+    measured HBM peak.  Batch invariance: for each shape, y (fp32) of the
+    first M rows of an 8-row activation matrix, for every M, is compared bit
+    for bit with rows 0..M-1 of the M = 8 call."""
+    import torch
+    from ternary_weight_int8_gb300 import pq2, synth
+    lib = pq2.lib()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sp = stream.cuda_stream
+    hbm, hbm_kind = measured_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    out = {"peak_gbs": hbm, "peak_source": hbm_kind, "shapes": {}}
+    for K, N, Ms, name in SWEEP:
+        wbytes = N * K * 34 // 128
+        n_mats = rotation_count(l2, wbytes)
+        mats = []
+        for i in range(n_mats):
+            raw = synth.raw_weights(N, K, seed=20000 + 100 * K + i, device=dev)
+            mats.append(pq2.pq2_prepare(raw, K))
+            del raw
+        x8 = synth.activations(max(Ms), K, seed=31 + K + N, device=dev)
+        shape = {"K": K, "N": N, "bytes_per_call": wbytes, "matrices": n_mats, "by_m": {}}
+        ref = None
+        invariant = True
+        for M in sorted(Ms, reverse=True):
+            x = x8[:M]
+            q, sx, qs = pq2.pq2_quantize_act(x, pq2.PQ2_Q_PLANES)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ws = torch.empty(pq2.linear_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
+            # batch invariance on the first matrix, fp32 output
+            c0, s0 = mats[0]
+            y32 = pq2.pq2_mmv(q, sx, qs, c0, s0, out_dtype=torch.float32)
+            torch.cuda.synchronize()
+            if ref is None:
+                ref = y32
+            elif not torch.equal(y32.view(torch.int32), ref[:M].view(torch.int32)):
+                invariant = False
+
+            def calls(flag):
+                def run():
+                    for c, sc in mats:
+                        st = lib.pq2_mmv_ex(q.data_ptr(), sx.data_ptr(), qs.data_ptr(),
+                                            c.data_ptr(), sc.data_ptr(), y.data_ptr(),
+                                            pq2.PQ2_BF16, M, N, K, lib.pq2_mmv_decoder(M), flag,
+                                            status.data_ptr(), sp)
+                        if st:
+                            raise RuntimeError(f"pq2_mmv_ex failed ({st})")
+                return run
+
+            def complete_calls():
+                for c, sc in mats:
+                    st = lib.pq2_linear(x.data_ptr(), pq2.PQ2_BF16, K, M, N, K, c.data_ptr(),
+                                        sc.data_ptr(), y.data_ptr(), pq2.PQ2_BF16, ws.data_ptr(),
+                                        ws.numel(), status.data_ptr(), sp)
+                    if st:
+                        raise RuntimeError(f"pq2_linear failed ({st})")
+
+            reps = 10
+            k_ms = timed([capture(calls(pq2.PQ2_MMV_INDEPENDENT))], reps, 3) / (reps * n_mats)
+            d_ms = timed([capture(calls(pq2.PQ2_MMV_OVERLAP_WEIGHTS))], reps, 3) / (reps * n_mats)
+            c_ms = timed([capture(complete_calls)], reps, 3) / (reps * n_mats)
+            gbs = wbytes / (k_ms * 1e-3) / 1e9
+            dgbs = wbytes / (d_ms * 1e-3) / 1e9
+            shape["by_m"][str(M)] = {"mmv_us": round(k_ms * 1e3, 3), "mmv_gbs": round(gbs, 1),
+                                     "mmv_frac": round(gbs / hbm, 3),
+                                     "dep_us": round(d_ms * 1e3, 3),
+                                     "dep_frac": round(dgbs / hbm, 3),
+                                     "complete_us": round(c_ms * 1e3, 3)}
+            del q, sx, qs, y, ws, y32
+        shape["by_m"] = dict(sorted(shape["by_m"].items(), key=lambda kv: int(kv[0])))
+        if len(Ms) > 1:
+            shape["batch_invariant"] = invariant
+        out["shapes"][name] = shape
+        del mats, x8, ref
+        torch.cuda.empty_cache()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -706,14 +889,15 @@ def run_ours(args):
         return max_over_ranks(e0.elapsed_time(e1), dev)
 
     warm_replays = -(-args.warmup // chunk)
-    # soak (untimed) while the clock sampler runs, then the timed region
-    with ClockSampler(local) as clocks:
-        t_end = time.time() + 1.5
-        while time.time() < t_end:
-            timed(step_graphs, 20, 0)
-        total_ms = timed(step_graphs, args.steps // chunk, warm_replays)
-        e2e_ms = timed(e2e_graphs, args.steps // chunk, warm_replays)
-        staged_ms = timed(staged_graphs, args.steps // chunk, warm_replays)
+    # soak (untimed) while the clock sampler runs, then the timed region; the
+    # sampler stays open over every leg below, so its summary covers them all
+    clocks = ClockSampler(local).__enter__()
+    t_end = time.time() + 1.5
+    while time.time() < t_end:
+        timed(step_graphs, 20, 0)
+    total_ms = timed(step_graphs, args.steps // chunk, warm_replays)
+    e2e_ms = timed(e2e_graphs, args.steps // chunk, warm_replays)
+    staged_ms = timed(staged_graphs, args.steps // chunk, warm_replays)
     ms_step = total_ms / args.steps
     us_call = job_us_per_call(ms_step, len(MS), world)
     e2e_us = job_us_per_call(e2e_ms / args.steps, len(MS), world)
@@ -730,30 +914,76 @@ def run_ours(args):
     # ------------------------------------------- per-M and kernel-only legs
     per_m = {}
     peak, peak_kind = measured_peaks()
+
+    def mmv_dep(M, mat, s):
+        """The GEMV in a dependent chain: each call waits for the kernel
+        before it to complete before reading its activations."""
+        q, sx, qs = qbuf[M]
+        c, sc = mats[mat]
+        st = lib.pq2_mmv_ex(q.data_ptr(), sx.data_ptr(), qs.data_ptr(), c.data_ptr(),
+                            sc.data_ptr(), ys[M].data_ptr(), pq2.PQ2_BF16, M, N_DIM, K_DIM,
+                            lib.pq2_mmv_decoder(M), pq2.PQ2_MMV_OVERLAP_WEIGHTS,
+                            status.data_ptr(), s)
+        if st:
+            raise RuntimeError(f"pq2_mmv failed ({st})")
+
     for M in MS:
         # one graph = one call on each of the n_mats matrices in turn
         g_c = [capture(lambda: [complete(M, i, xs[M], sp) for i in range(n_mats)])]
         g_k = [capture(lambda: [mmv_only(M, i, sp) for i in range(n_mats)])]
+        g_d = [capture(lambda: [mmv_dep(M, i, sp) for i in range(n_mats)])]
         reps = max(20, args.steps // 10)
         c_ms = timed(g_c, reps, 3) / (reps * n_mats)
         k_ms = timed(g_k, reps, 3) / (reps * n_mats)
+        d_ms = timed(g_d, reps, 3) / (reps * n_mats)
         per_m[str(M)] = {
             "complete_us": round(c_ms * 1e3, 3),
+            "complete_frac": round(wbytes / (c_ms * 1e-3) / 1e9 / peak, 3),
             "mmv_us": round(k_ms * 1e3, 3),
             "mmv_gbs": round(wbytes / (k_ms * 1e-3) / 1e9, 1),
             "mmv_frac": round(wbytes / (k_ms * 1e-3) / 1e9 / peak, 3),
+            "dep_us": round(d_ms * 1e3, 3),
+            "dep_frac": round(wbytes / (d_ms * 1e-3) / 1e9 / peak, 3),
         }
+    sweep = sweep_leg(args, dev, stream, timed, capture) if not args.no_sweep else None
     prefill = prefill_leg(args, dev, stream, timed, capture) if not args.no_prefill else None
     gated = gated_leg(args, dev, stream, timed, capture) if not args.no_gated else None
     prep = prep_leg(args, dev, stream, timed, capture) if not args.no_prep else None
     grouped = (grouped_leg(args, dev, stream, timed, capture, mats, wbytes)
                if not args.no_grouped else None)
     ptq = ptq_leg(args, dev, stream, timed, capture) if not args.no_ptq else None
+    clocks.__exit__(None, None, None)
     # dominant kernel: pq2_mmv over the step's M mix, kernel-only
     mean_k_us = statistics.mean(per_m[str(M)]["mmv_us"] for M in MS)
+    mean_d_us = statistics.mean(per_m[str(M)]["dep_us"] for M in MS)
     achieved = wbytes / (mean_k_us * 1e-6) / 1e9
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
+
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 3),
+                "traffic": recorded_traffic(),
+                "kernel": "pq2_mmv", "peak_source": peak_kind,
+                "bytes_per_launch": wbytes,
+                "timing": "independent calls (PQ2_MMV_INDEPENDENT), mean over M=1..4",
+                "dep_frac": round(wbytes / (mean_d_us * 1e-6) / 1e9 / peak, 3),
+                "dep_timing": "dependent chain (each call waits for the previous one before "
+                              "reading its activations), mean over M=1..4",
+                "attn_qkv_indep_us_frac": compact(per_m, "mmv_us", "mmv_frac"),
+                "attn_qkv_dep_us_frac": compact(per_m, "dep_us", "dep_frac"),
+                "attn_qkv_complete_us": compact(per_m, "complete_us")}
+    if sweep:
+        for name, sh in sweep["shapes"].items():
+            roofline[f"{name}_indep_us_frac"] = compact(sh["by_m"], "mmv_us", "mmv_frac")
+            roofline[f"{name}_dep_us_frac"] = compact(sh["by_m"], "dep_us", "dep_frac")
+            roofline[f"{name}_complete_us"] = compact(sh["by_m"], "complete_us")
+            if "batch_invariant" in sh:
+                roofline[f"{name}_batch_invariant"] = sh["batch_invariant"]
+    if prefill:
+        for M, d in prefill["by_m"].items():
+            for k in ("mm_us", "frac", "mm_f8_us", "f8_pipe_frac", "f8_e4m3_frac",
+                      "complete_us"):
+                prefill[f"m{M}_{k}"] = d[k]
 
     result = {
         "metric": METRIC, "value": round(us_call, 3), "unit": "us/call", "n_gpus": world,
@@ -776,12 +1006,9 @@ def run_ours(args):
                 "staged_transfer": "one pinned host-to-device copy of x and one "
                                    "device-to-host copy of y per step"},
         "gpu_launches": 2 * len(MS) * args.steps,
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 3),
-                     "traffic": MMV_TRAFFIC_BYTES,
-                     "kernel": "pq2_mmv", "peak_source": peak_kind,
-                     "bytes_per_launch": wbytes},
+        "roofline": roofline,
         "per_m": per_m,
+        "sweep": sweep,
         "prefill": prefill,
         "gated": gated,
         "prep": prep,
@@ -854,6 +1081,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill (pq2_mm) leg")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the GEMV sweep over the configured shapes and M = 1..8")
     ap.add_argument("--no-gated", action="store_true",
                     help="skip the gated gate/up (pq2_mmv_gated) leg")
     ap.add_argument("--no-prep", action="store_true",

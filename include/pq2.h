@@ -342,21 +342,32 @@ int pq2_linear_gated(const void *x, int x_dtype, int64_t ldx, int64_t M,
 #define PQ2_STATIC_SCRATCH_BYTES ((size_t)1 << 20)
 
 /* pq2_linear_static — pq2_linear for callers that cannot allocate device
- * memory.  The pages have no counterpart: this is a deployment convenience,
- * not a step of the method.  The call allocates nothing (no cudaMalloc,
- * cudaFree or allocating library routine): its workspace (q, s_x and sum(q),
- * laid out as for pq2_linear) is a file-scope static device array of
- * PQ2_STATIC_SCRATCH_BYTES per device, whose address is looked up once per
- * device (on the first call with that device current).
- *   Arguments, results and errors as for pq2_linear, without the workspace.
+ * memory (for example code running where cudaMalloc is not allowed, or
+ * runtimes whose allocator owns all device memory).  The pages have no
+ * counterpart: this is a deployment convenience, not a step of the method.
+ * The call allocates nothing (no cudaMalloc, cudaFree or allocating library
+ * routine): its workspace (q, s_x and sum(q), laid out as for pq2_linear) is
+ * a file-scope static device array of PQ2_STATIC_SCRATCH_BYTES in every
+ * device's context, which each device holds until the process exits.  Its
+ * device address is looked up (cudaGetSymbolAddress) with the device current
+ * on the first call on that device, which also creates the device's primary
+ * context, and again whenever the current context differs from the one the
+ * address was found in (after a device reset).  Make the first call on a
+ * device before capturing any stream into a graph.
+ *   Arguments, results and errors as for pq2_linear, without the workspace;
+ *   errors in pq2_linear's order (NULL, dtype, shape).
+ *   stream   must belong to the current device (NULL is the current
+ *            device's legacy default stream): the scratch address is the
+ *            current device's.  Another device's stream returns PQ2_ERR_CUDA.
  *   Returns PQ2_ERR_SHAPE, before any CUDA call, when
  *   pq2_linear_workspace_bytes(M, K) exceeds PQ2_STATIC_SCRATCH_BYTES (for
  *   example M = 8 with K above 123,264, or M = 16 with K above 31,744);
  *   PQ2_ERR_CUDA if the scratch address cannot be obtained.
- * Every call on a device shares the one scratch array.  Nothing in it needs
- * to start at zero: each call writes all of it that it reads.  Calls that may
- * run at the same time on the GPU (for example on two streams) race on it;
- * calls in order on one stream do not. */
+ * Every call on a device shares the one scratch array, which keeps the last
+ * call's contents.  Nothing in it needs to start at zero: each call writes
+ * all of it that it reads.  Calls that may run at the same time on the GPU
+ * (for example on two streams) race on it; calls in order on one stream do
+ * not. */
 int pq2_linear_static(const void *x, int x_dtype, int64_t ldx, int64_t M,
                       int64_t N, int64_t K, const uint8_t *codes,
                       const uint16_t *scales, void *y, int y_dtype,
@@ -447,6 +458,24 @@ int pq2_debug_group_dots(const void *q, const int32_t *qsum,
                          const uint8_t *codes, int64_t M, int64_t N, int64_t K,
                          int path, int32_t *dots, int32_t *dev_status,
                          void *stream);
+
+/* pq2_debug_mmv_drop_arrival — a test of the bounded device waits (the
+ * status convention above), not a step of the method: pq2_mmv (masked-plane
+ * decoder, no flags) in which one consumer warp does not release the first
+ * ring stage of its weight pipeline, so the producer's wait for that slot,
+ * limited here to wait_limit_cycles SM clocks (1000 .. 2^32), gives up.  The
+ * producer then issues no further copy, waits (bounded) until every copy it
+ * issued has landed, and tells the consumers to stop; the kernel writes
+ * PQ2_ERR_TIMEOUT to *dev_status (required here) and returns.  y is
+ * unspecified afterwards; the device and its context stay usable.  Returns
+ * PQ2_ERR_SHAPE when (N, K) gives a pipeline whose slots are never reused
+ * (nothing to wait for), else as pq2_mmv. */
+int pq2_debug_mmv_drop_arrival(const int8_t *q_planes, const float *sx,
+                               const int32_t *qsum, const uint8_t *codes,
+                               const uint16_t *scales, void *y, int y_dtype,
+                               int64_t M, int64_t N, int64_t K,
+                               int64_t wait_limit_cycles, int32_t *dev_status,
+                               void *stream);
 
 /* pq2_mmv_geometry — the launch geometry pq2_mmv uses for (N, K) on a device
  * with sm_count SMs (host only, no CUDA call): CTAs, threads per CTA,

@@ -466,6 +466,23 @@ int pq2_debug_group_dots(const void* q, const int32_t* qsum, const uint8_t* code
                          0, sms, dev_status, s);
 }
 
+int pq2_debug_mmv_drop_arrival(const int8_t* q, const float* sx, const int32_t* qsum,
+                               const uint8_t* codes, const uint16_t* scales, void* y,
+                               int y_dtype, int64_t M, int64_t N, int64_t K,
+                               int64_t wait_limit_cycles, int32_t* dev_status, void* stream) {
+  if (int st = check_mmv_args(q, sx, qsum, codes, scales, y, y_dtype, M, N, K,
+                              PQ2_DECODE_PLANES))
+    return st;
+  if (!dev_status) return PQ2_ERR_NULL;
+  if (wait_limit_cycles < 1000 || wait_limit_cycles > (int64_t)1 << 32) return PQ2_ERR_SHAPE;
+  if (!aligned(dev_status, 4)) return PQ2_ERR_ALIGN;
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  return pq2::launch_mmv_drop_arrival(q, sx, qsum, codes, scales, y, y_dtype, M, N, K,
+                                      (long long)wait_limit_cycles, sms, dev_status,
+                                      static_cast<cudaStream_t>(stream));
+}
+
 int pq2_mmv_geometry(int64_t N, int64_t K, int sm_count, int* ctas, int* threads,
                      int* splits, int* rows_max) {
   pq2::MmvGeometry g;

@@ -87,6 +87,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
+// As mbar_wait, with its own limit in SM clocks, and giving up early once
+// *abort (a shared-memory flag, may be NULL) is non-zero.
+__device__ __forceinline__ bool mbar_wait_until(uint64_t* bar, uint32_t parity, long long limit,
+                                                const volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long start = clock64();
+  while (!mbar_try_wait_sleep(bar, parity, kWaitSuspendNs)) {
+    if (abort && *abort) return false;
+    if (clock64() - start > limit) return false;
+  }
+  return true;
+}
+
 // 1-D bulk copy global -> shared of `bytes` (multiple of 16, both addresses
 // 16-byte aligned), completing `bytes` of transaction count on `bar`.
 __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem,

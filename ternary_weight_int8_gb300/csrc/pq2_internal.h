@@ -52,6 +52,15 @@ int launch_mmv_grouped(const int8_t* q, const float* sx, const int32_t* qsum,
                        int32_t* dots, int64_t M, int64_t N, int64_t K, int act_group,
                        int overlap, int sm_count, int32_t* status, cudaStream_t stream);
 
+// pq2_mmv (masked planes, no overlap) with consumer warp 0 skipping its
+// release of ring stage 0 and the producer's wait for a free slot limited to
+// wait_limit SM clocks: the bounded-wait path, for tests.  PQ2_ERR_SHAPE when
+// (N, K) gives no reused ring slot.
+int launch_mmv_drop_arrival(const int8_t* q, const float* sx, const int32_t* qsum,
+                            const uint8_t* codes, const uint16_t* scales, void* y, int y_dtype,
+                            int64_t M, int64_t N, int64_t K, long long wait_limit, int sm_count,
+                            int32_t* status, cudaStream_t stream);
+
 // Gated gate/up output: out[m][n] = silu(y[m][n]) * y[m][n + N/2] for
 // n < N/2, y as launch_mmv computes it (N even, dots not supported).
 int launch_mmv_gated(const int8_t* q, const float* sx, const int32_t* qsum,

@@ -49,6 +49,9 @@ constexpr int kSmemBudget = 110 * 1024;   // two CTAs per SM
 constexpr int kSoloSmem = 120 * 1024;     // one CTA per SM (dynamic request)
 constexpr int kMaxStages = 48;
 constexpr int kBoxBytes = 128;            // 4 groups of 32 code bytes
+// Shared-memory offset of the abort flag: after the largest barrier region
+// (full[kMaxStages], empty[kMaxStages], the scale barrier), before sw_off.
+constexpr int kAbortOff = 2 * 8 * kMaxStages + 8;
 
 struct MmvParams {
   const int8_t* q;        // [M][K], plane order inside each group
@@ -80,6 +83,11 @@ struct MmvParams {
   int up_row;             // I = N / 2: first up row of the weights
   int up_smem;            // rows between a gate box and its up box in smem
   int y_ld;               // output row stride (N, or I when gated)
+  // Test knobs of the bounded-wait path (pq2_debug_mmv_drop_arrival): consumer
+  // warp 0 skips its release of stage drop_stage (-1: none), and the
+  // producer's wait for a free ring slot gives up after empty_limit clocks.
+  int drop_stage;
+  long long empty_limit;
 };
 
 // Batched global -> shared copy of `count` 16-bit values by `threads`
@@ -343,6 +351,9 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + p.ring;
   uint64_t* swbar = empty + p.ring;
+  // Set by the producer when it stops early (a wait gave up), once every
+  // copy it issued has landed; the consumers' waits then give up too.
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortOff);
   __half* sw_s = reinterpret_cast<__half*>(smem + p.sw_off);    // [rows_max][G]
   float* sx_s = reinterpret_cast<float*>(smem + p.sx_off);      // [M][G]
   int32_t* qs_s = reinterpret_cast<int32_t*>(smem + p.qs_off);  // [M][G]
@@ -365,6 +376,7 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
       mbar_init(&empty[s], cons_warps);
     }
     mbar_init(swbar, 1);
+    *abort_flag = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -451,7 +463,28 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
         if (!independent) issue_inputs(i);
         continue;
       }
-      if (i >= p.ring) ok = ok && mbar_wait(&empty[i % p.ring], ((i / p.ring) - 1) & 1);
+      if (i >= p.ring) {
+        bool freed = true;
+        if (lane == 0)
+          freed = mbar_wait_until(&empty[i % p.ring], ((i / p.ring) - 1) & 1, p.empty_limit,
+                                  nullptr);
+        freed = __shfl_sync(0xffffffffu, freed, 0);
+        if (!freed) {
+          // Stop issuing: the slot may still be read.  Copies of the last
+          // `ring` issued stages may still be landing (earlier stages' slots
+          // were released, so theirs have); wait for them before the
+          // consumers are told to stop, so that no copy outlives the CTA.
+          ok = false;
+          if (lane == 0) {
+            for (int j = max(0, i - p.ring); j < i; ++j)
+              mbar_wait(&full[j % p.ring], (j / p.ring) & 1);
+            *abort_flag = 1;
+            __threadfence_block();
+          }
+          __syncwarp();
+          break;
+        }
+      }
       issue_weights(i);
       issue_inputs(i);
     }
@@ -583,7 +616,7 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
   const bool recycle = p.stages_total > p.ring;
   for (int i = 0; i < p.stages_total; ++i) {
     const int slot = i % p.ring;
-    ok = ok && mbar_wait(&full[slot], (i / p.ring) & 1);
+    ok = ok && mbar_wait_until(&full[slot], (i / p.ring) & 1, kWaitLimitCycles, abort_flag);
     const uint32_t st_s = ring_s + slot * p.stage_bytes;
     const int g0 = i * Gs;
     if (active && ok) {
@@ -604,7 +637,7 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
     }
     if (recycle) {
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);
+      if (lane == 0 && !(i == p.drop_stage && warp == 0)) mbar_arrive(&empty[slot]);
     }
   }
   if (!ok && lane == 0) report(p.status, PQ2_ERR_TIMEOUT);
@@ -803,7 +836,7 @@ int launch_mmv_impl(const int8_t* q, const float* sx, const int32_t* qsum,
                     const uint8_t* codes, const uint16_t* scales, void* y, int y_dtype,
                     int32_t* dots, int64_t M, int64_t N, int64_t K, int decode, int overlap,
                     bool gated, int sm_count, int32_t* status, cudaStream_t stream,
-                    int nsub = 1) {
+                    int nsub = 1, int drop_stage = -1, long long empty_limit = kWaitLimitCycles) {
   if (nsub != 1 && ((nsub != 2 && nsub != 4) || M > 4 || gated || decode != kDecodeMaskPlanes))
     return PQ2_ERR_SHAPE;
   MmvGeometry geo;
@@ -842,7 +875,7 @@ int launch_mmv_impl(const int8_t* q, const float* sx, const int32_t* qsum,
   const int slab = gated ? 2 * p.up_smem : R;
   p.box_stride = align_up(slab * kBoxBytes, 1024);
   // fixed region: barriers, weight scales, s_x, sum(q)
-  p.sw_off = align_up(2 * 8 * kMaxStages + 8, 128);
+  p.sw_off = align_up(kAbortOff + 4, 128);
   p.sx_off = align_up(p.sw_off + G * slab * 2, 16);
   p.qs_off = align_up(p.sx_off + mi * G * nsub * 4, 16);
   p.ring_off = align_up(p.qs_off + mi * G * nsub * 4, 1024);
@@ -877,6 +910,11 @@ int launch_mmv_impl(const int8_t* q, const float* sx, const int32_t* qsum,
   p.stages_total = (G + gs - 1) / gs;
   if (room < p.stage_bytes) return PQ2_ERR_SHAPE;
   p.ring = std::min(std::min(p.stages_total, room / p.stage_bytes), kMaxStages);
+  p.drop_stage = drop_stage;
+  p.empty_limit = empty_limit;
+  // A dropped release only matters where a slot is reused.
+  if (drop_stage >= 0 && (p.stages_total <= p.ring || drop_stage + p.ring >= p.stages_total))
+    return PQ2_ERR_SHAPE;
   int smem = 1024 + p.ring_off + p.ring * p.stage_bytes;  // + alignment slack
   // A call that waits for the kernel before it (weights-only overlap) takes
   // a whole SM: more than half the shared memory keeps a second CTA of any
@@ -920,6 +958,15 @@ int launch_mmv_grouped(const int8_t* q, const float* sx, const int32_t* qsum,
   return launch_mmv_impl(q, sx, qsum, codes, scales, y, y_dtype, dots, M, N, K,
                          kDecodeMaskPlanes, overlap, false, sm_count, status, stream,
                          128 / act_group);
+}
+
+int launch_mmv_drop_arrival(const int8_t* q, const float* sx, const int32_t* qsum,
+                            const uint8_t* codes, const uint16_t* scales, void* y, int y_dtype,
+                            int64_t M, int64_t N, int64_t K, long long wait_limit, int sm_count,
+                            int32_t* status, cudaStream_t stream) {
+  return launch_mmv_impl(q, sx, qsum, codes, scales, y, y_dtype, nullptr, M, N, K,
+                         kDecodeMaskPlanes, 0, false, sm_count, status, stream, 1, 0,
+                         wait_limit);
 }
 
 int launch_mmv_gated(const int8_t* q, const float* sx, const int32_t* qsum,

@@ -61,6 +61,8 @@ SIGNATURES = {
     "pq2_mm_f8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P]),
     "pq2_debug_group_dots": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P, _P, _P]),
     "pq2_mmv_geometry": (_I, [_I64, _I64, _I, _P, _P, _P, _P]),
+    "pq2_debug_mmv_drop_arrival": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I64, _P,
+                                        _P]),
 }
 
 _lock = threading.Lock()

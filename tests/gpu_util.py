@@ -65,6 +65,46 @@ def oracle_reference(x, codes_o, scales_o):
     return q, sx, O.qsum(q), dots, y32, y64, bound
 
 
+def oracle_rows(x, rows, codes_o, scales_o, chunk=16, threads=None):
+    """(y64, bound) of the oracle for the activation rows `rows` of x against
+    every output row of the prepared planes, formed in chunks of `chunk`
+    activation rows (the int32 dots of one chunk stay small) on a pool of
+    host threads.  Quantisation is per row, so each chunk is the oracle's
+    result for those rows exactly; the oracle's C calls release the
+    interpreter lock."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    xs = x[torch.as_tensor(np.asarray(rows))]
+    n = xs.shape[0]
+    pieces = [(i, min(i + chunk, n)) for i in range(0, n, chunk)]
+
+    def one(ab):
+        a, b = ab
+        *_, y64, bound = oracle_reference(xs[a:b], codes_o, scales_o)
+        return y64, bound
+
+    threads = threads or max(1, min(len(pieces), os.cpu_count() or 1))
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        parts = list(ex.map(one, pieces))
+    return np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts])
+
+
+def tile_rows(M, tile=128, total=64, seed=0):
+    """Rows to compare at a large M: every row up to M = 512; above that,
+    `total` seeded rows spread so that every tile of `tile` rows holds at
+    least one (the first and last row always included)."""
+    if M <= 512:
+        return np.arange(M)
+    rng = np.random.default_rng(seed)
+    tiles = (M + tile - 1) // tile
+    per = max(1, -(-total // tiles))
+    rows = {0, M - 1}
+    for t in range(tiles):
+        lo, hi = t * tile, min(M, (t + 1) * tile)
+        rows.update(rng.choice(np.arange(lo, hi), min(per, hi - lo), replace=False).tolist())
+    return np.array(sorted(rows))
+
+
 def mm_operand_order(q: np.ndarray) -> np.ndarray:
     """The PQ2_Q_F16 layout (include/pq2.h): inside every 16 consecutive
     elements, element 4b + s goes to position 4s + 2(b & 1) + (b >> 1)."""

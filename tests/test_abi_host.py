@@ -228,3 +228,39 @@ def test_ptq_validation(L):
     d = L.pq2_debug_ptq_dots
     assert d(A, A, A, A, 5, 10, 512, 32, A, None) == pq2.PQ2_ERR_SHAPE
     assert d(A, A, A, A, 4, 10, 512, 32, None, None) == pq2.PQ2_ERR_NULL
+
+
+def test_drop_arrival_validation(L):
+    """The bounded-wait test entry: a device status is required and the wait
+    limit must lie in 1000 .. 2^32 clocks; all rejected before any CUDA call."""
+    f = L.pq2_debug_mmv_drop_arrival
+    ok = [A, A, A, A, A, A, pq2.PQ2_F32, 1, 10, 128, 20000, A, None]
+    bad = list(ok)
+    bad[11] = None
+    assert f(*bad) == pq2.PQ2_ERR_NULL
+    for lim in (0, 999, (1 << 32) + 1):
+        bad = list(ok)
+        bad[10] = lim
+        assert f(*bad) == pq2.PQ2_ERR_SHAPE, lim
+    bad = list(ok)
+    bad[11] = A + 2
+    assert f(*bad) == pq2.PQ2_ERR_ALIGN
+    bad = list(ok)
+    bad[7] = 9
+    assert f(*bad) == pq2.PQ2_ERR_SHAPE
+    bad = list(ok)
+    bad[0] = None
+    assert f(*bad) == pq2.PQ2_ERR_NULL
+
+
+def test_linear_static_error_order(L):
+    """pq2_linear_static reports errors in pq2_linear's order: a bad dtype
+    before an oversized shape, before any CUDA call."""
+    f = L.pq2_linear_static
+    big = 123392  # M = 8 needs more than the static scratch at this K
+    assert f(A, 7, big, 8, 4, big, A, A, A, pq2.PQ2_F32, None, None) == pq2.PQ2_ERR_DTYPE
+    assert f(A, pq2.PQ2_BF16, big, 8, 4, big, A, A, A, 9, None, None) == pq2.PQ2_ERR_DTYPE
+    assert f(A, pq2.PQ2_BF16, big, 8, 4, big, A, A, A, pq2.PQ2_F32, None, None) == \
+        pq2.PQ2_ERR_SHAPE
+    assert f(None, pq2.PQ2_BF16, 128, 1, 4, 128, A, A, A, pq2.PQ2_F32, None, None) == \
+        pq2.PQ2_ERR_NULL

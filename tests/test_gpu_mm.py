@@ -94,20 +94,32 @@ def test_mm_y_within_bound(M, N, K):
 
 
 @pytest.mark.parametrize("M", [16, 128, 512, 2048, 4096])
-def test_mm_prefill_ffn_up_sampled(M):
+def test_mm_prefill_ffn_up_against_oracle(M):
     """Prefill ffn_up K=5120, N=17408 at the benchmark's M values, in the
-    benchmark's launch configuration; the oracle checks a seeded sample of
-    token rows against every output column."""
+    benchmark's launch configuration: every token row up to M = 512, and
+    above that at least 64 seeded rows covering every 128-token tile, against
+    every output column, for pq2_mm (fp16 operands) and pq2_mm_f8 (e4m3
+    planes); fp32 and bf16 outputs."""
     N, K = 17408, 5120
     codes, scales, codes_o, scales_o = _prep(N, K, seed=2024)
     x = synth.activations(M, K, seed=M)
-    q, sx, qs = pq2.pq2_quantize_act(x.cuda(), pq2.PQ2_Q_F16)
-    y = pq2.pq2_mm(q, sx, qs, codes, scales)
+    xd = x.cuda()
+    q, sx, qs = pq2.pq2_quantize_act(xd, pq2.PQ2_Q_F16)
+    q8, _, _ = pq2.pq2_quantize_act(xd, pq2.PQ2_Q_F8)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = pq2.pq2_mm(q, sx, qs, codes, scales, status=status)
+    y8 = pq2.pq2_mm_f8(q8, sx, qs, codes, scales, status=status)
+    yb = pq2.pq2_mm_f8(q8, sx, qs, codes, scales, out_dtype=torch.bfloat16, status=status)
     torch.cuda.synchronize()
-    rows = np.arange(M) if M <= 16 else np.sort(
-        np.random.default_rng(M).choice(M, 8, replace=False))
-    *_, y64, bound = U.oracle_reference(x[rows], codes_o, scales_o)
-    ok, worst = O.within_bound(y.cpu().numpy()[rows], y64, bound)
+    assert int(status.item()) == 0
+    rows = U.tile_rows(M, seed=M)
+    assert len(rows) == M or (len(rows) >= 64 and
+                              len(set((rows // 128).tolist())) == (M + 127) // 128)
+    y64, bound = U.oracle_rows(x, rows, codes_o, scales_o)
+    for got in (y, y8):
+        ok, worst = O.within_bound(got.cpu().numpy()[rows], y64, bound)
+        assert ok, worst
+    ok, worst = O.bf16_within_bound(yb.cpu().float().numpy()[rows], y64, bound)
     assert ok, worst
 
 
