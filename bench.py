@@ -699,6 +699,7 @@ def sweep_leg(args, dev, stream, timed, capture):
         for M in sorted(Ms, reverse=True):
             x = x8[:M]
             q, sx, qs = pq2.pq2_quantize_act(x, pq2.PQ2_Q_PLANES)
+            qt, sxt, corr = pq2.pq2_quantize_act(x, pq2.PQ2_Q_MMV16)
             y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             ws = torch.empty(pq2.linear_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
             # batch invariance on the first matrix, fp32 output
@@ -721,6 +722,16 @@ def sweep_leg(args, dev, stream, timed, capture):
                             raise RuntimeError(f"pq2_mmv_ex failed ({st})")
                 return run
 
+            def tc_calls(flag):
+                def run():
+                    for c, sc in mats:
+                        st = lib.pq2_mmv_tc(qt.data_ptr(), sxt.data_ptr(), corr.data_ptr(),
+                                            c.data_ptr(), sc.data_ptr(), y.data_ptr(),
+                                            pq2.PQ2_BF16, M, N, K, flag, status.data_ptr(), sp)
+                        if st:
+                            raise RuntimeError(f"pq2_mmv_tc failed ({st})")
+                return run
+
             def complete_calls():
                 for c, sc in mats:
                     st = lib.pq2_linear(x.data_ptr(), pq2.PQ2_BF16, K, M, N, K, c.data_ptr(),
@@ -733,14 +744,24 @@ def sweep_leg(args, dev, stream, timed, capture):
             k_ms = timed([capture(calls(pq2.PQ2_MMV_INDEPENDENT))], reps, 3) / (reps * n_mats)
             d_ms = timed([capture(calls(pq2.PQ2_MMV_OVERLAP_WEIGHTS))], reps, 3) / (reps * n_mats)
             c_ms = timed([capture(complete_calls)], reps, 3) / (reps * n_mats)
-            gbs = wbytes / (k_ms * 1e-3) / 1e9
-            dgbs = wbytes / (d_ms * 1e-3) / 1e9
-            shape["by_m"][str(M)] = {"mmv_us": round(k_ms * 1e3, 3), "mmv_gbs": round(gbs, 1),
-                                     "mmv_frac": round(gbs / hbm, 3),
-                                     "dep_us": round(d_ms * 1e3, 3),
-                                     "dep_frac": round(dgbs / hbm, 3),
+            t_ms = timed([capture(tc_calls(pq2.PQ2_MMV_INDEPENDENT))], reps, 3) / (reps * n_mats)
+            td_ms = timed([capture(tc_calls(pq2.PQ2_MMV_OVERLAP_WEIGHTS))], reps, 3) / (
+                reps * n_mats)
+            # the tensor-core GEMV's y must equal the dp4a GEMV's (same bits)
+            yt = pq2.pq2_mmv_tc(qt, sxt, corr, c0, s0, out_dtype=torch.float32)
+            torch.cuda.synchronize()
+            if not torch.equal(yt.view(torch.int32), y32.view(torch.int32)):
+                raise RuntimeError(f"pq2_mmv_tc differs from pq2_mmv ({name}, M={M})")
+            frac = lambda ms: round(wbytes / (ms * 1e-3) / 1e9 / hbm, 3)  # noqa: E731
+            shape["by_m"][str(M)] = {"mmv_us": round(k_ms * 1e3, 3),
+                                     "mmv_gbs": round(wbytes / (k_ms * 1e-3) / 1e9, 1),
+                                     "mmv_frac": frac(k_ms),
+                                     "dep_us": round(d_ms * 1e3, 3), "dep_frac": frac(d_ms),
+                                     "tc_us": round(t_ms * 1e3, 3), "tc_frac": frac(t_ms),
+                                     "tc_dep_us": round(td_ms * 1e3, 3),
+                                     "tc_dep_frac": frac(td_ms),
                                      "complete_us": round(c_ms * 1e3, 3)}
-            del q, sx, qs, y, ws, y32
+            del q, sx, qs, y, ws, y32, qt, sxt, corr, yt
         shape["by_m"] = dict(sorted(shape["by_m"].items(), key=lambda kv: int(kv[0])))
         if len(Ms) > 1:
             shape["batch_invariant"] = invariant
@@ -976,6 +997,7 @@ def run_ours(args):
         for name, sh in sweep["shapes"].items():
             roofline[f"{name}_indep_us_frac"] = compact(sh["by_m"], "mmv_us", "mmv_frac")
             roofline[f"{name}_dep_us_frac"] = compact(sh["by_m"], "dep_us", "dep_frac")
+            roofline[f"{name}_tc_indep_us_frac"] = compact(sh["by_m"], "tc_us", "tc_frac")
             roofline[f"{name}_complete_us"] = compact(sh["by_m"], "complete_us")
             if "batch_invariant" in sh:
                 roofline[f"{name}_batch_invariant"] = sh["batch_invariant"]
@@ -1027,7 +1049,8 @@ def run_ours(args):
 
 def run_profile_case(args):
     """A short fixed sequence for an ncu capture: the attn_qkv GEMV
-    (pq2_mmv, INDEPENDENT calls over 8 rotated matrices) or the ffn_up prefill
+    (pq2_mmv, or pq2_mmv_tc for "mmvtc", INDEPENDENT calls over 8 rotated
+    matrices) or the ffn_up prefill
     GEMM (pq2_mm, or pq2_mm_f8 for "mm8"), at --profile-m columns; 3 warm-up
     calls then 3 calls."""
     import torch
@@ -1048,9 +1071,9 @@ def run_profile_case(args):
         print(json.dumps({"profile_case": "ptq", "M": M, "N": N, "K": K, "act_group": A,
                           "launches": 6, "ok": True}))
         return 0
-    if args.profile_case == "mmv":
+    if args.profile_case in ("mmv", "mmvtc"):
         K, N, nm = K_DIM, N_DIM, 8
-        layout = pq2.PQ2_Q_PLANES
+        layout = pq2.PQ2_Q_PLANES if args.profile_case == "mmv" else pq2.PQ2_Q_MMV16
     else:
         K, N, nm = PREFILL_K, PREFILL_N, 2
         layout = pq2.PQ2_Q_F8 if args.profile_case == "mm8" else pq2.PQ2_Q_F16
@@ -1063,6 +1086,8 @@ def run_profile_case(args):
         c, sc = mats[i % nm]
         if args.profile_case == "mmv":
             pq2.pq2_mmv(q, sx, qs, c, sc, y=y, flags=pq2.PQ2_MMV_INDEPENDENT)
+        elif args.profile_case == "mmvtc":
+            pq2.pq2_mmv_tc(q, sx, qs, c, sc, y=y, flags=pq2.PQ2_MMV_INDEPENDENT)
         elif args.profile_case == "mm8":
             pq2.pq2_mm_f8(q, sx, qs, c, sc, y=y)
         else:
@@ -1091,7 +1116,7 @@ def main():
                     help="skip the activation-group 64/32 (pq2_mmv_grouped) leg")
     ap.add_argument("--no-ptq", action="store_true",
                     help="skip the PTQ1_0 weight-format (pq2_ptq_mmv) leg")
-    ap.add_argument("--profile-case", choices=["mmv", "mm", "mm8", "ptq"], default=None,
+    ap.add_argument("--profile-case", choices=["mmv", "mmvtc", "mm", "mm8", "ptq"], default=None,
                     help="run a short fixed call sequence for an ncu capture and exit")
     ap.add_argument("--profile-m", type=int, default=1, help="columns for --profile-case")
     ap.add_argument("--profile-act-group", type=int, default=32,

@@ -83,8 +83,17 @@ enum { PQ2_BF16 = 0, PQ2_F16 = 1, PQ2_F32 = 2 };
  *               the K order of pq2_mm_f8's weight decode: inside every 16
  *               consecutive elements, element 8h + 2e + o (h, o in {0, 1},
  *               e = 0..3) is stored at position 4(2h + o) + e.  Operand of
- *               pq2_mm_f8 (the 8-bit tensor path, two MMAs per K step). */
-enum { PQ2_Q_ROWS = 0, PQ2_Q_PLANES = 1, PQ2_Q_F16 = 2, PQ2_Q_F8 = 3 };
+ *               pq2_mm_f8 (the 8-bit tensor path, two MMAs per K step).
+ *  PQ2_Q_MMV16  fp16 [M][K], the B operand of the small-batch tensor-core
+ *               GEMV pq2_mmv_tc, 128-groups only: inside every group,
+ *               position 32t + 4j + 2r + e (t, j, r, e = 0..3, 0..7, 0..1,
+ *               0..1) holds element i = 16(t + 4(j/4)) + 8e + f with
+ *               f = 2(j%4) + r, divided by 4^f for f <= 4 and by 4^(f-3) for
+ *               f >= 5 (exact: powers of two).  With this layout qsum does
+ *               not receive sum(q) but the group's offset correction
+ *               sum_i q_i (1 + 1024 / scale_i), scale_i that element's
+ *               divisor (an exact integer, |.| < 2^22). */
+enum { PQ2_Q_ROWS = 0, PQ2_Q_PLANES = 1, PQ2_Q_F16 = 2, PQ2_Q_F8 = 3, PQ2_Q_MMV16 = 4 };
 
 /* Version of the prepared plane layout; bump whenever what a kernel reads
  * changes, so callers can key caches on it (BIB: a layout switch must change
@@ -116,7 +125,8 @@ int pq2_prepare(const uint8_t *raw, int64_t raw_row_stride, int64_t N,
  *   x        (device) x_dtype [M][ldx], ldx >= K elements.
  *   M        1 .. 1<<20.
  *   q        (device) written in q_layout: int8 [M][K] for ROWS/PLANES,
- *            fp16 [M][K] for F16; 16-byte aligned.
+ *            fp16 [M][K] for F16 and MMV16, bytes [M][2K] for F8; 16-byte
+ *            aligned.
  *   sx       (device) fp32 [M][K/128] activation scales; 4-byte aligned.
  *   qsum     (device, may be NULL) int32 [M][K/128], sum of q per group
  *            (KE Test 21, the correction for the codes' -1 offset). */
@@ -189,15 +199,51 @@ int pq2_mmv_ex(const int8_t *q_planes, const float *sx, const int32_t *qsum,
                int y_dtype, int64_t M, int64_t N, int64_t K, int decode,
                int flags, int32_t *dev_status, void *stream);
 
+/* pq2_mmv_tc — the small-batch GEMV (M = 1..8) on the legacy tensor-core
+ * path (mma.sync m16n8k16, fp16 operands, fp32 accumulation): the same
+ * output as pq2_mmv, bit for bit, at an arithmetic cost that does not grow
+ * with M.  Each code word is expanded in registers, one logic operation per
+ * two weights, into the exact fp16 values 1024 + c * 4^f; the activations
+ * come divided by the same powers of four (PQ2_Q_MMV16), so every product is
+ * an integer and the fp32 sum of a group is exact; subtracting the group's
+ * correction leaves the exact dot of BIB step 3.  The split of the groups,
+ * the scaling (float(dot) * s_x) * s_w and the order of the fp32 additions
+ * are pq2_mmv's (a function of N, K and the SM count only), hence the same
+ * bits and the same batch invariance.
+ *   q_mmv16  (device) fp16 [M][K] from pq2_quantize_act(PQ2_Q_MMV16);
+ *            16-byte aligned.
+ *   sx       (device) fp32 [M][K/128] from the same call.
+ *   qcorr    (device) int32 [M][K/128], the corrections that call writes to
+ *            its qsum argument.
+ *   codes, scales, y, y_dtype, M, N, K, flags, dev_status as for pq2_mmv_ex
+ *            (flags: the same stream contract).
+ * Returns PQ2_ERR_SHAPE for shapes whose per-CTA tiling it does not cover
+ * (none of the library's geometries), else as pq2_mmv_ex. */
+int pq2_mmv_tc(const uint16_t *q_mmv16, const float *sx, const int32_t *qcorr,
+               const uint8_t *codes, const uint16_t *scales, void *y, int y_dtype,
+               int64_t M, int64_t N, int64_t K, int flags, int32_t *dev_status,
+               void *stream);
+
+/* 1 if pq2_linear runs the tensor-core GEMV (pq2_mmv_tc on PQ2_Q_MMV16) for
+ * M columns of an N x K matrix on a device with sm_count SMs, 0 if it runs
+ * pq2_mmv (host only, no CUDA call); the results are the same.  The choice
+ * follows the two kernels' measured cost: the tensor-core GEMV from M = 6,
+ * and at M = 5 where a CTA of pq2_mmv_geometry holds at most 72 rows in at
+ * most 8 splits. */
+int pq2_linear_tensor_gemv(int64_t M, int64_t N, int64_t K, int sm_count);
+
 /* pq2_linear — the complete projection y = x W^T (quantise, then the GEMV),
  * as the pages time it ("complete call", KE Tests 3, 6): pq2_quantize_act
- * into the caller's workspace, then pq2_mmv (M = 1..8) with
- * PQ2_MMV_OVERLAP_WEIGHTS, so that it streams the weights while the
- * quantisation and the kernel before it finish, or pq2_mm_f8 on PQ2_Q_F8
+ * into the caller's workspace, then pq2_mmv (M = 1..8; pq2_mmv_tc on
+ * PQ2_Q_MMV16 for the M where pq2_linear_tensor_gemv says so, with the same
+ * bits) with PQ2_MMV_OVERLAP_WEIGHTS, so that it streams the weights while
+ * the quantisation and the kernel before it finish, or pq2_mm_f8 on PQ2_Q_F8
  * (M >= 16; bit-identical to pq2_mm, faster).  Hence
  * codes and scales must not be written by a kernel that may still run when
  * the call starts (see the flags of pq2_mmv_ex).
  * Results are bit-identical to pq2_quantize_act + pq2_mmv / pq2_mm_f8.
+ * The workspace holds q with one byte per element for M <= 4 and two
+ * otherwise (the tensor-core GEMV and the prefill GEMM take 16-bit q).
  *   x         (device) x_dtype [M][ldx], ldx >= K; M 1..8 or 16 .. 1<<20.
  *   workspace (device) pq2_linear_workspace_bytes(M, K) bytes, 256-byte
  *             aligned, holding q, s_x and sum(q); contents are scratch.
@@ -361,7 +407,8 @@ int pq2_linear_gated(const void *x, int x_dtype, int64_t ldx, int64_t M,
  *            current device's.  Another device's stream returns PQ2_ERR_CUDA.
  *   Returns PQ2_ERR_SHAPE, before any CUDA call, when
  *   pq2_linear_workspace_bytes(M, K) exceeds PQ2_STATIC_SCRATCH_BYTES (for
- *   example M = 8 with K above 123,264, or M = 16 with K above 31,744);
+ *   example M = 4 with K above 246,656, M = 8 with K above 63,488, or
+ *   M = 16 with K above 31,744);
  *   PQ2_ERR_CUDA if the scratch address cannot be obtained.
  * Every call on a device shares the one scratch array, which keeps the last
  * call's contents.  Nothing in it needs to start at zero: each call writes
@@ -445,14 +492,15 @@ int pq2_mm_f8(const uint8_t *q_f8, const float *sx, const int32_t *qsum,
 
 /* Paths of pq2_debug_group_dots. */
 enum { PQ2_PATH_MMV_ADDXOR = 0, PQ2_PATH_MM = 1, PQ2_PATH_MMV_PLANES = 2,
-       PQ2_PATH_MM_F8 = 3 };
+       PQ2_PATH_MM_F8 = 3, PQ2_PATH_MMV_TC = 4 };
 
 /* pq2_debug_group_dots — the exact per-group int32 dots
  * dots[m][n][g] = sum_{k in g} (c_{n,k} - 1) q_{m,k} computed by the SAME
  * device decode and dot code as pq2_mmv with either decoder (paths 0 and 2,
  * q int8 in PQ2_Q_PLANES order, qsum required for path 2, M 1..8) or as
  * pq2_mm (path 1, q fp16 PQ2_Q_F16 and qsum, M >= 16) or pq2_mm_f8 (path 3,
- * q PQ2_Q_F8 and qsum, M >= 16), for parity checks.
+ * q PQ2_Q_F8 and qsum, M >= 16) or pq2_mmv_tc (path 4, q PQ2_Q_MMV16 and
+ * its corrections in qsum, M 1..8), for parity checks.
  *   dots (device) int32 [M][N][K/128]. */
 int pq2_debug_group_dots(const void *q, const int32_t *qsum,
                          const uint8_t *codes, int64_t M, int64_t N, int64_t K,

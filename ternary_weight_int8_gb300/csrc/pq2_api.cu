@@ -56,6 +56,11 @@ int device_check(int* sm_count) {
 
 int elem_bytes(int dtype) { return dtype == PQ2_F32 ? 4 : 2; }
 
+bool valid_layout(int q_layout) {
+  return q_layout == PQ2_Q_ROWS || q_layout == PQ2_Q_PLANES || q_layout == PQ2_Q_F16 ||
+         q_layout == PQ2_Q_F8 || q_layout == PQ2_Q_MMV16;
+}
+
 int check_mmv_args(const int8_t* q, const float* sx, const int32_t* qsum,
                    const uint8_t* codes, const uint16_t* scales, const void* y,
                    int y_dtype, int64_t M, int64_t N, int64_t K, int decode) {
@@ -110,9 +115,7 @@ int pq2_quantize_act(const void* x, int x_dtype, int64_t ldx, int64_t M, int64_t
                      void* q, int q_layout, float* sx, int32_t* qsum, void* stream) {
   if (!x || !q || !sx) return PQ2_ERR_NULL;
   if (x_dtype != PQ2_BF16 && x_dtype != PQ2_F16 && x_dtype != PQ2_F32) return PQ2_ERR_DTYPE;
-  if (q_layout != PQ2_Q_ROWS && q_layout != PQ2_Q_PLANES && q_layout != PQ2_Q_F16 &&
-      q_layout != PQ2_Q_F8)
-    return PQ2_ERR_DTYPE;
+  if (!valid_layout(q_layout)) return PQ2_ERR_DTYPE;
   if (M < 1 || M > kMaxM || !valid_k(K) || ldx < K || ldx > ((int64_t)1 << 40))
     return PQ2_ERR_SHAPE;
   if (!aligned(x, elem_bytes(x_dtype)) || !aligned(q, 16) || !aligned(sx, 4) ||
@@ -145,6 +148,35 @@ int pq2_mmv_ex(const int8_t* q, const float* sx, const int32_t* qsum, const uint
                          overlap, sms, dev_status, static_cast<cudaStream_t>(stream));
 }
 
+int pq2_mmv_tc(const uint16_t* q_mmv16, const float* sx, const int32_t* qcorr,
+               const uint8_t* codes, const uint16_t* scales, void* y, int y_dtype, int64_t M,
+               int64_t N, int64_t K, int flags, int32_t* dev_status, void* stream) {
+  if (int st = check_mmv_args(reinterpret_cast<const int8_t*>(q_mmv16), sx, qcorr, codes, scales,
+                              y, y_dtype, M, N, K, PQ2_DECODE_PLANES))
+    return st;
+  if (flags & ~(PQ2_MMV_OVERLAP_WEIGHTS | PQ2_MMV_INDEPENDENT)) return PQ2_ERR_DTYPE;
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  const int overlap = (flags & PQ2_MMV_INDEPENDENT) ? 2 : (flags & PQ2_MMV_OVERLAP_WEIGHTS) ? 1 : 0;
+  return pq2::launch_mmv(reinterpret_cast<const int8_t*>(q_mmv16), sx, qcorr, codes, scales, y,
+                         y_dtype, nullptr, M, N, K, pq2::kDecodeTensor, overlap, sms, dev_status,
+                         static_cast<cudaStream_t>(stream));
+}
+
+// pq2_linear's choice between the two GEMVs (same bits), from their measured
+// cost in a chain of dependent calls on GB300: the dp4a kernel's cost grows
+// with M, the tensor-core kernel's does not.  The tensor-core kernel wins
+// from M = 6 on every layer shape, and at M = 5 where a CTA holds at most 72
+// rows of at most 8 splits (attn_qkv, 5120 x 6144; not ffn_up's 115-row or
+// ffn_down's 16-split slabs).
+int pq2_linear_tensor_gemv(int64_t M, int64_t N, int64_t K, int sm_count) {
+  if (M < 5 || M > 8) return 0;
+  if (M >= 6) return 1;
+  pq2::MmvGeometry g;
+  if (!pq2::mmv_geometry(N, K, sm_count, &g)) return 0;
+  return g.splits <= 8 && g.rows_max <= 72 ? 1 : 0;
+}
+
 int pq2_mmv(const int8_t* q, const float* sx, const int32_t* qsum, const uint8_t* codes,
             const uint16_t* scales, void* y, int y_dtype, int64_t M, int64_t N, int64_t K,
             int32_t* dev_status, void* stream) {
@@ -156,11 +188,10 @@ int pq2_quantize_act_grouped(const void* x, int x_dtype, int64_t ldx, int64_t M,
                              int act_group, void* q, int q_layout, float* sx, int32_t* qsum,
                              void* stream) {
   if (act_group != 128 && act_group != 64 && act_group != 32) return PQ2_ERR_SHAPE;
+  if (q_layout == PQ2_Q_MMV16 && act_group != 128) return PQ2_ERR_SHAPE;
   if (!x || !q || !sx) return PQ2_ERR_NULL;
   if (x_dtype != PQ2_BF16 && x_dtype != PQ2_F16 && x_dtype != PQ2_F32) return PQ2_ERR_DTYPE;
-  if (q_layout != PQ2_Q_ROWS && q_layout != PQ2_Q_PLANES && q_layout != PQ2_Q_F16 &&
-      q_layout != PQ2_Q_F8)
-    return PQ2_ERR_DTYPE;
+  if (!valid_layout(q_layout)) return PQ2_ERR_DTYPE;
   if (M < 1 || M > kMaxM || !valid_k(K) || ldx < K || ldx > ((int64_t)1 << 40))
     return PQ2_ERR_SHAPE;
   if (!aligned(x, elem_bytes(x_dtype)) || !aligned(q, 16) || !aligned(sx, 4) ||
@@ -312,10 +343,15 @@ int pq2_mmv_gated(const int8_t* q, const float* sx, const int32_t* qsum, const u
                                static_cast<cudaStream_t>(stream));
 }
 
+// q bytes per element in pq2_linear's workspace: int8 planes for the dp4a
+// GEMV (M <= 4), fp16 where the tensor-core GEMV (PQ2_Q_MMV16, M = 5..8)
+// or the prefill GEMM (M >= 16) may run.
+static size_t linear_q_elem(int64_t M) { return M <= 4 ? 1 : 2; }
+
 size_t pq2_linear_workspace_bytes(int64_t M, int64_t K) {
   if (M < 1 || M > kMaxM || !valid_k(K)) return 0;
   const size_t G = (size_t)(K / 128);
-  const size_t q_bytes = (size_t)M * (size_t)K * (M <= 8 ? 1 : 2);
+  const size_t q_bytes = (size_t)M * (size_t)K * linear_q_elem(M);
   const size_t sx_off = (q_bytes + 255) / 256 * 256;
   const size_t qs_off = (sx_off + (size_t)M * G * 4 + 255) / 256 * 256;
   return qs_off + (size_t)M * G * 4;
@@ -338,22 +374,24 @@ int pq2_linear(const void* x, int x_dtype, int64_t ldx, int64_t M, int64_t N, in
   if (int st = device_check(&sms)) return st;
   const size_t G = (size_t)(K / 128);
   const bool small = M <= 8;
+  const bool tensor = small && pq2_linear_tensor_gemv(M, N, K, sms);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const size_t q_bytes = (size_t)M * (size_t)K * (small ? 1 : 2);
+  const size_t q_bytes = (size_t)M * (size_t)K * linear_q_elem(M);
   const size_t sx_off = (q_bytes + 255) / 256 * 256;
   const size_t qs_off = (sx_off + (size_t)M * G * 4 + 255) / 256 * 256;
   float* sx = reinterpret_cast<float*>(ws + sx_off);
   int32_t* qs = reinterpret_cast<int32_t*>(ws + qs_off);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (int st = pq2::launch_quantize(x, x_dtype, ldx, M, K, ws,
-                                    small ? PQ2_Q_PLANES : PQ2_Q_F8, sx, qs, s))
-    return st;
+  const int layout = !small ? PQ2_Q_F8 : tensor ? PQ2_Q_MMV16 : PQ2_Q_PLANES;
+  if (int st = pq2::launch_quantize(x, x_dtype, ldx, M, K, ws, layout, sx, qs, s)) return st;
   // Prefill on the 8-bit tensor path: bit-identical to the fp16 one, faster.
   if (!small)
     return pq2::launch_mm(ws, true, sx, qs, codes, scales, y, y_dtype, nullptr, M, N, K, sms,
                           dev_status, s);
   return pq2::launch_mmv(reinterpret_cast<const int8_t*>(ws), sx, qs, codes, scales, y,
-                         y_dtype, nullptr, M, N, K, pq2_mmv_decoder(M), 1, sms, dev_status, s);
+                         y_dtype, nullptr, M, N, K,
+                         tensor ? pq2::kDecodeTensor : pq2_mmv_decoder(M), 1, sms, dev_status,
+                         s);
 }
 
 int pq2_linear_gated(const void* x, int x_dtype, int64_t ldx, int64_t M, int64_t N, int64_t K,
@@ -392,9 +430,7 @@ int pq2_norm_hadamard_quantize(const uint16_t* x, const uint16_t* residual,
                                float eps, int64_t M, int64_t K, uint16_t* norm_out, void* q,
                                int q_layout, float* sx, int32_t* qsum, void* stream) {
   if (!x || !w || !sign || !q || !sx) return PQ2_ERR_NULL;
-  if (q_layout != PQ2_Q_ROWS && q_layout != PQ2_Q_PLANES && q_layout != PQ2_Q_F16 &&
-      q_layout != PQ2_Q_F8)
-    return PQ2_ERR_DTYPE;
+  if (!valid_layout(q_layout)) return PQ2_ERR_DTYPE;
   if (M < 1 || M > kMaxM || K < 1024 || K > PQ2_PREP_MAX_K || K % 1024) return PQ2_ERR_SHAPE;
   if (!(eps >= 0.0f) || eps > 1.0f) return PQ2_ERR_SHAPE;
   if (!aligned(x, 2) || (residual && !aligned(residual, 2)) || (residual_out && !aligned(residual_out, 2)) ||
@@ -443,10 +479,10 @@ int pq2_debug_group_dots(const void* q, const int32_t* qsum, const uint8_t* code
                          int32_t* dev_status, void* stream) {
   if (!q || !codes || !dots) return PQ2_ERR_NULL;
   if (path != PQ2_PATH_MMV_ADDXOR && path != PQ2_PATH_MM && path != PQ2_PATH_MMV_PLANES &&
-      path != PQ2_PATH_MM_F8)
+      path != PQ2_PATH_MM_F8 && path != PQ2_PATH_MMV_TC)
     return PQ2_ERR_DTYPE;
   const bool mm = path == PQ2_PATH_MM || path == PQ2_PATH_MM_F8;
-  if ((path == PQ2_PATH_MMV_PLANES || mm) && !qsum) return PQ2_ERR_NULL;
+  if (path != PQ2_PATH_MMV_ADDXOR && !qsum) return PQ2_ERR_NULL;
   if (!valid_n(N) || !valid_k(K)) return PQ2_ERR_SHAPE;
   if (mm ? (M < 16 || M > kMaxM) : (M < 1 || M > 8)) return PQ2_ERR_SHAPE;
   if (!aligned(q, 16) || !aligned(codes, 16) || !aligned(dots, 4) ||
@@ -462,6 +498,7 @@ int pq2_debug_group_dots(const void* q, const int32_t* qsum, const uint8_t* code
   return pq2::launch_mmv(static_cast<const int8_t*>(q), nullptr, qsum, codes, nullptr, nullptr,
                          PQ2_F32, dots, M, N, K,
                          path == PQ2_PATH_MMV_PLANES ? pq2::kDecodeMaskPlanes
+                         : path == PQ2_PATH_MMV_TC   ? pq2::kDecodeTensor
                                                      : pq2::kDecodeAddXor,
                          0, sms, dev_status, s);
 }

@@ -22,8 +22,10 @@ bool mmv_geometry(int64_t N, int64_t K, int sm_count, MmvGeometry* g);
 
 // Decoders of the code bytes used by the small-batch kernel.
 enum MmvDecode {
-  kDecodeAddXor = 0,     // spread + 0x7F7F7F7F, ^ 0x80808080, signed dp4a
-  kDecodeMaskPlanes = 1  // masked planes, unsigned dp4a, minus sum(q)
+  kDecodeAddXor = 0,      // spread + 0x7F7F7F7F, ^ 0x80808080, signed dp4a
+  kDecodeMaskPlanes = 1,  // masked planes, unsigned dp4a, minus sum(q)
+  kDecodeTensor = 2       // fp16 fragments 1024 + c * 4^s, mma.sync, minus the
+                          // PQ2_Q_MMV16 correction (q in that layout)
 };
 
 int launch_prepare(const uint8_t* raw, int64_t raw_stride, int64_t N,

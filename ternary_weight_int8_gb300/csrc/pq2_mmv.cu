@@ -48,6 +48,14 @@ constexpr int kMaxBoxRows = 256;          // TMA box height limit
 constexpr int kSmemBudget = 110 * 1024;   // two CTAs per SM
 constexpr int kSoloSmem = 120 * 1024;     // one CTA per SM (dynamic request)
 constexpr int kMaxStages = 48;
+// Tensor-core consumer: 8 warps, each owning one split (two when S = 16) and
+// its 16-row tiles (a share of them when S < 8): at most kTcTiles tiles of
+// one split, or kTcTiles2 tiles of each of two.
+constexpr int kTcWarps = 8;
+constexpr int kTcTiles = 5;
+constexpr int kTcTiles2 = 3;
+constexpr int kTcUnits = 6;  // accumulators: max(kTcTiles, 2 * kTcTiles2)
+constexpr int kTcBlock = (kTcWarps + 1) * 32;
 constexpr int kBoxBytes = 128;            // 4 groups of 32 code bytes
 // Shared-memory offset of the abort flag: after the largest barrier region
 // (full[kMaxStages], empty[kMaxStages], the scale barrier), before sw_off.
@@ -71,6 +79,7 @@ struct MmvParams {
   int q_off;              // q region inside a stage
   int qbox_stride;        // bytes per column's q box inside a stage (1024-aligned)
   int sw_off, sx_off, qs_off, ring_off;
+  int part_off;           // tensor-core path: split partials [S][R][M] fp32
   int y_bf16;
   int overlap;            // 1: stream weights before the grid dependency
                           // resolves; 2: stream every input before it
@@ -171,6 +180,63 @@ __device__ __forceinline__ uint32_t lds16(uint32_t addr) {
   uint16_t v;
   asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
   return v;
+}
+
+// Tensor-core GEMV pieces (decoder kDecodeTensor).
+//
+// A code word holds 16 weights: bits 2f..2f+1 of its low half are weight
+// 16w + f and of its high half weight 16w + 8 + f (f = 0..7).  OR-ed into
+// fp16 1024 (0x6400), a field masked in place at bit 2f' is the exact value
+// 1024 + c * 4^f'; fields f = 0..4 sit at f' = f, fields 5..7 at f' = f - 3
+// after one shift of the word by 6.  h[f] is then a half pair (weight 16w + f,
+// weight 16w + 8 + f), one LOP3 each.  The activations arrive divided by the
+// same power of four (PQ2_Q_MMV16), so every product is 1024 q / 4^f' + c q,
+// an integer, and the fp32 accumulator holds the exact sum (|sum| < 2^22).
+__device__ __forceinline__ void decode_f16_fields(uint32_t w, uint32_t (&h)[8]) {
+  constexpr uint32_t kMagic = 0x64006400u;
+  h[0] = (w & 0x00030003u) | kMagic;
+  h[1] = (w & 0x000C000Cu) | kMagic;
+  h[2] = (w & 0x00300030u) | kMagic;
+  h[3] = (w & 0x00C000C0u) | kMagic;
+  h[4] = (w & 0x03000300u) | kMagic;
+  const uint32_t s = w >> 6;
+  h[5] = (s & 0x00300030u) | kMagic;
+  h[6] = (s & 0x00C000C0u) | kMagic;
+  h[7] = (s & 0x03000300u) | kMagic;
+}
+
+// d += A * B on a 16 x 8 x 16 tile, fp16 operands, fp32 accumulation.
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 16 bytes from global memory through the read-only path.
+__device__ __forceinline__ uint4 ldg_nc16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Combine the S split partials of one output (S a power of two, at most 16)
+// in the order of the dp4a consumer's xor butterfly, as lane 0 sees it: at
+// each step v[z] += v[z + off] for z < off, off = S/2 .. 1.
+template <int S>
+__device__ __forceinline__ float split_tree(const float* part, int stride) {
+  float v[S];
+#pragma unroll
+  for (int z = 0; z < S; ++z) v[z] = part[z * stride];
+#pragma unroll
+  for (int off = S >> 1; off > 0; off >>= 1)
+#pragma unroll
+    for (int z = 0; z < off; ++z) v[z] = __fadd_rn(v[z], v[z + off]);
+  return v[0];
 }
 
 // Exact int32 dots of one 128-group for RP weight rows and columns
@@ -340,7 +406,8 @@ __device__ __forceinline__ void group_dot_sub(const uint32_t (&c0)[RP], const ui
 // Up to four columns two CTAs fit on an SM (a call overlaps the next one);
 // more columns need the registers of one CTA per SM.
 template <int M, int DEC, bool DOTS, int NSUB = 1>
-__global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
+__global__ void __launch_bounds__(DEC == kDecodeTensor ? kTcBlock : kMaxBlock,
+                                  (M <= 4 || DEC == kDecodeTensor) ? 2 : 1)
     mmv_kernel(const __grid_constant__ CUtensorMap map_hi,
                const __grid_constant__ CUtensorMap map_lo,
                const MmvParams p) {
@@ -390,7 +457,7 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
     // ---------------------------------------------------------- producer
     if (lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
     bool ok = true;
-    const bool need_qs = DEC == kDecodeMaskPlanes;
+    const bool need_qs = DEC != kDecodeAddXor;  // sum(q), or the tensor path's corrections
     if (!DOTS && p.sw_bulk && lane == 0) {
       if (!p.overlap) grid_dep_wait();
       const uint32_t bytes = (uint32_t)(R * G * 2);
@@ -428,10 +495,11 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
       // Lane = 16-byte chunk c of row l of a block of four group rows; no
       // division in the address arithmetic.
       const int c = lane & 7;
-      for (int m = 0; m < M; ++m)
-        for (int l = lane >> 3; l < nb; l += 4)
-          cp_async16(dst0 + m * p.qbox_stride + l * kGroup + ((c ^ (l & 7)) << 4),
-                     src0 + ((size_t)m * G + l) * kGroup + c * 16);
+      if (DEC != kDecodeTensor)  // the tensor-core consumers read q themselves
+        for (int m = 0; m < M; ++m)
+          for (int l = lane >> 3; l < nb; l += 4)
+            cp_async16(dst0 + m * p.qbox_stride + l * kGroup + ((c ^ (l & 7)) << 4),
+                       src0 + ((size_t)m * G + l) * kGroup + c * 16);
       if (i == 0) {
         if (p.side16) {
           for (int idx = 4 * lane; idx < M * G * NSUB; idx += 128) {
@@ -507,6 +575,178 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
   }
   bool ok = true;
   if (!DOTS && p.sw_bulk) ok = ok && mbar_wait(swbar, 0);
+
+  if constexpr (DEC == kDecodeTensor) {
+    // ---------------------------------------------- tensor-core consumers
+    // Warp w owns the splits z = w % gstep + gstep * ss (ss < S / gstep; two
+    // when S = 16) and, when S < 8, the 16-row tiles tfirst + tw * ts.  For
+    // each of its groups, ascending (the split's order), it loads that
+    // group's B fragments (lane 4c + t: column c, 32 fp16 values) straight
+    // from global memory (every CTA reads the same q) and, per tile, decodes
+    // four code words (rows g, g + 8; words t, t + 4), runs eight mma.sync and
+    // adds the scaled exact dots to its split partials.
+    const __half* qf = reinterpret_cast<const __half*>(p.q);
+    if (p.overlap == 1) grid_dep_wait();  // q is read directly, not via the stages
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const int gstep = S < kTcWarps ? S : kTcWarps;
+    const int gfirst = warp % gstep;
+    const int tw = S < kTcWarps ? kTcWarps / S : 1;
+    const int tfirst = S < kTcWarps ? warp / S : 0;
+    const int nt = (R + 15) >> 4;
+    const int nts = tfirst < nt ? (nt - tfirst + tw - 1) / tw : 0;
+    const int nss = S / gstep;
+    const int c0 = 2 * t4, c1 = c0 + 1;
+    const uint32_t ring_s = smem_u32(ring), sw_base = smem_u32(sw_s);
+    // Split partials per unit: tile ts of the first split at [ts]; with two
+    // splits (S = 16, where a CTA holds at most 36 rows: 3 tiles) tile ts of
+    // the second at [kTcTiles2 + ts].
+    float yacc[kTcUnits][4];
+#pragma unroll
+    for (int u = 0; u < kTcUnits; ++u)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) yacc[u][k] = 0.0f;
+    uint32_t b[16];
+    const bool recycle = p.stages_total > p.ring;
+    for (int i = 0; i < p.stages_total; ++i) {
+      const int slot = i % p.ring;
+      ok = ok && mbar_wait_until(&full[slot], (i / p.ring) & 1, kWaitLimitCycles, abort_flag);
+      const uint32_t st_s = ring_s + slot * p.stage_bytes;
+      const int g0 = i * Gs;
+      if (ok) {
+#pragma unroll 1
+        for (int l = gfirst; l < Gs && g0 + l < G; l += gstep) {
+          const int g = g0 + l;
+          if (g8 < M) {
+            const uint8_t* src =
+                reinterpret_cast<const uint8_t*>(qf + ((size_t)g8 * G + g) * kGroup) + t4 * 64;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const uint4 v = ldg_nc16(src + 16 * c);
+              b[4 * c] = v.x; b[4 * c + 1] = v.y; b[4 * c + 2] = v.z; b[4 * c + 3] = v.w;
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) b[c] = 0u;
+          }
+          const int ss = (g % S) / gstep;
+          const uint32_t box = st_s + (l >> 2) * p.box_stride;
+          const int ch = (l & 3) * 2;
+          float xs0 = 0.0f, xs1 = 0.0f, cr0 = 0.0f, cr1 = 0.0f;
+          if (c0 < M) {
+            xs0 = sx_s[c0 * G + g];
+            cr0 = (float)qs_s[c0 * G + g];
+          }
+          if (c1 < M) {
+            xs1 = sx_s[c1 * G + g];
+            cr1 = (float)qs_s[c1 * G + g];
+          }
+#pragma unroll
+          for (int ts = 0; ts < kTcTiles; ++ts) {
+            if (ts >= nts) break;
+            const int tau = tfirst + ts * tw;
+            const int r0 = min(tau * 16 + g8, R - 1), r1 = min(tau * 16 + g8 + 8, R - 1);
+            const uint32_t a0 = box + r0 * kBoxBytes + 4 * t4, a1 = box + r1 * kBoxBytes + 4 * t4;
+            const uint32_t w00 = lds32(a0 + ((ch ^ (r0 & 7)) << 4));
+            const uint32_t w01 = lds32(a0 + (((ch + 1) ^ (r0 & 7)) << 4));
+            const uint32_t w10 = lds32(a1 + ((ch ^ (r1 & 7)) << 4));
+            const uint32_t w11 = lds32(a1 + (((ch + 1) ^ (r1 & 7)) << 4));
+            float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            {
+              uint32_t ha[8], hb[8];
+              decode_f16_fields(w00, ha);
+              decode_f16_fields(w10, hb);
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                mma_f16(d, ha[2 * j], hb[2 * j], ha[2 * j + 1], hb[2 * j + 1], b[2 * j],
+                        b[2 * j + 1]);
+            }
+            {
+              uint32_t ha[8], hb[8];
+              decode_f16_fields(w01, ha);
+              decode_f16_fields(w11, hb);
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                mma_f16(d, ha[2 * j], hb[2 * j], ha[2 * j + 1], hb[2 * j + 1], b[8 + 2 * j],
+                        b[8 + 2 * j + 1]);
+            }
+            // d: (row tau16 + g8, columns c0, c1), (row + 8, c0, c1); the
+            // exact dot is d minus the column's correction (exact in fp32).
+            if constexpr (DOTS) {
+              const int rr[2] = {tau * 16 + g8, tau * 16 + g8 + 8};
+              const float cr[2] = {cr0, cr1};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int row = rr[k >> 1], col = c0 + (k & 1);
+                if (row < R && col < M)
+                  p.dots[((size_t)col * p.N + n0 + row) * G + g] =
+                      (int)__fsub_rn(d[k], cr[k & 1]);
+              }
+            } else {
+              const float ws0 =
+                  __half2float(__ushort_as_half((uint16_t)lds16(sw_base + (r0 * G + g) * 2)));
+              const float ws1 =
+                  __half2float(__ushort_as_half((uint16_t)lds16(sw_base + (r1 * G + g) * 2)));
+              float tv[4];
+              tv[0] = __fmul_rn(__fmul_rn(__fsub_rn(d[0], cr0), xs0), ws0);
+              tv[1] = __fmul_rn(__fmul_rn(__fsub_rn(d[1], cr1), xs1), ws0);
+              tv[2] = __fmul_rn(__fmul_rn(__fsub_rn(d[2], cr0), xs0), ws1);
+              tv[3] = __fmul_rn(__fmul_rn(__fsub_rn(d[3], cr1), xs1), ws1);
+              if (ss == 0) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) yacc[ts][k] = __fadd_rn(yacc[ts][k], tv[k]);
+              } else if (ts < kTcTiles2) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  yacc[kTcTiles2 + ts][k] = __fadd_rn(yacc[kTcTiles2 + ts][k], tv[k]);
+              }
+            }
+          }
+        }
+      }
+      if (recycle) {
+        __syncwarp();
+        if (lane == 0 && !(i == p.drop_stage && warp == 0)) mbar_arrive(&empty[slot]);
+      }
+    }
+    if (!ok && lane == 0) report(p.status, PQ2_ERR_TIMEOUT);
+    if constexpr (!DOTS) {
+      // part[z][row][m]: every split's partial of every output of the CTA
+      float* part = reinterpret_cast<float*>(smem + p.part_off);
+#pragma unroll
+      for (int u = 0; u < kTcUnits; ++u) {
+        const int ss = nss == 1 ? 0 : u / kTcTiles2;
+        const int ts = nss == 1 ? u : u - kTcTiles2 * ss;
+        if (ts >= nts || (nss == 1 && u >= kTcTiles)) continue;
+        const int z = gfirst + ss * gstep;
+        const int tau = tfirst + ts * tw;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int row = tau * 16 + g8 + 8 * (k >> 1), col = c0 + (k & 1);
+          if (row < R && col < M) part[((size_t)z * R + row) * M + col] = yacc[u][k];
+        }
+      }
+      named_bar_sync(1, p.cons_threads);  // every partial is in place
+      grid_dep_wait();  // earlier kernels may still read or write y
+      for (int o = tid; o < R * M; o += p.cons_threads) {
+        const int row = o / M, m = o - row * M;
+        const float* src = part + (size_t)row * M + m;
+        const int stride = R * M;
+        float v;
+        switch (S) {
+          case 1: v = split_tree<1>(src, stride); break;
+          case 2: v = split_tree<2>(src, stride); break;
+          case 4: v = split_tree<4>(src, stride); break;
+          case 8: v = split_tree<8>(src, stride); break;
+          default: v = split_tree<16>(src, stride); break;
+        }
+        const size_t off = (size_t)m * p.y_ld + n0 + row;
+        if (p.y_bf16)
+          static_cast<__nv_bfloat16*>(p.y)[off] = __float2bfloat16_rn(v);
+        else
+          static_cast<float*>(p.y)[off] = v;
+      }
+    }
+  } else {
 
   // Thread t owns split z = t % S and the RP rows rb, rb + H, rb + 2H ..
   // (rb = t / S, H = ceil(R / RP)).  A warp then reads code rows with
@@ -678,6 +918,7 @@ __global__ void __launch_bounds__(kMaxBlock, M <= 4 ? 2 : 1)
       }
     }
   }
+  }
 }
 
 // ------------------------------------------------------------------- host
@@ -839,6 +1080,8 @@ int launch_mmv_impl(const int8_t* q, const float* sx, const int32_t* qsum,
                     int nsub = 1, int drop_stage = -1, long long empty_limit = kWaitLimitCycles) {
   if (nsub != 1 && ((nsub != 2 && nsub != 4) || M > 4 || gated || decode != kDecodeMaskPlanes))
     return PQ2_ERR_SHAPE;
+  const bool tensor = decode == kDecodeTensor;
+  if (tensor && gated) return PQ2_ERR_SHAPE;
   MmvGeometry geo;
   if (!mmv_geometry(N, K, sm_count, &geo)) return PQ2_ERR_SHAPE;
   if (gated && (N % 2 || dots)) return PQ2_ERR_SHAPE;
@@ -859,7 +1102,7 @@ int launch_mmv_impl(const int8_t* q, const float* sx, const int32_t* qsum,
   p.y = y; p.dots = dots; p.status = status;
   p.N = (int)rows_out; p.K = (int)K; p.G = (int)(K / kGroup);
   p.ctas = (int)ctas; p.splits = geo.splits; p.rows_max = rows_max;
-  p.cons_threads = threads;
+  p.cons_threads = tensor ? kTcWarps * 32 : threads;
   p.gated = gated;
   p.up_row = gated ? (int)(N / 2) : 0;
   p.up_smem = gated ? align_up(rows_max, 8) : 0;
@@ -878,11 +1121,14 @@ int launch_mmv_impl(const int8_t* q, const float* sx, const int32_t* qsum,
   p.sw_off = align_up(kAbortOff + 4, 128);
   p.sx_off = align_up(p.sw_off + G * slab * 2, 16);
   p.qs_off = align_up(p.sx_off + mi * G * nsub * 4, 16);
-  p.ring_off = align_up(p.qs_off + mi * G * nsub * 4, 1024);
+  p.part_off = align_up(p.qs_off + mi * G * nsub * 4, 16);
+  p.ring_off = align_up(p.part_off + (tensor ? S * R * mi * 4 : 0), 1024);
   const int room = kSmemBudget - p.ring_off;
-  // Stage: k units of lcm(4, S) groups, aiming at ~16-24 KB of codes.
+  // Stage: k units of lcm(4, S) groups, aiming at ~16-24 KB of codes.  The
+  // tensor-core consumers read q from global memory: no q in the stages.
+  const int q_cols = tensor ? 0 : mi;
   auto stage_bytes = [&](int gs) {
-    return (gs / 4) * p.box_stride + mi * align_up(gs * kGroup, 1024);
+    return (gs / 4) * p.box_stride + q_cols * align_up(gs * kGroup, 1024);
   };
   // Stage: 2S groups when two such stages fit the ring, else S (S >= 8), or
   // 8 groups (S = 4), so that a thread meets one or two groups per stage.
@@ -912,6 +1158,12 @@ int launch_mmv_impl(const int8_t* q, const float* sx, const int32_t* qsum,
   p.ring = std::min(std::min(p.stages_total, room / p.stage_bytes), kMaxStages);
   p.drop_stage = drop_stage;
   p.empty_limit = empty_limit;
+  if (tensor) {
+    const int nt = (R + 15) / 16, tw = S < kTcWarps ? kTcWarps / S : 1;
+    const int nts = (nt + tw - 1) / tw;
+    if (S > 2 * kTcWarps || nts > kTcTiles || (S > kTcWarps && nts > kTcTiles2))
+      return PQ2_ERR_SHAPE;
+  }
   // A dropped release only matters where a slot is reused.
   if (drop_stage >= 0 && (p.stages_total <= p.ring || drop_stage + p.ring >= p.stages_total))
     return PQ2_ERR_SHAPE;
@@ -931,6 +1183,9 @@ int launch_mmv_impl(const int8_t* q, const float* sx, const int32_t* qsum,
   if (nsub > 1)
     return dots ? launch_m_sub<true>(nsub, mi, hi, lo, p, smem, stream)
                 : launch_m_sub<false>(nsub, mi, hi, lo, p, smem, stream);
+  if (tensor)
+    return dots ? launch_m<kDecodeTensor, true>(mi, hi, lo, p, smem, stream)
+                : launch_m<kDecodeTensor, false>(mi, hi, lo, p, smem, stream);
   if (dots)
     return decode == kDecodeMaskPlanes
                ? launch_m<kDecodeMaskPlanes, true>(mi, hi, lo, p, smem, stream)

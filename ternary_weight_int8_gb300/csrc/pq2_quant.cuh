@@ -108,6 +108,47 @@ __device__ __forceinline__ void store_group4(const int qi[4], int lane, void* q,
     uint32_t* out = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(q) + 2 * base);
     out[lane] = __byte_perm(ha, hb, sel);
     out[32 + lane] = __byte_perm(la, lb, sel);
+  } else if (layout == PQ2_Q_MMV16) {
+    // Fragment order of the small-batch tensor-core GEMV (128-groups only):
+    // position P = 32t + 4j + 2r + e of the group (lane L writes P = 4L..4L+3,
+    // so t = L / 8, j = L % 8, (r, e) = the slot's two bits) holds element
+    // i = 16(t + 4(j / 4)) + 8e + f, f = 2(j % 4) + r, divided by 4^f (f <= 4)
+    // or 4^(f - 3) (f >= 5): the weight that meets it in the GEMV is then
+    // 1024 + code * that power of 4, and the group's correction below
+    // removes the 1024 and the code's -1 offset.
+    const int t = lane >> 3, j = lane & 7;
+    const int wbase = 16 * (t + 4 * (j >> 2)) + 2 * (j & 3);
+    uint32_t out[2];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int i = wbase + 8 * (s & 1) + (s >> 1);
+      const int f = 2 * (j & 3) + (s >> 1);
+      const uint32_t v = __shfl_sync(0xffffffffu, packed, i >> 2);
+      const int qv = (int)(int8_t)((v >> (8 * (i & 3))) & 0xffu);
+      // 1 / 4^f or 1 / 4^(f-3): exact powers of two, so q / scale is exact
+      const float inv = f <= 4 ? __int_as_float((127 - 2 * f) << 23)
+                               : __int_as_float((127 - 2 * (f - 3)) << 23);
+      const uint32_t h = (uint32_t)__half_as_ushort(__float2half_rn((float)qv * inv));
+      if (s & 1)
+        out[s >> 1] |= h << 16;
+      else
+        out[s >> 1] = h;
+    }
+    reinterpret_cast<uint2*>(static_cast<__half*>(q) + base)[lane] = make_uint2(out[0], out[1]);
+    // Correction: sum over the group of q * (1 + 1024 / scale), the scale of
+    // element i being that of its field f = i % 8 (weights 1025, 257, 65, 17,
+    // 5, 65, 17, 5); |correction| <= 127 * 16 * 1456 < 2^22.
+    int c = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int f = (4 * lane + k) & 7;
+      const int wgt = f <= 4 ? 1 + (1024 >> (2 * f)) : 1 + (1024 >> (2 * (f - 3)));
+      c += qi[k] * wgt;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+    if (qsum && lane == 0) qsum[0] = c;
+    return;
   } else {
     // Operand order of the prefill MMA: inside each 16-element chunk (lanes
     // 4c..4c+3, element 4b + s held by lane 4c + b), element 4b + s goes to

@@ -24,9 +24,10 @@ LIB_PATH = os.path.join(_PKG, "libpq2.so")
 PQ2_OK, PQ2_ERR_NULL, PQ2_ERR_SHAPE, PQ2_ERR_ALIGN, PQ2_ERR_DTYPE = 0, 1, 2, 3, 4
 PQ2_ERR_ARCH, PQ2_ERR_LAUNCH, PQ2_ERR_TIMEOUT, PQ2_ERR_CUDA = 5, 6, 7, 8
 PQ2_BF16, PQ2_F16, PQ2_F32 = 0, 1, 2
-PQ2_Q_ROWS, PQ2_Q_PLANES, PQ2_Q_F16, PQ2_Q_F8 = 0, 1, 2, 3
+PQ2_Q_ROWS, PQ2_Q_PLANES, PQ2_Q_F16, PQ2_Q_F8, PQ2_Q_MMV16 = 0, 1, 2, 3, 4
 PQ2_DECODE_ADDXOR, PQ2_DECODE_PLANES = 0, 1
-PQ2_PATH_MMV_ADDXOR, PQ2_PATH_MM, PQ2_PATH_MMV_PLANES, PQ2_PATH_MM_F8 = 0, 1, 2, 3
+PQ2_PATH_MMV_ADDXOR, PQ2_PATH_MM, PQ2_PATH_MMV_PLANES, PQ2_PATH_MM_F8, PQ2_PATH_MMV_TC = \
+    0, 1, 2, 3, 4
 PQ2_MMV_OVERLAP_WEIGHTS, PQ2_MMV_INDEPENDENT = 1, 2
 PQ2_STATIC_SCRATCH_BYTES = 1 << 20
 GROUP = 128
@@ -41,6 +42,8 @@ SIGNATURES = {
     "pq2_quantize_act": (_I, [_P, _I, _I64, _I64, _I64, _P, _I, _P, _P, _P]),
     "pq2_mmv": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P]),
     "pq2_mmv_ex": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _I, _P, _P]),
+    "pq2_mmv_tc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _P, _P]),
+    "pq2_linear_tensor_gemv": (_I, [_I64, _I64, _I64, _I]),
     "pq2_linear": (_I, [_P, _I, _I64, _I64, _I64, _I64, _P, _P, _P, _I, _P, _SZ, _P, _P]),
     "pq2_linear_workspace_bytes": (_SZ, [_I64, _I64]),
     "pq2_linear_static": (_I, [_P, _I, _I64, _I64, _I64, _I64, _P, _P, _P, _I, _P, _P]),
@@ -166,6 +169,20 @@ def pq2_mmv(q_planes, sx, qsum, codes, scales, y=None, out_dtype=torch.float32,
         dec = mmv_decoder(M) if decode is None else decode
         st = lib().pq2_mmv_ex(*args, dec, flags, _ptr(status), _stream(stream))
     _check("pq2_mmv", st)
+    return y
+
+
+def pq2_mmv_tc(q_mmv16, sx, qcorr, codes, scales, y=None, out_dtype=torch.float32, flags=0,
+               status=None, stream=None):
+    """Small-batch GEMV on the tensor-core path, M = 1..8, q from
+    pq2_quantize_act(PQ2_Q_MMV16) and its corrections; same bits as pq2_mmv."""
+    M, K = q_mmv16.shape
+    N = codes.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=q_mmv16.device)
+    _check("pq2_mmv_tc", lib().pq2_mmv_tc(_ptr(q_mmv16), _ptr(sx), _ptr(qcorr), _ptr(codes),
+                                          _ptr(scales), _ptr(y), _DT[y.dtype], M, N, K, flags,
+                                          _ptr(status), _stream(stream)))
     return y
 
 
@@ -338,9 +355,10 @@ def pq2_norm_hadamard_quantize(x, w, sign, eps, residual=None, layout: int = PQ2
 
 
 def q_buffer(M: int, K: int, layout: int, device):
-    """Output buffer of the quantiser for `layout`: fp16 [M][K] (PQ2_Q_F16),
-    uint8 [M][2K] (the two e4m3 planes of PQ2_Q_F8) or int8 [M][K]."""
-    if layout == PQ2_Q_F16:
+    """Output buffer of the quantiser for `layout`: fp16 [M][K] (PQ2_Q_F16,
+    PQ2_Q_MMV16), uint8 [M][2K] (the two e4m3 planes of PQ2_Q_F8) or int8
+    [M][K]."""
+    if layout in (PQ2_Q_F16, PQ2_Q_MMV16):
         return torch.empty((M, K), dtype=torch.float16, device=device)
     if layout == PQ2_Q_F8:
         return torch.empty((M, 2 * K), dtype=torch.uint8, device=device)

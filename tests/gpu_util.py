@@ -137,6 +137,32 @@ def mm_operand_order_f8(q: np.ndarray) -> np.ndarray:
     return out.reshape(M, 2 * K)
 
 
+def mmv16_layout(q: np.ndarray) -> np.ndarray:
+    """The PQ2_Q_MMV16 layout (include/pq2.h) as fp16 [M][K], built on the
+    host from int8 q: inside every 128-group, position 32t + 4j + 2r + e
+    holds element 16(t + 4(j // 4)) + 8e + f, f = 2(j % 4) + r, divided by
+    4^f (f <= 4) or 4^(f - 3) (f >= 5)."""
+    M, K = q.shape
+    qg = q.reshape(M, K // G, G).astype(np.float64)
+    out = np.empty((M, K // G, G), np.float64)
+    for P in range(G):
+        t, j, r, e = P // 32, (P % 32) // 4, (P % 4) // 2, P % 2
+        f = 2 * (j % 4) + r
+        i = 16 * (t + 4 * (j // 4)) + 8 * e + f
+        out[:, :, P] = qg[:, :, i] / 4.0 ** (f if f <= 4 else f - 3)
+    return out.astype(np.float16).reshape(M, K)
+
+
+def mmv16_correction(q: np.ndarray) -> np.ndarray:
+    """The PQ2_Q_MMV16 group corrections: sum over the group of
+    q_i * (1 + 1024 / scale_i), scale_i the divisor of element i (its field
+    f = i % 8 as above)."""
+    M, K = q.shape
+    f = np.arange(G) % 8
+    wt = 1 + 1024 // 4 ** np.where(f <= 4, f, f - 3)
+    return (q.reshape(M, K // G, G).astype(np.int64) * wt).sum(-1).astype(np.int32)
+
+
 def host_mapped(t) -> bool:
     """True when the pinned host tensor `t` is addressable by the device at
     its own address (asked of the CUDA runtime, not by touching it)."""

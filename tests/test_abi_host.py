@@ -66,7 +66,7 @@ def test_quantize_validation(L):
     f = L.pq2_quantize_act
     assert f(None, 0, 128, 1, 128, A, 1, A, A, None) == pq2.PQ2_ERR_NULL
     assert f(A, 3, 128, 1, 128, A, 1, A, A, None) == pq2.PQ2_ERR_DTYPE
-    assert f(A, 0, 128, 1, 128, A, 4, A, A, None) == pq2.PQ2_ERR_DTYPE
+    assert f(A, 0, 128, 1, 128, A, 5, A, A, None) == pq2.PQ2_ERR_DTYPE
     assert f(A, 0, 127, 1, 128, A, 1, A, A, None) == pq2.PQ2_ERR_SHAPE
     assert f(A, 0, 128, 0, 128, A, 1, A, A, None) == pq2.PQ2_ERR_SHAPE
     assert f(A, 0, 256, 1, 192, A, 1, A, A, None) == pq2.PQ2_ERR_SHAPE
@@ -177,14 +177,18 @@ def test_mm_f8_validation(L):
     d = L.pq2_debug_group_dots
     assert d(A, None, A, 16, 10, 128, pq2.PQ2_PATH_MM_F8, A, None, None) == pq2.PQ2_ERR_NULL
     assert d(A, A, A, 8, 10, 128, pq2.PQ2_PATH_MM_F8, A, None, None) == pq2.PQ2_ERR_SHAPE
-    assert d(A, A, A, 16, 10, 128, 4, A, None, None) == pq2.PQ2_ERR_DTYPE
+    assert d(A, A, A, 16, 10, 128, 5, A, None, None) == pq2.PQ2_ERR_DTYPE
+    # the tensor-core GEMV path takes M = 1..8 and its corrections
+    assert d(A, A, A, 16, 10, 128, pq2.PQ2_PATH_MMV_TC, A, None, None) == pq2.PQ2_ERR_SHAPE
+    assert d(A, None, A, 4, 10, 128, pq2.PQ2_PATH_MMV_TC, A, None, None) == pq2.PQ2_ERR_NULL
 
 
 def test_grouped_validation(L):
     q = L.pq2_quantize_act_grouped
     ok = [A, pq2.PQ2_BF16, 256, 2, 256, 32, A, pq2.PQ2_Q_PLANES, A, A, None]
     for idx, val, err in [(5, 16, pq2.PQ2_ERR_SHAPE), (5, 96, pq2.PQ2_ERR_SHAPE),
-                          (7, 4, pq2.PQ2_ERR_DTYPE), (1, 9, pq2.PQ2_ERR_DTYPE),
+                          (7, 5, pq2.PQ2_ERR_DTYPE), (1, 9, pq2.PQ2_ERR_DTYPE),
+                          (7, pq2.PQ2_Q_MMV16, pq2.PQ2_ERR_SHAPE),
                           (6, None, pq2.PQ2_ERR_NULL), (0, None, pq2.PQ2_ERR_NULL),
                           (6, A + 4, pq2.PQ2_ERR_ALIGN), (4, 200, pq2.PQ2_ERR_SHAPE)]:
         bad = list(ok); bad[idx] = val
@@ -264,3 +268,29 @@ def test_linear_static_error_order(L):
         pq2.PQ2_ERR_SHAPE
     assert f(None, pq2.PQ2_BF16, 128, 1, 4, 128, A, A, A, pq2.PQ2_F32, None, None) == \
         pq2.PQ2_ERR_NULL
+
+
+def test_mmv_tc_validation(L):
+    """pq2_mmv_tc rejects what pq2_mmv_ex rejects, before any CUDA call."""
+    f = L.pq2_mmv_tc
+    ok = [A, A, A, A, A, A, pq2.PQ2_F32, 4, 10, 128, 0, None, None]
+    for idx, val, err in [(0, None, pq2.PQ2_ERR_NULL), (2, None, pq2.PQ2_ERR_NULL),
+                          (7, 9, pq2.PQ2_ERR_SHAPE), (7, 0, pq2.PQ2_ERR_SHAPE),
+                          (9, 200, pq2.PQ2_ERR_SHAPE), (6, 1, pq2.PQ2_ERR_DTYPE),
+                          (10, 4, pq2.PQ2_ERR_DTYPE), (0, A + 8, pq2.PQ2_ERR_ALIGN),
+                          (5, A + 2, pq2.PQ2_ERR_ALIGN)]:
+        bad = list(ok); bad[idx] = val
+        assert f(*bad) == err, (idx, val)
+    # the GEMV choice of pq2_linear: dp4a for M <= 4, tensor cores from M = 6,
+    # at M = 5 only for slabs of at most 72 rows in at most 8 splits
+    for M in range(1, 5):
+        assert L.pq2_linear_tensor_gemv(M, 10240, 5120, 152) == 0
+    for M in range(6, 9):
+        for N, K in [(10240, 5120), (17408, 5120), (5120, 17408), (6144, 5120)]:
+            assert L.pq2_linear_tensor_gemv(M, N, K, 152) == 1
+    assert L.pq2_linear_tensor_gemv(5, 10240, 5120, 152) == 1   # 68 rows, 8 splits
+    assert L.pq2_linear_tensor_gemv(5, 6144, 5120, 152) == 1    # 41 rows, 8 splits
+    assert L.pq2_linear_tensor_gemv(5, 17408, 5120, 152) == 0   # 115 rows
+    assert L.pq2_linear_tensor_gemv(5, 5120, 17408, 152) == 0   # 16 splits
+    assert L.pq2_linear_tensor_gemv(16, 10240, 5120, 152) == 0
+    assert L.pq2_linear_tensor_gemv(9, 10240, 5120, 152) == 0

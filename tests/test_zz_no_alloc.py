@@ -80,13 +80,17 @@ def test_static_call_allocates_nothing():
 
 def test_static_rejects_shapes_beyond_its_scratch():
     lib = pq2.lib()
-    assert pq2.linear_workspace_bytes(8, 123264) <= pq2.PQ2_STATIC_SCRATCH_BYTES
-    assert pq2.linear_workspace_bytes(8, 123392) > pq2.PQ2_STATIC_SCRATCH_BYTES
-    x = torch.zeros((8, 123392), dtype=torch.bfloat16, device="cuda")
-    codes = torch.zeros((4, 123392 // 4), dtype=torch.uint8, device="cuda")
-    scales = torch.zeros((4, 123392 // 128), dtype=torch.int16, device="cuda")
+    # the largest K whose workspace fits the static scratch at M = 8
+    K = 128
+    while pq2.linear_workspace_bytes(8, K + 128) <= pq2.PQ2_STATIC_SCRATCH_BYTES:
+        K += 128
+    big = K + 128
+    assert pq2.linear_workspace_bytes(8, big) > pq2.PQ2_STATIC_SCRATCH_BYTES
+    x = torch.zeros((8, big), dtype=torch.bfloat16, device="cuda")
+    codes = torch.zeros((4, big // 4), dtype=torch.uint8, device="cuda")
+    scales = torch.zeros((4, big // 128), dtype=torch.int16, device="cuda")
     y = torch.empty((8, 4), dtype=torch.float32, device="cuda")
-    st = lib.pq2_linear_static(x.data_ptr(), pq2.PQ2_BF16, 123392, 8, 4, 123392,
+    st = lib.pq2_linear_static(x.data_ptr(), pq2.PQ2_BF16, big, 8, 4, big,
                                codes.data_ptr(), scales.data_ptr(), y.data_ptr(), pq2.PQ2_F32,
                                None, torch.cuda.current_stream().cuda_stream)
     assert st == pq2.PQ2_ERR_SHAPE
