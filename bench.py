@@ -31,7 +31,7 @@ replayed from CUDA graphs and timed with CUDA events on the launching stream.
               M = 16 .. 4096: microseconds, TOPS and the fraction of the
               measured dense tensor peak of the kernel's own operand type
   prep        the fused preparation (pq2_norm_hadamard_quantize) at K=5120,
-              M = 1..4 and 4096, with the stand-alone quantisation beside it
+              M = 1..4, 16, 64, 256 and 4096, with the stand-alone quantisation beside it
   gated       the gated gate/up projection (pq2_mmv_gated, silu(gate) * up
               in the GEMV's epilogue) on ffn gate/up (K=5120, 2 x 17408
               rows) at M = 1..4: microseconds, HBM GB/s and fraction, the
@@ -589,7 +589,7 @@ def ptq_leg(args, dev, stream, timed, capture):
 def prep_leg(args, dev, stream, timed, capture):
     """The fused preparation (pq2_norm_hadamard_quantize: RMSNorm with a
     residual, signs, 1024-point Walsh-Hadamard, group-128 INT8 in the plane
-    layout) at K=5120 for M = 1..4 and 4096, against the stand-alone
+    layout) at K=5120 for M = 1..4, 16, 64, 256 and 4096, against the stand-alone
     quantisation of the same rows; HBM bytes per call: x and residual in
     (2 x 2MK), w and signs (3K), q out (MK), s_x and sum(q) (8MK/128)."""
     import torch
@@ -603,7 +603,7 @@ def prep_leg(args, dev, stream, timed, capture):
     sp = stream.cuda_stream
     out = {"workload": f"K={K}, bf16 x and residual, eps 1e-6, q in plane order",
            "peak_gbs": hbm, "peak_source": hbm_kind, "by_m": {}}
-    for M in tuple(MS) + (4096,):
+    for M in tuple(MS) + (16, 64, 256, 4096):
         n_in = 8 if M < 64 else 1  # rotate inputs of small calls
         xs = [synth.activations(M, K, seed=40 + i, device=dev).to(torch.bfloat16)
               for i in range(n_in)]

@@ -16,8 +16,9 @@
 // orthonormal one (butterfly passes of half-width 1, 2, .., 512, then the
 // exact factor 1/32).
 //
-// One CTA per row (256 threads, four per SM, for many rows; 1024 threads for
-// few rows, where one row's latency counts): the row's h sits in shared
+// Rows of up to eight 1024-blocks: one cluster of CTAs per row (below).
+// Longer rows: one CTA per row (256 threads, four per SM, for many rows; 1024
+// threads for few rows, where one row's latency counts): the row's h sits in shared
 // memory between the passes.  With 1024 threads, 64 threads form the sum of
 // squares (levels 1024..64 of its tree inside a thread) and up to four warps
 // share each 1024-block of the transform; otherwise each warp owns whole
@@ -46,15 +47,15 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-// The transform of every 1024-block of a row by W warps per block (W = 2 or
-// 4): warp u of block b holds the elements b + (1024/W) u + 32 i + l,
+// The transform of every 1024-block of a row by W warps per block (W = 2, 4
+// or 8): warp u of block b holds the elements b + (1024/W) u + 32 i + l,
 // i < 32/W, of lane l.  Passes of half-width 1..16 are shuffles, those up to
 // 512/W pair registers of a lane, and the last log2(W) passes pair elements
 // of two warps through shared memory (the block's h, already read), in the
 // order 1, 2, .., 512 of the single-warp transform, so the bits are the
 // same.  Every warp of the CTA reaches the same barriers.
 // The norm weights (bf16 bits, two per word) and signs (bytes, four per
-// word) of a lane's elements in the transform_shared layout for W = 2 or 4,
+// word) of a lane's elements in the transform_shared layout for W = 2, 4, 8,
 // loaded at kernel entry so that their latency overlaps the first pass.
 struct TransformOperands {
   uint32_t wb[8];
@@ -373,6 +374,172 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepThreads == 256 ? 4 : 1)
   }
 }
 
+// ---------------------------------------------------------------- clusters
+// A row of K = 1024 C elements (C <= 8) spread over a cluster of C CTAs, CTA
+// c owning the transform block [1024c, 1024c + 1024): the load, the
+// transform and the quantisation of a row then run on C SMs at once.  Every
+// CTA writes h^2 of its block to its shared memory, and after one cluster
+// barrier forms the whole 2048-lane reduction tree itself from the cluster's
+// squares (distributed shared memory), in the order of the one-CTA kernel
+// with 256 threads, so every CTA holds the same bits of inv.
+
+constexpr int kClusterThreads = 256;  // 8 warps: one per group of a block
+constexpr int64_t kClusterMaxRows = 64;
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The float at the same shared-memory offset as `local` in CTA `rank` of the
+// cluster.
+__device__ __forceinline__ float ld_cluster(const float* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(remote)
+               : "r"(smem_u32(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+__global__ void __launch_bounds__(kClusterThreads)
+    prep_cluster_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ res,
+                        uint16_t* __restrict__ res_out, const uint16_t* __restrict__ w,
+                        const int8_t* __restrict__ sign, float eps, int K, int vec,
+                        uint16_t* __restrict__ norm_out, void* __restrict__ q, int layout,
+                        float* __restrict__ sx, int32_t* __restrict__ qsum) {
+  __shared__ __align__(16) float hs[kHad];   // h, then the transformed block
+  __shared__ __align__(16) float sq[kHad];   // h^2, read by the whole cluster
+  __shared__ float tree[kClusterThreads];
+  constexpr int kWarps = kClusterThreads / 32;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int C = K / kHad;
+  const uint32_t c = cluster_ctarank();
+  const int64_t m = blockIdx.x / C;
+  const int G = K / kGroup;
+  const int64_t row0 = m * K + (int64_t)c * kHad;  // first element of the block
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  TransformOperands ops;
+  load_transform_operands<kWarps>(w + c * kHad, sign + c * kHad, 1, warp, lane, ops);
+
+  // Pass 1a: h = x (+ residual) of the block, four elements per thread.
+  {
+    const int j = 4 * t;
+    float h4[4];
+    if (vec) {
+      const uint2 xv = *reinterpret_cast<const uint2*>(x + row0 + j);
+      uint2 rv = make_uint2(0u, 0u);
+      if (res) rv = *reinterpret_cast<const uint2*>(res + row0 + j);
+      const uint32_t xw[2] = {xv.x, xv.y}, rw[2] = {rv.x, rv.y};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float a = bf16_bits_to_float((uint16_t)(xw[e >> 1] >> (16 * (e & 1))));
+        if (res) a = __fadd_rn(a, bf16_bits_to_float((uint16_t)(rw[e >> 1] >> (16 * (e & 1)))));
+        h4[e] = a;
+      }
+      if (res_out)
+        *reinterpret_cast<uint2*>(res_out + row0 + j) =
+            make_uint2((uint32_t)float_to_bf16_bits(h4[0]) |
+                           ((uint32_t)float_to_bf16_bits(h4[1]) << 16),
+                       (uint32_t)float_to_bf16_bits(h4[2]) |
+                           ((uint32_t)float_to_bf16_bits(h4[3]) << 16));
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float a = bf16_bits_to_float(x[row0 + j + e]);
+        if (res) a = __fadd_rn(a, bf16_bits_to_float(res[row0 + j + e]));
+        h4[e] = a;
+        if (res_out) res_out[row0 + j + e] = float_to_bf16_bits(a);
+      }
+    }
+    *reinterpret_cast<float4*>(hs + j) = make_float4(h4[0], h4[1], h4[2], h4[3]);
+    *reinterpret_cast<float4*>(sq + j) =
+        make_float4(__fmul_rn(h4[0], h4[0]), __fmul_rn(h4[1], h4[1]), __fmul_rn(h4[2], h4[2]),
+                    __fmul_rn(h4[3], h4[3]));
+  }
+  cluster_arrive();  // the block's squares are visible to the cluster
+  cluster_wait();
+
+  // Pass 1b: lanes t + 256k (k < 8) of the 2048 strided partial sums, each
+  // in increasing j, element j read from CTA j / 1024 of the cluster; then
+  // the tree, as the 256-thread one-CTA kernel forms it.
+  // Every remote load goes out before the first addition (K <= 8192: at
+  // most four slices of 2048), then the sums are formed in increasing j.
+  constexpr int kPer = kLanes / kClusterThreads;
+  constexpr int kSlices = 8 * kHad / kLanes;
+  float v[kSlices][kPer];
+#pragma unroll
+  for (int sl = 0; sl < kSlices; ++sl)
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int j = sl * kLanes + t + kClusterThreads * k;
+      v[sl][k] = j < K ? ld_cluster(sq + (j & (kHad - 1)), (uint32_t)(j / kHad)) : 0.0f;
+    }
+  cluster_arrive();  // done reading the cluster's squares (waited for at exit)
+  float p[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    p[k] = 0.0f;
+#pragma unroll
+    for (int sl = 0; sl < kSlices; ++sl)
+      if (sl * kLanes + t + kClusterThreads * k < K) p[k] = __fadd_rn(p[k], v[sl][k]);
+  }
+#pragma unroll
+  for (int step = kLanes / kClusterThreads / 2; step >= 1; step >>= 1)
+#pragma unroll
+    for (int k = 0; k < step; ++k) p[k] = __fadd_rn(p[k], p[k + step]);
+  tree[t] = p[0];
+  __syncthreads();
+  if (warp == 0) {
+    // Levels 128, 64, 32 in the registers of warp 0 (lane l holds lanes
+    // l + 32k of the tree, so each pair i, i + len meets in one lane), then
+    // 16 .. 1 by shuffles.
+    float u[kWarps];
+#pragma unroll
+    for (int k = 0; k < kWarps; ++k) u[k] = tree[lane + 32 * k];
+#pragma unroll
+    for (int step = kWarps / 2; step >= 1; step >>= 1)
+#pragma unroll
+      for (int k = 0; k < step; ++k) u[k] = __fadd_rn(u[k], u[k + step]);
+    float v = u[0];
+#pragma unroll
+    for (int len = 16; len >= 1; len >>= 1) {
+      const float o = __shfl_down_sync(0xffffffffu, v, len);
+      if (lane < len) v = __fadd_rn(v, o);
+    }
+    if (lane == 0) tree[0] = v;
+  }
+  __syncthreads();
+  const float mean = __fdiv_rn(tree[0], (float)K);
+  const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+
+  // Pass 2: the block's transform by all eight warps (four values a lane).
+  transform_shared<kWarps, kWarps>(hs, ops, inv, norm_out ? norm_out + c * kHad : nullptr, m, K,
+                                   1, warp, lane);
+  __syncthreads();
+  // Pass 3: the block's eight 128-groups, one per warp.
+  {
+    const int gi = warp;
+    const int g = (int)c * (kHad / kGroup) + gi;
+    const float4 v4 = *reinterpret_cast<const float4*>(hs + gi * kGroup + 4 * lane);
+    const float a[4] = {v4.x, v4.y, v4.z, v4.w};
+    int qi[4];
+    const float s = quantize_group4(a, qi);
+    store_group4(qi, lane, q, layout, m * K + (int64_t)g * kGroup,
+                 qsum ? qsum + m * G + g : nullptr);
+    if (lane == 0) sx[m * G + g] = s;
+  }
+  cluster_wait();  // no CTA leaves while another may still read its squares
+}
+
 template <int kPrepThreads>
 int launch_prep(const uint16_t* x, const uint16_t* residual, uint16_t* residual_out,
                 const uint16_t* w, const int8_t* sign, float eps, int64_t M, int64_t K,
@@ -409,12 +576,46 @@ int launch_prep(const uint16_t* x, const uint16_t* residual, uint16_t* residual_
   return PQ2_OK;
 }
 
+int launch_prep_cluster(const uint16_t* x, const uint16_t* residual, uint16_t* residual_out,
+                        const uint16_t* w, const int8_t* sign, float eps, int64_t M, int64_t K,
+                        uint16_t* norm_out, void* q, int q_layout, float* sx, int32_t* qsum,
+                        cudaStream_t stream) {
+  const int C = (int)(K / kHad);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(M * C));
+  cfg.blockDim = dim3(kClusterThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)C;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  auto a8 = [](const void* ptr) { return reinterpret_cast<uintptr_t>(ptr) % 8 == 0; };
+  const int vec = a8(x) && (!residual || a8(residual)) && (!residual_out || a8(residual_out));
+  if (cudaLaunchKernelEx(&cfg, prep_cluster_kernel, x, residual, residual_out, w, sign, eps,
+                         (int)K, vec, norm_out, q, q_layout, sx, qsum) != cudaSuccess) {
+    cudaGetLastError();
+    return PQ2_ERR_LAUNCH;
+  }
+  return PQ2_OK;
+}
+
 }  // namespace
 
 int launch_norm_hadamard_quantize(const uint16_t* x, const uint16_t* residual,
                                   uint16_t* residual_out, const uint16_t* w, const int8_t* sign,
                                   float eps, int64_t M, int64_t K, uint16_t* norm_out, void* q,
                                   int q_layout, float* sx, int32_t* qsum, cudaStream_t stream) {
+  // Few rows of at most eight transform blocks: one cluster CTA per block
+  // (the latency of a row, spread over K / 1024 SMs).
+  if (K <= 8 * kHad && M <= kClusterMaxRows)
+    return launch_prep_cluster(x, residual, residual_out, w, sign, eps, M, K, norm_out, q,
+                               q_layout, sx, qsum, stream);
   // Rows resident at once with 256 threads: four per SM on 152 SMs.
   if (M < 4 * 152)
     return launch_prep<1024>(x, residual, residual_out, w, sign, eps, M, K, norm_out, q,
