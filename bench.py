@@ -478,7 +478,8 @@ def grouped_leg(args, dev, stream, timed, capture, mats, wbytes):
     """Activation groups of 64 and 32 on the step's attn_qkv shape and its
     rotated weight matrices (inputs larger than L2): pq2_mmv_grouped alone
     (back-to-back independent calls on pre-quantised activations) and
-    pq2_quantize_act_grouped, M = 1..4; GB/s of packed weight bytes."""
+    pq2_quantize_act_grouped, M = 1..4, 5 and 8 (M > 4: two passes over the
+    weights); GB/s of packed weight bytes."""
     import torch
     from ternary_weight_int8_gb300 import pq2, synth
     lib = pq2.lib()
@@ -490,7 +491,7 @@ def grouped_leg(args, dev, stream, timed, capture, mats, wbytes):
            "bytes_per_call": wbytes, "peak_gbs": hbm, "peak_source": hbm_kind, "by_a": {}}
     for A in (64, 32):
         by_m = {}
-        for M in MS:
+        for M in tuple(MS) + (5, 8):  # M > 4: two passes over the weights
             x = synth.activations(M, K_DIM, seed=500 + M + A, device=dev, outlier_frac=0.01)
             q, sx, qs = pq2.pq2_quantize_act_grouped(x, A, pq2.PQ2_Q_PLANES)
             y = torch.empty((M, N_DIM), dtype=torch.bfloat16, device=dev)

@@ -275,8 +275,11 @@ int pq2_quantize_act_grouped(const void *x, int x_dtype, int64_t ldx,
                              void *stream);
 
 /* pq2_mmv_grouped — pq2_mmv_ex (masked-plane decoder, flags) on activations
- * quantised by pq2_quantize_act_grouped with the same act_group; M 1..4.
- * Batch invariant like pq2_mmv.  Returns PQ2_ERR_SHAPE for M > 4 or another
+ * quantised by pq2_quantize_act_grouped with the same act_group; M 1..8.
+ * The kernel holds four columns' partial sums at most: M = 5..8 runs as two
+ * passes over the weights (columns 0..3, then 4..M-1), with the same bits as
+ * one pass (a column's result does not depend on the others).  Batch
+ * invariant like pq2_mmv.  Returns PQ2_ERR_SHAPE for M > 8 or another
  * act_group, else as pq2_mmv_ex. */
 int pq2_mmv_grouped(const int8_t *q_planes, const float *sx,
                     const int32_t *qsum, const uint8_t *codes,
@@ -286,7 +289,7 @@ int pq2_mmv_grouped(const int8_t *q_planes, const float *sx,
 
 /* The exact partial dots of pq2_mmv_grouped, dots[m][n][j] = sum over k in
  * [j*A, j*A + A) of (c_{n,k} - 1) q_{m,k}, from the same device code, for
- * parity checks (M 1..4, q in PQ2_Q_PLANES order, qsum from
+ * parity checks (M 1..8, q in PQ2_Q_PLANES order, qsum from
  * pq2_quantize_act_grouped).  dots (device) int32 [M][N][K / A]. */
 int pq2_debug_group_dots_grouped(const int8_t *q_planes, const int32_t *qsum,
                                  const uint8_t *codes, int64_t M, int64_t N,

@@ -209,30 +209,45 @@ int pq2_mmv_grouped(const int8_t* q, const float* sx, const int32_t* qsum, const
   if (int st = check_mmv_args(q, sx, qsum, codes, scales, y, y_dtype, M, N, K,
                               PQ2_DECODE_PLANES))
     return st;
-  if (M > 4 || (act_group != 128 && act_group != 64 && act_group != 32)) return PQ2_ERR_SHAPE;
+  if (act_group != 128 && act_group != 64 && act_group != 32) return PQ2_ERR_SHAPE;
   if (flags & ~(PQ2_MMV_OVERLAP_WEIGHTS | PQ2_MMV_INDEPENDENT)) return PQ2_ERR_DTYPE;
   int sms = 0;
   if (int st = device_check(&sms)) return st;
   const int overlap = (flags & PQ2_MMV_INDEPENDENT) ? 2 : (flags & PQ2_MMV_OVERLAP_WEIGHTS) ? 1 : 0;
-  return pq2::launch_mmv_grouped(q, sx, qsum, codes, scales, y, y_dtype, nullptr, M, N, K,
-                                 act_group, overlap, sms, dev_status,
-                                 static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The kernel holds at most four columns' partial sums: columns 4..M-1 run
+  // as a second pass over the weights.  A column's result does not depend on
+  // the others, so the bits are those of one pass.
+  const int64_t GA = K / act_group, first = M < 4 ? M : 4;
+  if (int st = pq2::launch_mmv_grouped(q, sx, qsum, codes, scales, y, y_dtype, nullptr, first, N,
+                                       K, act_group, overlap, sms, dev_status, s))
+    return st;
+  if (M == first) return PQ2_OK;
+  return pq2::launch_mmv_grouped(q + 4 * K, sx + 4 * GA, qsum + 4 * GA, codes, scales,
+                                 static_cast<uint8_t*>(y) + 4 * N * elem_bytes(y_dtype), y_dtype,
+                                 nullptr, M - 4, N, K, act_group, overlap, sms, dev_status, s);
 }
 
 int pq2_debug_group_dots_grouped(const int8_t* q, const int32_t* qsum, const uint8_t* codes,
                                  int64_t M, int64_t N, int64_t K, int act_group, int32_t* dots,
                                  int32_t* dev_status, void* stream) {
   if (!q || !qsum || !codes || !dots) return PQ2_ERR_NULL;
-  if (M < 1 || M > 4 || !valid_n(N) || !valid_k(K) ||
+  if (M < 1 || M > 8 || !valid_n(N) || !valid_k(K) ||
       (act_group != 128 && act_group != 64 && act_group != 32))
     return PQ2_ERR_SHAPE;
   if (!aligned(q, 16) || !aligned(codes, 16) || !aligned(dots, 4) || !aligned(qsum, 4))
     return PQ2_ERR_ALIGN;
   int sms = 0;
   if (int st = device_check(&sms)) return st;
-  return pq2::launch_mmv_grouped(q, nullptr, qsum, codes, nullptr, nullptr, PQ2_F32, dots, M, N,
-                                 K, act_group, 0, sms, dev_status,
-                                 static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t GA = K / act_group, first = M < 4 ? M : 4;
+  if (int st = pq2::launch_mmv_grouped(q, nullptr, qsum, codes, nullptr, nullptr, PQ2_F32, dots,
+                                       first, N, K, act_group, 0, sms, dev_status, s))
+    return st;
+  if (M == first) return PQ2_OK;
+  return pq2::launch_mmv_grouped(q + 4 * K, nullptr, qsum + 4 * GA, codes, nullptr, nullptr,
+                                 PQ2_F32, dots + 4 * N * GA, M - 4, N, K, act_group, 0, sms,
+                                 dev_status, s);
 }
 
 int pq2_ptq_prepare(const uint8_t* raw, int64_t raw_row_stride, int64_t N, int64_t K,

@@ -195,7 +195,7 @@ def test_grouped_validation(L):
         assert q(*bad) == err, (idx, val)
     m = L.pq2_mmv_grouped
     ok = [A, A, A, A, A, A, pq2.PQ2_F32, 4, 10, 256, 32, 0, None, None]
-    for idx, val, err in [(7, 5, pq2.PQ2_ERR_SHAPE), (10, 16, pq2.PQ2_ERR_SHAPE),
+    for idx, val, err in [(7, 9, pq2.PQ2_ERR_SHAPE), (10, 16, pq2.PQ2_ERR_SHAPE),
                           (11, 8, pq2.PQ2_ERR_DTYPE), (2, None, pq2.PQ2_ERR_NULL),
                           (3, A + 8, pq2.PQ2_ERR_ALIGN)]:
         bad = list(ok); bad[idx] = val

@@ -74,7 +74,7 @@ def test_quantize_grouped_128_is_the_plain_quantiser(M, K):
 
 
 @pytest.mark.parametrize("N,K", SHAPES)
-@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8])
 @pytest.mark.parametrize("A", [64, 32])
 def test_grouped_partial_dots_bitexact(N, K, M, A):
     raw, codes_o, scales_o = U.weights(N, K, seed=N * 3 + K + M + A, code_values=4)
@@ -88,7 +88,7 @@ def test_grouped_partial_dots_bitexact(N, K, M, A):
 
 
 @pytest.mark.parametrize("N,K", SHAPES)
-@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 6, 8])
 @pytest.mark.parametrize("A", [64, 32])
 def test_mmv_grouped_within_bound(N, K, M, A):
     raw, codes_o, scales_o = U.weights(N, K, seed=N + 5 * K + M + A)
@@ -132,26 +132,26 @@ def test_mmv_grouped_128_is_the_plain_gemv(N, K):
 @pytest.mark.parametrize("N,K", [(10240, 5120), (17408, 5120), (5120, 17408), (1000, 1152)])
 @pytest.mark.parametrize("A", [64, 32])
 def test_mmv_grouped_batch_invariance(N, K, A):
-    """Row j of the output is bit-identical for every M in 1..4, and equal to
-    the same activation row alone."""
+    """Row j of the output is bit-identical for every M in 1..8 (M > 4 runs
+    as two passes), and equal to the same activation row alone."""
     raw = synth.raw_weights(N, K, seed=N + A, device="cuda")
     codes, scales = pq2.pq2_prepare(raw, K)
-    x4 = synth.activations(4, K, seed=K + A, device="cuda", outlier_frac=0.01)
+    x8 = synth.activations(8, K, seed=K + A, device="cuda", outlier_frac=0.01)
     ref = None
-    for M in range(1, 5):
-        q, sx, qs = pq2.pq2_quantize_act_grouped(x4[:M].contiguous(), A, pq2.PQ2_Q_PLANES)
+    for M in range(1, 9):
+        q, sx, qs = pq2.pq2_quantize_act_grouped(x8[:M].contiguous(), A, pq2.PQ2_Q_PLANES)
         y = pq2.pq2_mmv_grouped(q, sx, qs, codes, scales, A)
         torch.cuda.synchronize()
         bits = y.cpu().numpy().view(np.uint32)
         if ref is None:
             ref = bits[0].copy()
         assert np.array_equal(bits[0], ref), M
-    q, sx, qs = pq2.pq2_quantize_act_grouped(x4, A, pq2.PQ2_Q_PLANES)
-    all4 = pq2.pq2_mmv_grouped(q, sx, qs, codes, scales, A).cpu().numpy().view(np.uint32)
-    for j in range(4):
-        q, sx, qs = pq2.pq2_quantize_act_grouped(x4[j:j + 1].contiguous(), A, pq2.PQ2_Q_PLANES)
+    q, sx, qs = pq2.pq2_quantize_act_grouped(x8, A, pq2.PQ2_Q_PLANES)
+    all8 = pq2.pq2_mmv_grouped(q, sx, qs, codes, scales, A).cpu().numpy().view(np.uint32)
+    for j in range(8):
+        q, sx, qs = pq2.pq2_quantize_act_grouped(x8[j:j + 1].contiguous(), A, pq2.PQ2_Q_PLANES)
         one = pq2.pq2_mmv_grouped(q, sx, qs, codes, scales, A).cpu().numpy().view(np.uint32)
-        assert np.array_equal(one[0], all4[j]), j
+        assert np.array_equal(one[0], all8[j]), j
 
 
 @pytest.mark.parametrize("A", [64, 32])
@@ -176,7 +176,7 @@ def test_mmv_grouped_full_size_sampled(A):
 
 def test_grouped_rejects_bad_arguments():
     lib = pq2.lib()
-    M, N, K = 5, 8, 256
+    M, N, K = 9, 8, 256
     x = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
     q = torch.zeros((M, K), dtype=torch.int8, device="cuda")
     sx = torch.zeros((M, 8), dtype=torch.float32, device="cuda")
@@ -198,7 +198,7 @@ def test_grouped_rejects_bad_arguments():
     assert quant(96) == pq2.PQ2_ERR_SHAPE
     assert quant(32, layout=9) == pq2.PQ2_ERR_DTYPE
     assert quant(32) == pq2.PQ2_OK
-    assert mmv(5, 32) == pq2.PQ2_ERR_SHAPE
+    assert mmv(9, 32) == pq2.PQ2_ERR_SHAPE
     assert mmv(4, 16) == pq2.PQ2_ERR_SHAPE
     assert mmv(4, 32, flags=64) == pq2.PQ2_ERR_DTYPE
     assert mmv(4, 32) == pq2.PQ2_OK
