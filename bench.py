@@ -1051,7 +1051,8 @@ def run_ours(args):
 def run_profile_case(args):
     """A short fixed sequence for an ncu capture: the attn_qkv GEMV
     (pq2_mmv, or pq2_mmv_tc for "mmvtc", INDEPENDENT calls over 8 rotated
-    matrices) or the ffn_up prefill
+    matrices), the fused preparation ("prep", K=5120 with a residual), or the
+    ffn_up prefill
     GEMM (pq2_mm, or pq2_mm_f8 for "mm8"), at --profile-m columns; 3 warm-up
     calls then 3 calls."""
     import torch
@@ -1071,6 +1072,18 @@ def run_profile_case(args):
         torch.cuda.synchronize()
         print(json.dumps({"profile_case": "ptq", "M": M, "N": N, "K": K, "act_group": A,
                           "launches": 6, "ok": True}))
+        return 0
+    if args.profile_case == "prep":
+        K = K_DIM
+        g = torch.Generator().manual_seed(17)
+        w = (torch.randn(K, generator=g) * 0.1).to(torch.bfloat16).to(dev)
+        sign = (torch.randint(0, 2, (K,), generator=g) * 2 - 1).to(torch.int8).to(dev)
+        xs = [synth.activations(M, K, seed=40 + i, device=dev).to(torch.bfloat16) for i in range(6)]
+        rs = [synth.activations(M, K, seed=80 + i, device=dev).to(torch.bfloat16) for i in range(6)]
+        for i in range(6):
+            pq2.pq2_norm_hadamard_quantize(xs[i], w, sign, 1e-6, residual=rs[i])
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_case": "prep", "M": M, "K": K, "launches": 6, "ok": True}))
         return 0
     if args.profile_case in ("mmv", "mmvtc"):
         K, N, nm = K_DIM, N_DIM, 8
@@ -1117,7 +1130,8 @@ def main():
                     help="skip the activation-group 64/32 (pq2_mmv_grouped) leg")
     ap.add_argument("--no-ptq", action="store_true",
                     help="skip the PTQ1_0 weight-format (pq2_ptq_mmv) leg")
-    ap.add_argument("--profile-case", choices=["mmv", "mmvtc", "mm", "mm8", "ptq"], default=None,
+    ap.add_argument("--profile-case", choices=["mmv", "mmvtc", "mm", "mm8", "ptq", "prep"],
+                    default=None,
                     help="run a short fixed call sequence for an ncu capture and exit")
     ap.add_argument("--profile-m", type=int, default=1, help="columns for --profile-case")
     ap.add_argument("--profile-act-group", type=int, default=32,
