@@ -30,7 +30,7 @@
 // One CTA computes a tile of 128 output rows x 128 tokens:
 //   warp 0      TMA producer: q tiles (two 64-column boxes per group, 128-byte
 //               swizzle, the canonical K-major layout) and code tiles
-//   warp 1      TMEM allocation; lane 0 issues the MMAs and commits
+//   warp 1      TMEM allocation; one elected lane issues the MMAs and commits
 //   warps 2-5   decoders: one weight row per thread, codes -> TMEM A tile
 //   warps 6-21  epilogue: one weight row and 32 tokens per thread, reads D
 //               (two buffers in flight, three on the 8-bit path), scales it
@@ -125,29 +125,54 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// D[tmem] (+)= A[tmem] * B[smem]^T, fp16 inputs, fp32 accumulation.
-__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                           uint32_t idesc, uint32_t accumulate) {
+// The MMA issue below is predicated, not branched: every lane of the MMA
+// warp runs the same instructions and only the lane that elect.sync picks
+// (`on` != 0) issues.  A branch around the issue (if lane == 0) made the
+// warp diverge and reconverge once per group, which cost more clocks per
+// group than the tensor pipe needs for the group's MMAs.
+__device__ __forceinline__ uint32_t elect_one() {
+  uint32_t r = 0;
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(r));
+  return r;
+}
+// D[tmem] (+)= A[tmem] * B[smem]^T, fp16 inputs, fp32 accumulation; issued
+// by the thread with on != 0.
+__device__ __forceinline__ void mma_f16_ta(uint32_t on, uint32_t d_tmem, uint32_t a_tmem,
+                                           uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(on)
       : "memory");
 }
-// D[tmem] (+)= A[tmem] * B[smem]^T, e4m3 inputs, fp32 accumulation.
-__device__ __forceinline__ void mma_f8_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                          uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem]^T, e4m3 inputs, fp32 accumulation; issued
+// by the thread with on != 0.
+__device__ __forceinline__ void mma_f8_ta(uint32_t on, uint32_t d_tmem, uint32_t a_tmem,
+                                          uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(on)
       : "memory");
 }
-// Arrive once on `bar` when every MMA issued so far by this thread is done.
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+// Arrive once on `bar` when every MMA issued so far by the issuing thread
+// (on != 0) is done.
+__device__ __forceinline__ void mma_commit(uint32_t on, uint64_t* bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+      "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar)),
+      "r"(on)
+      : "memory");
+}
+// One arrival on `bar` for the whole warp, by the lane elect.sync picks,
+// without a branch (the same release semantics as mbar_arrive).
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\t"
+      "@P mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_u32(bar))
       : "memory");
 }
 // Packed pairs of fp32 (element 0 in the low half): one instruction, two
@@ -378,33 +403,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tensor pipe idle between groups.  The scheduler warp does the waiting;
     // the two warps meet once per group at named barrier 1.
     constexpr uint32_t idesc = instr_desc_f16(BW, BT);
+    const uint32_t issuer = elect_one();
     for (int g = 0; g < G; ++g) {
       named_bar_sync(1, 64);
-      if (lane == 0) {
-        const int sq = g % kStagesQ, b = g % kABuf, db = g % kDBuf;
-        tc_fence_after();
-        // Between two MMAs of a group only an add: the descriptor's start
-        // address field is in 16-byte units.
-        const uint64_t qd = smem_desc_sw128(smem_u32(smem + kOffQ + sq * kQBytes));
-        const uint32_t d_tmem = tmem_base + kDCol + db * BT;
-        const uint32_t a_tmem = tmem_base + kACol + b * kACols;  // b = g % kABuf
+      const int sq = g % kStagesQ, b = g % kABuf, db = g % kDBuf;
+      tc_fence_after();
+      // Between two MMAs of a group only an add: the descriptor's start
+      // address field is in 16-byte units.
+      const uint64_t qd = smem_desc_sw128(smem_u32(smem + kOffQ + sq * kQBytes));
+      const uint32_t d_tmem = tmem_base + kDCol + db * BT;
+      const uint32_t a_tmem = tmem_base + kACol + b * kACols;  // b = g % kABuf
 #pragma unroll
-        for (int k = 0; k < kGroup / 16; ++k) {
-          // Step k reads B at atom k/4 (128 rows x 128 bytes), 32-byte offset
-          // (k%4) inside the swizzled row.  fp16: K step k, A columns
-          // 8k..8k+7.  e4m3: atom 0 is the 16a plane and atom 1 the b plane,
-          // K step k%4 of 32 elements, A columns 8(k%4)..+7 for both.
-          const uint64_t boff16 = (uint64_t)(((k >> 2) * (BT * 128) + (k & 3) * 32) >> 4);
-          if constexpr (F8)
-            mma_f8_ta(d_tmem, a_tmem + 8 * (k & 3), qd + boff16, idesc, k > 0 ? 1u : 0u);
-          else
-            mma_f16_ta(d_tmem, a_tmem + 8 * k, qd + boff16, idesc, k > 0 ? 1u : 0u);
-        }
-        // One commit per group tells the q producer, the decoders and the
-        // epilogue alike.
-        mma_commit(&g_done[g % kDone]);
+      for (int k = 0; k < kGroup / 16; ++k) {
+        // Step k reads B at atom k/4 (128 rows x 128 bytes), 32-byte offset
+        // (k%4) inside the swizzled row.  fp16: K step k, A columns
+        // 8k..8k+7.  e4m3: atom 0 is the 16a plane and atom 1 the b plane,
+        // K step k%4 of 32 elements, A columns 8(k%4)..+7 for both.
+        const uint64_t boff16 = (uint64_t)(((k >> 2) * (BT * 128) + (k & 3) * 32) >> 4);
+        if constexpr (F8)
+          mma_f8_ta(issuer, d_tmem, a_tmem + 8 * (k & 3), qd + boff16, idesc, k > 0 ? 1u : 0u);
+        else
+          mma_f16_ta(issuer, d_tmem, a_tmem + 8 * k, qd + boff16, idesc, k > 0 ? 1u : 0u);
       }
-      __syncwarp();
+      // One commit per group tells the q producer, the decoders and the
+      // epilogue alike.
+      mma_commit(issuer, &g_done[g % kDone]);
     }
   } else if (warp == kSchedWarp) {
     // ------------------------------------------------------------ scheduler
@@ -414,9 +437,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // wait that gives up (reported below) cannot leave the MMA warp stuck.
     for (int g = 0; g < G; ++g) {
       const int sq = g % kStagesQ, b = g % kABuf, db = g % kDBuf;
-      if (lane == 0) ok = ok && mbar_wait(&a_full[b], (g / kABuf) & 1);
-      if (lane == 1) ok = ok && mbar_wait(&q_full[sq], (g / kStagesQ) & 1);
-      if (lane == 2 && g >= kDBuf) ok = ok && mbar_wait(&d_empty[db], ((g / kDBuf) - 1) & 1);
+      // Lanes 0-2 wait at the same time, in one code path: three waits in
+      // three divergent branches cost several hundred clocks per group even
+      // when every phase has already completed.
+      uint64_t* bar = lane == 0 ? &a_full[b] : lane == 1 ? &q_full[sq] : &d_empty[db];
+      const uint32_t parity = lane == 0   ? (uint32_t)(g / kABuf) & 1u
+                              : lane == 1 ? (uint32_t)(g / kStagesQ) & 1u
+                                          : (uint32_t)((g / kDBuf) - 1) & 1u;
+      if (lane < 2 || (lane == 2 && g >= kDBuf)) ok = ok && mbar_wait(bar, parity);
       tc_fence_before();
       __syncwarp();
       named_bar_sync(1, 64);
@@ -456,10 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&c_empty[sc]);
-        mbar_arrive(&a_full[b]);
-      }
+      warp_arrive(&c_empty[sc]);
+      warp_arrive(&a_full[b]);
     }
   } else if (warp >= 6 && warp < 6 + kEpiWarps) {
     // ------------------------------------------------------------ epilogue
@@ -493,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // before every warp has released group g's buffer.
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&d_empty[db]);
+          warp_arrive(&d_empty[db]);
           continue;
         }
         const float* sxg = sxs + gg * BT + col0;
@@ -509,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // D has been read: release the buffer to the MMA before the math.
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&d_empty[db]);
+            warp_arrive(&d_empty[db]);
           }
 #pragma unroll
           for (int j4 = 0; j4 < 4; ++j4) {
@@ -535,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[slot]);
+      warp_arrive(&s_empty[slot]);
     }
     if (!DOTS && n < p.N) {
 #pragma unroll

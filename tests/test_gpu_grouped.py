@@ -38,7 +38,8 @@ def _oracle(x, codes_o, scales_o, A):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
-@pytest.mark.parametrize("M,K", [(1, 128), (3, 384), (4, 5120), (8, 1152), (64, 2048)])
+@pytest.mark.parametrize("M,K", [(1, 128), (3, 384), (4, 5120), (8, 1152), (64, 2048),
+                                 (13001, 384)])
 @pytest.mark.parametrize("A", [64, 32])
 def test_quantize_grouped_bitexact(dtype, M, K, A):
     x = synth.activations(M, K, seed=M * 7 + K + A, outlier_frac=0.01).to(dtype)

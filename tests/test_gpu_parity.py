@@ -80,6 +80,36 @@ def test_quantize_bitexact(dtype, M, K, ld_pad):
         assert np.array_equal(qs.cpu().numpy(), qs_o)
 
 
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("M,K,ld_pad", [(13001, 384, 0), (13001, 384, 3), (1024, 5120, 0)])
+def test_quantize_batched_bitexact(dtype, M, K, ld_pad):
+    """Enough groups for the quantiser to give each warp several of them
+    (39,003 groups, not a multiple of the batch; 40,960 groups of full rows):
+    the same bytes as the oracle in every layout."""
+    x = synth.activations(M, K, seed=M + K, outlier_frac=0.01, dtype=torch.float32)
+    x[:3] = _tie_rows(K, torch.float32)
+    x = x.to(dtype)
+    xs = torch.zeros((M, K + ld_pad), dtype=dtype, device="cuda")
+    xs[:, :K] = x.cuda()
+    xv = xs[:, :K]
+    q_o, sx_o = O.quantize(O.widen(U.x_bits(x), U.kind(x)))
+    qs_o = O.qsum(q_o)
+    for layout in (pq2.PQ2_Q_ROWS, pq2.PQ2_Q_PLANES, pq2.PQ2_Q_F16, pq2.PQ2_Q_F8):
+        q, sx, qs = pq2.pq2_quantize_act(xv, layout)
+        torch.cuda.synchronize()
+        if layout == pq2.PQ2_Q_ROWS:
+            assert np.array_equal(q.cpu().numpy(), q_o)
+        elif layout == pq2.PQ2_Q_PLANES:
+            assert np.array_equal(q.cpu().numpy(), O.q_planes(q_o))
+        elif layout == pq2.PQ2_Q_F8:
+            assert np.array_equal(q.cpu().numpy(), U.mm_operand_order_f8(q_o))
+        else:
+            assert np.array_equal(q.cpu().float().numpy(),
+                                  U.mm_operand_order(q_o).astype(np.float32))
+        assert np.array_equal(sx.cpu().numpy().view(np.uint32), sx_o.view(np.uint32))
+        assert np.array_equal(qs.cpu().numpy(), qs_o)
+
 # ----------------------------------------------------------------- mmv
 MMV_SHAPES = [(1, 128), (5, 384), (153, 256), (1000, 1152), (2048, 4096), (613, 17408)]
 
