@@ -48,6 +48,26 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
                : "memory");
 }
 
+// One arrival on `bar` for the whole warp, made by the lane that elect.sync
+// picks, without a branch: a warp that branches around a single lane's
+// arrival diverges and reconverges, which costs more than the arrival.  The
+// same release semantics as mbar_arrive.  Every lane of the warp must call it.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\t"
+      "@P mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+// As warp_arrive, made only when `on` (the same in every lane) is non-zero.
+__device__ __forceinline__ void warp_arrive_if(uint32_t on, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred P, Q;\n\telect.sync _|P, 0xffffffff;\n\tsetp.ne.b32 Q, %1, 0;\n\t"
+      "and.pred P, P, Q;\n\t@P mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n\t}" ::"r"(
+          smem_u32(bar)),
+      "r"(on)
+      : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t done;
   asm volatile(

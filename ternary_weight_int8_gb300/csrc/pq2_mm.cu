@@ -167,14 +167,6 @@ __device__ __forceinline__ void mma_commit(uint32_t on, uint64_t* bar) {
       "r"(on)
       : "memory");
 }
-// One arrival on `bar` for the whole warp, by the lane elect.sync picks,
-// without a branch (the same release semantics as mbar_arrive).
-__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
-  asm volatile(
-      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\t"
-      "@P mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_u32(bar))
-      : "memory");
-}
 // Packed pairs of fp32 (element 0 in the low half): one instruction, two
 // IEEE round-to-nearest results, the same as two scalar operations.
 __device__ __forceinline__ uint64_t f2_pack(uint32_t lo, uint32_t hi) {

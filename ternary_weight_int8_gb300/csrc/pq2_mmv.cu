@@ -516,7 +516,7 @@ __global__ void __launch_bounds__(DEC == kDecodeTensor ? kTcBlock : kMaxBlock,
       }
       cp_async_mbar_arrive(&full[slot]);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&full[slot]);
+      warp_arrive(&full[slot]);
     };
     // Stages that fit the ring go out at once: each stage's weights and then
     // its inputs (an independent call), or every stage's weights now and the
@@ -706,7 +706,7 @@ __global__ void __launch_bounds__(DEC == kDecodeTensor ? kTcBlock : kMaxBlock,
       }
       if (recycle) {
         __syncwarp();
-        if (lane == 0 && !(i == p.drop_stage && warp == 0)) mbar_arrive(&empty[slot]);
+        warp_arrive_if(!(i == p.drop_stage && warp == 0), &empty[slot]);
       }
     }
     if (!ok && lane == 0) report(p.status, PQ2_ERR_TIMEOUT);
@@ -878,7 +878,7 @@ __global__ void __launch_bounds__(DEC == kDecodeTensor ? kTcBlock : kMaxBlock,
     }
     if (recycle) {
       __syncwarp();
-      if (lane == 0 && !(i == p.drop_stage && warp == 0)) mbar_arrive(&empty[slot]);
+      warp_arrive_if(!(i == p.drop_stage && warp == 0), &empty[slot]);
     }
   }
   if (!ok && lane == 0) report(p.status, PQ2_ERR_TIMEOUT);
