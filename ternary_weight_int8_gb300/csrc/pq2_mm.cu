@@ -90,6 +90,7 @@ struct MmParams {
   int32_t* status;
   int M, N, K, G;
   int y_bf16;
+  int vec_scales;  // G % kGC == 0 and s_x / s_w 16- / 8-byte aligned: vector staging
 };
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
@@ -360,33 +361,78 @@ __global__ void __launch_bounds__(kThreads, 1)
     // of its own: the waits for a free slot (the epilogue's pace) never
     // delay the TMA issue of codes and q.
     const int nchunks = (G + kGC - 1) / kGC;
-    constexpr int kPer = kGC * BT / 32;
-    float xv[kPer];
-    uint16_t wv[kPer];
-    auto load_scales = [&](int ch) {
+    if (p.vec_scales) {
+      // Lane l stages tokens l + 32u and weight rows l + 32u: the kGC scales
+      // of one token (or one row) are consecutive in memory, so each is one
+      // 16-byte (8-byte) load, against kGC strided loads.  Every chunk is
+      // full (G % kGC == 0).
+      float4 xv[BT / 32];
+      uint2 wv[BW / 32];
+      auto load_scales = [&](int ch) {
 #pragma unroll
-      for (int j = 0; j < kPer; ++j) {
-        const int idx = lane + 32 * j;  // idx = gg * BT + t
-        const int gg = idx / BT, t = idx % BT, g = ch * kGC + gg, m = m0 + t;
-        xv[j] = (!DOTS && g < G && m < p.M) ? __ldg(p.sx + (size_t)m * G + g) : 0.0f;
-        const int r = idx / kGC, gw = ch * kGC + idx % kGC, n = n0 + r;  // idx = r*kGC + gg
-        wv[j] = (!DOTS && gw < G && n < p.N) ? __ldg(p.scales + (size_t)n * G + gw)
-                                             : (uint16_t)0;
-      }
-    };
-    load_scales(0);
-    for (int ch = 0; ch < nchunks; ++ch) {
-      const int slot = ch & 1;
-      if (ch >= 2) ok = ok && mbar_wait(&s_empty[slot], ((ch >> 1) - 1) & 1);
-      float* sxs = reinterpret_cast<float*>(smem + kOffS + slot * kSBytes);  // [kGC][BT]
-      uint16_t* sws = reinterpret_cast<uint16_t*>(smem + kOffS + slot * kSBytes + kSxBytes);
+        for (int u = 0; u < BT / 32; ++u) {
+          const int m = m0 + lane + 32 * u;
+          xv[u] = (!DOTS && m < p.M)
+                      ? __ldg(reinterpret_cast<const float4*>(p.sx + (size_t)m * G + ch * kGC))
+                      : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
 #pragma unroll
-      for (int j = 0; j < kPer; ++j) {
-        sxs[lane + 32 * j] = xv[j];
-        sws[lane + 32 * j] = wv[j];
+        for (int u = 0; u < BW / 32; ++u) {
+          const int n = n0 + lane + 32 * u;
+          wv[u] = (!DOTS && n < p.N)
+                      ? __ldg(reinterpret_cast<const uint2*>(p.scales + (size_t)n * G + ch * kGC))
+                      : make_uint2(0u, 0u);
+        }
+      };
+      load_scales(0);
+      for (int ch = 0; ch < nchunks; ++ch) {
+        const int slot = ch & 1;
+        if (ch >= 2) ok = ok && mbar_wait(&s_empty[slot], ((ch >> 1) - 1) & 1);
+        float* sxs = reinterpret_cast<float*>(smem + kOffS + slot * kSBytes);  // [kGC][BT]
+        uint16_t* sws = reinterpret_cast<uint16_t*>(smem + kOffS + slot * kSBytes + kSxBytes);
+#pragma unroll
+        for (int u = 0; u < BT / 32; ++u) {
+          const int t = lane + 32 * u;
+          sxs[0 * BT + t] = xv[u].x;
+          sxs[1 * BT + t] = xv[u].y;
+          sxs[2 * BT + t] = xv[u].z;
+          sxs[3 * BT + t] = xv[u].w;
+        }
+#pragma unroll
+        for (int u = 0; u < BW / 32; ++u)
+          *reinterpret_cast<uint2*>(sws + (lane + 32 * u) * kGC) = wv[u];  // [BW][kGC]
+        mbar_arrive(&s_full[slot]);
+        if (ch + 1 < nchunks) load_scales(ch + 1);
       }
-      mbar_arrive(&s_full[slot]);
-      if (ch + 1 < nchunks) load_scales(ch + 1);
+    } else {
+      constexpr int kPer = kGC * BT / 32;
+      float xv[kPer];
+      uint16_t wv[kPer];
+      auto load_scales = [&](int ch) {
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+          const int idx = lane + 32 * j;  // idx = gg * BT + t
+          const int gg = idx / BT, t = idx % BT, g = ch * kGC + gg, m = m0 + t;
+          xv[j] = (!DOTS && g < G && m < p.M) ? __ldg(p.sx + (size_t)m * G + g) : 0.0f;
+          const int r = idx / kGC, gw = ch * kGC + idx % kGC, n = n0 + r;  // idx = r*kGC + gg
+          wv[j] = (!DOTS && gw < G && n < p.N) ? __ldg(p.scales + (size_t)n * G + gw)
+                                               : (uint16_t)0;
+        }
+      };
+      load_scales(0);
+      for (int ch = 0; ch < nchunks; ++ch) {
+        const int slot = ch & 1;
+        if (ch >= 2) ok = ok && mbar_wait(&s_empty[slot], ((ch >> 1) - 1) & 1);
+        float* sxs = reinterpret_cast<float*>(smem + kOffS + slot * kSBytes);  // [kGC][BT]
+        uint16_t* sws = reinterpret_cast<uint16_t*>(smem + kOffS + slot * kSBytes + kSxBytes);
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+          sxs[lane + 32 * j] = xv[j];
+          sws[lane + 32 * j] = wv[j];
+        }
+        mbar_arrive(&s_full[slot]);
+        if (ch + 1 < nchunks) load_scales(ch + 1);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
@@ -669,6 +715,8 @@ int launch_mm(const void* q_op, bool f8, const float* sx, const int32_t* qsum,
   p.sx = sx; p.scales = scales; p.y = y; p.dots = dots; p.status = status;
   p.M = (int)M; p.N = (int)N; p.K = (int)K; p.G = (int)(K / kGroup);
   p.y_bf16 = y_dtype == PQ2_BF16;
+  p.vec_scales = (p.G % kGC == 0) && reinterpret_cast<uintptr_t>(sx) % 16 == 0 &&
+                 reinterpret_cast<uintptr_t>(scales) % 8 == 0;
   if (f8)
     return dots ? launch_mm_t<true, true>(mq, mc, p, stream)
                 : launch_mm_t<false, true>(mq, mc, p, stream);

@@ -16,11 +16,6 @@
 namespace pq2 {
 namespace {
 
-// Groups per warp of the quantiser for many rows, and the warps one wave of
-// the GPU holds (152 SMs x 64 resident warps): the batching threshold only.
-constexpr int kQuantBatch = 4;
-constexpr int64_t kQuantWarpsPerWave = 152 * 64;
-
 // One thread per 34-byte block: bytes 0-1 are the little-endian fp16 scale,
 // bytes 2..33 the 32 code bytes (weight k in bits 2(k%4) of byte k/4).
 // Raw rows have an arbitrary byte stride, so the block is read bytewise; the
@@ -91,16 +86,10 @@ __device__ __forceinline__ void load4(const void* x, int64_t i, bool vec,
   }
 }
 
-// One warp per U consecutive (row m, 128-group g) pairs of the row-major
-// group index m * G + g; lane L owns elements 4L..4L+3 of each group
-// (quantize_group4 / store_group4), in activation groups of 4 * LANES
-// elements: sx and qsum are [M][K / (4 * LANES)].  The warp issues the loads
-// of all its U groups before it quantises the first, so that U * 256 bytes of
-// a bf16 row are in flight per warp: with U = 1 a full SM keeps about 16 KB
-// of reads outstanding, too few to cover the memory latency at HBM rate when
-// many rows are quantised.  U changes which warp handles a group, never its
-// arithmetic.
-template <int XT, int LANES, int U>
+// One warp per (row m, 128-group g); lane L owns elements 4L..4L+3 of the
+// group (quantize_group4 / store_group4), in activation groups of 4 * LANES
+// elements: sx and qsum are [M][K / (4 * LANES)].
+template <int XT, int LANES>
 __global__ void __launch_bounds__(256) quantize_kernel(
     const void* __restrict__ x, int64_t ldx, int64_t M, int G, bool vec,
     void* __restrict__ q, int layout, float* __restrict__ sx,
@@ -112,32 +101,19 @@ __global__ void __launch_bounds__(256) quantize_kernel(
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t total = M * G, first = warp * U;
-  if (first >= total) return;
+  if (warp >= M * G) return;
+  const int64_t m = warp / G;
+  const int g = (int)(warp % G);
   const int64_t K = (int64_t)G * kGroup;
+
+  float a[4];
+  load4<XT>(x, m * ldx + (int64_t)g * kGroup + 4 * lane, vec, a);
   constexpr int NSUB = 32 / LANES;  // activation groups per 128-group
-  float a[U][4];
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const int64_t gi = first + u;
-    if (gi < total) {
-      const int64_t m = gi / G;
-      const int g = (int)(gi - m * G);
-      load4<XT>(x, m * ldx + (int64_t)g * kGroup + 4 * lane, vec, a[u]);
-    }
-  }
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const int64_t gi = first + u;
-    if (gi >= total) break;  // uniform across the warp
-    const int64_t m = gi / G;
-    const int g = (int)(gi - m * G);
-    int qi[4];
-    const float s = quantize_group4<LANES>(a[u], qi);
-    store_group4<LANES>(qi, lane, q, layout, m * K + (int64_t)g * kGroup,
-                        qsum ? qsum + gi * NSUB : nullptr);
-    if (lane % LANES == 0) sx[gi * NSUB + lane / LANES] = s;
-  }
+  int qi[4];
+  const float s = quantize_group4<LANES>(a, qi);
+  store_group4<LANES>(qi, lane, q, layout, m * K + (int64_t)g * kGroup,
+                      qsum ? qsum + (m * G + g) * NSUB : nullptr);
+  if (lane % LANES == 0) sx[(m * G + g) * NSUB + lane / LANES] = s;
 }
 
 }  // namespace
@@ -154,32 +130,21 @@ int launch_prepare(const uint8_t* raw, int64_t raw_stride, int64_t N,
 
 namespace {
 
-template <int XT, int U>
-cudaError_t launch_quantize_xu(const cudaLaunchConfig_t& cfg, int act_group, const void* x,
+template <int XT>
+cudaError_t launch_quantize_xt(const cudaLaunchConfig_t& cfg, int act_group, const void* x,
                                int64_t ldx, int64_t M, int G, bool vec, void* q, int q_layout,
                                float* sx, int32_t* qsum) {
   switch (act_group) {
     case 64:
-      return cudaLaunchKernelEx(&cfg, quantize_kernel<XT, 16, U>, x, ldx, M, G, vec, q, q_layout,
-                                sx, qsum);
+      return cudaLaunchKernelEx(&cfg, quantize_kernel<XT, 16>, x, ldx, M, G, vec, q, q_layout, sx,
+                                qsum);
     case 32:
-      return cudaLaunchKernelEx(&cfg, quantize_kernel<XT, 8, U>, x, ldx, M, G, vec, q, q_layout,
-                                sx, qsum);
+      return cudaLaunchKernelEx(&cfg, quantize_kernel<XT, 8>, x, ldx, M, G, vec, q, q_layout, sx,
+                                qsum);
     default:
-      return cudaLaunchKernelEx(&cfg, quantize_kernel<XT, 32, U>, x, ldx, M, G, vec, q, q_layout,
-                                sx, qsum);
+      return cudaLaunchKernelEx(&cfg, quantize_kernel<XT, 32>, x, ldx, M, G, vec, q, q_layout, sx,
+                                qsum);
   }
-}
-
-template <int XT>
-cudaError_t launch_quantize_xt(const cudaLaunchConfig_t& cfg, int u, int act_group, const void* x,
-                               int64_t ldx, int64_t M, int G, bool vec, void* q, int q_layout,
-                               float* sx, int32_t* qsum) {
-  return u == kQuantBatch
-             ? launch_quantize_xu<XT, kQuantBatch>(cfg, act_group, x, ldx, M, G, vec, q,
-                                                   q_layout, sx, qsum)
-             : launch_quantize_xu<XT, 1>(cfg, act_group, x, ldx, M, G, vec, q, q_layout, sx,
-                                         qsum);
 }
 
 }  // namespace
@@ -191,12 +156,7 @@ int launch_quantize(const void* x, int x_dtype, int64_t ldx, int64_t M,
   const int elem = x_dtype == PQ2_F32 ? 4 : 2;
   const uintptr_t addr = reinterpret_cast<uintptr_t>(x);
   const bool vec = (addr % (4 * elem) == 0) && (ldx % 4 == 0);
-  // Groups per warp: one while the grid holds fewer groups than
-  // kQuantBatch full waves of warps (small M: every warp's latency counts),
-  // kQuantBatch beyond that.
-  const int64_t groups = M * G;
-  const int u = groups >= (int64_t)kQuantBatch * kQuantWarpsPerWave ? kQuantBatch : 1;
-  const int64_t warps = (groups + u - 1) / u;
+  const int64_t warps = M * G;
   const unsigned blocks = (unsigned)((warps + 7) / 8);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(blocks);
@@ -210,13 +170,13 @@ int launch_quantize(const void* x, int x_dtype, int64_t ldx, int64_t M,
   cudaError_t e;
   switch (x_dtype) {
     case PQ2_BF16:
-      e = launch_quantize_xt<PQ2_BF16>(cfg, u, act_group, x, ldx, M, G, vec, q, q_layout, sx, qsum);
+      e = launch_quantize_xt<PQ2_BF16>(cfg, act_group, x, ldx, M, G, vec, q, q_layout, sx, qsum);
       break;
     case PQ2_F16:
-      e = launch_quantize_xt<PQ2_F16>(cfg, u, act_group, x, ldx, M, G, vec, q, q_layout, sx, qsum);
+      e = launch_quantize_xt<PQ2_F16>(cfg, act_group, x, ldx, M, G, vec, q, q_layout, sx, qsum);
       break;
     default:
-      e = launch_quantize_xt<PQ2_F32>(cfg, u, act_group, x, ldx, M, G, vec, q, q_layout, sx, qsum);
+      e = launch_quantize_xt<PQ2_F32>(cfg, act_group, x, ldx, M, G, vec, q, q_layout, sx, qsum);
       break;
   }
   if (e != cudaSuccess) {
