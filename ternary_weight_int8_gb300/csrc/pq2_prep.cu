@@ -46,6 +46,31 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
+// The bf16 value with bits b times the sign +1 / -1 held in the int8 s:
+// exact, so a flip of the sign bit.
+__device__ __forceinline__ float bf16_signed(uint16_t b, int8_t s) {
+  return __uint_as_float(((uint32_t)b << 16) ^ (((uint32_t)(uint8_t)s & 0x80u) << 24));
+}
+// One butterfly half: the lower lane of a pair keeps a + o, the upper o - a.
+// With sgn = +1 / -1, fma(a, sgn, o) rounds a * sgn + o once and a * sgn is
+// exact, so it equals __fadd_rn(a, o) / __fsub_rn(o, a), signed zeros
+// included, in one instruction instead of a select between two.
+__device__ __forceinline__ float butterfly(float a, float o, float sgn) {
+  return __fmaf_rn(a, sgn, o);
+}
+// Packed pairs of fp32 (element 0 in the low half): one instruction, two
+// IEEE round-to-nearest results, the same as two scalar operations.
+__device__ __forceinline__ void add_sub_f32x2(float& a0, float& a1, float& c0, float& c1) {
+  uint64_t a = ((uint64_t)__float_as_uint(a1) << 32) | __float_as_uint(a0);
+  uint64_t c = ((uint64_t)__float_as_uint(c1) << 32) | __float_as_uint(c0);
+  uint64_t sum, dif;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(sum) : "l"(a), "l"(c));
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(dif) : "l"(a), "l"(c));
+  a0 = __uint_as_float((uint32_t)sum);
+  a1 = __uint_as_float((uint32_t)(sum >> 32));
+  c0 = __uint_as_float((uint32_t)dif);
+  c1 = __uint_as_float((uint32_t)(dif >> 32));
+}
 
 // The transform of every 1024-block of a row by W warps per block (W = 2, 4
 // or 8): warp u of block b holds the elements b + (1024/W) u + 32 i + l,
@@ -96,19 +121,19 @@ __device__ __forceinline__ void transform_shared(float* hs, const TransformOpera
     for (int i = 0; i < E; ++i) {
       const int j = base + 32 * i + lane;
       const float w1 = __fadd_rn(bf16_bits_to_float((uint16_t)(o.wb[i / 2] >> (16 * (i & 1)))), 1.0f);
-      const float sg = (float)(int8_t)(uint8_t)(o.sb[i / 4] >> (8 * (i & 3)));
+      const int8_t sg = (int8_t)(uint8_t)(o.sb[i / 4] >> (8 * (i & 3)));
       const float tn = __fmul_rn(__fmul_rn(hs[j], inv), w1);
       const uint16_t nb = float_to_bf16_bits(tn);
       if (norm_out) norm_out[m * K + j] = nb;
-      r[i] = bf16_bits_to_float(nb) * sg;  // exact: the sign is +-1
+      r[i] = bf16_signed(nb, sg);  // exact: the sign is +-1
     }
 #pragma unroll
     for (int h = 1; h < 32; h <<= 1) {
-      const bool upper = (lane & h) != 0;
+      const float sgn = (lane & h) ? -1.0f : 1.0f;
 #pragma unroll
       for (int i = 0; i < E; ++i) {
         const float o = __shfl_xor_sync(0xffffffffu, r[i], h);
-        r[i] = upper ? __fsub_rn(o, r[i]) : __fadd_rn(r[i], o);
+        r[i] = butterfly(r[i], o, sgn);
       }
     }
 #pragma unroll
@@ -332,28 +357,33 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepThreads == 256 ? 4 : 1)
             __fmul_rn(__fmul_rn(hs[j], inv), __fadd_rn(bf16_bits_to_float(w[j]), 1.0f));
         const uint16_t nb = float_to_bf16_bits(tn);
         if (norm_out) norm_out[m * K + j] = nb;
-        r[i] = bf16_bits_to_float(nb) * (float)sign[j];  // exact: the sign is +-1
+        r[i] = bf16_signed(nb, sign[j]);  // exact: the sign is +-1
       }
       // Passes of half-width 1..16 pair lanes l and l ^ h (the lower lane of a
       // pair keeps a + c, the upper a - c) ...
 #pragma unroll
       for (int h = 1; h < 32; h <<= 1) {
-        const bool upper = (lane & h) != 0;
+        const float sgn = (lane & h) ? -1.0f : 1.0f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float o = __shfl_xor_sync(0xffffffffu, r[i], h);
-          r[i] = upper ? __fsub_rn(o, r[i]) : __fadd_rn(r[i], o);
+          r[i] = butterfly(r[i], o, sgn);
         }
       }
-      // ... those of 32..512 pair registers i and i + h/32 of one lane.
+      // ... those of 32..512 pair registers i and i + h/32 of one lane
+      // (half-width 64 and up on packed pairs of registers).
 #pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
+      for (int i = 0; i < 32; i += 2) {
+        const float a = r[i], c = r[i + 1];
+        r[i] = __fadd_rn(a, c);
+        r[i + 1] = __fsub_rn(a, c);
+      }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+      for (int d = 2; d < 32; d <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
           if (i & d) continue;
-          const float a = r[i], c = r[i + d];
-          r[i] = __fadd_rn(a, c);
-          r[i + d] = __fsub_rn(a, c);
+          add_sub_f32x2(r[i], r[i + 1], r[i + d], r[i + d + 1]);
         }
       }
 #pragma unroll
@@ -362,15 +392,39 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepThreads == 256 ? 4 : 1)
     }
     __syncthreads();
   }
-  // Pass 3: the row's 128-groups shared by all warps.
-  for (int gi = warp; gi < G; gi += kPrepWarps) {
-    const float4 v4 = *reinterpret_cast<const float4*>(hs + gi * kGroup + 4 * lane);
-    const float a[4] = {v4.x, v4.y, v4.z, v4.w};
-    int qi[4];
-    const float s = quantize_group4(a, qi);
-    store_group4(qi, lane, q, layout, m * K + (int64_t)gi * kGroup,
-                 qsum ? qsum + m * G + gi : nullptr);
-    if (lane == 0) sx[m * G + gi] = s;
+  // Pass 3: the row's 128-groups shared by all warps, four per warp with
+  // eight lanes per group (lane j holds elements 16j..16j+15) where the
+  // layout allows it: a quarter of the warp instructions per group of one
+  // group per warp, which is kept for the tensor-core GEMV's layout.
+  if (layout != PQ2_Q_MMV16 && (reinterpret_cast<uintptr_t>(q) & 15) == 0) {
+    const int j = lane & 7;
+    for (int g4 = 4 * warp; g4 < G; g4 += 4 * kPrepWarps) {
+      const int gi = g4 + (lane >> 3);
+      const bool valid = gi < G;  // lanes past the row keep the warp's shuffles
+      const float4* src =
+          reinterpret_cast<const float4*>(hs + (valid ? gi : 0) * kGroup + 16 * j);
+      float a[16];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4 v = src[k];
+        a[4 * k] = v.x; a[4 * k + 1] = v.y; a[4 * k + 2] = v.z; a[4 * k + 3] = v.w;
+      }
+      int qi[16];
+      const float s = quantize_group16<8>(a, qi);
+      store_group16<8>(qi, j, valid, q, layout, m * K + (int64_t)gi * kGroup,
+                       qsum ? qsum + m * G + gi : nullptr);
+      if (valid && j == 0) sx[m * G + gi] = s;
+    }
+  } else {
+    for (int gi = warp; gi < G; gi += kPrepWarps) {
+      const float4 v4 = *reinterpret_cast<const float4*>(hs + gi * kGroup + 4 * lane);
+      const float a[4] = {v4.x, v4.y, v4.z, v4.w};
+      int qi[4];
+      const float s = quantize_group4(a, qi);
+      store_group4(qi, lane, q, layout, m * K + (int64_t)gi * kGroup,
+                   qsum ? qsum + m * G + gi : nullptr);
+      if (lane == 0) sx[m * G + gi] = s;
+    }
   }
 }
 

@@ -175,4 +175,117 @@ __device__ __forceinline__ void store_group4(const int qi[4], int lane, void* q,
   if (qsum && lane % LANES == 0) qsum[lane / LANES] = t;
 }
 
+// ------------------------------------------------------------------------
+// The same quantisation with eight lanes per 128-group: lane j = L % 8 of a
+// group's eight lanes holds its elements 16j..16j+15, so a warp quantises
+// four groups at once.  The per-element arithmetic is quantize_group4's; the
+// reductions run over 8 lanes instead of 32 and the output layouts (except
+// the tensor-core GEMV's PQ2_Q_MMV16) are assembled inside the lane, so a
+// group costs about a quarter of the warp instructions.  Activation groups of
+// 16 * LG elements (LG = 8, 4, 2 lanes: 128, 64, 32); groups of LG lanes are
+// aligned.  Every lane of the warp must call it.
+template <int LG = 8>
+__device__ __forceinline__ float quantize_group16(const float (&a)[16], int (&qi)[16]) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(a[i]));
+#pragma unroll
+  for (int off = LG / 2; off > 0; off >>= 1)
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const float s = __fdiv_rn(amax, 127.0f);
+  const float d = s > 0.0f ? s : 1.0f;
+  const float inv = __frcp_rn(d);
+  bool near_tie = d < 7.52316385e-37f;  // 2^-120
+  float r[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float t = __fmul_rn(a[i], inv);
+    r[i] = rintf(t);
+    near_tie |= fabsf(t - r[i]) > 0.4999f;
+  }
+  // Any near tie in the warp sends all its groups through the IEEE
+  // divisions, which give the same q wherever the product is not near a tie.
+  if (__any_sync(0xffffffffu, near_tie)) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) r[i] = rintf(__fdiv_rn(a[i], d));
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) qi[i] = (int)fminf(fmaxf(r[i], -127.0f), 127.0f);
+  return s;
+}
+
+// Store the sixteen q of lane j (elements 16j..16j+15 of the 128-group that
+// starts at element `base` of q) in the requested layout (not PQ2_Q_MMV16),
+// and sum(q) of each activation group of 16 * LG elements (to qsum[0 ..
+// 8 / LG - 1] when non-null, which `store` says for this lane's group).  The
+// layouts are those of store_group4.  Every lane of the warp must call it.
+template <int LG = 8>
+__device__ __forceinline__ void store_group16(const int (&qi)[16], int j, bool store, void* q,
+                                              int layout, int64_t base, int32_t* qsum) {
+  auto byte = [&](int i) { return (uint32_t)(qi[i] & 0xff); };
+  if (store) {
+    if (layout == PQ2_Q_ROWS) {
+      uint32_t w[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        w[k] = byte(4 * k) | (byte(4 * k + 1) << 8) | (byte(4 * k + 2) << 16) |
+               (byte(4 * k + 3) << 24);
+      reinterpret_cast<uint4*>(static_cast<int8_t*>(q) + base)[j] =
+          make_uint4(w[0], w[1], w[2], w[3]);
+    } else if (layout == PQ2_Q_PLANES) {
+      // Plane word (s, w) = q[16w + 4b + s], b = 0..3, is word 8s + w of the
+      // group: chunk w = j holds all four of its bytes.
+      uint32_t* out = reinterpret_cast<uint32_t*>(static_cast<int8_t*>(q) + base);
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+        out[8 * s + j] =
+            byte(s) | (byte(4 + s) << 8) | (byte(8 + s) << 16) | (byte(12 + s) << 24);
+    } else if (layout == PQ2_Q_F8) {
+      // Word c of chunk j in each plane holds the chunk's elements
+      // 8(c >> 1) + (c & 1) + 2e, e = 0..3 (16a plane, then the b plane).
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        hi[c] = 0;
+        lo[c] = 0;
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+          const int i0 = 8 * (c >> 1) + (c & 1) + 2 * e, i1 = i0 + 2;
+          const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(
+              make_float2((float)(16 * (qi[i0] >> 4)), (float)(16 * (qi[i1] >> 4))),
+              __NV_SATFINITE, __NV_E4M3);
+          const __nv_fp8x2_storage_t l2 = __nv_cvt_float2_to_fp8x2(
+              make_float2((float)(qi[i0] & 15), (float)(qi[i1] & 15)), __NV_SATFINITE,
+              __NV_E4M3);
+          hi[c] |= (uint32_t)h2 << (8 * e);
+          lo[c] |= (uint32_t)l2 << (8 * e);
+        }
+      }
+      uint4* out = reinterpret_cast<uint4*>(static_cast<uint8_t*>(q) + 2 * base);
+      out[j] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      out[8 + j] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    } else {
+      // Prefill MMA operand order: element 4b + s of the chunk goes to
+      // position 4s + 2(b & 1) + (b >> 1).
+      uint32_t h[8];
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const __half2 p01 = __halves2half2(__int2half_rn(qi[s]), __int2half_rn(qi[8 + s]));
+        const __half2 p23 = __halves2half2(__int2half_rn(qi[4 + s]), __int2half_rn(qi[12 + s]));
+        h[2 * s] = *reinterpret_cast<const uint32_t*>(&p01);
+        h[2 * s + 1] = *reinterpret_cast<const uint32_t*>(&p23);
+      }
+      uint4* out = reinterpret_cast<uint4*>(static_cast<__half*>(q) + base);
+      out[2 * j] = make_uint4(h[0], h[1], h[2], h[3]);
+      out[2 * j + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+    }
+  }
+  int t = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) t += qi[i];
+#pragma unroll
+  for (int off = LG / 2; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+  if (store && qsum && j % LG == 0) qsum[j / LG] = t;
+}
+
 }  // namespace pq2

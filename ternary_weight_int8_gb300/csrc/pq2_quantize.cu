@@ -116,6 +116,58 @@ __global__ void __launch_bounds__(256) quantize_kernel(
   if (lane % LANES == 0) sx[(m * G + g) * NSUB + lane / LANES] = s;
 }
 
+// Many rows: eight lanes per (row m, 128-group g), four consecutive groups
+// of the row-major group index per warp (quantize_group16 / store_group16);
+// lane j = L % 8 loads its group's elements 16j..16j+15 with 16-byte loads
+// (the host guarantees the alignment).  The same bytes as quantize_kernel, in
+// about a quarter of its instructions per group.  Not for PQ2_Q_MMV16.
+template <int XT, int LG>
+__global__ void __launch_bounds__(256) quantize16_kernel(
+    const void* __restrict__ x, int64_t ldx, int64_t M, int G, void* __restrict__ q, int layout,
+    float* __restrict__ sx, int32_t* __restrict__ qsum) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31, j = lane & 7;
+  const int64_t total = M * G;
+  if (warp * 4 >= total) return;  // the whole warp leaves together
+  const int64_t gi = warp * 4 + (lane >> 3);
+  const bool valid = gi < total;  // a ragged last warp keeps its lanes for the shuffles
+  const int64_t m = valid ? gi / G : 0;
+  const int g = valid ? (int)(gi - m * G) : 0;
+  const int64_t K = (int64_t)G * kGroup;
+  constexpr int NSUB = 8 / LG;  // activation groups per 128-group
+  float a[16];
+  if (XT == PQ2_F32) {
+    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(x) + m * ldx +
+                                                        (int64_t)g * kGroup + 16 * j);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 v = valid ? src[k] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      a[4 * k] = v.x; a[4 * k + 1] = v.y; a[4 * k + 2] = v.z; a[4 * k + 3] = v.w;
+    }
+  } else {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + m * ldx +
+                                                      (int64_t)g * kGroup + 16 * j);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint4 v = valid ? src[k] : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint16_t h = (uint16_t)(w[e >> 1] >> (16 * (e & 1)));
+        a[8 * k + e] = XT == PQ2_BF16 ? __uint_as_float((uint32_t)h << 16)
+                                      : __half2float(__ushort_as_half(h));
+      }
+    }
+  }
+  int qi[16];
+  const float s = quantize_group16<LG>(a, qi);
+  store_group16<LG>(qi, j, valid, q, layout, m * K + (int64_t)g * kGroup,
+                    qsum ? qsum + gi * NSUB : nullptr);
+  if (valid && j % LG == 0) sx[gi * NSUB + j / LG] = s;
+}
+
 }  // namespace
 
 int launch_prepare(const uint8_t* raw, int64_t raw_stride, int64_t N,
@@ -147,6 +199,29 @@ cudaError_t launch_quantize_xt(const cudaLaunchConfig_t& cfg, int act_group, con
   }
 }
 
+// Groups from which the eight-lanes-per-group kernel runs (M >= 410 at
+// K = 5120): with fewer groups, one warp per group keeps more loads in
+// flight (measured faster at M = 128 and 256), and the few-row (decode)
+// calls keep that kernel.
+constexpr int64_t kQuant16Groups = 16384;
+
+template <int XT>
+cudaError_t launch_quantize16_xt(const cudaLaunchConfig_t& cfg, int lg, const void* x,
+                                 int64_t ldx, int64_t M, int G, void* q, int q_layout, float* sx,
+                                 int32_t* qsum) {
+  switch (lg) {
+    case 4:
+      return cudaLaunchKernelEx(&cfg, quantize16_kernel<XT, 4>, x, ldx, M, G, q, q_layout, sx,
+                                qsum);
+    case 2:
+      return cudaLaunchKernelEx(&cfg, quantize16_kernel<XT, 2>, x, ldx, M, G, q, q_layout, sx,
+                                qsum);
+    default:
+      return cudaLaunchKernelEx(&cfg, quantize16_kernel<XT, 8>, x, ldx, M, G, q, q_layout, sx,
+                                qsum);
+  }
+}
+
 }  // namespace
 
 int launch_quantize(const void* x, int x_dtype, int64_t ldx, int64_t M,
@@ -156,6 +231,33 @@ int launch_quantize(const void* x, int x_dtype, int64_t ldx, int64_t M,
   const int elem = x_dtype == PQ2_F32 ? 4 : 2;
   const uintptr_t addr = reinterpret_cast<uintptr_t>(x);
   const bool vec = (addr % (4 * elem) == 0) && (ldx % 4 == 0);
+  // Many rows (at least kQuant16Groups groups): eight lanes per group, when
+  // the layout allows it and every group's elements start on 16 bytes.
+  const bool wide = M * G >= kQuant16Groups && q_layout != PQ2_Q_MMV16 && addr % 16 == 0 &&
+                    (ldx * elem) % 16 == 0 && reinterpret_cast<uintptr_t>(q) % 16 == 0;
+  if (wide) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((M * G + 31) / 32));  // 8 warps x 4 groups per block
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int lg = act_group / 16;
+    cudaError_t e;
+    switch (x_dtype) {
+      case PQ2_BF16: e = launch_quantize16_xt<PQ2_BF16>(cfg, lg, x, ldx, M, G, q, q_layout, sx, qsum); break;
+      case PQ2_F16: e = launch_quantize16_xt<PQ2_F16>(cfg, lg, x, ldx, M, G, q, q_layout, sx, qsum); break;
+      default: e = launch_quantize16_xt<PQ2_F32>(cfg, lg, x, ldx, M, G, q, q_layout, sx, qsum); break;
+    }
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return PQ2_ERR_LAUNCH;
+    }
+    return PQ2_OK;
+  }
   const int64_t warps = M * G;
   const unsigned blocks = (unsigned)((warps + 7) / 8);
   cudaLaunchConfig_t cfg = {};

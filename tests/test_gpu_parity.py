@@ -81,12 +81,15 @@ def test_quantize_bitexact(dtype, M, K, ld_pad):
 
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("M,K,ld_pad", [(13001, 384, 0), (13001, 384, 3), (1024, 5120, 0)])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+@pytest.mark.parametrize("M,K,ld_pad", [(13001, 384, 0), (13001, 384, 3), (1024, 5120, 0),
+                                        (410, 5120, 8)])
 def test_quantize_batched_bitexact(dtype, M, K, ld_pad):
-    """Enough groups for the quantiser to give each warp several of them
-    (39,003 groups, not a multiple of the batch; 40,960 groups of full rows):
-    the same bytes as the oracle in every layout."""
+    """Enough groups for the many-row quantiser (eight lanes per group, four
+    groups per warp): 39,003 groups (a ragged last warp), 40,960 and 16,400
+    groups of full rows, and a row stride that is not a multiple of 16 bytes
+    (which keeps one warp per group).  The same bytes as the oracle in every
+    layout."""
     x = synth.activations(M, K, seed=M + K, outlier_frac=0.01, dtype=torch.float32)
     x[:3] = _tie_rows(K, torch.float32)
     x = x.to(dtype)
