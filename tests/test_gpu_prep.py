@@ -66,17 +66,35 @@ def test_prep_bitexact(M, K, residual):
             assert np.array_equal(synth.bits_u16(rb.cpu()), rb_o)
 
 
-def test_prep_prefill_rows_sampled():
-    """M = 4096, K = 5120 (the prefill shape): sampled rows bit-exact."""
-    M, K, eps = 4096, 5120, 1e-5
-    x, r, w, sign = _inputs(M, K, seed=11, residual=True)
-    q, sx, qs, _, _ = pq2.pq2_norm_hadamard_quantize(
-        x.cuda(), w.cuda(), sign.cuda(), eps, residual=r.cuda(), layout=pq2.PQ2_Q_F16)
-    torch.cuda.synchronize()
-    rows = np.array([0, 1, 777, 2048, 4095])
+@pytest.mark.parametrize("M", [4096, 700])
+def test_prep_prefill_rows_sampled(M):
+    """Many rows (the kernel with one 256-thread CTA per row; M = 4096, K = 5120
+    is the prefill shape): sampled rows bit-exact in every q layout, with
+    sum(q) (the tensor-core GEMV's correction for PQ2_Q_MMV16)."""
+    K, eps = 5120, 1e-5
+    x, r, w, sign = _inputs(M, K, seed=11 + M, residual=True)
+    rows = np.array([0, 1, 333, M // 2, M - 1])
     q_o, sx_o, _, _ = _oracle(x, r, w, sign, eps, rows=rows)
-    assert np.array_equal(q.cpu().float().numpy()[rows], U.mm_operand_order(q_o).astype(np.float32))
-    assert np.array_equal(sx.cpu().numpy()[rows].view(np.uint32), sx_o.view(np.uint32))
+    for layout in (pq2.PQ2_Q_ROWS, pq2.PQ2_Q_PLANES, pq2.PQ2_Q_F16, pq2.PQ2_Q_F8,
+                   pq2.PQ2_Q_MMV16):
+        q, sx, qs, _, _ = pq2.pq2_norm_hadamard_quantize(
+            x.cuda(), w.cuda(), sign.cuda(), eps, residual=r.cuda(), layout=layout)
+        torch.cuda.synchronize()
+        qh = q.cpu()
+        if layout == pq2.PQ2_Q_ROWS:
+            assert np.array_equal(qh.numpy()[rows], q_o)
+        elif layout == pq2.PQ2_Q_PLANES:
+            assert np.array_equal(qh.numpy()[rows], O.q_planes(q_o))
+        elif layout == pq2.PQ2_Q_F16:
+            assert np.array_equal(qh.float().numpy()[rows],
+                                  U.mm_operand_order(q_o).astype(np.float32))
+        elif layout == pq2.PQ2_Q_F8:
+            assert np.array_equal(qh.numpy()[rows], U.mm_operand_order_f8(q_o))
+        else:
+            assert np.array_equal(qh.float().numpy()[rows], U.mmv16_layout(q_o))
+        assert np.array_equal(sx.cpu().numpy()[rows].view(np.uint32), sx_o.view(np.uint32))
+        qs_o = U.mmv16_correction(q_o) if layout == pq2.PQ2_Q_MMV16 else O.qsum(q_o)
+        assert np.array_equal(qs.cpu().numpy()[rows], qs_o)
 
 
 def test_prep_rows_are_independent():
