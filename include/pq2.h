@@ -238,13 +238,15 @@ int pq2_linear_tensor_gemv(int64_t M, int64_t N, int64_t K, int sm_count);
  * PQ2_Q_MMV16 for the M where pq2_linear_tensor_gemv says so, with the same
  * bits) with PQ2_MMV_OVERLAP_WEIGHTS, so that it streams the weights while
  * the quantisation and the kernel before it finish, or pq2_mm_f8 on PQ2_Q_F8
- * (M >= 16; bit-identical to pq2_mm, faster).  Hence
+ * (M >= 9; bit-identical to pq2_mm, faster).  Hence
  * codes and scales must not be written by a kernel that may still run when
  * the call starts (see the flags of pq2_mmv_ex).
  * Results are bit-identical to pq2_quantize_act + pq2_mmv / pq2_mm_f8.
  * The workspace holds q with one byte per element for M <= 4 and two
  * otherwise (the tensor-core GEMV and the prefill GEMM take 16-bit q).
- *   x         (device) x_dtype [M][ldx], ldx >= K; M 1..8 or 16 .. 1<<20.
+ *   x         (device) x_dtype [M][ldx], ldx >= K; M 1 .. 1<<20 (M 9..15,
+ *             between the pages' GEMV and prefill sizes, run as the prefill
+ *             GEMM's one partial token tile).
  *   workspace (device) pq2_linear_workspace_bytes(M, K) bytes, 256-byte
  *             aligned, holding q, s_x and sum(q); contents are scratch.
  *   codes, scales, y, y_dtype, dev_status as for pq2_mmv. */
@@ -463,7 +465,7 @@ int pq2_norm_hadamard_quantize(const uint16_t *x, const uint16_t *residual,
                                int q_layout, float *sx, int32_t *qsum,
                                void *stream);
 
-/* pq2_mm — prefill (M >= 16) ternary x INT8 matmul as a dense tensor-core
+/* pq2_mm — prefill (M >= 16; any M >= 1) ternary x INT8 matmul as a dense tensor-core
  * contraction (KE Test 7 "INT8 tensor-core MMQ prefill"; BIB "Use matrix
  * hardware for prefill"): per 128-group the exact dot of q and the decoded
  * codes is formed on tcgen05 tensor cores (fp16 operands holding integer
@@ -475,7 +477,8 @@ int pq2_norm_hadamard_quantize(const uint16_t *x, const uint16_t *residual,
  *   qsum     (device) int32 [M][K/128] group sums of q.
  *   codes, scales as for pq2_mmv.
  *   y        (device) y_dtype [M][N] (PQ2_F32 or PQ2_BF16).
- *   M        16 .. 1<<20.
+ *   M        1 .. 1<<20 (the prefill sizes are M >= 16; a smaller M is one
+ *            partial 128-token tile).
  *   dev_status as for pq2_mmv. */
 int pq2_mm(const uint16_t *q_f16, const float *sx, const int32_t *qsum,
            const uint8_t *codes, const uint16_t *scales, void *y, int y_dtype,
@@ -501,8 +504,8 @@ enum { PQ2_PATH_MMV_ADDXOR = 0, PQ2_PATH_MM = 1, PQ2_PATH_MMV_PLANES = 2,
  * dots[m][n][g] = sum_{k in g} (c_{n,k} - 1) q_{m,k} computed by the SAME
  * device decode and dot code as pq2_mmv with either decoder (paths 0 and 2,
  * q int8 in PQ2_Q_PLANES order, qsum required for path 2, M 1..8) or as
- * pq2_mm (path 1, q fp16 PQ2_Q_F16 and qsum, M >= 16) or pq2_mm_f8 (path 3,
- * q PQ2_Q_F8 and qsum, M >= 16) or pq2_mmv_tc (path 4, q PQ2_Q_MMV16 and
+ * pq2_mm (path 1, q fp16 PQ2_Q_F16 and qsum, M >= 1) or pq2_mm_f8 (path 3,
+ * q PQ2_Q_F8 and qsum, M >= 1) or pq2_mmv_tc (path 4, q PQ2_Q_MMV16 and
  * its corrections in qsum, M 1..8), for parity checks.
  *   dots (device) int32 [M][N][K/128]. */
 int pq2_debug_group_dots(const void *q, const int32_t *qsum,

@@ -360,7 +360,7 @@ int pq2_mmv_gated(const int8_t* q, const float* sx, const int32_t* qsum, const u
 
 // q bytes per element in pq2_linear's workspace: int8 planes for the dp4a
 // GEMV (M <= 4), fp16 where the tensor-core GEMV (PQ2_Q_MMV16, M = 5..8)
-// or the prefill GEMM (M >= 16) may run.
+// or the prefill GEMM (M >= 9) may run.
 static size_t linear_q_elem(int64_t M) { return M <= 4 ? 1 : 2; }
 
 size_t pq2_linear_workspace_bytes(int64_t M, int64_t K) {
@@ -378,7 +378,7 @@ int pq2_linear(const void* x, int x_dtype, int64_t ldx, int64_t M, int64_t N, in
   if (!x || !codes || !scales || !y || !workspace) return PQ2_ERR_NULL;
   if (x_dtype != PQ2_BF16 && x_dtype != PQ2_F16 && x_dtype != PQ2_F32) return PQ2_ERR_DTYPE;
   if (y_dtype != PQ2_F32 && y_dtype != PQ2_BF16) return PQ2_ERR_DTYPE;
-  if (M < 1 || M > kMaxM || (M > 8 && M < 16) || !valid_n(N) || !valid_k(K) || ldx < K ||
+  if (M < 1 || M > kMaxM || !valid_n(N) || !valid_k(K) || ldx < K ||
       ldx > ((int64_t)1 << 40))
     return PQ2_ERR_SHAPE;
   if (workspace_bytes < pq2_linear_workspace_bytes(M, K)) return PQ2_ERR_SHAPE;
@@ -463,7 +463,7 @@ int pq2_mm(const uint16_t* q_f16, const float* sx, const int32_t* qsum, const ui
            const uint16_t* scales, void* y, int y_dtype, int64_t M, int64_t N, int64_t K,
            int32_t* dev_status, void* stream) {
   if (!q_f16 || !sx || !qsum || !codes || !scales || !y) return PQ2_ERR_NULL;
-  if (M < 16 || M > kMaxM || !valid_n(N) || !valid_k(K)) return PQ2_ERR_SHAPE;
+  if (M < 1 || M > kMaxM || !valid_n(N) || !valid_k(K)) return PQ2_ERR_SHAPE;
   if (y_dtype != PQ2_F32 && y_dtype != PQ2_BF16) return PQ2_ERR_DTYPE;
   if (!aligned(q_f16, 16) || !aligned(codes, 16) || !aligned(sx, 4) || !aligned(qsum, 4) ||
       !aligned(scales, 2) || !aligned(y, elem_bytes(y_dtype)))
@@ -478,7 +478,7 @@ int pq2_mm_f8(const uint8_t* q_f8, const float* sx, const int32_t* qsum, const u
               const uint16_t* scales, void* y, int y_dtype, int64_t M, int64_t N, int64_t K,
               int32_t* dev_status, void* stream) {
   if (!q_f8 || !sx || !qsum || !codes || !scales || !y) return PQ2_ERR_NULL;
-  if (M < 16 || M > kMaxM || !valid_n(N) || !valid_k(K)) return PQ2_ERR_SHAPE;
+  if (M < 1 || M > kMaxM || !valid_n(N) || !valid_k(K)) return PQ2_ERR_SHAPE;
   if (y_dtype != PQ2_F32 && y_dtype != PQ2_BF16) return PQ2_ERR_DTYPE;
   if (!aligned(q_f8, 16) || !aligned(codes, 16) || !aligned(sx, 4) || !aligned(qsum, 4) ||
       !aligned(scales, 2) || !aligned(y, elem_bytes(y_dtype)))
@@ -499,7 +499,7 @@ int pq2_debug_group_dots(const void* q, const int32_t* qsum, const uint8_t* code
   const bool mm = path == PQ2_PATH_MM || path == PQ2_PATH_MM_F8;
   if (path != PQ2_PATH_MMV_ADDXOR && !qsum) return PQ2_ERR_NULL;
   if (!valid_n(N) || !valid_k(K)) return PQ2_ERR_SHAPE;
-  if (mm ? (M < 16 || M > kMaxM) : (M < 1 || M > 8)) return PQ2_ERR_SHAPE;
+  if (mm ? (M < 1 || M > kMaxM) : (M < 1 || M > 8)) return PQ2_ERR_SHAPE;
   if (!aligned(q, 16) || !aligned(codes, 16) || !aligned(dots, 4) ||
       (qsum && !aligned(qsum, 4)))
     return PQ2_ERR_ALIGN;

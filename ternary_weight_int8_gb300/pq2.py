@@ -192,8 +192,8 @@ def linear_workspace_bytes(M: int, K: int) -> int:
 
 def pq2_linear(x, codes, scales, y=None, out_dtype=torch.float32, workspace=None,
                status=None, stream=None):
-    """Complete projection for M = 1..8: quantise x and run the GEMV, with the
-    GEMV streaming its weights while the quantisation runs."""
+    """Complete projection: quantise x, then the GEMV for M = 1..8 (streaming
+    its weights while the quantisation runs) or the prefill GEMM from M = 9."""
     if x.dim() != 2 or x.stride(1) != 1:
         raise ValueError("x must be 2-D with unit column stride")
     M, K = x.shape
@@ -367,7 +367,7 @@ def q_buffer(M: int, K: int, layout: int, device):
 
 def pq2_mm_f8(q_f8, sx, qsum, codes, scales, y=None, out_dtype=torch.float32, status=None,
               stream=None):
-    """Prefill matmul, M >= 16, on the 8-bit tcgen05 path (q from PQ2_Q_F8)."""
+    """Prefill matmul (M >= 16; any M >= 1) on the 8-bit tcgen05 path (q from PQ2_Q_F8)."""
     M, K = q_f8.shape[0], q_f8.shape[1] // 2
     N = codes.shape[0]
     if y is None:
@@ -380,7 +380,7 @@ def pq2_mm_f8(q_f8, sx, qsum, codes, scales, y=None, out_dtype=torch.float32, st
 
 def pq2_mm(q_f16, sx, qsum, codes, scales, y=None, out_dtype=torch.float32, status=None,
            stream=None):
-    """Prefill matmul, M >= 16, on tcgen05 tensor cores."""
+    """Prefill matmul (M >= 16; any M >= 1) on tcgen05 tensor cores."""
     M, K = q_f16.shape
     N = codes.shape[0]
     if y is None:
@@ -419,11 +419,6 @@ def mmv_decoder(M: int) -> int:
 
 
 def linear(x, codes, scales, out_dtype=torch.float32, stream=None):
-    """The complete projection: pq2_linear (M <= 8 or M >= 16), or quantise
-    + pq2_mm for 8 < M < 16 with the batch padded to 16 rows."""
-    M = x.shape[0]
-    if M <= 8 or M >= 16:
-        return pq2_linear(x, codes, scales, out_dtype=out_dtype, stream=stream)
-    xp = torch.zeros((16, x.shape[1]), dtype=x.dtype, device=x.device)
-    xp[:M] = x
-    return pq2_linear(xp, codes, scales, out_dtype=out_dtype, stream=stream)[:M]
+    """The complete projection: pq2_linear (the GEMV for M <= 8, the
+    prefill GEMM from M = 9)."""
+    return pq2_linear(x, codes, scales, out_dtype=out_dtype, stream=stream)

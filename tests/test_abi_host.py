@@ -104,7 +104,7 @@ def test_linear_validation(L):
     for i in (0, 6, 7, 8, 10):
         bad = list(ok); bad[i] = None
         assert f(*bad) == pq2.PQ2_ERR_NULL, i
-    for idx, val, err in [(3, 12, pq2.PQ2_ERR_SHAPE), (3, 0, pq2.PQ2_ERR_SHAPE),
+    for idx, val, err in [(3, (1 << 20) + 1, pq2.PQ2_ERR_SHAPE), (3, 0, pq2.PQ2_ERR_SHAPE),
                           (2, 5000, pq2.PQ2_ERR_SHAPE), (11, ws - 1, pq2.PQ2_ERR_SHAPE),
                           (1, 9, pq2.PQ2_ERR_DTYPE), (9, pq2.PQ2_F16, pq2.PQ2_ERR_DTYPE),
                           (10, A + 16, pq2.PQ2_ERR_ALIGN), (6, A + 8, pq2.PQ2_ERR_ALIGN),
@@ -114,7 +114,8 @@ def test_linear_validation(L):
 
 
 def test_mm_and_debug_validation(L):
-    assert L.pq2_mm(A, A, A, A, A, A, 2, 15, 10, 128, None, None) == pq2.PQ2_ERR_SHAPE
+    assert L.pq2_mm(A, A, A, A, A, A, 2, 0, 10, 128, None, None) == pq2.PQ2_ERR_SHAPE
+    assert L.pq2_mm(A, A, A, A, A, A, 2, (1 << 20) + 1, 10, 128, None, None) == pq2.PQ2_ERR_SHAPE
     assert L.pq2_mm(A, A, A, A, A, None, 2, 16, 10, 128, None, None) == pq2.PQ2_ERR_NULL
     assert L.pq2_mm(A, A, None, A, A, A, 2, 16, 10, 128, None, None) == pq2.PQ2_ERR_NULL
     assert L.pq2_mm(A + 2, A, A, A, A, A, 2, 16, 10, 128, None, None) == pq2.PQ2_ERR_ALIGN
@@ -123,7 +124,7 @@ def test_mm_and_debug_validation(L):
     assert d(A, None, A, 1, 10, 128, 7, A, None, None) == pq2.PQ2_ERR_DTYPE
     assert d(A, None, A, 1, 10, 128, 2, A, None, None) == pq2.PQ2_ERR_NULL
     assert d(A, A, A, 9, 10, 128, 0, A, None, None) == pq2.PQ2_ERR_SHAPE
-    assert d(A, A, A, 8, 10, 128, 1, A, None, None) == pq2.PQ2_ERR_SHAPE
+    assert d(A, A, A, 0, 10, 128, 1, A, None, None) == pq2.PQ2_ERR_SHAPE
 
 
 def test_valid_call_without_gpu_reports_cuda_error(L):
@@ -168,7 +169,7 @@ def test_mmv_geometry_fills_the_gb300_shapes(L):
 
 def test_mm_f8_validation(L):
     f = L.pq2_mm_f8
-    assert f(A, A, A, A, A, A, 2, 15, 10, 128, None, None) == pq2.PQ2_ERR_SHAPE
+    assert f(A, A, A, A, A, A, 2, 0, 10, 128, None, None) == pq2.PQ2_ERR_SHAPE
     assert f(None, A, A, A, A, A, 2, 16, 10, 128, None, None) == pq2.PQ2_ERR_NULL
     assert f(A, A, None, A, A, A, 2, 16, 10, 128, None, None) == pq2.PQ2_ERR_NULL
     assert f(A, A, A, A, A, A, 1, 16, 10, 128, None, None) == pq2.PQ2_ERR_DTYPE
@@ -176,7 +177,7 @@ def test_mm_f8_validation(L):
     assert f(A, A, A, A, A, A, 2, 16, 10, 200, None, None) == pq2.PQ2_ERR_SHAPE
     d = L.pq2_debug_group_dots
     assert d(A, None, A, 16, 10, 128, pq2.PQ2_PATH_MM_F8, A, None, None) == pq2.PQ2_ERR_NULL
-    assert d(A, A, A, 8, 10, 128, pq2.PQ2_PATH_MM_F8, A, None, None) == pq2.PQ2_ERR_SHAPE
+    assert d(A, A, A, 0, 10, 128, pq2.PQ2_PATH_MM_F8, A, None, None) == pq2.PQ2_ERR_SHAPE
     assert d(A, A, A, 16, 10, 128, 5, A, None, None) == pq2.PQ2_ERR_DTYPE
     # the tensor-core GEMV path takes M = 1..8 and its corrections
     assert d(A, A, A, 16, 10, 128, pq2.PQ2_PATH_MMV_TC, A, None, None) == pq2.PQ2_ERR_SHAPE

@@ -73,6 +73,27 @@ def test_linear_against_oracle(M):
     assert np.all(diff <= 1e-5 * bound), float((diff - 1e-5 * bound).max())
 
 
+@pytest.mark.parametrize("M", [9, 12, 15])
+def test_linear_between_gemv_and_prefill_sizes(M):
+    """M = 9..15 run the prefill GEMM's 8-bit path as one partial token tile:
+    bit-identical to quantising to PQ2_Q_F8 and calling pq2_mm_f8, and within
+    the oracle's bound."""
+    N, K = 1000, 4096
+    raw, codes_o, scales_o = U.weights(N, K, seed=91 + M)
+    codes, scales = pq2.pq2_prepare(raw, K)
+    x = synth.activations(M, K, seed=600 + M, device="cuda", outlier_frac=0.01)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = pq2.pq2_linear(x, codes, scales, status=status)
+    q8, sx8, qs8 = pq2.pq2_quantize_act(x, pq2.PQ2_Q_F8)
+    y_two = pq2.pq2_mm_f8(q8, sx8, qs8, codes, scales)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(y.view(torch.int32), y_two.view(torch.int32))
+    _, _, _, _, _, y64, bound = U.oracle_reference(x, codes_o, scales_o)
+    diff = np.abs(y.cpu().numpy().astype(np.float64) - y64)
+    assert np.all(diff <= 1e-5 * bound), float((diff - 1e-5 * bound).max())
+
+
 def test_all_zero_and_single_outlier_groups():
     """Degenerate groups: all zeros (s = 0, q = 0) and one large value among
     zeros (q = +-127 there, 0 elsewhere)."""

@@ -32,7 +32,8 @@ def _prep(N, K, seed, code_values=3):
     return codes, scales, codes_o, scales_o
 
 
-SHAPES = [(16, 128, 128), (128, 128, 384), (200, 300, 1152), (384, 1000, 640), (130, 136, 2048)]
+SHAPES = [(16, 128, 128), (128, 128, 384), (200, 300, 1152), (384, 1000, 640), (130, 136, 2048),
+          (1, 256, 640), (9, 300, 1152)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)

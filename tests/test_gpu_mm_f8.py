@@ -24,7 +24,8 @@ def _cuda():
     torch.cuda.synchronize()
 
 
-SHAPES = [(16, 128, 128), (128, 128, 384), (200, 300, 1152), (384, 1000, 640), (130, 136, 2048)]
+SHAPES = [(16, 128, 128), (128, 128, 384), (200, 300, 1152), (384, 1000, 640), (130, 136, 2048),
+          (1, 256, 640), (9, 300, 1152)]
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
