@@ -59,6 +59,7 @@ METRIC = ("µs/call and HBM GB/s (frac of peak) for ternary×INT8 matmul at "
           "M=1–8; prefill TOPS")
 K_DIM, N_DIM, MS = 5120, 10240, (1, 2, 3, 4)
 PREFILL_K, PREFILL_N, PREFILL_MS = 5120, 17408, (16, 128, 512, 2048, 4096)
+PREFILL_GROUPED_MS = (128, 512, 4096)  # the grouped calls the pages time, and the largest
 GATED_K, GATED_I = 5120, 17408
 # The GEMV sweep: the layer shapes at every M in 1..8 (with the batch
 # invariance check) and the 4096 x 14336 shape at M = 1, as (K, N, Ms, name).
@@ -393,6 +394,47 @@ def prefill_leg(args, dev, stream, timed, capture):
                                "complete_us": round(c_ms * 1e3, 2),
                                "complete_tflops": round(2.0 * M * N * K / (c_ms * 1e-3) / 1e12, 1)}
         del x, q, q8, sx, qs, y, ws
+    # Activation groups of 128 / 64 / 32 (the pages time the complete call at
+    # M = 128 and 512): the 8-bit grouped GEMM alone and pq2_linear_grouped.
+    out["grouped"] = {}
+    for M in PREFILL_GROUPED_MS:
+        x = synth.activations(M, K, seed=950 + M, device=dev)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        by_a = {}
+        for A in (128, 64, 32):
+            q8, sx, qs = pq2.pq2_quantize_act_grouped(x, A, pq2.PQ2_Q_F8)
+            ws = torch.empty(pq2.linear_grouped_workspace_bytes(M, K, A), dtype=torch.uint8,
+                             device=dev)
+
+            def mm_calls():
+                for c, sc in mats:
+                    st = lib.pq2_mm_f8_grouped(q8.data_ptr(), sx.data_ptr(), qs.data_ptr(),
+                                               c.data_ptr(), sc.data_ptr(), y.data_ptr(),
+                                               pq2.PQ2_BF16, M, N, K, A, status.data_ptr(), sp)
+                    if st:
+                        raise RuntimeError(f"pq2_mm_f8_grouped failed ({st})")
+
+            def linear_calls():
+                for c, sc in mats:
+                    st = lib.pq2_linear_grouped(x.data_ptr(), pq2.PQ2_BF16, K, M, N, K,
+                                                c.data_ptr(), sc.data_ptr(), A, y.data_ptr(),
+                                                pq2.PQ2_BF16, ws.data_ptr(), ws.numel(),
+                                                status.data_ptr(), sp)
+                    if st:
+                        raise RuntimeError(f"pq2_linear_grouped failed ({st})")
+
+            reps = max(3, min(50, 20000 // M))
+            k_ms = timed([capture(mm_calls)], reps, 3) / (reps * nm)
+            c_ms = timed([capture(linear_calls)], reps, 3) / (reps * nm)
+            by_a[str(A)] = {"mm_f8_us": round(k_ms * 1e3, 2),
+                            "mm_f8_tops": round(2.0 * M * N * K / (k_ms * 1e-3) / 1e12, 1),
+                            "complete_us": round(c_ms * 1e3, 2)}
+            del q8, sx, qs, ws
+        for A in ("64", "32"):
+            by_a[A]["complete_cost_vs_128"] = round(
+                by_a[A]["complete_us"] / by_a["128"]["complete_us"] - 1.0, 3)
+        out["grouped"][str(M)] = by_a
+        del x, y
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
     del mats
@@ -1053,8 +1095,9 @@ def run_profile_case(args):
     (pq2_mmv, or pq2_mmv_tc for "mmvtc", INDEPENDENT calls over 8 rotated
     matrices), the fused preparation ("prep", K=5120 with a residual), or the
     ffn_up prefill
-    GEMM (pq2_mm, or pq2_mm_f8 for "mm8"), at --profile-m columns; 3 warm-up
-    calls then 3 calls."""
+    GEMM (pq2_mm, pq2_mm_f8 for "mm8", pq2_mm_f8_grouped with
+    --profile-act-group for "mm8g"), at --profile-m columns; 3 warm-up calls
+    then 3 calls."""
     import torch
     from ternary_weight_int8_gb300 import pq2, synth
     dev = torch.device("cuda", 0)
@@ -1090,11 +1133,12 @@ def run_profile_case(args):
         layout = pq2.PQ2_Q_PLANES if args.profile_case == "mmv" else pq2.PQ2_Q_MMV16
     else:
         K, N, nm = PREFILL_K, PREFILL_N, 2
-        layout = pq2.PQ2_Q_F8 if args.profile_case == "mm8" else pq2.PQ2_Q_F16
+        layout = pq2.PQ2_Q_F8 if args.profile_case in ("mm8", "mm8g") else pq2.PQ2_Q_F16
     mats = [pq2.pq2_prepare(synth.raw_weights(N, K, seed=7000 + i, device=dev), K)
             for i in range(nm)]
     x = synth.activations(M, K, seed=11, device=dev, outlier_frac=0.01)
-    q, sx, qs = pq2.pq2_quantize_act(x, layout)
+    A = args.profile_act_group if args.profile_case == "mm8g" else 128
+    q, sx, qs = pq2.pq2_quantize_act_grouped(x, A, layout)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     for i in range(6):
         c, sc = mats[i % nm]
@@ -1104,11 +1148,13 @@ def run_profile_case(args):
             pq2.pq2_mmv_tc(q, sx, qs, c, sc, y=y, flags=pq2.PQ2_MMV_INDEPENDENT)
         elif args.profile_case == "mm8":
             pq2.pq2_mm_f8(q, sx, qs, c, sc, y=y)
+        elif args.profile_case == "mm8g":
+            pq2.pq2_mm_f8_grouped(q, sx, qs, c, sc, A, y=y)
         else:
             pq2.pq2_mm(q, sx, qs, c, sc, y=y)
     torch.cuda.synchronize()
     print(json.dumps({"profile_case": args.profile_case, "M": M, "N": N, "K": K,
-                      "launches": 6, "ok": True}))
+                      "act_group": A, "launches": 6, "ok": True}))
     return 0
 
 
@@ -1130,12 +1176,13 @@ def main():
                     help="skip the activation-group 64/32 (pq2_mmv_grouped) leg")
     ap.add_argument("--no-ptq", action="store_true",
                     help="skip the PTQ1_0 weight-format (pq2_ptq_mmv) leg")
-    ap.add_argument("--profile-case", choices=["mmv", "mmvtc", "mm", "mm8", "ptq", "prep"],
+    ap.add_argument("--profile-case", choices=["mmv", "mmvtc", "mm", "mm8", "mm8g", "ptq",
+                                               "prep"],
                     default=None,
                     help="run a short fixed call sequence for an ncu capture and exit")
     ap.add_argument("--profile-m", type=int, default=1, help="columns for --profile-case")
     ap.add_argument("--profile-act-group", type=int, default=32,
-                    help="activation group for --profile-case ptq")
+                    help="activation group for --profile-case ptq and mm8g")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -496,6 +496,48 @@ int pq2_mm_f8(const uint8_t *q_f8, const float *sx, const int32_t *qsum,
               int y_dtype, int64_t M, int64_t N, int64_t K,
               int32_t *dev_status, void *stream);
 
+/* pq2_mm_grouped, pq2_mm_f8_grouped — pq2_mm and pq2_mm_f8 on activations
+ * quantised by pq2_quantize_act_grouped with activation groups of act_group
+ * A = 128, 64 or 32 elements (KE Test 9, "Smaller Q8 activation groups":
+ * the weights and their 128-weight scales stay as they are, each weight
+ * group's dot splits into 128 / A separately scaled partial dots):
+ *   y[m][n] = sum over weight groups g, then over h = 0 .. 128/A - 1, of
+ *             (dot_gh * s_x[m][g*128/A + h]) * s_w[n][g]
+ * with dot_gh the exact integer dot of activation group h of block g, each
+ * a separate tensor-core accumulation (exact, as for pq2_mm), scaled in fp32.
+ *   q_f16 / q_f8 as for pq2_mm / pq2_mm_f8, from pq2_quantize_act_grouped
+ *            (PQ2_Q_F16 / PQ2_Q_F8, the same act_group).
+ *   sx, qsum (device) [M][K / act_group].
+ * act_group 128 gives exactly pq2_mm / pq2_mm_f8.  Returns PQ2_ERR_SHAPE for
+ * another act_group, else as pq2_mm. */
+int pq2_mm_grouped(const uint16_t *q_f16, const float *sx, const int32_t *qsum,
+                   const uint8_t *codes, const uint16_t *scales, void *y,
+                   int y_dtype, int64_t M, int64_t N, int64_t K, int act_group,
+                   int32_t *dev_status, void *stream);
+int pq2_mm_f8_grouped(const uint8_t *q_f8, const float *sx, const int32_t *qsum,
+                      const uint8_t *codes, const uint16_t *scales, void *y,
+                      int y_dtype, int64_t M, int64_t N, int64_t K,
+                      int act_group, int32_t *dev_status, void *stream);
+
+/* pq2_linear_grouped — the complete projection with activation groups of
+ * act_group elements (128, 64, 32; KE Test 9 times exactly this call at
+ * M = 128 and 512): pq2_quantize_act_grouped into the caller's workspace,
+ * then pq2_mmv_grouped (M = 1..8, masked-plane decoder, weights streamed
+ * while the quantisation runs) or pq2_mm_f8_grouped (M >= 9).
+ * Bit-identical to those calls.
+ *   x, ldx, codes, scales, y, y_dtype, dev_status as for pq2_linear.
+ *   workspace (device) pq2_linear_grouped_workspace_bytes(M, K, act_group)
+ *             bytes, 256-byte aligned; contents are scratch.
+ * pq2_linear_grouped_workspace_bytes returns 0 for invalid arguments.
+ * Returns PQ2_ERR_SHAPE for a workspace that is too small or another
+ * act_group, else as the calls it makes. */
+size_t pq2_linear_grouped_workspace_bytes(int64_t M, int64_t K, int act_group);
+int pq2_linear_grouped(const void *x, int x_dtype, int64_t ldx, int64_t M,
+                       int64_t N, int64_t K, const uint8_t *codes,
+                       const uint16_t *scales, int act_group, void *y,
+                       int y_dtype, void *workspace, size_t workspace_bytes,
+                       int32_t *dev_status, void *stream);
+
 /* Paths of pq2_debug_group_dots. */
 enum { PQ2_PATH_MMV_ADDXOR = 0, PQ2_PATH_MM = 1, PQ2_PATH_MMV_PLANES = 2,
        PQ2_PATH_MM_F8 = 3, PQ2_PATH_MMV_TC = 4 };
@@ -512,6 +554,17 @@ int pq2_debug_group_dots(const void *q, const int32_t *qsum,
                          const uint8_t *codes, int64_t M, int64_t N, int64_t K,
                          int path, int32_t *dots, int32_t *dev_status,
                          void *stream);
+
+/* pq2_debug_mm_dots_grouped — the exact partial dots of pq2_mm_grouped
+ * (path PQ2_PATH_MM, q PQ2_Q_F16) or pq2_mm_f8_grouped (PQ2_PATH_MM_F8,
+ * q PQ2_Q_F8) from the same device code, for parity checks:
+ * dots[m][n][j] = sum over k in [j*A, j*A + A) of (c_{n,k} - 1) q_{m,k}.
+ *   q from pq2_quantize_act_grouped with the same act_group; M >= 1.
+ *   dots (device) int32 [M][N][K / act_group]. */
+int pq2_debug_mm_dots_grouped(const void *q, int path, const uint8_t *codes,
+                              int64_t M, int64_t N, int64_t K, int act_group,
+                              int32_t *dots, int32_t *dev_status,
+                              void *stream);
 
 /* pq2_debug_mmv_drop_arrival — a test of the bounded device waits (the
  * status convention above), not a step of the method: pq2_mmv (masked-plane

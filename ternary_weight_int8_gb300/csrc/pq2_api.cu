@@ -459,34 +459,111 @@ int pq2_norm_hadamard_quantize(const uint16_t* x, const uint16_t* residual,
                                             static_cast<cudaStream_t>(stream));
 }
 
-int pq2_mm(const uint16_t* q_f16, const float* sx, const int32_t* qsum, const uint8_t* codes,
-           const uint16_t* scales, void* y, int y_dtype, int64_t M, int64_t N, int64_t K,
-           int32_t* dev_status, void* stream) {
-  if (!q_f16 || !sx || !qsum || !codes || !scales || !y) return PQ2_ERR_NULL;
-  if (M < 1 || M > kMaxM || !valid_n(N) || !valid_k(K)) return PQ2_ERR_SHAPE;
+namespace {
+int mm_call(const void* q, bool f8, const float* sx, const int32_t* qsum, const uint8_t* codes,
+            const uint16_t* scales, void* y, int y_dtype, int64_t M, int64_t N, int64_t K,
+            int act_group, int32_t* dev_status, void* stream) {
+  if (!q || !sx || !qsum || !codes || !scales || !y) return PQ2_ERR_NULL;
+  if (M < 1 || M > kMaxM || !valid_n(N) || !valid_k(K) ||
+      (act_group != 128 && act_group != 64 && act_group != 32))
+    return PQ2_ERR_SHAPE;
   if (y_dtype != PQ2_F32 && y_dtype != PQ2_BF16) return PQ2_ERR_DTYPE;
-  if (!aligned(q_f16, 16) || !aligned(codes, 16) || !aligned(sx, 4) || !aligned(qsum, 4) ||
+  if (!aligned(q, 16) || !aligned(codes, 16) || !aligned(sx, 4) || !aligned(qsum, 4) ||
       !aligned(scales, 2) || !aligned(y, elem_bytes(y_dtype)))
     return PQ2_ERR_ALIGN;
   int sms = 0;
   if (int st = device_check(&sms)) return st;
-  return pq2::launch_mm(q_f16, false, sx, qsum, codes, scales, y, y_dtype, nullptr, M, N, K, sms,
-                        dev_status, static_cast<cudaStream_t>(stream));
+  return pq2::launch_mm(q, f8, sx, qsum, codes, scales, y, y_dtype, nullptr, M, N, K, sms,
+                        dev_status, static_cast<cudaStream_t>(stream), act_group);
+}
+}  // namespace
+
+int pq2_mm(const uint16_t* q_f16, const float* sx, const int32_t* qsum, const uint8_t* codes,
+           const uint16_t* scales, void* y, int y_dtype, int64_t M, int64_t N, int64_t K,
+           int32_t* dev_status, void* stream) {
+  return mm_call(q_f16, false, sx, qsum, codes, scales, y, y_dtype, M, N, K, 128, dev_status,
+                 stream);
 }
 
 int pq2_mm_f8(const uint8_t* q_f8, const float* sx, const int32_t* qsum, const uint8_t* codes,
               const uint16_t* scales, void* y, int y_dtype, int64_t M, int64_t N, int64_t K,
               int32_t* dev_status, void* stream) {
-  if (!q_f8 || !sx || !qsum || !codes || !scales || !y) return PQ2_ERR_NULL;
-  if (M < 1 || M > kMaxM || !valid_n(N) || !valid_k(K)) return PQ2_ERR_SHAPE;
+  return mm_call(q_f8, true, sx, qsum, codes, scales, y, y_dtype, M, N, K, 128, dev_status,
+                 stream);
+}
+
+int pq2_mm_grouped(const uint16_t* q_f16, const float* sx, const int32_t* qsum,
+                   const uint8_t* codes, const uint16_t* scales, void* y, int y_dtype, int64_t M,
+                   int64_t N, int64_t K, int act_group, int32_t* dev_status, void* stream) {
+  return mm_call(q_f16, false, sx, qsum, codes, scales, y, y_dtype, M, N, K, act_group,
+                 dev_status, stream);
+}
+
+int pq2_mm_f8_grouped(const uint8_t* q_f8, const float* sx, const int32_t* qsum,
+                      const uint8_t* codes, const uint16_t* scales, void* y, int y_dtype,
+                      int64_t M, int64_t N, int64_t K, int act_group, int32_t* dev_status,
+                      void* stream) {
+  return mm_call(q_f8, true, sx, qsum, codes, scales, y, y_dtype, M, N, K, act_group,
+                 dev_status, stream);
+}
+
+// q bytes per element in pq2_linear_grouped's workspace: int8 planes for
+// the grouped GEMV (M <= 8), the two e4m3 planes for the prefill GEMM.
+static size_t linear_grouped_q_elem(int64_t M) { return M <= 8 ? 1 : 2; }
+
+size_t pq2_linear_grouped_workspace_bytes(int64_t M, int64_t K, int act_group) {
+  if (M < 1 || M > kMaxM || !valid_k(K) ||
+      (act_group != 128 && act_group != 64 && act_group != 32))
+    return 0;
+  const size_t GA = (size_t)(K / act_group);
+  const size_t q_bytes = (size_t)M * (size_t)K * linear_grouped_q_elem(M);
+  const size_t sx_off = (q_bytes + 255) / 256 * 256;
+  const size_t qs_off = (sx_off + (size_t)M * GA * 4 + 255) / 256 * 256;
+  return qs_off + (size_t)M * GA * 4;
+}
+
+int pq2_linear_grouped(const void* x, int x_dtype, int64_t ldx, int64_t M, int64_t N, int64_t K,
+                       const uint8_t* codes, const uint16_t* scales, int act_group, void* y,
+                       int y_dtype, void* workspace, size_t workspace_bytes,
+                       int32_t* dev_status, void* stream) {
+  if (!x || !codes || !scales || !y || !workspace) return PQ2_ERR_NULL;
+  if (x_dtype != PQ2_BF16 && x_dtype != PQ2_F16 && x_dtype != PQ2_F32) return PQ2_ERR_DTYPE;
   if (y_dtype != PQ2_F32 && y_dtype != PQ2_BF16) return PQ2_ERR_DTYPE;
-  if (!aligned(q_f8, 16) || !aligned(codes, 16) || !aligned(sx, 4) || !aligned(qsum, 4) ||
+  const size_t need = pq2_linear_grouped_workspace_bytes(M, K, act_group);
+  if (need == 0 || !valid_n(N) || ldx < K || ldx > ((int64_t)1 << 40)) return PQ2_ERR_SHAPE;
+  if (workspace_bytes < need) return PQ2_ERR_SHAPE;
+  if (!aligned(x, elem_bytes(x_dtype)) || !aligned(workspace, 256) || !aligned(codes, 16) ||
       !aligned(scales, 2) || !aligned(y, elem_bytes(y_dtype)))
     return PQ2_ERR_ALIGN;
   int sms = 0;
   if (int st = device_check(&sms)) return st;
-  return pq2::launch_mm(q_f8, true, sx, qsum, codes, scales, y, y_dtype, nullptr, M, N, K, sms,
-                        dev_status, static_cast<cudaStream_t>(stream));
+  const size_t GA = (size_t)(K / act_group);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t q_bytes = (size_t)M * (size_t)K * linear_grouped_q_elem(M);
+  const size_t sx_off = (q_bytes + 255) / 256 * 256;
+  const size_t qs_off = (sx_off + (size_t)M * GA * 4 + 255) / 256 * 256;
+  float* sx = reinterpret_cast<float*>(ws + sx_off);
+  int32_t* qs = reinterpret_cast<int32_t*>(ws + qs_off);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool small = M <= 8;
+  if (int st = pq2::launch_quantize(x, x_dtype, ldx, M, K, ws, small ? PQ2_Q_PLANES : PQ2_Q_F8,
+                                    sx, qs, s, act_group))
+    return st;
+  if (!small)
+    return pq2::launch_mm(ws, true, sx, qs, codes, scales, y, y_dtype, nullptr, M, N, K, sms,
+                          dev_status, s, act_group);
+  // The grouped GEMV holds four columns' partial sums: columns 4..M-1 run as
+  // a second pass (same bits as one pass).  The first pass streams its
+  // weights while the quantisation runs.
+  const int8_t* q = reinterpret_cast<const int8_t*>(ws);
+  const int64_t first = M < 4 ? M : 4;
+  if (int st = pq2::launch_mmv_grouped(q, sx, qs, codes, scales, y, y_dtype, nullptr, first, N,
+                                       K, act_group, 1, sms, dev_status, s))
+    return st;
+  if (M == first) return PQ2_OK;
+  return pq2::launch_mmv_grouped(q + 4 * K, sx + 4 * GA, qs + 4 * GA, codes, scales,
+                                 static_cast<uint8_t*>(y) + 4 * N * elem_bytes(y_dtype), y_dtype,
+                                 nullptr, M - 4, N, K, act_group, 1, sms, dev_status, s);
 }
 
 int pq2_debug_group_dots(const void* q, const int32_t* qsum, const uint8_t* codes,
@@ -516,6 +593,22 @@ int pq2_debug_group_dots(const void* q, const int32_t* qsum, const uint8_t* code
                          : path == PQ2_PATH_MMV_TC   ? pq2::kDecodeTensor
                                                      : pq2::kDecodeAddXor,
                          0, sms, dev_status, s);
+}
+
+int pq2_debug_mm_dots_grouped(const void* q, int path, const uint8_t* codes, int64_t M,
+                              int64_t N, int64_t K, int act_group, int32_t* dots,
+                              int32_t* dev_status, void* stream) {
+  if (!q || !codes || !dots) return PQ2_ERR_NULL;
+  if (path != PQ2_PATH_MM && path != PQ2_PATH_MM_F8) return PQ2_ERR_DTYPE;
+  if (M < 1 || M > kMaxM || !valid_n(N) || !valid_k(K) ||
+      (act_group != 128 && act_group != 64 && act_group != 32))
+    return PQ2_ERR_SHAPE;
+  if (!aligned(q, 16) || !aligned(codes, 16) || !aligned(dots, 4)) return PQ2_ERR_ALIGN;
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  return pq2::launch_mm(q, path == PQ2_PATH_MM_F8, nullptr, nullptr, codes, nullptr, nullptr,
+                        PQ2_F32, dots, M, N, K, sms, dev_status,
+                        static_cast<cudaStream_t>(stream), act_group);
 }
 
 int pq2_debug_mmv_drop_arrival(const int8_t* q, const float* sx, const int32_t* qsum,

@@ -92,6 +92,6 @@ int launch_ptq_mmv(const int8_t* q, const float* sx, const int32_t* qsum, const 
 int launch_mm(const void* q_op, bool f8, const float* sx, const int32_t* qsum,
               const uint8_t* codes, const uint16_t* scales, void* y, int y_dtype,
               int32_t* dots, int64_t M, int64_t N, int64_t K, int sm_count,
-              int32_t* status, cudaStream_t stream);
+              int32_t* status, cudaStream_t stream, int act_group = 128);
 
 }  // namespace pq2

@@ -27,6 +27,11 @@
 // the decode costs 11 instead of 17 instructions per 16 weights and A takes
 // half the tensor memory, leaving room for a third D buffer.
 //
+// Activation groups of 64 or 32 (KE Test 9, "Smaller Q8 activation groups";
+// pq2_mm_grouped, pq2_mm_f8_grouped): a weight group's K steps split into
+// 128 / A accumulation units, each into its own fresh D buffer of the same
+// ring and scaled by its own s_x (the kernel's NSUB template parameter).
+//
 // One CTA computes a tile of 128 output rows x 128 tokens:
 //   warp 0      TMA producer: q tiles (two 64-column boxes per group, 128-byte
 //               swizzle, the canonical K-major layout) and code tiles
@@ -36,7 +41,7 @@
 //               (two buffers in flight, three on the 8-bit path), scales it
 //               and adds it into fp32 running sums in registers, finally
 //               stores y
-//   warp 22     scheduler: waits until a group's A, q and D buffer are
+//   warp 22     scheduler: waits until a unit's A, q and D buffer are
 //               ready, then releases the MMA warp (named barrier)
 //   warp 23     scales: stages s_x and s_w chunk by chunk for the epilogue
 // A warp may only reach the TMEM lanes 32*(warp % 4) .. +31, so each role
@@ -49,6 +54,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "pq2_device.cuh"
 #include "pq2_internal.h"
@@ -60,7 +66,7 @@ constexpr int BW = 128;          // weight rows per tile (MMA M, A in TMEM)
 constexpr int BT = 128;          // tokens per tile (MMA N, B in shared memory)
 constexpr int kStagesQ = 6;      // q tile stages
 constexpr int kStagesC = 4;      // code tile stages
-constexpr int kGC = 4;           // groups per scale chunk
+constexpr int kGC = 4;           // accumulation units per scale chunk
 constexpr int kEpiWarps = 16;     // warps 6-21: four per TMEM lane quarter
 constexpr int kSchedWarp = 6 + kEpiWarps;  // warp 22: waits on the MMA's inputs
 constexpr int kScaleWarp = 7 + kEpiWarps;  // warp 23: stages the scales
@@ -73,7 +79,10 @@ template <bool F8> constexpr int kDBufT = F8 ? 3 : 2;  // D buffers in flight
 template <bool F8> constexpr int kAColsT = F8 ? 32 : 64;  // A columns per group
 constexpr int kDBufMax = 3;
 constexpr int kABuf = 4;          // decoded weight (A) buffers in flight
-constexpr int kDone = 8;          // group-completion barriers (> every reuse distance)
+// Unit-completion barriers: more than every distance by which the MMA can
+// lead a waiter (5 groups of NSUB units for the q producer).
+template <int NSUB> constexpr int kDoneT = 8 * NSUB;
+constexpr int kDoneMax = 32;
 constexpr int kQBytes = BT * kGroup * 2;       // 32 KB: q tile of one group (fp16)
 constexpr int kCBytes = BW * kGroupCodeBytes;  // 4 KB: code bytes of one group
 constexpr int kDCol = 0;                       // D buffers: columns [0, kDBuf*BT)
@@ -83,26 +92,27 @@ static_assert(kAColT<false> + kABuf * kAColsT<false> <= kTmemCols, "tensor memor
 static_assert(kAColT<true> + kABuf * kAColsT<true> <= kTmemCols, "tensor memory budget");
 
 struct MmParams {
-  const float* sx;         // [M][G]
+  const float* sx;         // [M][G * NSUB]
   const uint16_t* scales;  // [N][G]
   void* y;                 // [M][N]
-  int32_t* dots;           // [M][N][G] (dot-only variant)
+  int32_t* dots;           // [M][N][G * NSUB] (dot-only variant)
   int32_t* status;
   int M, N, K, G;
   int y_bf16;
-  int vec_scales;  // G % kGC == 0 and s_x / s_w 16- / 8-byte aligned: vector staging
+  int vec_scales;  // whole chunks and s_x / s_w aligned for one vector load each
 };
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
 constexpr int kOffQ = 0;
 constexpr int kOffC = kOffQ + kStagesQ * kQBytes;
-// Scale ring: 2 chunks of {s_x [kGC][BT] fp32, s_w [BW][kGC] fp16}.
+// Scale ring: 2 chunks of {s_x [kGC][BT] fp32, s_w [BW][kGC / NSUB] fp16}
+// (a chunk is kGC accumulation units, kGC / NSUB weight groups).
 constexpr int kSxBytes = kGC * BT * 4;
 constexpr int kSwBytes = BW * kGC * 2;
 constexpr int kSBytes = kSxBytes + kSwBytes;
 constexpr int kOffS = kOffC + kStagesC * kCBytes;
 constexpr int kOffBar = kOffS + 2 * kSBytes;
-constexpr int kNumBars = kStagesQ + 2 * kStagesC + kABuf + kDone + kDBufMax + 4;
+constexpr int kNumBars = kStagesQ + 2 * kStagesC + kABuf + kDoneMax + kDBufMax + 4;
 constexpr int kOffTmemAddr = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffTmemAddr + 16 + 1024;  // + alignment slack
 
@@ -173,15 +183,16 @@ __device__ __forceinline__ void mma_commit(uint32_t on, uint64_t* bar) {
 __device__ __forceinline__ uint64_t f2_pack(uint32_t lo, uint32_t hi) {
   return ((uint64_t)hi << 32) | lo;
 }
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
+// acc += (d * x) * sw for two tokens: (d0, d1) and (x0, x1) become 64-bit
+// operands as register pairs inside the asm.  Built with shifts and ORs in
+// C++ instead, the pairs cost about as many instructions as the arithmetic
+// (measured: the epilogue took 5-9 % longer).
+__device__ __forceinline__ void epi_fma2(uint64_t& acc, uint32_t d0, uint32_t d1, uint32_t x0,
+                                         uint32_t x1, uint64_t sw2) {
+  asm("{\n\t.reg .b64 d, x, t;\n\tmov.b64 d, {%1, %2};\n\tmov.b64 x, {%3, %4};\n\t"
+      "mul.rn.f32x2 t, d, x;\n\tfma.rn.f32x2 %0, t, %5, %0;\n\t}"
+      : "+l"(acc)
+      : "r"(d0), "r"(d1), "r"(x0), "r"(x1), "l"(sw2));
 }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
@@ -281,11 +292,23 @@ __device__ __forceinline__ void decode_word_f8(uint32_t w, uint32_t* out) {
   out[3] = __byte_perm(kTable, 0u, (w2 >> 16) & 0x3333u);
 }
 
-template <bool DOTS, bool F8>
+// NSUB accumulation units per weight group: 1 for activation groups of 128,
+// 2 for 64 and 4 for 32 (KE Test 9).  Unit u = g * NSUB + h is the partial
+// dot of weight group g over activation group h: 8 / NSUB of the group's K
+// steps accumulated into one fresh D buffer, scaled by s_x[m][u] and
+// s_w[n][g].  The units of all groups share the ring of D buffers, so the
+// tensor-memory layout and the 128-token tile are the same for every NSUB;
+// a smaller activation group costs more D round trips and more epilogue
+// arithmetic per weight group, not more decoding.
+template <bool DOTS, bool F8, int NSUB>
 __global__ void __launch_bounds__(kThreads, 1)
     mm_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_c,
               const MmParams p) {
   constexpr int kDBuf = kDBufT<F8>, kACol = kAColT<F8>, kACols = kAColsT<F8>;
+  constexpr int kDone = kDoneT<NSUB>;
+  constexpr int kGW = kGC / NSUB;  // weight groups per scale chunk
+  static_assert(NSUB == 1 || NSUB == 2 || NSUB == 4, "activation groups of 128, 64 or 32");
+  static_assert(kDone <= kDoneMax, "completion barriers");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
@@ -294,8 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* c_full = q_full + kStagesQ;
   uint64_t* c_empty = c_full + kStagesC;
   uint64_t* a_full = c_empty + kStagesC;
-  uint64_t* g_done = a_full + kABuf;   // kDone: group g's MMAs are complete
-  uint64_t* d_empty = g_done + kDone;
+  uint64_t* g_done = a_full + kABuf;   // kDone: unit u's MMAs are complete
+  uint64_t* d_empty = g_done + kDoneMax;
   uint64_t* s_full = d_empty + kDBufMax;
   uint64_t* s_empty = s_full + 2;
   uint32_t* tmem_addr_s = reinterpret_cast<uint32_t*>(smem + kOffTmemAddr);
@@ -304,9 +327,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Token tiles vary fastest: CTAs running together read different q tiles
   // (no L2 hot spot) and share a few weight tiles.
   const int m0 = blockIdx.x * BT, n0 = blockIdx.y * BW;
-  const int G = p.G;
-  // Wait until group j's MMAs are complete (ring of kDone barriers, one
-  // phase per kDone groups; no waiter lags the MMA by kDone groups).
+  const int G = p.G, GU = p.G * NSUB;
+  // Wait until unit j's MMAs are complete (ring of kDone barriers, one
+  // phase per kDone units; no waiter lags the MMA by kDone units).
   auto done_wait = [&](int j) { return mbar_wait(&g_done[j % kDone], (j / kDone) & 1); };
 
   if (tid == 0) {
@@ -345,7 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (g >= kStagesC) ok = ok && mbar_wait(&c_empty[sc], ((g / kStagesC) - 1) & 1);
         mbar_arrive_expect_tx(&c_full[sc], kCBytes);
         tma_2d(smem + kOffC + sc * kCBytes, &map_c, g * kGroupCodeBytes, n0, &c_full[sc]);
-        if (g >= kStagesQ) ok = ok && done_wait(g - kStagesQ);
+        // The q stage is free once the last unit of its previous group is done.
+        if (g >= kStagesQ) ok = ok && done_wait((g - kStagesQ) * NSUB + NSUB - 1);
         uint8_t* qs = smem + kOffQ + sq * kQBytes;
         mbar_arrive_expect_tx(&q_full[sq], kQBytes);
         tma_2d(qs, &map_q, g * kGroup, m0, &q_full[sq]);
@@ -355,33 +379,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kScaleWarp) {
     // ------------------------------------------------------------- scales
-    // All 32 lanes stage the scales of each chunk of kGC groups (s_x of the
+    // All 32 lanes stage the scales of each chunk of kGC units (s_x of the
     // tile's tokens, s_w of its rows) into the two-slot scale ring, loading
     // chunk ch + 1 into registers while chunk ch waits for its slot.  A warp
     // of its own: the waits for a free slot (the epilogue's pace) never
     // delay the TMA issue of codes and q.
-    const int nchunks = (G + kGC - 1) / kGC;
+    const int nchunks = (GU + kGC - 1) / kGC;
     if (p.vec_scales) {
-      // Lane l stages tokens l + 32u and weight rows l + 32u: the kGC scales
-      // of one token (or one row) are consecutive in memory, so each is one
-      // 16-byte (8-byte) load, against kGC strided loads.  Every chunk is
-      // full (G % kGC == 0).
+      // Lane l stages tokens l + 32u and weight rows l + 32u: the chunk's
+      // kGC s_x of one token (and its kGW s_w of one row) are consecutive in
+      // memory, so each is one vector load, against kGC strided loads.
+      // Every chunk is full (GU % kGC == 0).
+      using WVec = typename std::conditional<
+          kGW == 4, uint2, typename std::conditional<kGW == 2, uint32_t, uint16_t>::type>::type;
       float4 xv[BT / 32];
-      uint2 wv[BW / 32];
+      WVec wv[BW / 32];
       auto load_scales = [&](int ch) {
 #pragma unroll
         for (int u = 0; u < BT / 32; ++u) {
           const int m = m0 + lane + 32 * u;
           xv[u] = (!DOTS && m < p.M)
-                      ? __ldg(reinterpret_cast<const float4*>(p.sx + (size_t)m * G + ch * kGC))
+                      ? __ldg(reinterpret_cast<const float4*>(p.sx + (size_t)m * GU + ch * kGC))
                       : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
 #pragma unroll
         for (int u = 0; u < BW / 32; ++u) {
           const int n = n0 + lane + 32 * u;
           wv[u] = (!DOTS && n < p.N)
-                      ? __ldg(reinterpret_cast<const uint2*>(p.scales + (size_t)n * G + ch * kGC))
-                      : make_uint2(0u, 0u);
+                      ? __ldg(reinterpret_cast<const WVec*>(p.scales + (size_t)n * G + ch * kGW))
+                      : WVec{};
         }
       };
       load_scales(0);
@@ -400,21 +426,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int u = 0; u < BW / 32; ++u)
-          *reinterpret_cast<uint2*>(sws + (lane + 32 * u) * kGC) = wv[u];  // [BW][kGC]
+          *reinterpret_cast<WVec*>(sws + (lane + 32 * u) * kGW) = wv[u];  // [BW][kGW]
         mbar_arrive(&s_full[slot]);
         if (ch + 1 < nchunks) load_scales(ch + 1);
       }
     } else {
-      constexpr int kPer = kGC * BT / 32;
-      float xv[kPer];
-      uint16_t wv[kPer];
+      constexpr int kPerX = kGC * BT / 32, kPerW = kGW * BW / 32;
+      float xv[kPerX];
+      uint16_t wv[kPerW];
       auto load_scales = [&](int ch) {
 #pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-          const int idx = lane + 32 * j;  // idx = gg * BT + t
-          const int gg = idx / BT, t = idx % BT, g = ch * kGC + gg, m = m0 + t;
-          xv[j] = (!DOTS && g < G && m < p.M) ? __ldg(p.sx + (size_t)m * G + g) : 0.0f;
-          const int r = idx / kGC, gw = ch * kGC + idx % kGC, n = n0 + r;  // idx = r*kGC + gg
+        for (int j = 0; j < kPerX; ++j) {
+          const int idx = lane + 32 * j;  // idx = uu * BT + t
+          const int uu = idx / BT, t = idx % BT, u = ch * kGC + uu, m = m0 + t;
+          xv[j] = (!DOTS && u < GU && m < p.M) ? __ldg(p.sx + (size_t)m * GU + u) : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < kPerW; ++j) {
+          const int idx = lane + 32 * j;  // idx = r * kGW + gg
+          const int r = idx / kGW, gw = ch * kGW + idx % kGW, n = n0 + r;
           wv[j] = (!DOTS && gw < G && n < p.N) ? __ldg(p.scales + (size_t)n * G + gw)
                                                : (uint16_t)0;
         }
@@ -426,10 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* sxs = reinterpret_cast<float*>(smem + kOffS + slot * kSBytes);  // [kGC][BT]
         uint16_t* sws = reinterpret_cast<uint16_t*>(smem + kOffS + slot * kSBytes + kSxBytes);
 #pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-          sxs[lane + 32 * j] = xv[j];
-          sws[lane + 32 * j] = wv[j];
-        }
+        for (int j = 0; j < kPerX; ++j) sxs[lane + 32 * j] = xv[j];
+#pragma unroll
+        for (int j = 0; j < kPerW; ++j) sws[lane + 32 * j] = wv[j];
         mbar_arrive(&s_full[slot]);
         if (ch + 1 < nchunks) load_scales(ch + 1);
       }
@@ -439,50 +468,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The issuing thread touches no shared memory and no mbarrier while its
     // MMAs run: such an access waits for the MMAs in flight, which left the
     // tensor pipe idle between groups.  The scheduler warp does the waiting;
-    // the two warps meet once per group at named barrier 1.
+    // the two warps meet once per unit at named barrier 1.
     constexpr uint32_t idesc = instr_desc_f16(BW, BT);
+    // K steps per unit: fp16 has eight K = 16 steps per group, e4m3 four
+    // K = 32 steps, each one MMA per q plane.
+    constexpr int kSteps = (F8 ? 4 : 8) / NSUB;
     const uint32_t issuer = elect_one();
-    for (int g = 0; g < G; ++g) {
+    for (int u = 0; u < GU; ++u) {
       named_bar_sync(1, 64);
-      const int sq = g % kStagesQ, b = g % kABuf, db = g % kDBuf;
+      const int g = u / NSUB, h = u % NSUB;
+      const int sq = g % kStagesQ, b = g % kABuf, db = u % kDBuf;
       tc_fence_after();
-      // Between two MMAs of a group only an add: the descriptor's start
+      // Between two MMAs of a unit only an add: the descriptor's start
       // address field is in 16-byte units.
       const uint64_t qd = smem_desc_sw128(smem_u32(smem + kOffQ + sq * kQBytes));
       const uint32_t d_tmem = tmem_base + kDCol + db * BT;
       const uint32_t a_tmem = tmem_base + kACol + b * kACols;  // b = g % kABuf
+      if constexpr (F8) {
+        // Plane 0 (16a) is B atom 0 and plane 1 (b) atom 1 (128 rows x 128
+        // bytes each); K step k sits at 32-byte offset k in the swizzled row
+        // and in A columns 8k..8k+7, for both planes.
 #pragma unroll
-      for (int k = 0; k < kGroup / 16; ++k) {
-        // Step k reads B at atom k/4 (128 rows x 128 bytes), 32-byte offset
-        // (k%4) inside the swizzled row.  fp16: K step k, A columns
-        // 8k..8k+7.  e4m3: atom 0 is the 16a plane and atom 1 the b plane,
-        // K step k%4 of 32 elements, A columns 8(k%4)..+7 for both.
-        const uint64_t boff16 = (uint64_t)(((k >> 2) * (BT * 128) + (k & 3) * 32) >> 4);
-        if constexpr (F8)
-          mma_f8_ta(issuer, d_tmem, a_tmem + 8 * (k & 3), qd + boff16, idesc, k > 0 ? 1u : 0u);
-        else
-          mma_f16_ta(issuer, d_tmem, a_tmem + 8 * k, qd + boff16, idesc, k > 0 ? 1u : 0u);
+        for (int pl = 0; pl < 2; ++pl)
+#pragma unroll
+          for (int i = 0; i < kSteps; ++i) {
+            const int k = h * kSteps + i;
+            const uint64_t boff16 = (uint64_t)((pl * (BT * 128) + k * 32) >> 4);
+            mma_f8_ta(issuer, d_tmem, a_tmem + 8 * k, qd + boff16, idesc,
+                      (pl > 0 || i > 0) ? 1u : 0u);
+          }
+      } else {
+#pragma unroll
+        for (int i = 0; i < kSteps; ++i) {
+          // fp16 K step k: B atom k/4 at 32-byte offset (k%4) inside the
+          // swizzled row, A columns 8k..8k+7.
+          const int k = h * kSteps + i;
+          const uint64_t boff16 = (uint64_t)(((k >> 2) * (BT * 128) + (k & 3) * 32) >> 4);
+          mma_f16_ta(issuer, d_tmem, a_tmem + 8 * k, qd + boff16, idesc, i > 0 ? 1u : 0u);
+        }
       }
-      // One commit per group tells the q producer, the decoders and the
+      // One commit per unit tells the q producer, the decoders and the
       // epilogue alike.
-      mma_commit(issuer, &g_done[g % kDone]);
+      mma_commit(issuer, &g_done[u % kDone]);
     }
   } else if (warp == kSchedWarp) {
     // ------------------------------------------------------------ scheduler
-    // Per group: A decoded (lane 0), q tile landed (lane 1), D buffer read
-    // by the epilogue (lane 2); then release the MMA warp.  Both warps run
-    // exactly G rounds of named barrier 1, whatever the waits return, so a
-    // wait that gives up (reported below) cannot leave the MMA warp stuck.
-    for (int g = 0; g < G; ++g) {
-      const int sq = g % kStagesQ, b = g % kABuf, db = g % kDBuf;
+    // Per unit: A decoded (lane 0) and q tile landed (lane 1) for the first
+    // unit of a group, D buffer read by the epilogue (lane 2); then release
+    // the MMA warp.  Both warps run exactly GU rounds of named barrier 1,
+    // whatever the waits return, so a wait that gives up (reported below)
+    // cannot leave the MMA warp stuck.
+    for (int u = 0; u < GU; ++u) {
+      const int g = u / NSUB, h = u % NSUB;
+      const int sq = g % kStagesQ, b = g % kABuf, db = u % kDBuf;
       // Lanes 0-2 wait at the same time, in one code path: three waits in
       // three divergent branches cost several hundred clocks per group even
       // when every phase has already completed.
       uint64_t* bar = lane == 0 ? &a_full[b] : lane == 1 ? &q_full[sq] : &d_empty[db];
       const uint32_t parity = lane == 0   ? (uint32_t)(g / kABuf) & 1u
                               : lane == 1 ? (uint32_t)(g / kStagesQ) & 1u
-                                          : (uint32_t)((g / kDBuf) - 1) & 1u;
-      if (lane < 2 || (lane == 2 && g >= kDBuf)) ok = ok && mbar_wait(bar, parity);
+                                          : (uint32_t)((u / kDBuf) - 1) & 1u;
+      if ((lane < 2 && h == 0) || (lane == 2 && u >= kDBuf)) ok = ok && mbar_wait(bar, parity);
       tc_fence_before();
       __syncwarp();
       named_bar_sync(1, 64);
@@ -495,7 +541,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int g = 0; g < G; ++g) {
       const int sc = g % kStagesC, b = g % kABuf;
       ok = ok && mbar_wait(&c_full[sc], (g / kStagesC) & 1);
-      if (g >= kABuf) ok = ok && done_wait(g - kABuf);
+      // The A buffer is free once the last unit of its previous group is done.
+      if (g >= kABuf) ok = ok && done_wait((g - kABuf) * NSUB + NSUB - 1);
       tc_fence_after();
       const uint8_t* cs = smem + kOffC + sc * kCBytes + row * kGroupCodeBytes;
       const uint4 c0 = *reinterpret_cast<const uint4*>(cs);
@@ -536,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t acc2[kEpiCols / 2];
 #pragma unroll
     for (int j = 0; j < kEpiCols / 2; ++j) acc2[j] = 0ull;
-    const int nchunks = (G + kGC - 1) / kGC;
+    const int nchunks = (GU + kGC - 1) / kGC;
     const bool live = m0 + col0 < p.M;  // some token of the warp's columns is real
     for (int ch = 0; ch < nchunks; ++ch) {
       const int slot = ch & 1;
@@ -544,24 +591,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* sxs = reinterpret_cast<const float*>(smem + kOffS + slot * kSBytes);
       const __half* sws = reinterpret_cast<const __half*>(smem + kOffS + slot * kSBytes + kSxBytes);
 #pragma unroll 1
-      for (int gg = 0; gg < kGC; ++gg) {
-        const int g = ch * kGC + gg;
-        if (g >= G) break;
-        const int db = g % kDBuf;
-        ok = ok && done_wait(g);
+      for (int uu = 0; uu < kGC; ++uu) {
+        const int u = ch * kGC + uu;
+        if (u >= GU) break;
+        const int db = u % kDBuf;
+        ok = ok && done_wait(u);
         tc_fence_after();
         if (!live) {
           // No valid token in this warp's columns (a partial last tile, as
           // for M = 16): release D without reading it.  The wait above keeps
-          // the warp in step: its arrival for group g + kDBuf cannot come
-          // before every warp has released group g's buffer.
+          // the warp in step: its arrival for unit u + kDBuf cannot come
+          // before every warp has released unit u's buffer.
           tc_fence_before();
           __syncwarp();
           warp_arrive(&d_empty[db]);
           continue;
         }
-        const float* sxg = sxs + gg * BT + col0;
-        const float sw = __half2float(sws[row * kGC + gg]);
+        const float* sxg = sxs + uu * BT + col0;
+        const float sw = __half2float(sws[row * kGW + uu / NSUB]);
         const uint64_t sw2 = f2_pack(__float_as_uint(sw), __float_as_uint(sw));
         const uint32_t taddr = tmem_base + lane_base + kDCol + db * BT + col0;
 #pragma unroll
@@ -583,17 +630,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int jj = 0; jj < 4; ++jj) {
                 const int m = m0 + col0 + 16 * hh + 4 * j4 + jj;
-                const float dot = __uint_as_float(v[4 * j4 + jj]);  // exact integer group dot
-                if (m < p.M && n < p.N) p.dots[((size_t)m * p.N + n) * G + g] = (int32_t)dot;
+                const float dot = __uint_as_float(v[4 * j4 + jj]);  // exact integer unit dot
+                if (m < p.M && n < p.N) p.dots[((size_t)m * p.N + n) * GU + u] = (int32_t)dot;
               }
             } else {
-              // acc += (dot * s_x) * s_w for two tokens per instruction
+              // acc += (dot * s_x) * s_w for two tokens per instruction pair
               const int t2 = (16 * hh + 4 * j4) / 2;
-              const uint64_t x01 = f2_pack(xv.x, xv.y), x23 = f2_pack(xv.z, xv.w);
-              const uint64_t d01 = f2_pack(v[4 * j4], v[4 * j4 + 1]);
-              const uint64_t d23 = f2_pack(v[4 * j4 + 2], v[4 * j4 + 3]);
-              acc2[t2] = f2_fma(f2_mul(d01, x01), sw2, acc2[t2]);
-              acc2[t2 + 1] = f2_fma(f2_mul(d23, x23), sw2, acc2[t2 + 1]);
+              epi_fma2(acc2[t2], v[4 * j4], v[4 * j4 + 1], xv.x, xv.y, sw2);
+              epi_fma2(acc2[t2 + 1], v[4 * j4 + 2], v[4 * j4 + 3], xv.z, xv.w, sw2);
             }
           }
         }
@@ -647,10 +691,10 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-template <bool DOTS, bool F8>
+template <bool DOTS, bool F8, int NSUB>
 int launch_mm_t(const CUtensorMap& mq, const CUtensorMap& mc, const MmParams& p,
                 cudaStream_t stream) {
-  auto kern = mm_kernel<DOTS, F8>;
+  auto kern = mm_kernel<DOTS, F8, NSUB>;
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
@@ -675,13 +719,25 @@ int launch_mm_t(const CUtensorMap& mq, const CUtensorMap& mc, const MmParams& p,
   return PQ2_OK;
 }
 
+template <int NSUB>
+int launch_mm_n(bool f8, bool dots, const CUtensorMap& mq, const CUtensorMap& mc,
+                const MmParams& p, cudaStream_t stream) {
+  if (f8)
+    return dots ? launch_mm_t<true, true, NSUB>(mq, mc, p, stream)
+                : launch_mm_t<false, true, NSUB>(mq, mc, p, stream);
+  return dots ? launch_mm_t<true, false, NSUB>(mq, mc, p, stream)
+              : launch_mm_t<false, false, NSUB>(mq, mc, p, stream);
+}
+
 }  // namespace
 
 int launch_mm(const void* q_op, bool f8, const float* sx, const int32_t* qsum,
               const uint8_t* codes, const uint16_t* scales, void* y, int y_dtype, int32_t* dots,
               int64_t M, int64_t N, int64_t K, int sm_count, int32_t* status,
-              cudaStream_t stream) {
+              cudaStream_t stream, int act_group) {
   (void)sm_count;
+  if (act_group != 128 && act_group != 64 && act_group != 32) return PQ2_ERR_SHAPE;
+  const int nsub = kGroup / act_group;
   if (M > (int64_t)1 << 20 || N > (int64_t)1 << 30) return PQ2_ERR_SHAPE;
   if ((M + BT - 1) / BT > 0x7fffffff || (N + BW - 1) / BW > 65535) return PQ2_ERR_SHAPE;
   EncodeTiledFn enc = encode_fn();
@@ -715,13 +771,14 @@ int launch_mm(const void* q_op, bool f8, const float* sx, const int32_t* qsum,
   p.sx = sx; p.scales = scales; p.y = y; p.dots = dots; p.status = status;
   p.M = (int)M; p.N = (int)N; p.K = (int)K; p.G = (int)(K / kGroup);
   p.y_bf16 = y_dtype == PQ2_BF16;
-  p.vec_scales = (p.G % kGC == 0) && reinterpret_cast<uintptr_t>(sx) % 16 == 0 &&
-                 reinterpret_cast<uintptr_t>(scales) % 8 == 0;
-  if (f8)
-    return dots ? launch_mm_t<true, true>(mq, mc, p, stream)
-                : launch_mm_t<false, true>(mq, mc, p, stream);
-  return dots ? launch_mm_t<true, false>(mq, mc, p, stream)
-              : launch_mm_t<false, false>(mq, mc, p, stream);
+  // One vector load per token (kGC s_x) and per row (kGC / nsub s_w) for
+  // every chunk: whole chunks, and both start addresses aligned to the load.
+  const int gw = kGC / nsub;
+  p.vec_scales = (p.G % gw == 0) && reinterpret_cast<uintptr_t>(sx) % 16 == 0 &&
+                 reinterpret_cast<uintptr_t>(scales) % (2 * gw) == 0;
+  if (nsub == 2) return launch_mm_n<2>(f8, dots != nullptr, mq, mc, p, stream);
+  if (nsub == 4) return launch_mm_n<4>(f8, dots != nullptr, mq, mc, p, stream);
+  return launch_mm_n<1>(f8, dots != nullptr, mq, mc, p, stream);
 }
 
 }  // namespace pq2

@@ -63,6 +63,12 @@ SIGNATURES = {
     "pq2_mm": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P]),
     "pq2_mm_f8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P]),
     "pq2_debug_group_dots": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P, _P, _P]),
+    "pq2_mm_grouped": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _P, _P]),
+    "pq2_mm_f8_grouped": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _P, _P]),
+    "pq2_debug_mm_dots_grouped": (_I, [_P, _I, _P, _I64, _I64, _I64, _I, _P, _P, _P]),
+    "pq2_linear_grouped_workspace_bytes": (_SZ, [_I64, _I64, _I]),
+    "pq2_linear_grouped": (_I, [_P, _I, _I64, _I64, _I64, _I64, _P, _P, _I, _P, _I, _P, _SZ, _P,
+                                _P]),
     "pq2_mmv_geometry": (_I, [_I64, _I64, _I, _P, _P, _P, _P]),
     "pq2_debug_mmv_drop_arrival": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I64, _P,
                                         _P]),
@@ -404,6 +410,72 @@ def pq2_debug_group_dots(q, codes, path: int, qsum=None, dots=None, status=None,
            lib().pq2_debug_group_dots(_ptr(q), _ptr(qsum), _ptr(codes), M, N, K, path,
                                       _ptr(dots), _ptr(status), _stream(stream)))
     return dots
+
+
+def pq2_mm_grouped(q_f16, sx, qsum, codes, scales, act_group: int, y=None,
+                   out_dtype=torch.float32, status=None, stream=None):
+    """Prefill matmul with activation groups of A (q from
+    pq2_quantize_act_grouped, PQ2_Q_F16)."""
+    M, K = q_f16.shape
+    N = codes.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=q_f16.device)
+    _check("pq2_mm_grouped", lib().pq2_mm_grouped(
+        _ptr(q_f16), _ptr(sx), _ptr(qsum), _ptr(codes), _ptr(scales), _ptr(y), _DT[y.dtype],
+        M, N, K, act_group, _ptr(status), _stream(stream)))
+    return y
+
+
+def pq2_mm_f8_grouped(q_f8, sx, qsum, codes, scales, act_group: int, y=None,
+                      out_dtype=torch.float32, status=None, stream=None):
+    """pq2_mm_grouped on the 8-bit tensor path (q PQ2_Q_F8)."""
+    M, K = q_f8.shape[0], q_f8.shape[1] // 2
+    N = codes.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=q_f8.device)
+    _check("pq2_mm_f8_grouped", lib().pq2_mm_f8_grouped(
+        _ptr(q_f8), _ptr(sx), _ptr(qsum), _ptr(codes), _ptr(scales), _ptr(y), _DT[y.dtype],
+        M, N, K, act_group, _ptr(status), _stream(stream)))
+    return y
+
+
+def pq2_debug_mm_dots_grouped(q, codes, path: int, act_group: int, dots=None, status=None,
+                              stream=None):
+    """Exact partial dots [M][N][K/A] of the grouped prefill kernels."""
+    M, K = q.shape
+    if path == PQ2_PATH_MM_F8:
+        K //= 2
+    N = codes.shape[0]
+    if dots is None:
+        dots = torch.empty((M, N, K // act_group), dtype=torch.int32, device=q.device)
+    _check("pq2_debug_mm_dots_grouped", lib().pq2_debug_mm_dots_grouped(
+        _ptr(q), path, _ptr(codes), M, N, K, act_group, _ptr(dots), _ptr(status),
+        _stream(stream)))
+    return dots
+
+
+def linear_grouped_workspace_bytes(M: int, K: int, act_group: int) -> int:
+    return lib().pq2_linear_grouped_workspace_bytes(M, K, act_group)
+
+
+def pq2_linear_grouped(x, codes, scales, act_group: int, y=None, out_dtype=torch.float32,
+                       workspace=None, status=None, stream=None):
+    """Complete projection with activation groups of A: the grouped quantiser,
+    then the grouped GEMV (M = 1..8) or the grouped prefill GEMM (M >= 9)."""
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit column stride")
+    M, K = x.shape
+    N = codes.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(linear_grouped_workspace_bytes(M, K, act_group),
+                                dtype=torch.uint8, device=x.device)
+    _check("pq2_linear_grouped", lib().pq2_linear_grouped(
+        _ptr(x), _DT[x.dtype], x.stride(0), M, N, K, _ptr(codes), _ptr(scales), act_group,
+        _ptr(y), _DT[y.dtype], _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(status), _stream(stream)))
+    return y
 
 
 def mmv_geometry(N: int, K: int, sm_count: int):

@@ -89,6 +89,35 @@ def oracle_rows(x, rows, codes_o, scales_o, chunk=16, threads=None):
     return np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts])
 
 
+def oracle_reference_grouped(x, codes_o, scales_o, A):
+    """(q, sx, qsum, dots, y32, y64, bound) of the oracle with activation
+    groups of A elements."""
+    a = O.widen(x_bits(x), kind(x))
+    q, sx = O.quantize_grouped(a, A)
+    dots = O.group_dots_grouped(q, codes_o, A)
+    y32, y64, bound = O.scale_accumulate_grouped(dots, sx, scales_o, A)
+    return q, sx, O.qsum_grouped(q, A), dots, y32, y64, bound
+
+
+def oracle_rows_grouped(x, rows, codes_o, scales_o, A, chunk=16, threads=None):
+    """oracle_rows with activation groups of A elements."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    xs = x[torch.as_tensor(np.asarray(rows))]
+    n = xs.shape[0]
+    pieces = [(i, min(i + chunk, n)) for i in range(0, n, chunk)]
+
+    def one(ab):
+        a, b = ab
+        *_, y64, bound = oracle_reference_grouped(xs[a:b], codes_o, scales_o, A)
+        return y64, bound
+
+    threads = threads or max(1, min(len(pieces), os.cpu_count() or 1))
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        parts = list(ex.map(one, pieces))
+    return np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts])
+
+
 def tile_rows(M, tile=128, total=64, seed=0):
     """Rows to compare at a large M: every row up to M = 512; above that,
     `total` seeded rows spread so that every tile of `tile` rows holds at

@@ -203,6 +203,42 @@ def test_grouped_validation(L):
         assert m(*bad) == err, (idx, val)
 
 
+def test_mm_grouped_validation(L):
+    for f in (L.pq2_mm_grouped, L.pq2_mm_f8_grouped):
+        ok = [A, A, A, A, A, A, pq2.PQ2_F32, 16, 10, 256, 64, None, None]
+        for idx, val, err in [(10, 16, pq2.PQ2_ERR_SHAPE), (10, 96, pq2.PQ2_ERR_SHAPE),
+                              (7, 0, pq2.PQ2_ERR_SHAPE), (9, 200, pq2.PQ2_ERR_SHAPE),
+                              (6, 1, pq2.PQ2_ERR_DTYPE), (0, None, pq2.PQ2_ERR_NULL),
+                              (2, None, pq2.PQ2_ERR_NULL), (0, A + 8, pq2.PQ2_ERR_ALIGN),
+                              (4, A + 1, pq2.PQ2_ERR_ALIGN)]:
+            bad = list(ok); bad[idx] = val
+            assert f(*bad) == err, (f, idx, val)
+    d = L.pq2_debug_mm_dots_grouped
+    ok = [A, pq2.PQ2_PATH_MM_F8, A, 16, 10, 256, 32, A, None, None]
+    for idx, val, err in [(1, pq2.PQ2_PATH_MMV_PLANES, pq2.PQ2_ERR_DTYPE),
+                          (6, 128 + 32, pq2.PQ2_ERR_SHAPE), (3, 0, pq2.PQ2_ERR_SHAPE),
+                          (7, None, pq2.PQ2_ERR_NULL), (7, A + 2, pq2.PQ2_ERR_ALIGN)]:
+        bad = list(ok); bad[idx] = val
+        assert d(*bad) == err, (idx, val)
+
+
+def test_linear_grouped_validation(L):
+    wb = L.pq2_linear_grouped_workspace_bytes
+    # q (int8 planes up to M = 8, two e4m3 planes from M = 9), s_x, sum(q)
+    assert wb(4, 256, 32) == 4 * 256 + 256 + 4 * 8 * 4
+    assert wb(9, 256, 64) == 9 * 512 + 256 + 9 * 4 * 4
+    assert wb(4, 256, 16) == 0 and wb(0, 256, 32) == 0 and wb(4, 200, 32) == 0
+    f = L.pq2_linear_grouped
+    need = wb(16, 256, 64)
+    ok = [A, pq2.PQ2_BF16, 256, 16, 10, 256, A, A, 64, A, pq2.PQ2_F32, A, need, None, None]
+    for idx, val, err in [(8, 16, pq2.PQ2_ERR_SHAPE), (12, need - 1, pq2.PQ2_ERR_SHAPE),
+                          (2, 255, pq2.PQ2_ERR_SHAPE), (1, 7, pq2.PQ2_ERR_DTYPE),
+                          (10, pq2.PQ2_F16, pq2.PQ2_ERR_DTYPE), (11, None, pq2.PQ2_ERR_NULL),
+                          (11, A + 16, pq2.PQ2_ERR_ALIGN), (6, A + 4, pq2.PQ2_ERR_ALIGN)]:
+        bad = list(ok); bad[idx] = val
+        assert f(*bad) == err, (idx, val)
+
+
 def test_ptq_validation(L):
     p = L.pq2_ptq_prepare
     assert p(A, 56, 1, 384, A, A, None) == pq2.PQ2_ERR_SHAPE       # K % 256
