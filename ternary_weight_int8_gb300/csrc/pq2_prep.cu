@@ -182,10 +182,19 @@ template <int kPrepThreads>
 __global__ void __launch_bounds__(kPrepThreads, kPrepThreads == 256 ? 4 : 1)
     prep_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ res,
                 uint16_t* __restrict__ res_out, const uint16_t* __restrict__ w,
-                const int8_t* __restrict__ sign, float eps, int K, int vec,
+                const int8_t* __restrict__ sign, float eps, int K, int vec, int fused_arg,
                 uint16_t* __restrict__ norm_out, void* __restrict__ q, int layout,
                 float* __restrict__ sx, int32_t* __restrict__ qsum) {
   extern __shared__ float sh[];
+  // Many rows (256 threads): each warp transforms and quantises its 1024-blocks
+  // in registers, 32 consecutive elements per lane (below), and h is stored
+  // with its 4-element chunks swizzled so that those reads are free of bank
+  // conflicts: element e sits at hpos(e).  The host sets fused_arg when the
+  // layout and alignments allow it.
+  const bool fused = kPrepThreads == 256 && fused_arg != 0;
+  auto hpos = [&](int e) {
+    return fused ? 32 * (e >> 5) + 4 * (((e >> 2) & 7) ^ ((e >> 5) & 7)) + (e & 3) : e;
+  };
   float* hs = sh;          // [K]    h = x (+ residual), then the transformed row
   float* tree = sh + K;    // [512]  cross-thread levels of the sum
   constexpr int kPrepWarps = kPrepThreads / 32;
@@ -239,8 +248,9 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepThreads == 256 ? 4 : 1)
           for (int e = 0; e < 4; ++e)
             ob[e] = (uint32_t)float_to_bf16_bits(h8[2 * e]) |
                     ((uint32_t)float_to_bf16_bits(h8[2 * e + 1]) << 16);
-          reinterpret_cast<float4*>(hs)[2 * c] = make_float4(h8[0], h8[1], h8[2], h8[3]);
-          reinterpret_cast<float4*>(hs)[2 * c + 1] = make_float4(h8[4], h8[5], h8[6], h8[7]);
+          *reinterpret_cast<float4*>(hs + hpos(8 * c)) = make_float4(h8[0], h8[1], h8[2], h8[3]);
+          *reinterpret_cast<float4*>(hs + hpos(8 * c + 4)) =
+              make_float4(h8[4], h8[5], h8[6], h8[7]);
           if (res_out)
             reinterpret_cast<uint4*>(res_out + m * K)[c] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
         }
@@ -250,7 +260,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepThreads == 256 ? 4 : 1)
     for (int j = t; j < K; j += kPrepThreads) {
       float a = bf16_bits_to_float(xr[j]);
       if (res) a = __fadd_rn(a, bf16_bits_to_float(res[m * K + j]));
-      hs[j] = a;
+      hs[hpos(j)] = a;
       if (res_out) res_out[m * K + j] = float_to_bf16_bits(a);
     }
   }
@@ -298,11 +308,17 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepThreads == 256 ? 4 : 1)
     float p[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) p[k] = 0.0f;
+    // Every j this thread reads has the same chunk and row bits below 2^8,
+    // so its swizzled position is j plus one offset.
+    const int dj = hpos(t) - t;
     for (int base = 0; base < K; base += kLanes) {
 #pragma unroll
       for (int k = 0; k < kPer; ++k) {
         const int j = base + t + kPrepThreads * k;
-        if (j < K) p[k] = __fadd_rn(p[k], __fmul_rn(hs[j], hs[j]));
+        if (j < K) {
+          const float v = hs[j + dj];
+          p[k] = __fadd_rn(p[k], __fmul_rn(v, v));
+        }
       }
     }
     // p[i] += p[i + len]: len 1024 .. kPrepThreads inside the thread (lane
@@ -345,6 +361,146 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepThreads == 256 ? 4 : 1)
   } else if (W == 2) {
     transform_shared<2, kPrepWarps>(hs, ops, inv, norm_out, m, K, nblk, warp, lane);
     __syncthreads();
+  } else if (fused) {
+    // Passes 2 and 3 together, one 1024-block per warp at a time, with no
+    // block-wide barrier: lane l holds the block's elements 32l + i
+    // (i = 0..31), so the transform's passes of half-width 1..16 pair
+    // registers of one lane.  A transpose through the block's own shared
+    // memory gives lane l the elements 32i + l for the passes of half-width
+    // 32..512 (again registers of one lane), and a second one brings the
+    // rounded block back to 32 consecutive elements per lane: a quarter of a
+    // 128-group, quantised by four lanes.  Every operation and its order are
+    // those of the other paths.
+    for (int b = warp * kHad; b < K; b += kPrepWarps * kHad) {
+      float* blk = hs + b;
+      const int sw = lane & 7;  // the lane's chunk swizzle (row 32 * lane)
+      float r[32];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float4 v = *reinterpret_cast<const float4*>(blk + 32 * lane + 4 * (k ^ sw));
+        r[4 * k] = v.x; r[4 * k + 1] = v.y; r[4 * k + 2] = v.z; r[4 * k + 3] = v.w;
+      }
+      // Normalise, round to bf16 and apply the signs, eight elements per
+      // 16-byte load of norm weights (and 8-byte load of signs).
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint4 wq = __ldg(reinterpret_cast<const uint4*>(w + b + 32 * lane) + k);
+        const uint2 sq = __ldg(reinterpret_cast<const uint2*>(sign + b + 32 * lane) + k);
+        const uint32_t wv[4] = {wq.x, wq.y, wq.z, wq.w};
+        const uint32_t sv[2] = {sq.x, sq.y};
+        uint32_t nb2[4];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int i = 8 * k + e;
+          const uint16_t wb = (uint16_t)(wv[e >> 1] >> (16 * (e & 1)));
+          const int8_t sg = (int8_t)(sv[e >> 2] >> (8 * (e & 3)));
+          const float tn =
+              __fmul_rn(__fmul_rn(r[i], inv), __fadd_rn(bf16_bits_to_float(wb), 1.0f));
+          const uint16_t nb = float_to_bf16_bits(tn);
+          if (e & 1) nb2[e >> 1] |= (uint32_t)nb << 16;
+          else nb2[e >> 1] = nb;
+          r[i] = bf16_signed(nb, sg);  // exact: the sign is +-1
+        }
+        if (norm_out)
+          reinterpret_cast<uint4*>(norm_out + m * K + b + 32 * lane)[k] =
+              make_uint4(nb2[0], nb2[1], nb2[2], nb2[3]);
+      }
+      // Half-width 1 (registers i, i + 1), then 2..16 on packed pairs.
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        const float a = r[i], c = r[i + 1];
+        r[i] = __fadd_rn(a, c);
+        r[i + 1] = __fsub_rn(a, c);
+      }
+#pragma unroll
+      for (int d = 2; d < 32; d <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          if (i & d) continue;
+          add_sub_f32x2(r[i], r[i + 1], r[i + d], r[i + d + 1]);
+        }
+      }
+      // Transpose: element 32i + l to lane l, register i.  Element e sits at
+      // hpos(e) - b: with row 32 * (e >> 5) and chunk (e >> 2) & 7, each
+      // access below touches 32 different banks.
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        *reinterpret_cast<float4*>(blk + 32 * lane + 4 * (k ^ sw)) =
+            make_float4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[i] = blk[32 * i + 4 * ((lane >> 2) ^ (i & 7)) + (lane & 3)];
+      // Half-width 32 (registers i, i + 1), then 64..512 on packed pairs.
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        const float a = r[i], c = r[i + 1];
+        r[i] = __fadd_rn(a, c);
+        r[i + 1] = __fsub_rn(a, c);
+      }
+#pragma unroll
+      for (int d = 2; d < 32; d <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          if (i & d) continue;
+          add_sub_f32x2(r[i], r[i + 1], r[i + d], r[i + d + 1]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i)  // 1/32 is exact
+        r[i] = bf16_bits_to_float(float_to_bf16_bits(r[i] * 0.03125f));
+      // Back to 32 consecutive elements per lane.
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) blk[32 * i + 4 * ((lane >> 2) ^ (i & 7)) + (lane & 3)] = r[i];
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float4 v = *reinterpret_cast<const float4*>(blk + 32 * lane + 4 * (k ^ sw));
+        r[4 * k] = v.x; r[4 * k + 1] = v.y; r[4 * k + 2] = v.z; r[4 * k + 3] = v.w;
+      }
+      // Lane j = l % 4 of group b / 128 + l / 4 holds its elements 32j..32j+31,
+      // its chunks 2j and 2j + 1, quantised and stored one chunk at a time.
+      const GroupScale z = quantize_scale32(r);
+      const int gi = b / kGroup + (lane >> 2);
+      const int64_t gbase = m * K + (int64_t)gi * kGroup;
+      int tsum = 0;
+      if (!z.exact) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          int qh[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            qh[e] = quantize_clamp(rintf(__fmul_rn(r[16 * hf + e], z.inv)));
+            tsum += qh[e];
+          }
+          store_chunk16(qh, 2 * (lane & 3) + hf, q, layout, gbase);
+        }
+      } else {
+        // Some group of the warp has a near tie (rare, warp-uniform): the
+        // IEEE divisions, on the values the block's shared memory still
+        // holds (so the registers above need not live through this path).
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          int qh[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int i = 16 * hf + e;
+            const float a = blk[32 * lane + 4 * ((i >> 2) ^ sw) + (i & 3)];
+            qh[e] = quantize_clamp(rintf(__fdiv_rn(a, z.d)));
+            tsum += qh[e];
+          }
+          store_chunk16(qh, 2 * (lane & 3) + hf, q, layout, gbase);
+        }
+      }
+#pragma unroll
+      for (int off = 2; off > 0; off >>= 1) tsum += __shfl_xor_sync(0xffffffffu, tsum, off);
+      if ((lane & 3) == 0) {
+        sx[m * G + gi] = z.s;
+        if (qsum) qsum[m * G + gi] = tsum;
+      }
+    }
+    return;
   } else {
     // Pass 2, one 1024-block per warp at a time: normalise, round to bf16,
     // apply the signs, transform, round to bf16, and store the block back.
@@ -621,8 +777,12 @@ int launch_prep(const uint16_t* x, const uint16_t* residual, uint16_t* residual_
   cfg.numAttrs = 1;
   auto a16 = [](const void* ptr) { return reinterpret_cast<uintptr_t>(ptr) % 16 == 0; };
   const int vec = a16(x) && (!residual || a16(residual)) && (!residual_out || a16(residual_out));
+  // The register path of the many-row kernel: 16-byte loads of the norm
+  // weights and signs, 16-byte stores of q (and of the normalised row).
+  const int fused = q_layout != PQ2_Q_MMV16 && a16(q) && a16(w) && a16(sign) &&
+                    (!norm_out || a16(norm_out));
   if (cudaLaunchKernelEx(&cfg, prep_kernel<kPrepThreads>, x, residual, residual_out, w, sign,
-                         eps, (int)K, vec,
+                         eps, (int)K, vec, fused,
                          norm_out, q, q_layout, sx, qsum) != cudaSuccess) {
     cudaGetLastError();
     return PQ2_ERR_LAUNCH;

@@ -288,4 +288,99 @@ __device__ __forceinline__ void store_group16(const int (&qi)[16], int j, bool s
   if (store && qsum && j % LG == 0) qsum[j / LG] = t;
 }
 
+// ------------------------------------------------------------------------
+// The same quantisation with four lanes per 128-group: lane j = L % 4 of a
+// group's four lanes holds its elements 32j..32j+31 (the fused
+// preparation's layout after its transform), so a warp quantises eight
+// groups at once with two shuffle levels per reduction.  The per-element
+// arithmetic is quantize_group4's.  quantize_scale32 forms the group's
+// scale and decides, warp-wide, between the product and the IEEE division
+// (near ties); the caller then forms each q (the product or the division,
+// rounded, then quantize_clamp), so the 32 rounded values never need
+// registers beside the 32 inputs.  Every lane of the warp must call
+// quantize_scale32.
+struct GroupScale {
+  float s, d, inv;
+  bool exact;  // some group of the warp has a near tie: IEEE divisions
+};
+__device__ __forceinline__ GroupScale quantize_scale32(const float (&a)[32]) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(a[i]));
+#pragma unroll
+  for (int off = 2; off > 0; off >>= 1)
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  GroupScale z;
+  z.s = __fdiv_rn(amax, 127.0f);
+  z.d = z.s > 0.0f ? z.s : 1.0f;
+  z.inv = __frcp_rn(z.d);
+  bool near_tie = z.d < 7.52316385e-37f;  // 2^-120
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float t = __fmul_rn(a[i], z.inv);
+    near_tie |= fabsf(t - rintf(t)) > 0.4999f;
+  }
+  z.exact = __any_sync(0xffffffffu, near_tie);
+  return z;
+}
+// The clamp of a rounded quotient to the int8 range of q.
+__device__ __forceinline__ int quantize_clamp(float r) {
+  return (int)fminf(fmaxf(r, -127.0f), 127.0f);
+}
+
+// Store the sixteen q of one 16-element chunk c (0..7) of the 128-group that
+// starts at element `base` of q, in the requested layout (not PQ2_Q_MMV16):
+// the layouts of store_group16.
+__device__ __forceinline__ void store_chunk16(const int (&qi)[16], int c, void* q, int layout,
+                                              int64_t base) {
+  auto byte = [&](int i) { return (uint32_t)(qi[i] & 0xff); };
+  if (layout == PQ2_Q_ROWS) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      w[k] = byte(4 * k) | (byte(4 * k + 1) << 8) | (byte(4 * k + 2) << 16) |
+             (byte(4 * k + 3) << 24);
+    reinterpret_cast<uint4*>(static_cast<int8_t*>(q) + base)[c] =
+        make_uint4(w[0], w[1], w[2], w[3]);
+  } else if (layout == PQ2_Q_PLANES) {
+    uint32_t* out = reinterpret_cast<uint32_t*>(static_cast<int8_t*>(q) + base);
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+      out[8 * s + c] = byte(s) | (byte(4 + s) << 8) | (byte(8 + s) << 16) | (byte(12 + s) << 24);
+  } else if (layout == PQ2_Q_F8) {
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int cw = 0; cw < 4; ++cw) {
+      hi[cw] = 0;
+      lo[cw] = 0;
+#pragma unroll
+      for (int e = 0; e < 4; e += 2) {
+        const int i0 = 8 * (cw >> 1) + (cw & 1) + 2 * e, i1 = i0 + 2;
+        const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(
+            make_float2((float)(16 * (qi[i0] >> 4)), (float)(16 * (qi[i1] >> 4))),
+            __NV_SATFINITE, __NV_E4M3);
+        const __nv_fp8x2_storage_t l2 = __nv_cvt_float2_to_fp8x2(
+            make_float2((float)(qi[i0] & 15), (float)(qi[i1] & 15)), __NV_SATFINITE, __NV_E4M3);
+        hi[cw] |= (uint32_t)h2 << (8 * e);
+        lo[cw] |= (uint32_t)l2 << (8 * e);
+      }
+    }
+    uint4* out = reinterpret_cast<uint4*>(static_cast<uint8_t*>(q) + 2 * base);
+    out[c] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    out[8 + c] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  } else {
+    uint32_t h[8];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const __half2 p01 = __halves2half2(__int2half_rn(qi[s]), __int2half_rn(qi[8 + s]));
+      const __half2 p23 = __halves2half2(__int2half_rn(qi[4 + s]), __int2half_rn(qi[12 + s]));
+      h[2 * s] = *reinterpret_cast<const uint32_t*>(&p01);
+      h[2 * s + 1] = *reinterpret_cast<const uint32_t*>(&p23);
+    }
+    uint4* out = reinterpret_cast<uint4*>(static_cast<__half*>(q) + base);
+    out[2 * c] = make_uint4(h[0], h[1], h[2], h[3]);
+    out[2 * c + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
 }  // namespace pq2

@@ -97,6 +97,83 @@ def test_prep_prefill_rows_sampled(M):
         assert np.array_equal(qs.cpu().numpy()[rows], qs_o)
 
 
+@pytest.mark.parametrize("K", [1024, 5120, 16384, 32768])
+def test_prep_many_rows_every_output(K):
+    """The many-row kernel (M = 608, the smallest M it runs) with one to 32
+    transform blocks per row: q in the four register-path layouts and the
+    tensor-core GEMV's, s_x, sum(q), the normalised row and the residual
+    output bit-exact on sampled rows."""
+    M, eps = 608, 1e-6
+    x, r, w, sign = _inputs(M, K, seed=K + 7, residual=True)
+    rows = np.array([0, 5, 301, M - 1])
+    q_o, sx_o, nb_o, rb_o = _oracle(x, r, w, sign, eps, rows=rows)
+    for layout in (pq2.PQ2_Q_ROWS, pq2.PQ2_Q_PLANES, pq2.PQ2_Q_F16, pq2.PQ2_Q_F8,
+                   pq2.PQ2_Q_MMV16):
+        q, sx, qs, nb, rb = pq2.pq2_norm_hadamard_quantize(
+            x.cuda(), w.cuda(), sign.cuda(), eps, residual=r.cuda(), layout=layout,
+            want_norm=True, want_residual=True)
+        torch.cuda.synchronize()
+        qh = q.cpu()
+        if layout == pq2.PQ2_Q_ROWS:
+            assert np.array_equal(qh.numpy()[rows], q_o)
+        elif layout == pq2.PQ2_Q_PLANES:
+            assert np.array_equal(qh.numpy()[rows], O.q_planes(q_o))
+        elif layout == pq2.PQ2_Q_F16:
+            assert np.array_equal(qh.float().numpy()[rows],
+                                  U.mm_operand_order(q_o).astype(np.float32))
+        elif layout == pq2.PQ2_Q_F8:
+            assert np.array_equal(qh.numpy()[rows], U.mm_operand_order_f8(q_o))
+        else:
+            assert np.array_equal(qh.float().numpy()[rows], U.mmv16_layout(q_o))
+        assert np.array_equal(sx.cpu().numpy()[rows].view(np.uint32), sx_o.view(np.uint32))
+        qs_o = U.mmv16_correction(q_o) if layout == pq2.PQ2_Q_MMV16 else O.qsum(q_o)
+        assert np.array_equal(qs.cpu().numpy()[rows], qs_o)
+        assert np.array_equal(synth.bits_u16(nb.cpu())[rows], nb_o)
+        assert np.array_equal(synth.bits_u16(rb.cpu())[rows], rb_o)
+
+
+def _walsh(k):
+    """Walsh function k of length 1024: (-1)^popcount(j & k)."""
+    j = np.arange(1024)
+    bits = np.array([bin(v).count("1") for v in (j & k)])
+    return np.where(bits % 2 == 0, 1.0, -1.0)
+
+
+def test_prep_many_rows_near_tie():
+    """A quotient on a half-integer in the many-row kernel: x = 1, eps = 0
+    (so inv = 1), w + 1 and the signs shaped so that each block's input is
+    W_a + W_b / 2 (two Walsh functions of the same 128-group).  The
+    transform then gives 32 at a and 16 at b, so q(16) = 16 / fl(32/127),
+    within 1e-4 of 63.5, which takes the IEEE-division branch; the other
+    elements are 0.  Bit-exact against the oracle on the first and last row."""
+    M, K = 608, 5120
+    w = np.empty(K, np.float32)
+    sign = np.empty(K, np.int8)
+    for blk in range(K // 1024):
+        a = 128 * (blk % 8) + 3 + blk
+        b = a + 64 + blk
+        v = _walsh(a) + 0.5 * _walsh(b)
+        w[1024 * blk:1024 * (blk + 1)] = np.abs(v) - 1.0   # w + 1 = |v|: 1.5 or 0.5
+        sign[1024 * blk:1024 * (blk + 1)] = np.where(v > 0, 1, -1)
+    x = torch.ones((M, K), dtype=torch.bfloat16)
+    wt = torch.from_numpy(w).to(torch.bfloat16)
+    st = torch.from_numpy(sign)
+    rows = np.array([0, M - 1])
+    q_o, sx_o, _, _ = _oracle(x, None, wt, st, 0.0, rows=rows)
+    assert set(np.unique(np.abs(q_o)).tolist()) <= {0, 63, 64, 127} and (np.abs(q_o) == 127).any()
+    assert ((np.abs(q_o) == 63) | (np.abs(q_o) == 64)).any()
+    for layout in (pq2.PQ2_Q_ROWS, pq2.PQ2_Q_F8):
+        q, sx, qs, _, _ = pq2.pq2_norm_hadamard_quantize(x.cuda(), wt.cuda(), st.cuda(), 0.0,
+                                                         layout=layout)
+        torch.cuda.synchronize()
+        if layout == pq2.PQ2_Q_ROWS:
+            assert np.array_equal(q.cpu().numpy()[rows], q_o)
+        else:
+            assert np.array_equal(q.cpu().numpy()[rows], U.mm_operand_order_f8(q_o))
+        assert np.array_equal(sx.cpu().numpy()[rows].view(np.uint32), sx_o.view(np.uint32))
+        assert np.array_equal(qs.cpu().numpy()[rows], O.qsum(q_o))
+
+
 def test_prep_rows_are_independent():
     """Row j of an 8-row call equals the same row prepared alone."""
     K, eps = 5120, 1e-6
