@@ -46,6 +46,12 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
+// Two roundings to bf16 in one conversion instruction (each half rounded to
+// nearest even, as float_to_bf16_bits): a in the low half, b in the high.
+__device__ __forceinline__ uint32_t float2_to_bf16x2_bits(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
 // The bf16 value with bits b times the sign +1 / -1 held in the int8 s:
 // exact, so a flip of the sign bit.
 __device__ __forceinline__ float bf16_signed(uint16_t b, int8_t s) {
@@ -245,9 +251,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepThreads == 256 ? 4 : 1)
             h8[e] = a;
           }
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            ob[e] = (uint32_t)float_to_bf16_bits(h8[2 * e]) |
-                    ((uint32_t)float_to_bf16_bits(h8[2 * e + 1]) << 16);
+          for (int e = 0; e < 4; ++e) ob[e] = float2_to_bf16x2_bits(h8[2 * e], h8[2 * e + 1]);
           *reinterpret_cast<float4*>(hs + hpos(8 * c)) = make_float4(h8[0], h8[1], h8[2], h8[3]);
           *reinterpret_cast<float4*>(hs + hpos(8 * c + 4)) =
               make_float4(h8[4], h8[5], h8[6], h8[7]);
@@ -390,16 +394,20 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepThreads == 256 ? 4 : 1)
         const uint32_t sv[2] = {sq.x, sq.y};
         uint32_t nb2[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int i = 8 * k + e;
-          const uint16_t wb = (uint16_t)(wv[e >> 1] >> (16 * (e & 1)));
-          const int8_t sg = (int8_t)(sv[e >> 2] >> (8 * (e & 3)));
-          const float tn =
-              __fmul_rn(__fmul_rn(r[i], inv), __fadd_rn(bf16_bits_to_float(wb), 1.0f));
-          const uint16_t nb = float_to_bf16_bits(tn);
-          if (e & 1) nb2[e >> 1] |= (uint32_t)nb << 16;
-          else nb2[e >> 1] = nb;
-          r[i] = bf16_signed(nb, sg);  // exact: the sign is +-1
+        for (int e2 = 0; e2 < 4; ++e2) {
+          const int i = 8 * k + 2 * e2;
+          const uint32_t wp2 = wv[e2];  // norm weights of elements i, i + 1
+          const float tn0 =
+              __fmul_rn(__fmul_rn(r[i], inv), __fadd_rn(__uint_as_float(wp2 << 16), 1.0f));
+          const float tn1 = __fmul_rn(__fmul_rn(r[i + 1], inv),
+                                      __fadd_rn(__uint_as_float(wp2 & 0xffff0000u), 1.0f));
+          nb2[e2] = float2_to_bf16x2_bits(tn0, tn1);
+          // The signs of elements i and i + 1 (bytes 2 (e2 & 1), + 1 of a
+          // sign word) flip bits 15 and 31 of the pair: exact.
+          const uint32_t sw2 = sv[e2 >> 1] >> (16 * (e2 & 1));
+          const uint32_t v = nb2[e2] ^ (((sw2 & 0x80u) << 8) | ((sw2 & 0x8000u) << 16));
+          r[i] = __uint_as_float(v << 16);
+          r[i + 1] = __uint_as_float(v & 0xffff0000u);
         }
         if (norm_out)
           reinterpret_cast<uint4*>(norm_out + m * K + b + 32 * lane)[k] =
@@ -447,8 +455,11 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepThreads == 256 ? 4 : 1)
         }
       }
 #pragma unroll
-      for (int i = 0; i < 32; ++i)  // 1/32 is exact
-        r[i] = bf16_bits_to_float(float_to_bf16_bits(r[i] * 0.03125f));
+      for (int i = 0; i < 32; i += 2) {  // 1/32 is exact; two bf16 roundings at once
+        const uint32_t v = float2_to_bf16x2_bits(r[i] * 0.03125f, r[i + 1] * 0.03125f);
+        r[i] = __uint_as_float(v << 16);
+        r[i + 1] = __uint_as_float(v & 0xffff0000u);
+      }
       // Back to 32 consecutive elements per lane.
       __syncwarp();
 #pragma unroll
@@ -471,7 +482,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepThreads == 256 ? 4 : 1)
           int qh[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            qh[e] = quantize_clamp(rintf(__fmul_rn(r[16 * hf + e], z.inv)));
+            qh[e] = quantize_product(r[16 * hf + e], z.inv);
             tsum += qh[e];
           }
           store_chunk16(qh, 2 * (lane & 3) + hf, q, layout, gbase);

@@ -303,6 +303,19 @@ struct GroupScale {
   float s, d, inv;
   bool exact;  // some group of the warp has a near tie: IEEE divisions
 };
+// Round to the nearest integer, ties to even, for |t| < 2^22: t + 1.5 * 2^23
+// lies in [2^23, 2^24), where the float spacing is 1, so the addition rounds
+// t's fraction exactly as rint does (1.5 * 2^23 is even), and the integer
+// sits in the low mantissa bits.  Two full-rate instructions instead of a
+// round and a conversion.  rint_magic_int is the integer, rint_magic_f the
+// float (the subtraction is exact).
+constexpr float kRintMagic = 12582912.0f;  // 1.5 * 2^23
+__device__ __forceinline__ int rint_magic_int(float t) {
+  return __float_as_int(__fadd_rn(t, kRintMagic)) - __float_as_int(kRintMagic);
+}
+__device__ __forceinline__ float rint_magic_f(float t) {
+  return __fsub_rn(__fadd_rn(t, kRintMagic), kRintMagic);
+}
 __device__ __forceinline__ GroupScale quantize_scale32(const float (&a)[32]) {
   float amax = 0.0f;
 #pragma unroll
@@ -317,8 +330,8 @@ __device__ __forceinline__ GroupScale quantize_scale32(const float (&a)[32]) {
   bool near_tie = z.d < 7.52316385e-37f;  // 2^-120
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
-    const float t = __fmul_rn(a[i], z.inv);
-    near_tie |= fabsf(t - rintf(t)) > 0.4999f;
+    const float t = __fmul_rn(a[i], z.inv);  // |t| <= 127 (1 + 2^-22)
+    near_tie |= fabsf(t - rint_magic_f(t)) > 0.4999f;
   }
   z.exact = __any_sync(0xffffffffu, near_tie);
   return z;
@@ -326,6 +339,12 @@ __device__ __forceinline__ GroupScale quantize_scale32(const float (&a)[32]) {
 // The clamp of a rounded quotient to the int8 range of q.
 __device__ __forceinline__ int quantize_clamp(float r) {
   return (int)fminf(fmaxf(r, -127.0f), 127.0f);
+}
+// q of one element on the product path of quantize_scale32: |a * inv| is at
+// most 127 (1 + 2^-22), so rint_magic_int applies and the clamp is on the
+// integer.
+__device__ __forceinline__ int quantize_product(float a, float inv) {
+  return max(min(rint_magic_int(__fmul_rn(a, inv)), 127), -127);
 }
 
 // Store the sixteen q of one 16-element chunk c (0..7) of the 128-group that
