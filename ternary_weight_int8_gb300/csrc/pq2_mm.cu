@@ -32,6 +32,11 @@
 // 128 / A accumulation units, each into its own fresh D buffer of the same
 // ring and scaled by its own s_x (the kernel's NSUB template parameter).
 //
+// At most 16 tokens (activation groups of 128): the narrow kernel, NW = 16.
+// The MMA's N is 16, a D buffer takes 16 columns (eight in flight), q
+// arrives in 16-row boxes, and one epilogue warp per lane quarter reads D.
+// The arithmetic of every output is that of the full tile.
+//
 // One CTA computes a tile of 128 output rows x 128 tokens:
 //   warp 0      TMA producer: q tiles (two 64-column boxes per group, 128-byte
 //               swizzle, the canonical K-major layout) and code tiles
@@ -64,8 +69,6 @@ namespace {
 
 constexpr int BW = 128;          // weight rows per tile (MMA M, A in TMEM)
 constexpr int BT = 128;          // tokens per tile (MMA N, B in shared memory)
-constexpr int kStagesQ = 6;      // q tile stages
-constexpr int kStagesC = 4;      // code tile stages
 constexpr int kGC = 4;           // accumulation units per scale chunk
 constexpr int kEpiWarps = 16;     // warps 6-21: four per TMEM lane quarter
 constexpr int kSchedWarp = 6 + kEpiWarps;  // warp 22: waits on the MMA's inputs
@@ -77,13 +80,17 @@ constexpr int kEpiCols = BT / 4;  // tokens per epilogue thread
 // which leaves room for a third D buffer.
 template <bool F8> constexpr int kDBufT = F8 ? 3 : 2;  // D buffers in flight
 template <bool F8> constexpr int kAColsT = F8 ? 32 : 64;  // A columns per group
-constexpr int kDBufMax = 3;
+// Few tokens (M <= kNarrowN): the MMA's N is kNarrowN, a D buffer takes
+// kNarrowN columns and kNarrowDBuf of them fit beside the A buffers.
+constexpr int kNarrowN = 16;
+constexpr int kNarrowDBuf = 8;
+constexpr int kDBufMax = 8;
 constexpr int kABuf = 4;          // decoded weight (A) buffers in flight
 // Unit-completion barriers: more than every distance by which the MMA can
 // lead a waiter (5 groups of NSUB units for the q producer).
 template <int NSUB> constexpr int kDoneT = 8 * NSUB;
 constexpr int kDoneMax = 32;
-constexpr int kQBytes = BT * kGroup * 2;       // 32 KB: q tile of one group (fp16)
+static_assert(kNarrowDBuf * kNarrowN + kABuf * 64 <= 512, "tensor memory budget (narrow)");
 constexpr int kCBytes = BW * kGroupCodeBytes;  // 4 KB: code bytes of one group
 constexpr int kDCol = 0;                       // D buffers: columns [0, kDBuf*BT)
 template <bool F8> constexpr int kAColT = kDBufT<F8> * BT;  // A buffers after them
@@ -102,19 +109,31 @@ struct MmParams {
   int vec_scales;  // whole chunks and s_x / s_w aligned for one vector load each
 };
 
-// Shared-memory layout (offsets from a 1024-byte aligned base).
-constexpr int kOffQ = 0;
-constexpr int kOffC = kOffQ + kStagesQ * kQBytes;
+// Shared-memory layout (offsets from a 1024-byte aligned base) for MMA width
+// NW (tokens per accumulation unit).  The q stage of a group holds two
+// 64-column boxes of NW rows (32 KB for a 128-token tile, 4 KB for the
+// narrow kernel).  (Deeper code rings, 12 stages beside 5 q stages and 32
+// in the narrow kernel, measured the same at M = 16 .. 4096.)
 // Scale ring: 2 chunks of {s_x [kGC][BT] fp32, s_w [BW][kGC / NSUB] fp16}
 // (a chunk is kGC accumulation units, kGC / NSUB weight groups).
 constexpr int kSxBytes = kGC * BT * 4;
 constexpr int kSwBytes = BW * kGC * 2;
 constexpr int kSBytes = kSxBytes + kSwBytes;
-constexpr int kOffS = kOffC + kStagesC * kCBytes;
-constexpr int kOffBar = kOffS + 2 * kSBytes;
-constexpr int kNumBars = kStagesQ + 2 * kStagesC + kABuf + kDoneMax + kDBufMax + 4;
-constexpr int kOffTmemAddr = kOffBar + kNumBars * 8;
-constexpr int kSmemBytes = kOffTmemAddr + 16 + 1024;  // + alignment slack
+template <int NW>
+struct Layout {
+  static constexpr int stagesQ = 6;  // q tile stages
+  static constexpr int stagesC = 4;  // code tile stages
+  static constexpr int qBytes = NW * kGroup * 2;    // q tile of one group
+  static constexpr int offQ = 0;
+  static constexpr int offC = offQ + stagesQ * qBytes;
+  static constexpr int offS = offC + stagesC * kCBytes;
+  static constexpr int offBar = offS + 2 * kSBytes;
+  static constexpr int numBars = stagesQ + 2 * stagesC + kABuf + kDoneMax + kDBufMax + 4;
+  static constexpr int offTmemAddr = offBar + numBars * 8;
+  static constexpr int smemBytes = offTmemAddr + 16 + 1024;  // + alignment slack
+  static_assert(qBytes % 2048 == 0, "each 64-column q box starts on a 1024-byte swizzle atom");
+  static_assert(smemBytes <= 227 * 1024, "shared memory per CTA");
+};
 
 // ------------------------------------------------------------ tcgen05 PTX
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
@@ -300,12 +319,28 @@ __device__ __forceinline__ void decode_word_f8(uint32_t w, uint32_t* out) {
 // tensor-memory layout and the 128-token tile are the same for every NSUB;
 // a smaller activation group costs more D round trips and more epilogue
 // arithmetic per weight group, not more decoding.
-template <bool DOTS, bool F8, int NSUB>
+template <bool DOTS, bool F8, int NSUB, int NW>
 __global__ void __launch_bounds__(kThreads, 1)
     mm_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_c,
               const MmParams p) {
-  constexpr int kDBuf = kDBufT<F8>, kACol = kAColT<F8>, kACols = kAColsT<F8>;
-  constexpr int kDone = kDoneT<NSUB>;
+  // NW: the MMA's N, tokens per accumulation unit.  BT for a full token tile;
+  // kNarrowN when the call has at most that many tokens: the q copies are
+  // NW rows, a D buffer is NW columns (kNarrowDBuf of them in flight, a
+  // ring eight deep instead of two or three), and one epilogue warp per
+  // lane quarter reads it.
+  constexpr bool kNarrow = NW < BT;
+  static_assert(NW == BT || (NW == kNarrowN && NSUB == 1), "token widths");
+  constexpr int kDBuf = kNarrow ? kNarrowDBuf : kDBufT<F8>;
+  constexpr int kACol = kDBuf * NW, kACols = kAColsT<F8>;
+  constexpr int kDone = kNarrow ? 2 * kNarrowDBuf : kDoneT<NSUB>;
+  constexpr int kEpiLive = kNarrow ? 4 : kEpiWarps;  // epilogue warps that take part
+  constexpr int kCols = kNarrow ? NW : kEpiCols;      // tokens per epilogue thread
+  constexpr int kQTx = NW * kGroup * 2;               // q bytes per group
+  static_assert(kDBuf <= kDBufMax && kACol + kABuf * kACols <= kTmemCols, "buffers");
+  using L = Layout<NW>;
+  constexpr int kStagesQ = L::stagesQ, kStagesC = L::stagesC, kQBytes = L::qBytes;
+  constexpr int kOffQ = L::offQ, kOffC = L::offC, kOffS = L::offS, kOffBar = L::offBar;
+  constexpr int kOffTmemAddr = L::offTmemAddr;
   constexpr int kGW = kGC / NSUB;  // weight groups per scale chunk
   static_assert(NSUB == 1 || NSUB == 2 || NSUB == 4, "activation groups of 128, 64 or 32");
   static_assert(kDone <= kDoneMax, "completion barriers");
@@ -339,9 +374,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kABuf; ++i) mbar_init(&a_full[i], 4);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 32);
-      mbar_init(&s_empty[i], kEpiWarps);
+      mbar_init(&s_empty[i], kEpiLive);
     }
-    for (int i = 0; i < kDBuf; ++i) mbar_init(&d_empty[i], kEpiWarps);
+    for (int i = 0; i < kDBuf; ++i) mbar_init(&d_empty[i], kEpiLive);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -371,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The q stage is free once the last unit of its previous group is done.
         if (g >= kStagesQ) ok = ok && done_wait((g - kStagesQ) * NSUB + NSUB - 1);
         uint8_t* qs = smem + kOffQ + sq * kQBytes;
-        mbar_arrive_expect_tx(&q_full[sq], kQBytes);
+        mbar_arrive_expect_tx(&q_full[sq], kQTx);
         tma_2d(qs, &map_q, g * kGroup, m0, &q_full[sq]);
         tma_2d(qs + kQBytes / 2, &map_q, g * kGroup + 64, m0, &q_full[sq]);
       }
@@ -469,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // MMAs run: such an access waits for the MMAs in flight, which left the
     // tensor pipe idle between groups.  The scheduler warp does the waiting;
     // the two warps meet once per unit at named barrier 1.
-    constexpr uint32_t idesc = instr_desc_f16(BW, BT);
+    constexpr uint32_t idesc = instr_desc_f16(BW, NW);
     // K steps per unit: fp16 has eight K = 16 steps per group, e4m3 four
     // K = 32 steps, each one MMA per q plane.
     constexpr int kSteps = (F8 ? 4 : 8) / NSUB;
@@ -482,10 +517,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Between two MMAs of a unit only an add: the descriptor's start
       // address field is in 16-byte units.
       const uint64_t qd = smem_desc_sw128(smem_u32(smem + kOffQ + sq * kQBytes));
-      const uint32_t d_tmem = tmem_base + kDCol + db * BT;
+      const uint32_t d_tmem = tmem_base + kDCol + db * NW;
       const uint32_t a_tmem = tmem_base + kACol + b * kACols;  // b = g % kABuf
       if constexpr (F8) {
-        // Plane 0 (16a) is B atom 0 and plane 1 (b) atom 1 (128 rows x 128
+        // Plane 0 (16a) is B box 0 and plane 1 (b) box 1 (NW rows x 128
         // bytes each); K step k sits at 32-byte offset k in the swizzled row
         // and in A columns 8k..8k+7, for both planes.
 #pragma unroll
@@ -493,17 +528,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < kSteps; ++i) {
             const int k = h * kSteps + i;
-            const uint64_t boff16 = (uint64_t)((pl * (BT * 128) + k * 32) >> 4);
+            const uint64_t boff16 = (uint64_t)((pl * (NW * 128) + k * 32) >> 4);
             mma_f8_ta(issuer, d_tmem, a_tmem + 8 * k, qd + boff16, idesc,
                       (pl > 0 || i > 0) ? 1u : 0u);
           }
       } else {
 #pragma unroll
         for (int i = 0; i < kSteps; ++i) {
-          // fp16 K step k: B atom k/4 at 32-byte offset (k%4) inside the
-          // swizzled row, A columns 8k..8k+7.
+          // fp16 K step k: B box k/4 (NW rows x 128 bytes) at 32-byte offset
+          // (k%4) inside the swizzled row, A columns 8k..8k+7.
           const int k = h * kSteps + i;
-          const uint64_t boff16 = (uint64_t)(((k >> 2) * (BT * 128) + (k & 3) * 32) >> 4);
+          const uint64_t boff16 = (uint64_t)(((k >> 2) * (NW * 128) + (k & 3) * 32) >> 4);
           mma_f16_ta(issuer, d_tmem, a_tmem + 8 * k, qd + boff16, idesc, i > 0 ? 1u : 0u);
         }
       }
@@ -572,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       warp_arrive(&c_empty[sc]);
       warp_arrive(&a_full[b]);
     }
-  } else if (warp >= 6 && warp < 6 + kEpiWarps) {
+  } else if (warp >= 6 && warp < 6 + kEpiLive) {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     const int col0 = ((warp - 6) >> 2) * kEpiCols;
@@ -580,9 +615,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n = n0 + row;
     const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
     // Token pairs (2j, 2j+1) of the thread's columns, as packed fp32 pairs.
-    uint64_t acc2[kEpiCols / 2];
+    uint64_t acc2[kCols / 2];
 #pragma unroll
-    for (int j = 0; j < kEpiCols / 2; ++j) acc2[j] = 0ull;
+    for (int j = 0; j < kCols / 2; ++j) acc2[j] = 0ull;
     const int nchunks = (GU + kGC - 1) / kGC;
     const bool live = m0 + col0 < p.M;  // some token of the warp's columns is real
     for (int ch = 0; ch < nchunks; ++ch) {
@@ -610,13 +645,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* sxg = sxs + uu * BT + col0;
         const float sw = __half2float(sws[row * kGW + uu / NSUB]);
         const uint64_t sw2 = f2_pack(__float_as_uint(sw), __float_as_uint(sw));
-        const uint32_t taddr = tmem_base + lane_base + kDCol + db * BT + col0;
+        const uint32_t taddr = tmem_base + lane_base + kDCol + db * NW + col0;
 #pragma unroll
-        for (int hh = 0; hh < kEpiCols / 16; ++hh) {
+        for (int hh = 0; hh < kCols / 16; ++hh) {
           uint32_t v[16];
           tmem_ld16(taddr + 16 * hh, v);
           tmem_ld_wait();
-          if (hh == kEpiCols / 16 - 1) {
+          if (hh == kCols / 16 - 1) {
             // D has been read: release the buffer to the MMA before the math.
             tc_fence_before();
             __syncwarp();
@@ -647,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!DOTS && n < p.N) {
 #pragma unroll
-      for (int t = 0; t < kEpiCols; ++t) {
+      for (int t = 0; t < kCols; ++t) {
         const int m = m0 + col0 + t;
         const float a = __uint_as_float((uint32_t)(acc2[t / 2] >> (32 * (t & 1))));
         if (m < p.M) {
@@ -691,13 +726,14 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-template <bool DOTS, bool F8, int NSUB>
+template <bool DOTS, bool F8, int NSUB, int NW>
 int launch_mm_t(const CUtensorMap& mq, const CUtensorMap& mc, const MmParams& p,
                 cudaStream_t stream) {
-  auto kern = mm_kernel<DOTS, F8, NSUB>;
+  auto kern = mm_kernel<DOTS, F8, NSUB, NW>;
   static bool configured = false;
   if (!configured) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Layout<NW>::smemBytes) !=
         cudaSuccess)
       return PQ2_ERR_LAUNCH;
     configured = true;
@@ -705,7 +741,7 @@ int launch_mm_t(const CUtensorMap& mq, const CUtensorMap& mc, const MmParams& p,
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((p.M + BT - 1) / BT, (p.N + BW - 1) / BW);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = Layout<NW>::smemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -719,14 +755,14 @@ int launch_mm_t(const CUtensorMap& mq, const CUtensorMap& mc, const MmParams& p,
   return PQ2_OK;
 }
 
-template <int NSUB>
+template <int NSUB, int NW = BT>
 int launch_mm_n(bool f8, bool dots, const CUtensorMap& mq, const CUtensorMap& mc,
                 const MmParams& p, cudaStream_t stream) {
   if (f8)
-    return dots ? launch_mm_t<true, true, NSUB>(mq, mc, p, stream)
-                : launch_mm_t<false, true, NSUB>(mq, mc, p, stream);
-  return dots ? launch_mm_t<true, false, NSUB>(mq, mc, p, stream)
-              : launch_mm_t<false, false, NSUB>(mq, mc, p, stream);
+    return dots ? launch_mm_t<true, true, NSUB, NW>(mq, mc, p, stream)
+                : launch_mm_t<false, true, NSUB, NW>(mq, mc, p, stream);
+  return dots ? launch_mm_t<true, false, NSUB, NW>(mq, mc, p, stream)
+              : launch_mm_t<false, false, NSUB, NW>(mq, mc, p, stream);
 }
 
 }  // namespace
@@ -742,13 +778,16 @@ int launch_mm(const void* q_op, bool f8, const float* sx, const int32_t* qsum,
   if ((M + BT - 1) / BT > 0x7fffffff || (N + BW - 1) / BW > 65535) return PQ2_ERR_SHAPE;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return PQ2_ERR_LAUNCH;
+  // At most kNarrowN tokens (activation groups of 128): the narrow kernel.
+  const bool narrow = nsub == 1 && M <= kNarrowN;
   CUtensorMap mq, mc;
   {
     // q: fp16 [M][K] (or its e4m3 planes, the same 2 bytes per element),
-    // box 64 x 128 (128-byte rows), 128-byte swizzle.
+    // box 64 x 128 (128-byte rows; kNarrowN rows for the narrow kernel),
+    // 128-byte swizzle.
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)BT};
+    const cuuint32_t box[2] = {64, (cuuint32_t)(narrow ? kNarrowN : BT)};
     const cuuint32_t es[2] = {1, 1};
     if (enc(&mq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(q_op), dims, strides,
             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -778,6 +817,7 @@ int launch_mm(const void* q_op, bool f8, const float* sx, const int32_t* qsum,
                  reinterpret_cast<uintptr_t>(scales) % (2 * gw) == 0;
   if (nsub == 2) return launch_mm_n<2>(f8, dots != nullptr, mq, mc, p, stream);
   if (nsub == 4) return launch_mm_n<4>(f8, dots != nullptr, mq, mc, p, stream);
+  if (narrow) return launch_mm_n<1, kNarrowN>(f8, dots != nullptr, mq, mc, p, stream);
   return launch_mm_n<1>(f8, dots != nullptr, mq, mc, p, stream);
 }
 
