@@ -51,10 +51,11 @@ def test_mm_group_dots_bitexact(M, N, K):
     assert U.guards_intact(back, guard)
 
 
-def test_mm_extreme_dots_exact():
+@pytest.mark.parametrize("M", [128, 16, 9])
+def test_mm_extreme_dots_exact(M):
     """The largest group dots (|dot| = 128 * 127 * 2 = 32512) and alternating
     signs stay exact on the fp16 tensor path."""
-    M, N, K = 128, 128, 512
+    N, K = 128, 512
     codes_np = np.full((N, K), 3, np.uint8)          # weight +2 everywhere
     codes_np[1::2, :] = 0                            # odd rows: weight -1
     codes_np[2::4, ::2] = 2                          # some +1

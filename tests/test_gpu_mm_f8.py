@@ -70,10 +70,11 @@ def test_mm_f8_group_dots_bitexact(M, N, K):
     assert U.guards_intact(back, guard)
 
 
-def test_mm_f8_extreme_dots_exact():
+@pytest.mark.parametrize("M", [128, 16, 9])
+def test_mm_f8_extreme_dots_exact(M):
     """|dot| = 32512 (weight +2 from code 3 against q = 127) and q = -127
     (16a = -128, b = 1) stay exact on the 8-bit path."""
-    M, N, K = 128, 128, 512
+    N, K = 128, 512
     codes_np = np.full((N, K), 3, np.uint8)
     codes_np[1::2, :] = 0
     codes_np[2::4, ::2] = 2
