@@ -1049,6 +1049,12 @@ def run_ours(args):
             for k in ("mm_us", "frac", "mm_f8_us", "f8_pipe_frac", "f8_e4m3_frac",
                       "complete_us"):
                 prefill[f"m{M}_{k}"] = d[k]
+        # activation groups of 64 / 32: "A:f8 GEMM us/complete us/cost" per M
+        for M, by_a in prefill.get("grouped", {}).items():
+            prefill[f"grouped_m{M}"] = " ".join(
+                f"{A}:{v['mm_f8_us']}/{v['complete_us']}"
+                + (f"/{v['complete_cost_vs_128']:+.3f}" if "complete_cost_vs_128" in v else "")
+                for A, v in by_a.items())
 
     result = {
         "metric": METRIC, "value": round(us_call, 3), "unit": "us/call", "n_gpus": world,
