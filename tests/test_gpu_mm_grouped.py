@@ -171,3 +171,21 @@ def test_linear_grouped_is_its_two_calls(M, A):
     *_, y64, bound = U.oracle_reference_grouped(x, codes_o, scales_o, A)
     ok, worst = O.within_bound(y.cpu().numpy(), y64, bound)
     assert ok, worst
+
+
+@pytest.mark.parametrize("M", [9, 16, 300])
+def test_prefill_kernels_are_deterministic(M):
+    """Repeated calls give the same bits: the grouped GEMM on both tensor
+    paths (A = 64, 32) and the A = 128 kernels, including the narrow kernel
+    at M <= 16 (fixed reduction order, no atomics)."""
+    N, K = 1000, 1152
+    raw = synth.raw_weights(N, K, seed=M, device="cuda")
+    codes, scales = pq2.pq2_prepare(raw, K)
+    x = synth.activations(M, K, seed=M + 1, device="cuda", outlier_frac=0.01)
+    for A in (128, 64, 32):
+        for mm, layout in ((pq2.pq2_mm_grouped, pq2.PQ2_Q_F16),
+                           (pq2.pq2_mm_f8_grouped, pq2.PQ2_Q_F8)):
+            q, sx, qs = pq2.pq2_quantize_act_grouped(x, A, layout)
+            ys = [mm(q, sx, qs, codes, scales, A) for _ in range(3)]
+            torch.cuda.synchronize()
+            assert all(torch.equal(ys[0].view(torch.int32), y.view(torch.int32)) for y in ys[1:])
